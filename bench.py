@@ -1,0 +1,358 @@
+"""Benchmark: block forward + fine-grained recompute + backward TFLOP/s on one GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME] [--recompute fine|full|none]
+
+One step = one oases_stack_step call (forward, recompute, backward of the whole
+block, weight gradients accumulated) on synthetic seeded inputs resident in HBM.
+The default workload is the pre-LN bf16 FFN block with hidden 1024, ffn 4096,
+seq 512, batch 8, w = 4 simulated shards, 2 sub-batches.  FLOPs are algorithmic
+and counted for the fine-grained schedule (FFN: 14 M H F; attention:
+30 M H^2 + 9 B S^2 H with causal halving), whatever mode is timed.
+
+L2: each timed step is bracketed by CUDA events on the call's first stream and
+followed, outside the events, by a 256 MiB write that flushes the 129 MB L2.
+
+--impl reference times the CPU oracle (fp64 numpy, oracle/) on this host's
+cores on a bounded sample of the same workload; it is a deliberately slow
+reference, not a competitor.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the block does not shard across GPUs here: all w shards live
+on one device); value = total FLOPs of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300"
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel (the fused column GEMM + bias + GeLU of the FFN, one sub-batch), with
+# the sha256 of the kernel source it was measured on; traffic is reported only
+# while the source is unchanged.
+NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+
+
+def flops_fine(shape) -> float:
+    M, H, B, S = shape.rows, shape.hidden, shape.batch, shape.seq
+    f = 0.0
+    if shape.kind in ("ffn", "layer"):
+        f += 14.0 * M * H * shape.ffn
+    if shape.kind in ("attn", "layer"):
+        att = 9.0 * B * S * S * H * (1.0 if shape.causal else 2.0)
+        f += 30.0 * M * H * H + att
+    return f * shape.n_layers
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+         "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            if k in d:
+                p[k] = float(d[k])
+        p["source"] = "measured"
+    return p
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                s, m = float(parts[0]), float(parts[1])
+                r = int(parts[2], 16)
+            except ValueError:
+                continue
+            sm.append(s)
+            mx = m
+            for bit, name in self.REASONS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args, shape):
+    """The oracle as it stands, on this host's cores, on a bounded sample."""
+    import numpy as np
+
+    import oracle
+    from synth import block_inputs
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    # sample: the first sequences of the workload (the FFN is row-wise, the
+    # attention per sequence), sized to a few seconds of fp64 work per step
+    per_seq = flops_fine(shape.replace(batch=1))
+    nb = max(shape.sub_batches, int(20e9 // max(per_seq, 1.0)))
+    nb = min(shape.batch, nb - nb % shape.sub_batches or shape.sub_batches)
+    sample = shape.replace(batch=nb)
+    inp = block_inputs(sample, seed=0)
+    for _ in range(args.warmup):
+        oracle.run_step(sample, inp, mode=args.recompute)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_step(sample, inp, mode=args.recompute)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = flops_fine(sample) / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded normal inputs, seed 0)",
+            "config": {"workload": args.workload, "batch_sample": nb, "recompute": args.recompute},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "%d of %d sequences per step" % (nb, shape.batch)},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(shape, recompute):
+    """Oracle timed once on a bounded sample (rank 0, N = 1 only)."""
+    import oracle
+    from synth import block_inputs
+    per_seq = flops_fine(shape.replace(batch=1))
+    nb = max(shape.sub_batches, int(15e9 // max(per_seq, 1.0)))
+    nb = min(shape.batch, nb - nb % shape.sub_batches or shape.sub_batches)
+    sample = shape.replace(batch=nb)
+    inp = block_inputs(sample, seed=0)
+    t0 = time.perf_counter()
+    oracle.run_step(sample, inp, mode=recompute)
+    dt = time.perf_counter() - t0
+    return {"value": flops_fine(sample) / dt / 1e12, "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": "one step on %d of %d sequences (%.1f s)" % (nb, shape.batch, dt)}
+
+
+def dominant_kernel_roofline(blk, shape, pk, torch):
+    """Average duration of the fused column GEMM (+bias+GeLU) at the step's
+    per-sub-batch shape, timed with CUDA events on its launch stream."""
+    import ctypes
+    import tensor_model_transformer_tp_gb300 as oz
+    L = oz.lib()
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    L.oases_debug_gemm.argtypes = [i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, i64,
+                                   i32, vp, vp, vp, i64, i32, vp]
+    L.oases_debug_gemm.restype = i32
+    Ms = shape.rows // shape.sub_batches
+    H = shape.hidden
+    if shape.kind == "attn":
+        N, wname, bname = 3 * H, "wqkv", "bqkv"
+        epi = 1
+    else:
+        N, wname, bname = shape.ffn, "w1", "b1"
+        epi = 2
+    p = blk.params[0]
+    dev = blk.device
+    u = torch.randn(Ms, H, device=dev).to(blk.dtype)
+    C = torch.empty(Ms, N, device=dev, dtype=blk.dtype)
+    C2 = torch.empty(Ms, N, device=dev, dtype=blk.dtype)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    sp = st.cuda_stream
+
+    def launch():
+        r = L.oases_debug_gemm(Ms, N, H, 1, u.data_ptr(), H, 1, p[wname].data_ptr(), H, 1, epi,
+                               C.data_ptr(), N, 1, C2.data_ptr(), p[bname].data_ptr(), None, 0, 0,
+                               sp)
+        assert r == 0, r
+
+    for _ in range(5):
+        launch()
+    times = []
+    for _ in range(20):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        launch()
+        e1.record(st)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    t = sum(times) / len(times)
+    fl = 2.0 * Ms * N * H
+    achieved = fl / t / 1e12
+    traffic = None
+    src = os.path.join(ROOT, "tensor_model_transformer_tp_gb300", "csrc", "gemm_tc.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if NCU_TRAFFIC["source_sha256"] == sha:
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    return {"kernel": "gemm_tc_kernel (column GEMM + bias + GeLU, %dx%dx%d)" % (Ms, N, H),
+            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+            "peak_source": pk["source"] + " (burst, kernel timed alone)",
+            "algorithmic_flops_per_launch": fl, "avg_launch_s": t}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ffn_bf16_h1024")
+    ap.add_argument("--recompute", default="fine", choices=["fine", "full", "none"])
+    ap.add_argument("--sub-batches", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from synth import SHAPES
+    shape = SHAPES[args.workload]
+    if args.sub_batches:
+        shape = shape.replace(sub_batches=args.sub_batches)
+    if args.impl == "reference":
+        run_reference(args, shape)
+        return
+
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from synth import block_inputs
+    from tensor_model_transformer_tp_gb300 import build_library, oases_last_launch_count
+    from tensor_model_transformer_tp_gb300.device import DeviceBlock
+    build_library()
+    inp = block_inputs(shape, seed=0)
+    blk = DeviceBlock(shape, inp["layers"], recompute=args.recompute,
+                      device="cuda:%d" % local)
+    x, g = blk.tensor(inp["x"]), blk.tensor(inp["g"])
+    y, dx = blk.empty_like_io(), blk.empty_like_io()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        blk.step(x, g, y, dx)
+    launches = oases_last_launch_count()
+    barrier()
+    with ClockSampler(local) as clk:
+        evs = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(blk.s0)
+            blk.step(x, g, y, dx)
+            e1.record(blk.s0)
+            evs.append((e0, e1))
+            flush.zero_()
+        barrier()
+    t_step = sum(a.elapsed_time(b) for a, b in evs) * 1e-3 / args.steps
+    if world > 1:
+        tt = torch.tensor([t_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_step = float(tt.item())
+    fl = flops_fine(shape)
+    value = fl * world / t_step / 1e12
+
+    # end to end: host (pinned) buffers through the same C-ABI call
+    xh = x.cpu().pin_memory()
+    gh = g.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(xh).pin_memory()
+    for _ in range(2):
+        blk.step(xh, gh, yh, dxh)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(blk.s0)
+    for _ in range(args.steps):
+        blk.step(xh, gh, yh, dxh)
+    e1.record(blk.s0)
+    barrier()
+    t_e2e = e0.elapsed_time(e1) * 1e-3 / args.steps
+    io = shape.rows * shape.hidden * (2 if shape.dtype == "bf16" else 4)
+
+    pk = peaks()
+    roof = dominant_kernel_roofline(blk, shape, pk, torch)
+    out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t_step * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": shape.dtype, "data": "synthetic (seeded normal inputs, seed 0)",
+           "config": {"workload": args.workload, "kind": shape.kind, "batch": shape.batch,
+                      "seq": shape.seq, "hidden": shape.hidden, "ffn": shape.ffn,
+                      "heads": shape.heads, "w": shape.w, "sub_batches": shape.sub_batches,
+                      "n_layers": shape.n_layers, "recompute": args.recompute,
+                      "parallelism": "replicas" if world > 1 else "single-gpu",
+                      "l2": "flushed between timed steps (256 MiB write)"},
+           "pct_bf16_peak": 100.0 * value / world / pk["bf16_tflops_sustained"],
+           "e2e": {"value": fl / t_e2e / 1e12 * world, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": 2 * io, "d2h_bytes_per_step": 2 * io},
+           "gpu_launches": launches * args.steps,
+           "clocks": clk.summary(),
+           "roofline": roof}
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(shape, args.recompute)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,43 @@
+/*
+ * oases_debug.h — kernel-level entry points of liboases.so, for testing the
+ * building blocks of the Oases block in isolation.
+ *
+ * The column-parallel F_i and row-parallel F_j of a segment (Oases, arXiv
+ * 2305.16121, §IV-A, Fig. 4a) and all their backward products are GEMMs of the
+ * form below with a fused epilogue; oases_debug_gemm runs exactly the kernel
+ * the block uses for such a product.
+ */
+#ifndef OASES_DEBUG_H
+#define OASES_DEBUG_H
+
+#include <stdint.h>
+
+#include "oases.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* D[m, n] = sum_k A(m, k) * B(n, k) for m < M, n < N, k < K, then epilogue:
+ *   0 Store      C = D
+ *   1 Bias       C = D + bias[n]
+ *   2 BiasGelu   C2 = D + bias[n] (if C2 != NULL); C = gelu(D + bias[n])
+ *   3 BiasResid  C = D + bias[n] + aux[m * ld_aux + n]
+ *   4 GeluBwd    C = D * gelu'(aux[m * ld_aux + n])
+ *   5 Accum      C (fp32) += D
+ * A(m, k) = a_kmajor ? A[m * lda + k] : A[k * lda + m]; B(n, k) likewise with
+ * b_kmajor / ldb.  A, B, bias and aux have type in_dtype (oases_dtype); C and
+ * C2 have type c_dtype, leading dimension ldc.  All pointers are device
+ * memory.  path: 0 = the block's own choice, 1 = CUDA-core kernel,
+ * 2 = tensor-core kernel (OASES_ERR_UNSUPPORTED if the operands do not meet
+ * its rules: bf16, K > 0, lda and ldb multiples of 8, 16-byte aligned A, B).
+ * Asynchronous on stream. */
+oases_status oases_debug_gemm(int M, int N, int K, int in_dtype, const void *A, int64_t lda,
+                              int a_kmajor, const void *B, int64_t ldb, int b_kmajor, int epilogue,
+                              void *C, int64_t ldc, int c_dtype, void *C2, const void *bias,
+                              const void *aux, int64_t ld_aux, int path, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OASES_DEBUG_H */

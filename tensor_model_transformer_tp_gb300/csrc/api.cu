@@ -1,0 +1,832 @@
+// C ABI and two-stream sub-batch scheduler of the Oases block library.
+//
+// The scheduler turns a call into the operator schedule of Oases §IV,
+// Algorithm 1 — a list of steps (event, operator, segment, sub-batch) — and
+// then executes every step by enqueueing its kernels on stream (sub-batch % 2):
+//
+//   forward    for every segment s, for every sub-batch b:
+//                F(ln) F(col) F(row) C(F)       C(F) is fused into the row GEMM:
+//                                              it contracts over all w shards'
+//                                              K-slices into one accumulator
+//   backward   for every segment s in reverse, for every sub-batch b:
+//                Sync  B(ln) of the later segment  (its input-gradient sum is done)
+//                R(ln) R(col) [R(row) C(R) in FULL mode]
+//                B(g)  B(row)  B(col)  C(B)
+//              and finally Sync B(ln) of segment 0.
+//
+// Because sub-batch b always runs on the same stream, a Sync needs no event:
+// stream order already places it after the sub-batch's own reduction.  The
+// other sub-batch's stream runs meanwhile, which is the pages' overlap of one
+// sub-batch's reduction with the other's compute (Fig. 4b, Fig. 4d).  The only
+// cross-stream dependencies are the weight-gradient accumulations, which are
+// chained sub-batch 0 -> 1 -> ... per (segment, parameter) with events so the
+// sums are taken in a fixed order.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "oases.h"
+
+namespace oases {
+thread_local int g_launch_count = 0;
+}
+
+namespace {
+using namespace oases;
+
+thread_local std::string t_last_error;
+thread_local int t_last_launches = 0;
+
+enum Ev { EV_F = 0, EV_R = 1, EV_B = 2, EV_CF = 3, EV_CR = 4, EV_CB = 5, EV_SYNC = 6 };
+enum OpN { OP_LN = 0, OP_F = 1, OP_COL = 2, OP_ROW = 3, OP_G = 4 };
+enum SegKind { SEG_FFN = 0, SEG_ATTN = 1 };
+// Weight-gradient groups of one segment, each accumulated in sub-batch order.
+enum Grp { GRP_BR = 0, GRP_WR = 1, GRP_BC = 2, GRP_WC = 3, GRP_LN = 4, GRP_N = 5 };
+
+struct Step {
+  int ev, op, seg, sb;
+};
+
+struct Shape {
+  int kind, B, S, H, F, nh, d, w, nsb, pre_ln, residual, causal, mode;
+  DType t;
+  float eps;
+  int64_t M, Ms;
+  size_t esz;
+  int segs_per_layer, nseg;
+  int seg_kind(int s) const {
+    if (kind == OASES_BLOCK_LAYER) return (s % 2 == 0) ? SEG_ATTN : SEG_FFN;
+    return kind == OASES_BLOCK_ATTN ? SEG_ATTN : SEG_FFN;
+  }
+};
+
+oases_status validate(const oases_block_desc* d, int n_layers, Shape* s) {
+  if (!d || n_layers < 1) return OASES_ERR_INVALID_ARG;
+  if (d->kind < 0 || d->kind > 2 || d->dtype < 0 || d->dtype > 1) return OASES_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->seq < 0 || d->hidden <= 0 || d->w < 1 || d->sub_batches < 1)
+    return OASES_ERR_INVALID_ARG;
+  if (d->batch % d->sub_batches != 0) return OASES_ERR_INVALID_ARG;
+  if (d->recompute < 0 || d->recompute > 2) return OASES_ERR_INVALID_ARG;
+  if (!(d->ln_eps >= 0.f)) return OASES_ERR_INVALID_ARG;
+  const bool has_ffn = d->kind != OASES_BLOCK_ATTN, has_attn = d->kind != OASES_BLOCK_FFN;
+  if (has_ffn && (d->ffn <= 0 || d->ffn % d->w != 0)) return OASES_ERR_INVALID_ARG;
+  if (has_attn) {
+    if (d->heads <= 0 || d->hidden % d->heads != 0 || d->heads % d->w != 0)
+      return OASES_ERR_INVALID_ARG;
+    const int hd = d->hidden / d->heads;
+    if (hd > 128 || hd % 8 != 0) return OASES_ERR_UNSUPPORTED;
+  }
+  if (d->dtype == OASES_BF16 && (d->hidden % 8 != 0 || (has_ffn && d->ffn % 8 != 0)))
+    return OASES_ERR_UNSUPPORTED;
+  const int64_t M = (int64_t)d->batch * d->seq;
+  const int64_t widest = has_ffn ? (d->ffn > 3 * d->hidden ? d->ffn : 3 * (int64_t)d->hidden)
+                                 : 3 * (int64_t)d->hidden;
+  if (M > (1ll << 30) || widest > (1ll << 30)) return OASES_ERR_UNSUPPORTED;
+  s->kind = d->kind;
+  s->B = d->batch;
+  s->S = d->seq;
+  s->H = d->hidden;
+  s->F = has_ffn ? d->ffn : 0;
+  s->nh = has_attn ? d->heads : 0;
+  s->d = has_attn ? d->hidden / d->heads : 0;
+  s->w = d->w;
+  s->nsb = d->sub_batches;
+  s->pre_ln = d->pre_ln != 0;
+  s->residual = d->residual != 0;
+  s->causal = d->causal != 0;
+  s->mode = d->recompute;
+  s->t = d->dtype == OASES_F32 ? DType::F32 : DType::BF16;
+  s->eps = d->ln_eps;
+  s->M = M;
+  s->Ms = M / d->sub_batches;
+  s->esz = dtype_size(s->t);
+  s->segs_per_layer = d->kind == OASES_BLOCK_LAYER ? 2 : 1;
+  s->nseg = s->segs_per_layer * n_layers;
+  return OASES_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout.  Every region spans all M rows; sub-batch b uses rows
+// [b*Ms, (b+1)*Ms) (per-head statistics: block b of [nsb][heads][Ms]).
+// ---------------------------------------------------------------------------
+constexpr size_t ALIGN = 256;
+inline size_t up(size_t v) { return (v + ALIGN - 1) / ALIGN * ALIGN; }
+
+struct ActSet {  // offsets relative to the workspace base
+  size_t u = 0, mu = 0, rstd = 0, a = 0, h = 0, qkv = 0, o = 0, lse = 0, delta = 0, d_o = 0,
+         dqkv = 0, du = 0, cpart = 0, lpart_g = 0, lpart_b = 0;
+};
+
+struct Layout {
+  size_t stage[4] = {0, 0, 0, 0};  // x, g, y, dx staging for host buffers
+  std::vector<size_t> ckpt;        // input of segment s (s >= 1)
+  size_t grad[2] = {0, 0};
+  size_t yr = 0;
+  std::vector<ActSet> act;  // per segment
+  size_t cpart_n = 0;       // floats per sub-batch in a colsum partial buffer
+  size_t lpart_n = 0;       // floats per sub-batch in an LN partial buffer
+  size_t total = 0;
+};
+
+Layout make_layout(const Shape& s) {
+  Layout L;
+  size_t off = ALIGN;  // first 256 bytes reserved
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += up(bytes);
+    return o;
+  };
+  const size_t MH = (size_t)s.M * s.H * s.esz;
+  for (int i = 0; i < 4; ++i) L.stage[i] = take(MH);
+  L.ckpt.assign(s.nseg, 0);
+  for (int i = 1; i < s.nseg; ++i) L.ckpt[i] = take(MH);
+  L.grad[0] = take(MH);
+  L.grad[1] = take(MH);
+  L.yr = take(MH);
+  const size_t maxN = (size_t)std::max<int64_t>(std::max(s.H, s.F), 3 * (int64_t)s.H);
+  L.cpart_n = (size_t)colsum_blocks((int)s.Ms) * maxN;
+  L.lpart_n = (size_t)ln_bwd_blocks((int)s.Ms) * s.H;
+  auto make_set = [&](int kind) {
+    ActSet a;
+    const size_t M = (size_t)s.M;
+    if (s.pre_ln) a.u = take(M * s.H * s.esz);
+    a.mu = take(M * 4);
+    a.rstd = take(M * 4);
+    if (kind == SEG_FFN) {
+      a.a = take(M * s.F * s.esz);
+      a.h = take(M * s.F * s.esz);
+    } else {
+      a.qkv = take(M * 3 * s.H * s.esz);
+      a.o = take(M * s.H * s.esz);
+      a.lse = take(M * s.nh * 4);
+      a.delta = take(M * s.nh * 4);
+      a.d_o = take(M * s.H * s.esz);
+      a.dqkv = take(M * 3 * s.H * s.esz);
+    }
+    a.du = take(M * s.H * 4);
+    a.cpart = take(s.nsb * L.cpart_n * 4);
+    a.lpart_g = take(s.nsb * L.lpart_n * 4);
+    a.lpart_b = take(s.nsb * L.lpart_n * 4);
+    return a;
+  };
+  L.act.resize(s.nseg);
+  if (s.mode == OASES_RECOMPUTE_NONE) {
+    for (int i = 0; i < s.nseg; ++i) L.act[i] = make_set(s.seg_kind(i));
+  } else {
+    ActSet per_kind[2];
+    bool made[2] = {false, false};
+    for (int i = 0; i < s.nseg; ++i) {
+      const int k = s.seg_kind(i);
+      if (!made[k]) {
+        per_kind[k] = make_set(k);
+        made[k] = true;
+      }
+      L.act[i] = per_kind[k];
+    }
+  }
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Schedule (Algorithm 1).
+// ---------------------------------------------------------------------------
+std::vector<Step> schedule(const Shape& s, int phase) {
+  std::vector<Step> out;
+  if (phase == 0) {
+    for (int seg = 0; seg < s.nseg; ++seg)
+      for (int b = 0; b < s.nsb; ++b) {
+        if (seg > 0) out.push_back({EV_SYNC, OP_G, seg - 1, b});
+        out.push_back({EV_F, OP_LN, seg, b});
+        out.push_back({EV_F, OP_COL, seg, b});
+        out.push_back({EV_F, OP_ROW, seg, b});
+        out.push_back({EV_CF, OP_G, seg, b});
+      }
+    for (int b = 0; b < s.nsb; ++b) out.push_back({EV_SYNC, OP_G, s.nseg - 1, b});
+    return out;
+  }
+  for (int seg = s.nseg - 1; seg >= 0; --seg)
+    for (int b = 0; b < s.nsb; ++b) {
+      if (seg < s.nseg - 1) {
+        out.push_back({EV_SYNC, OP_F, seg + 1, b});
+        out.push_back({EV_B, OP_LN, seg + 1, b});
+      }
+      if (s.mode != OASES_RECOMPUTE_NONE) {
+        out.push_back({EV_R, OP_LN, seg, b});
+        out.push_back({EV_R, OP_COL, seg, b});
+        if (s.mode == OASES_RECOMPUTE_FULL) {
+          out.push_back({EV_R, OP_ROW, seg, b});
+          out.push_back({EV_CR, OP_G, seg, b});
+        }
+      }
+      out.push_back({EV_B, OP_G, seg, b});
+      out.push_back({EV_B, OP_ROW, seg, b});
+      out.push_back({EV_B, OP_COL, seg, b});
+      out.push_back({EV_CB, OP_F, seg, b});
+    }
+  for (int b = 0; b < s.nsb; ++b) {
+    out.push_back({EV_SYNC, OP_F, 0, b});
+    out.push_back({EV_B, OP_LN, 0, b});
+  }
+  return out;
+}
+
+bool injected(const std::vector<Step>& steps) {
+  const char* v = std::getenv("OASES_TEST_FAIL_AT");
+  if (!v || !*v) return false;
+  int e, o, sg, b;
+  if (std::sscanf(v, "%d:%d:%d:%d", &e, &o, &sg, &b) != 4) return false;
+  for (const Step& st : steps)
+    if (st.ev == e && st.op == o && st.seg == sg && st.sb == b) return true;
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// Execution.
+// ---------------------------------------------------------------------------
+struct EventPool {
+  std::mutex mu;
+  std::vector<cudaEvent_t> ev;
+  cudaError_t ensure(size_t n) {
+    std::lock_guard<std::mutex> lock(mu);
+    while (ev.size() < n) {
+      cudaEvent_t e;
+      cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+      if (r != cudaSuccess) return r;
+      ev.push_back(e);
+    }
+    return cudaSuccess;
+  }
+};
+EventPool& pool() {
+  static EventPool p;
+  return p;
+}
+
+struct SegParams {  // one segment's weights / grads, typed by role
+  const void *g, *b, *wc, *bc, *wr, *br;
+  float *dg, *db, *dwc, *dbc, *dwr, *dbr;
+};
+
+struct Exec {
+  Shape s;
+  Layout L;
+  uint8_t* ws;
+  cudaStream_t st[2];
+  std::vector<SegParams> sp;  // per segment
+  const void* x;              // input of segment 0
+  void* y;                    // output of the last segment
+  const void* dy;             // gradient w.r.t. y
+  void* dx;                   // gradient w.r.t. x
+  cudaError_t err = cudaSuccess;
+  size_t ev_base = 2;  // pool()[0], [1]: call entry / exit joins
+
+  template <typename T = void>
+  T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+  size_t rows_off(int b, int64_t width, size_t esz) const {
+    return (size_t)b * s.Ms * width * esz;
+  }
+  const void* seg_in(int seg) const { return seg == 0 ? x : at(L.ckpt[seg]); }
+  void* seg_out(int seg) const { return seg == s.nseg - 1 ? y : at(L.ckpt[seg + 1]); }
+  const void* grad_out(int seg) const {  // dL/d(output of seg)
+    return seg == s.nseg - 1 ? dy : at(L.grad[seg & 1]);
+  }
+  void* grad_in(int seg) const {  // dL/d(input of seg)
+    return seg == 0 ? dx : at(L.grad[(seg - 1) & 1]);
+  }
+  template <typename P>
+  P rowp(P base, int b, int64_t width, size_t esz) const {
+    return reinterpret_cast<P>(reinterpret_cast<uintptr_t>(base) + rows_off(b, width, esz));
+  }
+  cudaStream_t stream(int b) const { return st[b & 1]; }
+
+  void ok(cudaError_t e) {
+    if (err == cudaSuccess && e != cudaSuccess) err = e;
+  }
+
+  // Weight-gradient ordering across sub-batches on different streams.
+  cudaEvent_t gev(int seg, int grp) const { return pool().ev[ev_base + seg * GRP_N + grp]; }
+  void grad_wait(int seg, int grp, int b) {
+    if (b > 0 && st[0] != st[1]) ok(cudaStreamWaitEvent(stream(b), gev(seg, grp), 0));
+  }
+  void grad_done(int seg, int grp, int b) {
+    if (b + 1 < s.nsb && st[0] != st[1]) ok(cudaEventRecord(gev(seg, grp), stream(b)));
+  }
+
+  GemmArgs base_gemm() const {
+    GemmArgs g;
+    g.in_t = s.t;
+    g.c_t = s.t;
+    g.aux_t = s.t;
+    return g;
+  }
+
+  // u = LN(x_seg) (or u = x_seg without LayerNorm).
+  const void* ln_fwd(int seg, int b) {
+    const ActSet& a = L.act[seg];
+    const void* xin = rowp(seg_in(seg), b, s.H, s.esz);
+    if (!s.pre_ln) return xin;
+    void* u = rowp(at(a.u), b, s.H, s.esz);
+    ok(layer_norm_fwd(xin, sp[seg].g, sp[seg].b, u, rowp(at<float>(a.mu), b, 1, 4),
+                      rowp(at<float>(a.rstd), b, 1, 4), (int)s.Ms, s.H, s.eps, s.t, stream(b)));
+    return u;
+  }
+  const void* u_of(int seg, int b) const {
+    return s.pre_ln ? rowp(at(L.act[seg].u), b, s.H, s.esz) : rowp(seg_in(seg), b, s.H, s.esz);
+  }
+
+  void col_fwd(int seg, int b, bool keep_preact) {
+    const ActSet& a = L.act[seg];
+    const SegParams& p = sp[seg];
+    const void* u = u_of(seg, b);
+    GemmArgs g = base_gemm();
+    g.M = (int)s.Ms;
+    g.K = s.H;
+    g.A = u;
+    g.lda = s.H;
+    if (s.seg_kind(seg) == SEG_FFN) {
+      g.N = s.F;
+      g.B = p.wc;
+      g.ldb = s.H;
+      g.epi = Epi::BiasGelu;
+      g.bias = p.bc;
+      g.C = rowp(at(a.h), b, s.F, s.esz);
+      g.ldc = s.F;
+      g.C2 = keep_preact ? rowp(at(a.a), b, s.F, s.esz) : nullptr;
+      ok(gemm(g, stream(b)));
+    } else {
+      g.N = 3 * s.H;
+      g.B = p.wc;
+      g.ldb = s.H;
+      g.epi = Epi::Bias;
+      g.bias = p.bc;
+      g.C = rowp(at(a.qkv), b, 3 * s.H, s.esz);
+      g.ldc = 3 * s.H;
+      ok(gemm(g, stream(b)));
+      AttnArgs at_;
+      at_.batch = s.B / s.nsb;
+      at_.seq = s.S;
+      at_.heads = s.nh;
+      at_.head_dim = s.d;
+      at_.hidden = s.H;
+      at_.causal = s.causal;
+      at_.t = s.t;
+      at_.qkv = g.C;
+      at_.o = rowp(at(a.o), b, s.H, s.esz);
+      at_.lse = at<float>(a.lse) + (size_t)b * s.nh * s.Ms;
+      ok(attention_fwd(at_, stream(b)));
+    }
+  }
+
+  // Row GEMM with the shard sum fused (C_i(F)); out = seg output or recompute scratch.
+  void row_fwd(int seg, int b, void* out) {
+    const ActSet& a = L.act[seg];
+    const SegParams& p = sp[seg];
+    const bool ffn = s.seg_kind(seg) == SEG_FFN;
+    GemmArgs g = base_gemm();
+    g.M = (int)s.Ms;
+    g.N = s.H;
+    g.K = ffn ? s.F : s.H;
+    g.A = ffn ? rowp(at(a.h), b, s.F, s.esz) : rowp(at(a.o), b, s.H, s.esz);
+    g.lda = g.K;
+    g.B = p.wr;
+    g.ldb = g.K;
+    g.bias = p.br;
+    g.C = rowp(out, b, s.H, s.esz);
+    g.ldc = s.H;
+    if (s.residual) {
+      g.epi = Epi::BiasResid;
+      g.aux = rowp(seg_in(seg), b, s.H, s.esz);
+      g.ld_aux = s.H;
+    } else {
+      g.epi = Epi::Bias;
+    }
+    ok(gemm(g, stream(b)));
+  }
+
+  float* cpart(int seg, int b) const {
+    return at<float>(L.act[seg].cpart) + (size_t)b * L.cpart_n;
+  }
+
+  void bwd_g(int seg, int b) {  // db_row += colsum(dy); Eq. (1): dP_k = dy, nothing else to do
+    grad_wait(seg, GRP_BR, b);
+    ok(colsum_accum(rowp(grad_out(seg), b, s.H, s.esz), s.H, (int)s.Ms, s.H, s.t, cpart(seg, b),
+                    sp[seg].dbr, stream(b)));
+    grad_done(seg, GRP_BR, b);
+  }
+
+  void bwd_row(int seg, int b) {
+    const ActSet& a = L.act[seg];
+    const SegParams& p = sp[seg];
+    const bool ffn = s.seg_kind(seg) == SEG_FFN;
+    const int Kin = ffn ? s.F : s.H;  // width of the row GEMM's input
+    const void* dyb = rowp(grad_out(seg), b, s.H, s.esz);
+    const void* hin = ffn ? rowp(at(a.h), b, s.F, s.esz) : rowp(at(a.o), b, s.H, s.esz);
+    // dW_row[H, Kin] += dy^T hin   (contraction over the sub-batch rows)
+    GemmArgs w = base_gemm();
+    w.M = s.H;
+    w.N = Kin;
+    w.K = (int)s.Ms;
+    w.A = dyb;
+    w.lda = s.H;
+    w.a_kmajor = false;
+    w.B = hin;
+    w.ldb = Kin;
+    w.b_kmajor = false;
+    w.epi = Epi::Accum;
+    w.C = p.dwr;
+    w.c_t = DType::F32;
+    w.ldc = Kin;
+    grad_wait(seg, GRP_WR, b);
+    ok(gemm(w, stream(b)));
+    grad_done(seg, GRP_WR, b);
+    // d(hin) = dy W_row; FFN: dA = dH * gelu'(A), written over A.
+    GemmArgs d = base_gemm();
+    d.M = (int)s.Ms;
+    d.N = Kin;
+    d.K = s.H;
+    d.A = dyb;
+    d.lda = s.H;
+    d.B = p.wr;
+    d.ldb = Kin;
+    d.b_kmajor = false;
+    d.ldc = Kin;
+    if (ffn) {
+      void* A = rowp(at(a.a), b, s.F, s.esz);
+      d.epi = Epi::GeluBwd;
+      d.aux = A;
+      d.ld_aux = s.F;
+      d.C = A;
+    } else {
+      d.epi = Epi::Store;
+      d.C = rowp(at(a.d_o), b, s.H, s.esz);
+    }
+    ok(gemm(d, stream(b)));
+  }
+
+  void bwd_col(int seg, int b) {
+    const ActSet& a = L.act[seg];
+    const SegParams& p = sp[seg];
+    const bool ffn = s.seg_kind(seg) == SEG_FFN;
+    const int Nc = ffn ? s.F : 3 * s.H;  // column GEMM output width
+    const void* dcol;
+    if (ffn) {
+      dcol = rowp(at(a.a), b, s.F, s.esz);  // dA
+    } else {
+      AttnArgs at_;
+      at_.batch = s.B / s.nsb;
+      at_.seq = s.S;
+      at_.heads = s.nh;
+      at_.head_dim = s.d;
+      at_.hidden = s.H;
+      at_.causal = s.causal;
+      at_.t = s.t;
+      at_.qkv = rowp(at(a.qkv), b, 3 * s.H, s.esz);
+      at_.o = rowp(at(a.o), b, s.H, s.esz);
+      at_.lse = at<float>(a.lse) + (size_t)b * s.nh * s.Ms;
+      at_.d_o = rowp(at(a.d_o), b, s.H, s.esz);
+      at_.delta = at<float>(a.delta) + (size_t)b * s.nh * s.Ms;
+      at_.dqkv = rowp(at(a.dqkv), b, 3 * s.H, s.esz);
+      ok(attention_bwd(at_, stream(b)));
+      dcol = at_.dqkv;
+    }
+    grad_wait(seg, GRP_BC, b);
+    ok(colsum_accum(dcol, Nc, (int)s.Ms, Nc, s.t, cpart(seg, b), p.dbc, stream(b)));
+    grad_done(seg, GRP_BC, b);
+    // dW_col[Nc, H] += dcol^T u
+    GemmArgs w = base_gemm();
+    w.M = Nc;
+    w.N = s.H;
+    w.K = (int)s.Ms;
+    w.A = dcol;
+    w.lda = Nc;
+    w.a_kmajor = false;
+    w.B = u_of(seg, b);
+    w.ldb = s.H;
+    w.b_kmajor = false;
+    w.epi = Epi::Accum;
+    w.C = p.dwc;
+    w.c_t = DType::F32;
+    w.ldc = s.H;
+    grad_wait(seg, GRP_WC, b);
+    ok(gemm(w, stream(b)));
+    grad_done(seg, GRP_WC, b);
+  }
+
+  // C_i(B): du = sum over shards of dcol_k W_col_k = dcol W_col (full-K contraction), fp32.
+  void comm_bwd(int seg, int b) {
+    const ActSet& a = L.act[seg];
+    const bool ffn = s.seg_kind(seg) == SEG_FFN;
+    const int Nc = ffn ? s.F : 3 * s.H;
+    GemmArgs g = base_gemm();
+    g.M = (int)s.Ms;
+    g.N = s.H;
+    g.K = Nc;
+    g.A = ffn ? rowp(at(a.a), b, s.F, s.esz) : rowp(at(a.dqkv), b, 3 * s.H, s.esz);
+    g.lda = Nc;
+    g.B = sp[seg].wc;
+    g.ldb = s.H;
+    g.b_kmajor = false;
+    g.epi = Epi::Store;
+    g.C = rowp(at<float>(a.du), b, s.H, 4);
+    g.c_t = DType::F32;
+    g.ldc = s.H;
+    ok(gemm(g, stream(b)));
+  }
+
+  void bwd_ln(int seg, int b) {
+    const ActSet& a = L.act[seg];
+    const float* du = rowp(at<float>(a.du), b, s.H, 4);
+    const void* dres = s.residual ? rowp(grad_out(seg), b, s.H, s.esz) : nullptr;
+    void* dxo = rowp(grad_in(seg), b, s.H, s.esz);
+    if (s.pre_ln) {
+      grad_wait(seg, GRP_LN, b);
+      ok(layer_norm_bwd(du, rowp(seg_in(seg), b, s.H, s.esz), rowp(at<float>(a.mu), b, 1, 4),
+                        rowp(at<float>(a.rstd), b, 1, 4), sp[seg].g, dres, dxo,
+                        at<float>(a.lpart_g) + (size_t)b * L.lpart_n,
+                        at<float>(a.lpart_b) + (size_t)b * L.lpart_n, sp[seg].dg, sp[seg].db,
+                        (int)s.Ms, s.H, s.t, stream(b)));
+      grad_done(seg, GRP_LN, b);
+    } else {
+      ok(add_into(dres, du, dxo, (int64_t)s.Ms * s.H, s.t, stream(b)));
+    }
+  }
+
+  void run(const Step& st_) {
+    const int seg = st_.seg, b = st_.sb;
+    switch (st_.ev) {
+      case EV_F:
+        if (st_.op == OP_LN) ln_fwd(seg, b);
+        else if (st_.op == OP_COL) col_fwd(seg, b, s.mode == OASES_RECOMPUTE_NONE);
+        else if (st_.op == OP_ROW) row_fwd(seg, b, seg_out(seg));
+        break;
+      case EV_R:
+        if (st_.op == OP_LN) ln_fwd(seg, b);
+        else if (st_.op == OP_COL) col_fwd(seg, b, true);
+        else if (st_.op == OP_ROW) row_fwd(seg, b, at(L.yr));
+        break;
+      case EV_B:
+        if (st_.op == OP_G) bwd_g(seg, b);
+        else if (st_.op == OP_ROW) bwd_row(seg, b);
+        else if (st_.op == OP_COL) bwd_col(seg, b);
+        else if (st_.op == OP_LN) bwd_ln(seg, b);
+        break;
+      case EV_CB:
+        comm_bwd(seg, b);
+        break;
+      default:  // C(F), C(R): fused into the row GEMM; Sync: stream order
+        break;
+    }
+  }
+};
+
+SegParams seg_params(const Shape& s, int seg, const oases_weights* w, const oases_grads* gr) {
+  const int layer = seg / s.segs_per_layer;
+  const oases_weights& W = w[layer];
+  SegParams p{};
+  const oases_grads* G = gr ? &gr[layer] : nullptr;
+  if (s.seg_kind(seg) == SEG_FFN) {
+    p = {W.ln2_g, W.ln2_b, W.w1, W.b1, W.w2, W.b2,
+         G ? G->ln2_g : nullptr, G ? G->ln2_b : nullptr, G ? G->w1 : nullptr,
+         G ? G->b1 : nullptr, G ? G->w2 : nullptr, G ? G->b2 : nullptr};
+  } else {
+    p = {W.ln1_g, W.ln1_b, W.wqkv, W.bqkv, W.wo, W.bo,
+         G ? G->ln1_g : nullptr, G ? G->ln1_b : nullptr, G ? G->wqkv : nullptr,
+         G ? G->bqkv : nullptr, G ? G->wo : nullptr, G ? G->bo : nullptr};
+  }
+  return p;
+}
+
+bool params_ok(const Shape& s, const std::vector<SegParams>& sp, bool need_grads) {
+  for (const SegParams& p : sp) {
+    if (!p.wc || !p.bc || !p.wr || !p.br) return false;
+    if (s.pre_ln && (!p.g || !p.b)) return false;
+    if (need_grads) {
+      if (!p.dwc || !p.dbc || !p.dwr || !p.dbr) return false;
+      if (s.pre_ln && (!p.dg || !p.db)) return false;
+    }
+  }
+  return true;
+}
+
+oases_status cuda_fail(cudaError_t e) {
+  t_last_error = cudaGetErrorString(e);
+  return OASES_ERR_CUDA;
+}
+
+// Runs the given phases (0 forward, 1 recompute + backward) of an n-layer call.
+oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const oases_grads* gr,
+                     const void* x, void* y, const void* dy, void* dx, void* ws, size_t ws_bytes,
+                     void* s0, void* s1, bool fwd, bool bwd, bool stage_host,
+                     const void* g_host_or_dev) {
+  t_last_error.clear();
+  g_launch_count = 0;
+  std::vector<Step> steps;
+  if (fwd) {
+    auto f = schedule(s, 0);
+    steps.insert(steps.end(), f.begin(), f.end());
+  }
+  if (bwd) {
+    auto b = schedule(s, 1);
+    steps.insert(steps.end(), b.begin(), b.end());
+  }
+  if (injected(steps)) return OASES_ERR_INJECTED;
+  Exec ex;
+  ex.s = s;
+  ex.L = make_layout(s);
+  if (!ws || ws_bytes < ex.L.total) return OASES_ERR_WORKSPACE;
+  if (((uintptr_t)ws) % ALIGN != 0) return OASES_ERR_INVALID_ARG;
+  ex.ws = static_cast<uint8_t*>(ws);
+  ex.st[0] = static_cast<cudaStream_t>(s0);
+  ex.st[1] = static_cast<cudaStream_t>(s1);
+  ex.sp.resize(s.nseg);
+  for (int i = 0; i < s.nseg; ++i) ex.sp[i] = seg_params(s, i, w, gr);
+  if (!params_ok(s, ex.sp, bwd)) return OASES_ERR_INVALID_ARG;
+  cudaError_t e = pool().ensure(ex.ev_base + (size_t)s.nseg * GRP_N);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  // Host buffers (oases_stack_step only) are staged through the workspace.
+  const size_t MH = (size_t)s.M * s.H * s.esz;
+  bool host[4] = {false, false, false, false};
+  const void* ptrs[4] = {x, g_host_or_dev, y, dx};
+  if (stage_host) {
+    for (int i = 0; i < 4; ++i) {
+      cudaPointerAttributes at{};
+      e = cudaPointerGetAttributes(&at, ptrs[i]);
+      if (e != cudaSuccess) return cuda_fail(e);
+      host[i] = at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+    }
+  }
+  ex.x = host[0] ? ex.at(ex.L.stage[0]) : x;
+  ex.dy = host[1] ? ex.at(ex.L.stage[1]) : dy;
+  ex.y = host[2] ? ex.at(ex.L.stage[2]) : y;
+  ex.dx = host[3] ? ex.at(ex.L.stage[3]) : dx;
+
+  cudaEvent_t ev_in = pool().ev[0], ev_out = pool().ev[1];
+  const bool two = ex.st[0] != ex.st[1];
+  if (host[0] && MH) ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[0]), x, MH, cudaMemcpyHostToDevice, ex.st[0]));
+  if (host[1] && MH) ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[1]), g_host_or_dev, MH, cudaMemcpyHostToDevice, ex.st[0]));
+  if (two) {
+    ex.ok(cudaEventRecord(ev_in, ex.st[0]));
+    ex.ok(cudaStreamWaitEvent(ex.st[1], ev_in, 0));
+  }
+  if (s.M > 0)
+    for (const Step& st : steps) {
+      ex.run(st);
+      if (ex.err != cudaSuccess) break;
+    }
+  if (two) {
+    ex.ok(cudaEventRecord(ev_out, ex.st[1]));
+    ex.ok(cudaStreamWaitEvent(ex.st[0], ev_out, 0));
+  }
+  if (host[2] && MH) ex.ok(cudaMemcpyAsync(const_cast<void*>(y), ex.y, MH, cudaMemcpyDeviceToHost, ex.st[0]));
+  if (host[3] && MH) ex.ok(cudaMemcpyAsync(dx, ex.dx, MH, cudaMemcpyDeviceToHost, ex.st[0]));
+  t_last_launches = g_launch_count;
+  if (ex.err != cudaSuccess) return cuda_fail(ex.err);
+  return OASES_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t oases_workspace_bytes(const oases_block_desc* desc, int n_layers) {
+  Shape s;
+  if (validate(desc, n_layers, &s) != OASES_OK) return 0;
+  return make_layout(s).total;
+}
+
+oases_status oases_block_fwd(const oases_block_desc* desc, const oases_weights* wts,
+                             const void* x, void* y, void* workspace, size_t ws_bytes, void* s0,
+                             void* s1) {
+  Shape s;
+  oases_status r = validate(desc, 1, &s);
+  if (r != OASES_OK) return r;
+  if (!wts || ((!x || !y) && s.M > 0)) return OASES_ERR_INVALID_ARG;
+  return execute(s, 1, wts, nullptr, x, y, nullptr, nullptr, workspace, ws_bytes, s0, s1, true,
+                 false, false, nullptr);
+}
+
+oases_status oases_block_recompute_bwd(const oases_block_desc* desc, const oases_weights* wts,
+                                       const void* x_saved, const void* dy, void* dx,
+                                       const oases_grads* grads, void* workspace,
+                                       size_t ws_bytes, void* s0, void* s1) {
+  Shape s;
+  oases_status r = validate(desc, 1, &s);
+  if (r != OASES_OK) return r;
+  if (!wts || !grads || ((!x_saved || !dy || !dx) && s.M > 0)) return OASES_ERR_INVALID_ARG;
+  return execute(s, 1, wts, grads, x_saved, nullptr, dy, dx, workspace, ws_bytes, s0, s1, false,
+                 true, false, nullptr);
+}
+
+oases_status oases_stack_step(const oases_block_desc* desc, int n_layers,
+                              const oases_weights* per_layer, const void* x, const void* g,
+                              void* y, void* dx, const oases_grads* per_layer_grads,
+                              void* workspace, size_t ws_bytes, void* s0, void* s1) {
+  Shape s;
+  oases_status r = validate(desc, n_layers, &s);
+  if (r != OASES_OK) return r;
+  if (!per_layer || !per_layer_grads || ((!x || !g || !y || !dx) && s.M > 0))
+    return OASES_ERR_INVALID_ARG;
+  return execute(s, n_layers, per_layer, per_layer_grads, x, y, g, dx, workspace, ws_bytes, s0,
+                 s1, true, true, s.M > 0, g);
+}
+
+const char* oases_status_str(oases_status st) {
+  switch (st) {
+    case OASES_OK: return "ok";
+    case OASES_ERR_INVALID_ARG: return "invalid argument";
+    case OASES_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case OASES_ERR_WORKSPACE: return "workspace missing or too small";
+    case OASES_ERR_CUDA: return "CUDA error";
+    case OASES_ERR_TIMEOUT: return "bounded device wait expired";
+    case OASES_ERR_INJECTED: return "injected failure (OASES_TEST_FAIL_AT)";
+  }
+  return "unknown status";
+}
+
+const char* oases_last_error(void) { return t_last_error.c_str(); }
+const char* oases_version(void) { return "oases-gb300 0.1 (sm_103a)"; }
+
+int oases_schedule_trace(const oases_block_desc* desc, int n_layers, int phase, int32_t* ops,
+                         int cap) {
+  Shape s;
+  if (validate(desc, n_layers, &s) != OASES_OK || (phase != 0 && phase != 1)) return -1;
+  std::vector<Step> st = schedule(s, phase);
+  for (int i = 0; i < (int)st.size() && i < cap && ops; ++i)
+    ops[i] = st[i].ev | (st[i].op << 4) | (st[i].sb << 8) | (st[i].seg << 16);
+  return (int)st.size();
+}
+
+int oases_last_launch_count(void) { return t_last_launches; }
+
+oases_status oases_check_device(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int v = gemm_read_and_clear_error();
+  if (v < 0) return cuda_fail(cudaGetLastError());
+  return v ? OASES_ERR_TIMEOUT : OASES_OK;
+}
+
+}  // extern "C"
+
+#include "oases_debug.h"
+
+extern "C" oases_status oases_debug_gemm(int M, int N, int K, int in_dtype, const void* A,
+                                         int64_t lda, int a_kmajor, const void* B, int64_t ldb,
+                                         int b_kmajor, int epilogue, void* C, int64_t ldc,
+                                         int c_dtype, void* C2, const void* bias, const void* aux,
+                                         int64_t ld_aux, int path, void* stream) {
+  using namespace oases;
+  t_last_error.clear();
+  g_launch_count = 0;
+  if (M < 0 || N < 0 || K < 0 || in_dtype < 0 || in_dtype > 1 || c_dtype < 0 || c_dtype > 1 ||
+      epilogue < 0 || epilogue > 5 || path < 0 || path > 2)
+    return OASES_ERR_INVALID_ARG;
+  if ((M > 0 && N > 0) && (!C || (K > 0 && (!A || !B)))) return OASES_ERR_INVALID_ARG;
+  const Epi epi = static_cast<Epi>(epilogue);
+  if ((epi == Epi::Bias || epi == Epi::BiasGelu || epi == Epi::BiasResid) && !bias)
+    return OASES_ERR_INVALID_ARG;
+  if ((epi == Epi::BiasResid || epi == Epi::GeluBwd) && !aux) return OASES_ERR_INVALID_ARG;
+  if (epi == Epi::Accum && c_dtype != OASES_F32) return OASES_ERR_INVALID_ARG;
+  GemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.in_t = static_cast<DType>(in_dtype);
+  g.A = A;
+  g.lda = lda;
+  g.a_kmajor = a_kmajor != 0;
+  g.B = B;
+  g.ldb = ldb;
+  g.b_kmajor = b_kmajor != 0;
+  g.epi = epi;
+  g.C = C;
+  g.ldc = ldc;
+  g.c_t = static_cast<DType>(c_dtype);
+  g.C2 = C2;
+  g.bias = bias;
+  g.aux = aux;
+  g.ld_aux = ld_aux;
+  g.aux_t = g.in_t;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (path == 1) {
+    e = gemm_simt(g, st);
+  } else if (path == 2) {
+    if (M == 0 || N == 0) return OASES_OK;
+    if (!gemm_tc_supported(g)) return OASES_ERR_UNSUPPORTED;
+    e = gemm_tc(g, st);
+  } else {
+    e = gemm(g, st);
+  }
+  t_last_launches = g_launch_count;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}

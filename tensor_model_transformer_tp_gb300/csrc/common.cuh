@@ -1,0 +1,148 @@
+// Shared device helpers of the Oases GB300 library: element types, GeLU, and
+// the launch descriptors every kernel family takes.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace oases {
+
+enum class DType : int { F32 = 0, BF16 = 1 };
+
+// Kernel launches issued by this host thread (read and reset by the scheduler).
+extern thread_local int g_launch_count;
+#define OASES_COUNT_LAUNCH() (++::oases::g_launch_count)
+
+inline size_t dtype_size(DType t) { return t == DType::F32 ? 4 : 2; }
+
+// Element load / store in fp32 registers.
+__device__ __forceinline__ float ld_elem(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_elem(float* p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16* p, int64_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ float load_any(const void* p, DType t, int64_t i) {
+  return t == DType::F32 ? static_cast<const float*>(p)[i]
+                         : __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+__device__ __forceinline__ void store_any(void* p, DType t, int64_t i, float v) {
+  if (t == DType::F32)
+    static_cast<float*>(p)[i] = v;
+  else
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+}
+
+// GeLU in its exact form a * Phi(a), Phi the standard normal CDF, and its
+// derivative Phi(a) + a * phi(a).  erff / expf are CUDA's own.
+__device__ __forceinline__ float gelu_f(float a) {
+  return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+}
+__device__ __forceinline__ float gelu_grad_f(float a) {
+  const float cdf = 0.5f * (1.0f + erff(a * 0.70710678118654752f));
+  const float pdf = 0.39894228040143268f * expf(-0.5f * a * a);
+  return cdf + a * pdf;
+}
+
+// ---------------------------------------------------------------------------
+// GEMM description shared by the SIMT and the tensor-core kernels.
+//   D[m, n] = sum_k A(m, k) * B(n, k), m < M, n < N, k < K.
+//   A(m, k) = a_kmajor ? A[m * lda + k] : A[k * lda + m]
+//   B(n, k) = b_kmajor ? B[n * ldb + k] : B[k * ldb + n]
+// followed by an epilogue on the fp32 accumulator.
+// ---------------------------------------------------------------------------
+enum class Epi : int {
+  Store = 0,      // C = acc
+  Bias = 1,       // C = acc + bias[n]
+  BiasGelu = 2,   // C2 = acc + bias[n] (pre-activation, if C2), C = gelu(acc + bias[n])
+  BiasResid = 3,  // C = acc + bias[n] + aux[m, n]
+  GeluBwd = 4,    // C = acc * gelu'(aux[m, n])
+  Accum = 5,      // C (fp32) += acc
+};
+
+struct GemmArgs {
+  int M = 0, N = 0, K = 0;
+  DType in_t = DType::BF16;
+  const void* A = nullptr;
+  int64_t lda = 0;
+  bool a_kmajor = true;
+  const void* B = nullptr;
+  int64_t ldb = 0;
+  bool b_kmajor = true;
+  Epi epi = Epi::Store;
+  void* C = nullptr;
+  int64_t ldc = 0;
+  DType c_t = DType::BF16;
+  void* C2 = nullptr;  // BiasGelu pre-activation output, type c_t, leading dim ldc
+  const void* bias = nullptr;  // [N], type in_t
+  const void* aux = nullptr;   // [M, N] with leading dim ld_aux, type aux_t
+  int64_t ld_aux = 0;
+  DType aux_t = DType::BF16;
+};
+
+// Returns cudaSuccess or the launch error.  Picks the tensor-core kernel when
+// the operands allow it and the SIMT kernel otherwise.
+cudaError_t gemm(const GemmArgs& g, cudaStream_t st);
+cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st);
+// Tensor-core path (tcgen05 + TMA); returns cudaErrorNotSupported when the
+// operands do not meet its alignment rules.
+cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st);
+bool gemm_tc_supported(const GemmArgs& g);
+
+// ---------------------------------------------------------------------------
+// Row-wise LayerNorm and column reductions (norm.cu).
+// ---------------------------------------------------------------------------
+// u = (x - mean) * rstd * gamma + beta over each row of [M, H]; writes mean,
+// rstd (fp32, [M]).
+cudaError_t layer_norm_fwd(const void* x, const void* gamma, const void* beta, void* u,
+                           float* mean, float* rstd, int M, int H, float eps, DType t,
+                           cudaStream_t st);
+// dx = rstd * (g - mean(g) - xhat * mean(g * xhat)) (+ dres), g = du * gamma;
+// du fp32 [M, H]; x, dres, dx in t.  Per-row-block partial sums of du * xhat
+// and du go to part_g / part_b ([n_blocks, H] fp32, n_blocks from
+// ln_bwd_blocks(M)); a second pass adds their column sums to dgamma / dbeta.
+int ln_bwd_blocks(int M);
+cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, const float* rstd,
+                           const void* gamma, const void* dres, void* dx, float* part_g,
+                           float* part_b, float* dgamma, float* dbeta, int M, int H, DType t,
+                           cudaStream_t st);
+// out[n] += sum_m in[m, n] for in [M, N] (type t, leading dim ld); partials in
+// part ([colsum_blocks(M), N] fp32).  Deterministic: fixed summation order.
+int colsum_blocks(int M);
+cudaError_t colsum_accum(const void* in, int64_t ld, int M, int N, DType t, float* part,
+                         float* out, cudaStream_t st);
+// y = x + a elementwise (n elements, type t); used for the residual gradient
+// when there is no LayerNorm.
+cudaError_t add_into(const void* a, const float* b, void* out, int64_t n, DType t,
+                     cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// Causal softmax attention over heads (attn.cu).
+//   qkv [M, 3H] (rows of one sequence contiguous; Q at column h*d, K at
+//   H + h*d, V at 2H + h*d), o [M, H], lse [heads, M] fp32.
+// ---------------------------------------------------------------------------
+struct AttnArgs {
+  int batch = 0, seq = 0, heads = 0, head_dim = 0, hidden = 0;
+  bool causal = true;
+  DType t = DType::BF16;
+  const void* qkv = nullptr;
+  void* o = nullptr;
+  float* lse = nullptr;
+  // backward
+  const void* d_o = nullptr;  // [M, H]
+  float* delta = nullptr;     // [heads, M]: rowsum(dO * O)
+  void* dqkv = nullptr;       // [M, 3H]
+};
+cudaError_t attention_fwd(const AttnArgs& a, cudaStream_t st);
+cudaError_t attention_bwd(const AttnArgs& a, cudaStream_t st);
+cudaError_t attention_fwd_simt(const AttnArgs& a, cudaStream_t st);
+cudaError_t attention_bwd_simt(const AttnArgs& a, cudaStream_t st);
+
+// Reads and clears the error word the tensor-core kernels set when a bounded
+// wait expires (0 = none, -1 = could not read).
+int gemm_read_and_clear_error();
+
+}  // namespace oases

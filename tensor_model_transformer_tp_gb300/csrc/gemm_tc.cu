@@ -1,0 +1,438 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   D[m, n] = sum_k A(m, k) B(n, k), fp32 accumulation in tensor memory,
+//   followed by the block's fused epilogue (bias, GeLU, residual, GeLU',
+//   fp32 accumulate).
+//
+// One CTA per SM, persistent over 128 x BN output tiles (BN = 128 or 256).
+// Warp roles (192 threads):
+//   warp 0      one thread issues TMA loads of A and B K-slices (64 bf16 =
+//               128 bytes deep, 128-byte swizzle) into a STAGES-deep ring;
+//   warp 1      allocates 2*BN TMEM columns (two accumulators) and one thread
+//               issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction);
+//               tcgen05.commit frees a ring slot once its MMAs are done and
+//               hands a finished accumulator to the epilogue;
+//   warps 2..5  read the accumulator (TMEM lane = output row; a warp may only
+//               touch lanes 32*(warp % 4) .. +31), apply the epilogue and store.
+// The accumulator is double-buffered so the epilogue of tile t overlaps the
+// main loop of tile t+1.  Operands may be K-major or MN-major; MN-major tiles
+// are loaded as 64-element-wide chunks and described with LBO = chunk stride.
+//
+// The row-parallel GEMM (F_j) of a segment contracts over all w shards'
+// K-slices into one accumulator: that is the on-chip form of the AllReduce
+// y = sum_k P_k of Oases §IV, Eq. (1).
+//
+// Every mbarrier wait is bounded (2 s); on expiry the thread records an error
+// in g_gemm_error, drains what it has in flight and leaves, so the kernel
+// always terminates.
+#include <cuda.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "epilogue.cuh"
+#include "sm100_ptx.cuh"
+
+namespace oases {
+
+__device__ int g_gemm_error;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BKE = 64;  // K elements per stage (128 bytes of bf16)
+constexpr int NTHREADS = 192;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int A_BYTES = BM * BKE * 2;
+  static constexpr int B_BYTES = BN * BKE * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8;
+  static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+  static constexpr int TMEM_COLS = 2 * BN;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void unpack8(uint4 u, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void load32_bf16(const void* p, float* f) {
+  const uint4* q = static_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack8(__ldg(q + i), f + 8 * i);
+}
+__device__ __forceinline__ void store32_bf16(void* p, const float* f) {
+  uint4* q = static_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    q[i] = make_uint4(pack_bf16(f[8 * i], f[8 * i + 1]), pack_bf16(f[8 * i + 2], f[8 * i + 3]),
+                      pack_bf16(f[8 * i + 4], f[8 * i + 5]), pack_bf16(f[8 * i + 6], f[8 * i + 7]));
+}
+
+// Epilogue of 32 consecutive outputs (m, n .. n+31) held in v.
+__device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int n, float (&v)[32]) {
+  const bool vec = (n + 32 <= g.N) && g.in_t == DType::BF16 &&
+                   (g.c_t == DType::BF16 ? (g.ldc % 8 == 0) : (g.ldc % 4 == 0)) &&
+                   (g.aux == nullptr || (g.ld_aux % 8 == 0 && g.aux_t == DType::BF16)) &&
+                   (((uintptr_t)g.C | (uintptr_t)g.C2 | (uintptr_t)g.aux | (uintptr_t)g.bias) & 15) == 0;
+  if (!vec) {
+    for (int i = 0; i < 32; ++i)
+      if (n + i < g.N) epi_apply(g, m, n + i, v[i]);
+    return;
+  }
+  const int64_t ci = (int64_t)m * g.ldc + n;
+  if (g.epi == Epi::Accum) {
+    float4* c = reinterpret_cast<float4*>(static_cast<float*>(g.C) + ci);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 o = c[i];
+      o.x += v[4 * i];
+      o.y += v[4 * i + 1];
+      o.z += v[4 * i + 2];
+      o.w += v[4 * i + 3];
+      c[i] = o;
+    }
+    return;
+  }
+  float t[32];
+  if (g.epi == Epi::Bias || g.epi == Epi::BiasGelu || g.epi == Epi::BiasResid) {
+    load32_bf16(static_cast<const __nv_bfloat16*>(g.bias) + n, t);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += t[i];
+  }
+  if (g.epi == Epi::BiasResid || g.epi == Epi::GeluBwd) {
+    load32_bf16(static_cast<const __nv_bfloat16*>(g.aux) + (int64_t)m * g.ld_aux + n, t);
+    if (g.epi == Epi::BiasResid) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += t[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(t[i]);
+    }
+  }
+  if (g.epi == Epi::BiasGelu) {
+    if (g.C2) {
+      if (g.c_t == DType::BF16) store32_bf16(static_cast<__nv_bfloat16*>(g.C2) + ci, v);
+      else {
+        float4* c = reinterpret_cast<float4*>(static_cast<float*>(g.C2) + ci);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+  }
+  if (g.c_t == DType::BF16) {
+    store32_bf16(static_cast<__nv_bfloat16*>(g.C) + ci, v);
+  } else {
+    float4* c = reinterpret_cast<float4*>(static_cast<float*>(g.C) + ci);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+template <int BN, bool A_K, bool B_K>
+__global__ void __launch_bounds__(NTHREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmArgs g) {
+  using C = TcCfg<BN>;
+  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, !A_K, !B_K);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + C::STAGES * C::STAGE;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
+  auto tfull = [&](int b) { return bars + 8u * (2 * C::STAGES + b); };
+  auto tempty = [&](int b) { return bars + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t drain = bars + 8u * (2 * C::STAGES + 4);
+  const uint32_t tslot = bars + 8u * (2 * C::STAGES + 5);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int num_m = (g.M + BM - 1) / BM, num_n = (g.N + BN - 1) / BN;
+  const int tiles = num_m * num_n, nkb = (g.K + BKE - 1) / BKE;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(full(s), 1);
+      ptx::mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull(b), 1);
+      ptx::mbar_init(tempty(b), 128);
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tslot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t issued = 0;  // bit s: stage s has a load outstanding at some phase
+      uint32_t iphase = 0;  // bit s: parity of the last load issued into stage s
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!ptx::mbar_wait(empty(stage), phase ^ 1u)) { ok = false; break; }
+          const uint32_t fb = full(stage);
+          ptx::mbar_arrive_expect_tx(fb, C::STAGE);
+          const uint32_t sa = base + stage * C::STAGE, sb = sa + C::A_BYTES;
+          const int k0 = kb * BKE;
+          if (A_K) {
+            ptx::tma_load_2d(sa, &tmA, fb, k0, m0);
+          } else {
+            ptx::tma_load_2d(sa, &tmA, fb, m0, k0);
+            ptx::tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
+          }
+          if (B_K) {
+            ptx::tma_load_2d(sb, &tmB, fb, k0, n0);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) ptx::tma_load_2d(sb + c * 8192, &tmB, fb, n0 + 64 * c, k0);
+          }
+          issued |= 1u << stage;
+          iphase = (iphase & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Drain: every TMA load this thread issued has landed before the CTA exits.
+      for (int s = 0; s < C::STAGES; ++s)
+        if ((issued >> s) & 1u)
+          if (!ptx::mbar_wait(full(s), (iphase >> s) & 1u)) ok = false;
+      if (!ok) atomicExch(&g_gemm_error, 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int t = 0;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++t) {
+        const int buf = t & 1;
+        if (!ptx::mbar_wait(tempty(buf), (((uint32_t)t >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!ptx::mbar_wait(full(stage), phase)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t sa = base + stage * C::STAGE, sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BKE / 16; ++kk) {
+            const uint64_t ad = A_K ? ptx::smem_desc_sw128(sa + kk * 32, 16, 1024)
+                                    : ptx::smem_desc_sw128(sa + kk * 2048, 8192, 1024);
+            const uint64_t bd = B_K ? ptx::smem_desc_sw128(sb + kk * 32, 16, 1024)
+                                    : ptx::smem_desc_sw128(sb + kk * 2048, 8192, 1024);
+            ptx::mma_bf16(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(empty(stage));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(tfull(buf));
+      }
+      // Drain: all MMAs issued by this thread are complete before TMEM is freed.
+      ptx::mma_commit(drain);
+      if (!ptx::mbar_wait(drain, 0)) ok = false;
+      if (!ok) atomicExch(&g_gemm_error, 2);
+    }
+  } else {
+    const int q = warp & 3;
+    int t = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
+      const int buf = t & 1;
+      if (!ptx::mbar_wait(tfull(buf), ((uint32_t)t >> 1) & 1u)) {
+        if (lane == 0) atomicExch(&g_gemm_error, 3);
+        break;
+      }
+      ptx::tc_fence_after();
+      const int m = (tile % num_m) * BM + q * 32 + lane;
+      const int nb0 = (tile / num_m) * BN;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(trow + c0, v);
+        if (m < g.M && nb0 + c0 < g.N) epi_chunk(g, m, nb0 + c0, v);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty(buf));
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---- host side -------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  uintptr_t ptr;
+  uint64_t inner, outer, ld;
+  uint32_t box_inner, box_outer;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && inner == o.inner && outer == o.outer && ld == o.ld &&
+           box_inner == o.box_inner && box_outer == o.box_outer;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+    h ^= k.inner + 0x9E37 + (h << 6) + (h >> 2);
+    h ^= k.outer + 0x79B9 + (h << 6) + (h >> 2);
+    h ^= k.ld + (h << 6) + (h >> 2);
+    h ^= ((uint64_t)k.box_inner << 32 | k.box_outer) + (h << 6) + (h >> 2);
+    return h;
+  }
+};
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with leading
+// dimension ld (elements), box [box_outer, box_inner], 128-byte swizzle,
+// out-of-bounds elements read as zero.  Cached by its arguments.
+bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+              uint32_t box_inner, uint32_t box_outer) {
+  static std::mutex mu;
+  static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+  const MapKey key{(uintptr_t)ptr, inner, outer, ld, box_inner, box_outer};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return true;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  if (cache.size() > 4096) cache.clear();
+  cache.emplace(key, m);
+  *out = m;
+  return true;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int BN, bool A_K, bool B_K>
+cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
+  using C = TcCfg<BN>;
+  CUtensorMap ma, mb;
+  bool ok = A_K ? make_map(&ma, g.A, g.K, g.M, g.lda, BKE, BM)
+                : make_map(&ma, g.A, g.M, g.K, g.lda, 64, BKE);
+  ok = ok && (B_K ? make_map(&mb, g.B, g.K, g.N, g.ldb, BKE, BN)
+                  : make_map(&mb, g.B, g.N, g.K, g.ldb, 64, BKE));
+  if (!ok) return cudaErrorInvalidValue;
+  auto kern = gemm_tc_kernel<BN, A_K, B_K>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, NTHREADS, C::SMEM, st>>>(ma, mb, g);
+  OASES_COUNT_LAUNCH();
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t dispatch_major(const GemmArgs& g, cudaStream_t st) {
+  if (g.a_kmajor)
+    return g.b_kmajor ? launch_tc<BN, true, true>(g, st) : launch_tc<BN, true, false>(g, st);
+  return g.b_kmajor ? launch_tc<BN, false, true>(g, st) : launch_tc<BN, false, false>(g, st);
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const GemmArgs& g) {
+  if (g.in_t != DType::BF16) return false;
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
+  if (g.lda % 8 != 0 || g.ldb % 8 != 0) return false;
+  if ((((uintptr_t)g.A) | ((uintptr_t)g.B)) & 15) return false;
+  if (g.epi == Epi::Accum && g.c_t != DType::F32) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st) {
+  if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
+  const int tiles256 = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
+  if (g.N <= 128 || tiles256 < num_sms()) return dispatch_major<128>(g, st);
+  return dispatch_major<256>(g, st);
+}
+
+cudaError_t gemm(const GemmArgs& g, cudaStream_t st) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (gemm_tc_supported(g)) return gemm_tc(g, st);
+  return gemm_simt(g, st);
+}
+
+int gemm_read_and_clear_error() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(int)) != cudaSuccess) return -1;
+  if (v) cudaMemcpyToSymbol(g_gemm_error, &z, sizeof(int));
+  return v;
+}
+
+}  // namespace oases

@@ -1,0 +1,193 @@
+"""CUDA path against the CPU oracle, through the C ABI (oases_stack_step,
+oases_block_fwd / oases_block_recompute_bwd), on the same seeded inputs.
+
+Tolerance: per output tensor (y, dx and every weight gradient) the relative L2
+error ||gpu - oracle|| / ||oracle|| is at most 1e-5 for fp32 workloads and
+2e-2 for bf16 workloads (activations stored in bf16, fp32 accumulation).
+The causal mask is structural in both implementations.  Properties that must
+hold bit for bit on the GPU (recompute modes, sub-batch split, determinism) are
+checked with exact equality.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import SHAPES, BlockShape, block_inputs
+from tensor_model_transformer_tp_gb300 import OasesError, oases_check_device, oases_last_launch_count
+from tensor_model_transformer_tp_gb300.device import DeviceBlock, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tensor_model_transformer_tp_gb300 import build_library
+    build_library()
+
+
+def rel(a, b):
+    n = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (n if n > 0 else 1.0))
+
+
+def run_gpu(shape, inp, mode="fine", sub_batches=None, api="stack"):
+    blk = DeviceBlock(shape, inp["layers"], recompute=mode, sub_batches=sub_batches)
+    x, g = blk.tensor(inp["x"]), blk.tensor(inp["g"])
+    if api == "stack":
+        y, dx = blk.step(x, g)
+    else:
+        y = blk.fwd(x)
+        dx = blk.recompute_bwd(x, g)
+    torch.cuda.synchronize()
+    oases_check_device(None)
+    return {"y": to_numpy(y), "dx": to_numpy(dx), "grads": blk.grads_numpy(),
+            "launches": oases_last_launch_count()}
+
+
+def compare(shape, got, ref, tol=None):
+    tol = TOL[shape.dtype] if tol is None else tol
+    errs = {"y": rel(got["y"], ref["y"]), "dx": rel(got["dx"], ref["dx"])}
+    for li, (gl, rl) in enumerate(zip(got["grads"], ref["grads"])):
+        for k in rl:
+            errs["L%d.%s" % (li, k)] = rel(gl[k], rl[k])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, bad
+    return errs
+
+
+def assert_identical(a, b):
+    np.testing.assert_array_equal(a["y"], b["y"])
+    np.testing.assert_array_equal(a["dx"], b["dx"])
+    for ga, gb in zip(a["grads"], b["grads"]):
+        for k in ga:
+            np.testing.assert_array_equal(ga[k], gb[k])
+
+
+# ------------------------------------------------------------------ fp32 workload
+@pytest.mark.parametrize("mode", ["fine", "full", "none"])
+def test_ffn_f32_h256_full_size(mode):
+    """FFN block fp32, hidden 256, ffn 1024, seq 128, batch 2, w=2, 2 sub-batches."""
+    shape = SHAPES["ffn_f32_h256"]
+    inp = block_inputs(shape, seed=0)
+    compare(shape, run_gpu(shape, inp, mode), oracle.run_step(shape, inp, mode=mode))
+
+
+def test_f32_layer_with_ragged_rows_and_affine():
+    shape = BlockShape("layer", "f32", batch=2, seq=37, hidden=128, ffn=192, heads=4, w=2)
+    inp = block_inputs(shape, seed=1, affine=True)
+    compare(shape, run_gpu(shape, inp), oracle.run_step(shape, inp, mode="fine"))
+
+
+# ------------------------------------------------------------------ bf16 FFN
+def test_ffn_bf16_reduced_ragged():
+    shape = BlockShape("ffn", "bf16", batch=4, seq=100, hidden=256, ffn=1024, w=4)
+    inp = block_inputs(shape, seed=2, affine=True)
+    compare(shape, run_gpu(shape, inp), oracle.run_step(shape, inp, mode="fine"))
+
+
+def test_ffn_bf16_h1024_full_size():
+    """FFN bf16 hidden 1024, ffn 4096, seq 512, batch 8, w=4, 2 sub-batches, pre-LN."""
+    shape = SHAPES["ffn_bf16_h1024"]
+    inp = block_inputs(shape, seed=0)
+    got = run_gpu(shape, inp, "fine")
+    compare(shape, got, oracle.run_step(shape, inp, mode="fine"))
+    assert got["launches"] > 0
+
+
+def test_ffn_bf16_modes_bit_identical():
+    shape = BlockShape("ffn", "bf16", batch=4, seq=96, hidden=256, ffn=512, w=2)
+    inp = block_inputs(shape, seed=3, affine=True)
+    r = {m: run_gpu(shape, inp, m) for m in ("none", "full", "fine")}
+    assert_identical(r["fine"], r["none"])
+    assert_identical(r["full"], r["none"])
+
+
+def test_ffn_bf16_sub_batch_split():
+    """The split changes the schedule, not the math: y and dx bit-identical,
+    weight gradients equal up to fp32 summation order."""
+    shape = BlockShape("ffn", "bf16", batch=4, seq=64, hidden=256, ffn=512, w=4)
+    inp = block_inputs(shape, seed=4, affine=True)
+    r1 = run_gpu(shape, inp, sub_batches=1)
+    r2 = run_gpu(shape, inp, sub_batches=2)
+    r4 = run_gpu(shape, inp, sub_batches=4)
+    for r in (r2, r4):
+        np.testing.assert_array_equal(r["y"], r1["y"])
+        np.testing.assert_array_equal(r["dx"], r1["dx"])
+        for k in r1["grads"][0]:
+            assert rel(r["grads"][0][k], r1["grads"][0][k]) <= 1e-5, k
+
+
+def test_deterministic():
+    shape = BlockShape("layer", "bf16", batch=2, seq=64, hidden=256, ffn=512, heads=2, w=2)
+    inp = block_inputs(shape, seed=5, affine=True)
+    assert_identical(run_gpu(shape, inp), run_gpu(shape, inp))
+
+
+def test_block_api_equals_stack_step():
+    shape = BlockShape("layer", "bf16", batch=2, seq=64, hidden=256, ffn=512, heads=2, w=2)
+    inp = block_inputs(shape, seed=6, affine=True)
+    assert_identical(run_gpu(shape, inp, api="block"), run_gpu(shape, inp, api="stack"))
+
+
+# ------------------------------------------------------------------ attention / layer
+def test_attn_bf16_reduced_ragged():
+    shape = BlockShape("attn", "bf16", batch=2, seq=160, hidden=256, heads=2, w=2)
+    inp = block_inputs(shape, seed=7, affine=True)
+    compare(shape, run_gpu(shape, inp), oracle.run_step(shape, inp, mode="fine"))
+
+
+def test_attn_bf16_noncausal_no_ln():
+    shape = BlockShape("attn", "bf16", batch=2, seq=72, hidden=256, heads=4, w=4, causal=False,
+                       pre_ln=False, residual=False)
+    inp = block_inputs(shape, seed=8, affine=True)
+    compare(shape, run_gpu(shape, inp), oracle.run_step(shape, inp, mode="fine"))
+
+
+def test_layer_stack_bf16_reduced():
+    shape = BlockShape("layer", "bf16", batch=2, seq=96, hidden=256, ffn=768, heads=2, w=2,
+                       n_layers=2)
+    inp = block_inputs(shape, seed=9, affine=True)
+    compare(shape, run_gpu(shape, inp), oracle.run_step(shape, inp, mode="fine"))
+
+
+# ------------------------------------------------------------------ edge cases
+def test_empty_batch():
+    shape = BlockShape("layer", "bf16", batch=0, seq=16, hidden=256, ffn=512, heads=2, w=2)
+    inp = block_inputs(shape, seed=10)
+    got = run_gpu(shape, inp)
+    assert got["y"].shape == (0, 256)
+    for g in got["grads"][0].values():
+        assert np.all(g == 0)
+
+
+def test_single_token_sequences():
+    shape = BlockShape("layer", "bf16", batch=4, seq=1, hidden=128, ffn=256, heads=1, w=1)
+    inp = block_inputs(shape, seed=11, affine=True)
+    compare(shape, run_gpu(shape, inp), oracle.run_step(shape, inp, mode="fine"))
+
+
+def test_invalid_shape_raises_before_launch():
+    shape = BlockShape("attn", "bf16", batch=2, seq=8, hidden=272, heads=2, w=1)  # head dim 136
+    with pytest.raises((OasesError, ValueError)):
+        DeviceBlock(shape, block_inputs(shape, seed=0)["layers"])
+
+
+def test_host_buffers_through_stack_step():
+    """x, g, y, dx in pinned host memory: staged through the workspace."""
+    shape = BlockShape("ffn", "bf16", batch=2, seq=64, hidden=256, ffn=512, w=2)
+    inp = block_inputs(shape, seed=12, affine=True)
+    dev = run_gpu(shape, inp)
+    blk = DeviceBlock(shape, inp["layers"])
+    xh = blk.tensor(inp["x"]).cpu().pin_memory()
+    gh = blk.tensor(inp["g"]).cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(xh).pin_memory()
+    blk.step(xh, gh, yh, dxh)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(yh.double().numpy(), dev["y"])
+    np.testing.assert_array_equal(dxh.double().numpy(), dev["dx"])
