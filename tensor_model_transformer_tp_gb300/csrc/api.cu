@@ -120,7 +120,7 @@ inline size_t up(size_t v) { return (v + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct ActSet {  // offsets relative to the workspace base
   size_t u = 0, mu = 0, rstd = 0, a = 0, h = 0, qkv = 0, o = 0, lse = 0, delta = 0, d_o = 0,
-         dqkv = 0, du = 0, cpart = 0, lpart_g = 0, lpart_b = 0;
+         dqkv = 0, du = 0, cpart = 0, lpart_g = 0, lpart_b = 0, lstat = 0;
 };
 
 struct Layout {
@@ -173,6 +173,7 @@ Layout make_layout(const Shape& s) {
     a.cpart = take(s.nsb * L.cpart_n * 4);
     a.lpart_g = take(s.nsb * L.lpart_n * 4);
     a.lpart_b = take(s.nsb * L.lpart_n * 4);
+    a.lstat = take(M * 8);
     return a;
   };
   L.act.resize(s.nseg);
@@ -550,7 +551,8 @@ struct Exec {
       ok(layer_norm_bwd(du, rowp(seg_in(seg), b, s.H, s.esz), rowp(at<float>(a.mu), b, 1, 4),
                         rowp(at<float>(a.rstd), b, 1, 4), sp[seg].g, dres, dxo,
                         at<float>(a.lpart_g) + (size_t)b * L.lpart_n,
-                        at<float>(a.lpart_b) + (size_t)b * L.lpart_n, sp[seg].dg, sp[seg].db,
+                        at<float>(a.lpart_b) + (size_t)b * L.lpart_n,
+                        rowp(at<float2>(a.lstat), b, 1, 8), sp[seg].dg, sp[seg].db,
                         (int)s.Ms, s.H, s.t, stream(b)));
       grad_done(seg, GRP_LN, b);
     } else {

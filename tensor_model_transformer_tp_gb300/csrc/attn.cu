@@ -45,6 +45,8 @@ attn_fwd_kernel(const T* __restrict__ qkv, T* __restrict__ o, float* __restrict_
                 int M, bool causal, float scale) {
   __shared__ float Ks[KT][DMAX + 1];
   __shared__ float Vs[KT][DMAX + 1];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.z, h = blockIdx.y;
   const int r = threadIdx.x / TPR, t = threadIdx.x % TPR;
   const int i = blockIdx.x * ROWS + r;  // query position in the sequence
@@ -103,6 +105,8 @@ attn_fwd_kernel(const T* __restrict__ qkv, T* __restrict__ o, float* __restrict_
 template <typename T>
 __global__ void attn_delta_kernel(const T* __restrict__ o, const T* __restrict__ d_o,
                                   float* __restrict__ delta, int M, int H, int d, int heads) {
+  pdl_wait();
+  pdl_trigger();
   const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x % 32;
   if (w >= M * heads) return;
   const int row = w / heads, h = w % heads;
@@ -124,6 +128,8 @@ attn_bwd_dq_kernel(const T* __restrict__ qkv, const T* __restrict__ d_o,
                    T* __restrict__ dqkv, Geo g, int M, bool causal, float scale) {
   __shared__ float Ks[KT][DMAX + 1];
   __shared__ float Vs[KT][DMAX + 1];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.z, h = blockIdx.y;
   const int r = threadIdx.x / TPR, t = threadIdx.x % TPR;
   const int i = blockIdx.x * ROWS + r;
@@ -190,6 +196,8 @@ attn_bwd_dkv_kernel(const T* __restrict__ qkv, const T* __restrict__ d_o,
   __shared__ float Qs[KT][DMAX + 1];
   __shared__ float dOs[KT][DMAX + 1];
   __shared__ float Ls[KT], Ds[KT];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.z, h = blockIdx.y;
   const int r = threadIdx.x / TPR, t = threadIdx.x % TPR;
   const int j = blockIdx.x * ROWS + r;  // key position
@@ -270,13 +278,11 @@ cudaError_t attention_fwd_simt(const AttnArgs& a, cudaStream_t st) {
   dim3 grid((a.seq + ROWS - 1) / ROWS, a.heads, a.batch);
   const float scale = 1.f / sqrtf((float)a.head_dim);
   if (a.t == DType::F32)
-    attn_fwd_kernel<float><<<grid, NT, 0, st>>>((const float*)a.qkv, (float*)a.o, a.lse, g, M,
-                                                a.causal, scale);
-  else
-    attn_fwd_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(
-        (const __nv_bfloat16*)a.qkv, (__nv_bfloat16*)a.o, a.lse, g, M, a.causal, scale);
-  OASES_COUNT_LAUNCH();
-  return cudaGetLastError();
+    return launch_pdl(attn_fwd_kernel<float>, grid, dim3(NT), 0, st, (const float*)a.qkv,
+                      (float*)a.o, a.lse, g, M, a.causal, scale);
+  return launch_pdl(attn_fwd_kernel<__nv_bfloat16>, grid, dim3(NT), 0, st,
+                    (const __nv_bfloat16*)a.qkv, (__nv_bfloat16*)a.o, a.lse, g, M, a.causal,
+                    scale);
 }
 
 cudaError_t attention_delta(const AttnArgs& a, cudaStream_t st) {
@@ -285,14 +291,11 @@ cudaError_t attention_delta(const AttnArgs& a, cudaStream_t st) {
   const int warps = M * a.heads;
   const int grid = (warps + 7) / 8;
   if (a.t == DType::F32)
-    attn_delta_kernel<float><<<grid, 256, 0, st>>>((const float*)a.o, (const float*)a.d_o,
-                                                   a.delta, M, a.hidden, a.head_dim, a.heads);
-  else
-    attn_delta_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.d_o, a.delta, M, a.hidden,
-        a.head_dim, a.heads);
-  OASES_COUNT_LAUNCH();
-  return cudaGetLastError();
+    return launch_pdl(attn_delta_kernel<float>, dim3(grid), dim3(256), 0, st, (const float*)a.o,
+                      (const float*)a.d_o, a.delta, M, a.hidden, a.head_dim, a.heads);
+  return launch_pdl(attn_delta_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
+                    (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.d_o, a.delta, M, a.hidden,
+                    a.head_dim, a.heads);
 }
 
 cudaError_t attention_bwd_simt(const AttnArgs& a, cudaStream_t st) {
@@ -305,22 +308,22 @@ cudaError_t attention_bwd_simt(const AttnArgs& a, cudaStream_t st) {
   dim3 grid((a.seq + ROWS - 1) / ROWS, a.heads, a.batch);
   const float scale = 1.f / sqrtf((float)a.head_dim);
   if (a.t == DType::F32) {
-    attn_bwd_dq_kernel<float><<<grid, NT, 0, st>>>((const float*)a.qkv, (const float*)a.d_o,
-                                                   a.lse, a.delta, (float*)a.dqkv, g, M,
-                                                   a.causal, scale);
-    attn_bwd_dkv_kernel<float><<<grid, NT, 0, st>>>((const float*)a.qkv, (const float*)a.d_o,
-                                                    a.lse, a.delta, (float*)a.dqkv, g, M,
-                                                    a.causal, scale);
-  } else {
-    attn_bwd_dq_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(
-        (const __nv_bfloat16*)a.qkv, (const __nv_bfloat16*)a.d_o, a.lse, a.delta,
-        (__nv_bfloat16*)a.dqkv, g, M, a.causal, scale);
-    attn_bwd_dkv_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(
-        (const __nv_bfloat16*)a.qkv, (const __nv_bfloat16*)a.d_o, a.lse, a.delta,
-        (__nv_bfloat16*)a.dqkv, g, M, a.causal, scale);
+    e = launch_pdl(attn_bwd_dq_kernel<float>, grid, dim3(NT), 0, st, (const float*)a.qkv,
+                   (const float*)a.d_o, (const float*)a.lse, (const float*)a.delta,
+                   (float*)a.dqkv, g, M, a.causal, scale);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_bwd_dkv_kernel<float>, grid, dim3(NT), 0, st, (const float*)a.qkv,
+                      (const float*)a.d_o, (const float*)a.lse, (const float*)a.delta,
+                      (float*)a.dqkv, g, M, a.causal, scale);
   }
-  g_launch_count += 2;
-  return cudaGetLastError();
+  e = launch_pdl(attn_bwd_dq_kernel<__nv_bfloat16>, grid, dim3(NT), 0, st,
+                 (const __nv_bfloat16*)a.qkv, (const __nv_bfloat16*)a.d_o, (const float*)a.lse,
+                 (const float*)a.delta, (__nv_bfloat16*)a.dqkv, g, M, a.causal, scale);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_bwd_dkv_kernel<__nv_bfloat16>, grid, dim3(NT), 0, st,
+                    (const __nv_bfloat16*)a.qkv, (const __nv_bfloat16*)a.d_o,
+                    (const float*)a.lse, (const float*)a.delta, (__nv_bfloat16*)a.dqkv, g, M,
+                    a.causal, scale);
 }
 
 }  // namespace oases

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace oases {
 
 enum class DType : int { F32 = 0, BF16 = 1 };
@@ -15,6 +17,34 @@ extern thread_local int g_launch_count;
 #define OASES_COUNT_LAUNCH() (++::oases::g_launch_count)
 
 inline size_t dtype_size(DType t) { return t == DType::F32 ? 4 : 2; }
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization, so it may start while its predecessor on
+// the stream is finishing; it must call pdl_wait() before its first global
+// memory access (read or write), which returns once the predecessor grid has
+// completed and its writes are visible.  pdl_trigger() lets the next kernel on
+// the stream be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ++g_launch_count;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Element load / store in fp32 registers.
 __device__ __forceinline__ float ld_elem(const float* p, int64_t i) { return p[i]; }
@@ -102,13 +132,14 @@ cudaError_t layer_norm_fwd(const void* x, const void* gamma, const void* beta, v
                            cudaStream_t st);
 // dx = rstd * (g - mean(g) - xhat * mean(g * xhat)) (+ dres), g = du * gamma;
 // du fp32 [M, H]; x, dres, dx in t.  Per-row-block partial sums of du * xhat
-// and du go to part_g / part_b ([n_blocks, H] fp32, n_blocks from
-// ln_bwd_blocks(M)); a second pass adds their column sums to dgamma / dbeta.
+// and du go to part_g / part_b ([ln_bwd_blocks(M), H] fp32) and the two row
+// means to stat ([M] float2); a last pass adds the partials' column sums to
+// dgamma / dbeta in a fixed order.
 int ln_bwd_blocks(int M);
 cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, const float* rstd,
                            const void* gamma, const void* dres, void* dx, float* part_g,
-                           float* part_b, float* dgamma, float* dbeta, int M, int H, DType t,
-                           cudaStream_t st);
+                           float* part_b, float2* stat, float* dgamma, float* dbeta, int M, int H,
+                           DType t, cudaStream_t st);
 // out[n] += sum_m in[m, n] for in [M, N] (type t, leading dim ld); partials in
 // part ([colsum_blocks(M), N] fp32).  Deterministic: fixed summation order.
 int colsum_blocks(int M);

@@ -17,6 +17,8 @@ template <typename T>
 __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
+  pdl_wait();
+  pdl_trigger();
   const T* A = static_cast<const T*>(g.A);
   const T* B = static_cast<const T*>(g.B);
   const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
@@ -78,12 +80,8 @@ cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-  if (g.in_t == DType::F32)
-    gemm_simt_kernel<float><<<grid, NT, 0, st>>>(g);
-  else
-    gemm_simt_kernel<__nv_bfloat16><<<grid, NT, 0, st>>>(g);
-  OASES_COUNT_LAUNCH();
-  return cudaGetLastError();
+  if (g.in_t == DType::F32) return launch_pdl(gemm_simt_kernel<float>, grid, dim3(NT), 0, st, g);
+  return launch_pdl(gemm_simt_kernel<__nv_bfloat16>, grid, dim3(NT), 0, st, g);
 }
 
 }  // namespace oases

@@ -5,15 +5,16 @@
 //   fp32 accumulate).
 //
 // One CTA per SM, persistent over 128 x BN output tiles (BN = 128 or 256).
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      one thread issues TMA loads of A and B K-slices (64 bf16 =
 //               128 bytes deep, 128-byte swizzle) into a STAGES-deep ring;
 //   warp 1      allocates 2*BN TMEM columns (two accumulators) and one thread
 //               issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction);
 //               tcgen05.commit frees a ring slot once its MMAs are done and
 //               hands a finished accumulator to the epilogue;
-//   warps 2..5  read the accumulator (TMEM lane = output row; a warp may only
-//               touch lanes 32*(warp % 4) .. +31), apply the epilogue and store.
+//   warps 2..9  read the accumulator (TMEM lane = output row; a warp may only
+//               touch lanes 32*(warp % 4) .. +31; two warps share a lane
+//               quarter and split its columns), apply the epilogue and store.
 // The accumulator is double-buffered so the epilogue of tile t overlaps the
 // main loop of tile t+1.  Operands may be K-major or MN-major; MN-major tiles
 // are loaded as 64-element-wide chunks and described with LBO = chunk stride.
@@ -41,7 +42,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BKE = 64;  // K elements per stage (128 bytes of bf16)
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;  // 2 control warps + 8 epilogue warps
+constexpr int EPI_THREADS = 256;
 
 template <int BN>
 struct TcCfg {
@@ -87,6 +89,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int n, float
                    (g.aux == nullptr || (g.ld_aux % 8 == 0 && g.aux_t == DType::BF16)) &&
                    (((uintptr_t)g.C | (uintptr_t)g.C2 | (uintptr_t)g.aux | (uintptr_t)g.bias) & 15) == 0;
   if (!vec) {
+#pragma unroll
     for (int i = 0; i < 32; ++i)
       if (n + i < g.N) epi_apply(g, m, n + i, v[i]);
     return;
@@ -171,7 +174,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull(b), 1);
-      ptx::mbar_init(tempty(b), 128);
+      ptx::mbar_init(tempty(b), EPI_THREADS);
     }
     ptx::mbar_init(drain, 1);
     ptx::fence_mbar_init();
@@ -188,6 +191,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
+  // Everything above touched only shared memory, TMEM and kernel parameters, so
+  // it overlapped the previous kernel on the stream; global memory from here on.
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -263,6 +270,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;  // which half of the BN columns
     int t = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
       const int buf = t & 1;
@@ -275,7 +283,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int nb0 = (tile / num_m) * BN;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
         float v[32];
         ptx::tmem_ld32(trow + c0, v);
         if (m < g.M && nb0 + c0 < g.N) epi_chunk(g, m, nb0 + c0, v);
@@ -392,9 +400,7 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
   }
   const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, NTHREADS, C::SMEM, st>>>(ma, mb, g);
-  OASES_COUNT_LAUNCH();
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(NTHREADS), C::SMEM, st, ma, mb, g);
 }
 
 template <int BN>

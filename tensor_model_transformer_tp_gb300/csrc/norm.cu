@@ -1,10 +1,12 @@
 // LayerNorm forward / backward and deterministic column reductions.
 //
-// These kernels are HBM-bound: one warp owns one row for the row-wise passes
-// (mean, variance, normalise; or the two row means of the backward), and the
-// column sums (dgamma, dbeta, bias gradients) are taken in two fixed-order
-// stages — per block of ROWS_PER_PART rows into a partial buffer, then over the
-// partials — so the result does not depend on scheduling.
+// All of these are HBM-bound.  Row statistics are taken by one warp per row
+// with 16-byte loads (bf16 rows whose width is a multiple of 256 are held in
+// registers, so the row is read once).  Column sums (dgamma, dbeta, bias
+// gradients) are taken in two fixed-order stages: a CTA owns a block of
+// ROWS_PER_PART rows and a strip of columns, reads them coalesced (adjacent
+// threads, adjacent columns) and writes one partial row; a second kernel adds
+// the partial rows in order.  No atomics, so results are bit-reproducible.
 #include <algorithm>
 
 #include "common.cuh"
@@ -12,8 +14,11 @@
 namespace oases {
 namespace {
 
-constexpr int ROWS_PER_PART = 64;
+constexpr int ROWS_PER_PART = 32;
 constexpr int WARPS = 8;
+constexpr int COLS_PER_THREAD = 2;
+constexpr int COL_THREADS = 256;
+constexpr int COLS_PER_CTA = COL_THREADS * COLS_PER_THREAD;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -21,11 +26,83 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+// ---- LayerNorm forward -------------------------------------------------------
+// bf16, H = 256 * NV: lane j holds 16-byte vectors j, j+32, ... of its row.
+template <int NV>
+__global__ void __launch_bounds__(WARPS * 32)
+ln_fwd_bf16_reg(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+                const __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ u,
+                float* __restrict__ mean, float* __restrict__ rstd, int M, int H, float eps) {
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x * WARPS + threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (row >= M) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)row * H);
+  uint4 v[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) v[j] = __ldg(xr + lane + 32 * j);
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    float f[8];
+    bf16x8_to_f32(v[j], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += f[i];
+  }
+  const float mu = warp_sum(s) / H;
+  float q = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    float f[8];
+    bf16x8_to_f32(v[j], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q = fmaf(f[i] - mu, f[i] - mu, q);
+  }
+  const float rs = rsqrtf(warp_sum(q) / H + eps);
+  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+  const uint4* br = reinterpret_cast<const uint4*>(beta);
+  uint4* ur = reinterpret_cast<uint4*>(u + (int64_t)row * H);
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    float f[8], g[8], b[8];
+    bf16x8_to_f32(v[j], f);
+    bf16x8_to_f32(__ldg(gr + lane + 32 * j), g);
+    bf16x8_to_f32(__ldg(br + lane + 32 * j), b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = (f[i] - mu) * rs * g[i] + b[i];
+    ur[lane + 32 * j] = f32_to_bf16x8(f);
+  }
+  if (lane == 0) {
+    mean[row] = mu;
+    rstd[row] = rs;
+  }
+}
+
+// Any type, any width: three passes over the row (the later two hit L1).
 template <typename T>
 __global__ void __launch_bounds__(WARPS * 32)
 ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
               T* __restrict__ u, float* __restrict__ mean, float* __restrict__ rstd, int M, int H,
               float eps) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x * WARPS + threadIdx.x / 32, lane = threadIdx.x % 32;
   if (row >= M) return;
   const T* xr = x + (int64_t)row * H;
@@ -47,93 +124,184 @@ ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma, const T* __r
   }
 }
 
-// dx = rstd * (g - mean(g) - xhat * mean(g * xhat)) (+ dres), g = du * gamma.
+// ---- LayerNorm backward --------------------------------------------------------
+// Row pass: m1 = mean(du * gamma), m2 = mean(du * gamma * xhat), one warp per row.
 template <typename T>
 __global__ void __launch_bounds__(WARPS * 32)
-ln_bwd_dx_kernel(const float* __restrict__ du, const T* __restrict__ x,
-                 const float* __restrict__ mean, const float* __restrict__ rstd,
-                 const T* __restrict__ gamma, const T* __restrict__ dres, T* __restrict__ dx,
-                 int M, int H) {
+ln_bwd_rowstat(const float* __restrict__ du, const T* __restrict__ x,
+               const float* __restrict__ mean, const float* __restrict__ rstd,
+               const T* __restrict__ gamma, float2* __restrict__ stat, int M, int H) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x * WARPS + threadIdx.x / 32, lane = threadIdx.x % 32;
   if (row >= M) return;
   const float* dur = du + (int64_t)row * H;
   const T* xr = x + (int64_t)row * H;
   const float mu = mean[row], rs = rstd[row];
   float s1 = 0.f, s2 = 0.f;
-  for (int c = lane; c < H; c += 32) {
-    const float gg = dur[c] * ld_elem(gamma, c);
-    const float xh = (ld_elem(xr, c) - mu) * rs;
-    s1 += gg;
-    s2 = fmaf(gg, xh, s2);
+  if (sizeof(T) == 2 && H % 8 == 0) {
+    const float4* d4 = reinterpret_cast<const float4*>(dur);
+    const uint4* x8 = reinterpret_cast<const uint4*>(xr);
+    const uint4* g8 = reinterpret_cast<const uint4*>(gamma);
+    for (int j = lane; j < H / 8; j += 32) {
+      float xf[8], gf[8];
+      bf16x8_to_f32(__ldg(x8 + j), xf);
+      bf16x8_to_f32(__ldg(g8 + j), gf);
+      const float4 a = __ldg(d4 + 2 * j), b = __ldg(d4 + 2 * j + 1);
+      const float df[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float gg = df[i] * gf[i];
+        s1 += gg;
+        s2 = fmaf(gg, (xf[i] - mu) * rs, s2);
+      }
+    }
+  } else {
+    for (int c = lane; c < H; c += 32) {
+      const float gg = dur[c] * ld_elem(gamma, c);
+      s1 += gg;
+      s2 = fmaf(gg, (ld_elem(xr, c) - mu) * rs, s2);
+    }
   }
-  const float m1 = warp_sum(s1) / H, m2 = warp_sum(s2) / H;
-  T* dxr = dx + (int64_t)row * H;
-  const T* dr = dres ? dres + (int64_t)row * H : nullptr;
-  for (int c = lane; c < H; c += 32) {
-    const float gg = dur[c] * ld_elem(gamma, c);
-    const float xh = (ld_elem(xr, c) - mu) * rs;
-    float v = rs * (gg - m1 - xh * m2);
-    if (dr) v += ld_elem(dr, c);
-    st_elem(dxr, c, v);
-  }
+  s1 = warp_sum(s1);
+  s2 = warp_sum(s2);
+  if (lane == 0) stat[row] = make_float2(s1 / H, s2 / H);
 }
 
-// part_g[blk, n] = sum_{m in blk} du[m, n] * xhat[m, n]; part_b[blk, n] = sum du.
+// Column pass over ROWS_PER_PART rows x COLS_PER_CTA columns:
+//   dx = rstd * (du * gamma - m1 - xhat * m2) (+ dres), and the partial sums
+//   pg = sum du * xhat, pb = sum du of this row block.
 template <typename T>
-__global__ void ln_bwd_param_part_kernel(const float* __restrict__ du, const T* __restrict__ x,
-                                         const float* __restrict__ mean,
-                                         const float* __restrict__ rstd, float* __restrict__ pg,
-                                         float* __restrict__ pb, int M, int H) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= H) return;
+__global__ void __launch_bounds__(COL_THREADS)
+ln_bwd_colpass(const float* __restrict__ du, const T* __restrict__ x,
+               const float* __restrict__ mean, const float* __restrict__ rstd,
+               const float2* __restrict__ stat, const T* __restrict__ gamma,
+               const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ pg,
+               float* __restrict__ pb, int M, int H) {
+  pdl_wait();
+  pdl_trigger();
+  const int c0 = (blockIdx.x * COL_THREADS + threadIdx.x) * COLS_PER_THREAD;
   const int m0 = blockIdx.y * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
-  float sg = 0.f, sb = 0.f;
+  if (c0 >= H) return;
+  float ag[COLS_PER_THREAD] = {}, ab[COLS_PER_THREAD] = {};
+  float g[COLS_PER_THREAD];
+#pragma unroll
+  for (int i = 0; i < COLS_PER_THREAD; ++i) g[i] = c0 + i < H ? ld_elem(gamma, c0 + i) : 0.f;
+#pragma unroll 4
   for (int m = m0; m < m1; ++m) {
-    const float d = du[(int64_t)m * H + n];
-    sg = fmaf(d, (ld_elem(x, (int64_t)m * H + n) - mean[m]) * rstd[m], sg);
-    sb += d;
+    const float mu = mean[m], rs = rstd[m];
+    const float2 st = stat[m];
+    const int64_t base = (int64_t)m * H + c0;
+#pragma unroll
+    for (int i = 0; i < COLS_PER_THREAD; ++i) {
+      if (c0 + i >= H) continue;
+      const float d = du[base + i];
+      const float xh = (ld_elem(x, base + i) - mu) * rs;
+      float v = rs * (d * g[i] - st.x - xh * st.y);
+      if (dres) v += ld_elem(dres, base + i);
+      st_elem(dx, base + i, v);
+      ag[i] = fmaf(d, xh, ag[i]);
+      ab[i] += d;
+    }
   }
-  pg[(int64_t)blockIdx.y * H + n] = sg;
-  pb[(int64_t)blockIdx.y * H + n] = sb;
+#pragma unroll
+  for (int i = 0; i < COLS_PER_THREAD; ++i)
+    if (c0 + i < H) {
+      pg[(int64_t)blockIdx.y * H + c0 + i] = ag[i];
+      pb[(int64_t)blockIdx.y * H + c0 + i] = ab[i];
+    }
 }
 
 template <typename T>
-__global__ void colsum_part_kernel(const T* __restrict__ in, int64_t ld, int M, int N,
-                                   float* __restrict__ part) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= N) return;
+__global__ void __launch_bounds__(COL_THREADS)
+colsum_part_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
+  const int c0 = (blockIdx.x * COL_THREADS + threadIdx.x) * COLS_PER_THREAD;
+  if (c0 >= N) return;
   const int m0 = blockIdx.y * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
-  float s = 0.f;
-  for (int m = m0; m < m1; ++m) s += ld_elem(in, (int64_t)m * ld + n);
-  part[(int64_t)blockIdx.y * N + n] = s;
+  float s[COLS_PER_THREAD] = {};
+#pragma unroll 8
+  for (int m = m0; m < m1; ++m) {
+#pragma unroll
+    for (int i = 0; i < COLS_PER_THREAD; ++i)
+      if (c0 + i < N) s[i] += ld_elem(in, (int64_t)m * ld + c0 + i);
+  }
+#pragma unroll
+  for (int i = 0; i < COLS_PER_THREAD; ++i)
+    if (c0 + i < N) part[(int64_t)blockIdx.y * N + c0 + i] = s[i];
 }
 
-// out[n] += sum_b part[b, n] in order b = 0, 1, ...; two outputs at once when
-// part2/out2 are given.
-__global__ void part_reduce_kernel(const float* __restrict__ part, float* __restrict__ out,
-                                   const float* __restrict__ part2, float* __restrict__ out2,
-                                   int nb, int N) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= N) return;
-  float s = 0.f;
-  for (int b = 0; b < nb; ++b) s += part[(int64_t)b * N + n];
-  out[n] += s;
-  if (part2) {
-    float s2 = 0.f;
-    for (int b = 0; b < nb; ++b) s2 += part2[(int64_t)b * N + n];
-    out2[n] += s2;
+// out[n] += sum_b part[b, n] over b = 0 .. nb-1 in a fixed order: thread group g
+// (of 4) sums b = g, g+4, ... and the four group sums are added in order 0..3.
+// A second (part2, out2) pair is reduced by the same launch when given.
+constexpr int RED_COLS = 64, RED_GROUPS = 4;
+__global__ void __launch_bounds__(RED_COLS * RED_GROUPS)
+part_reduce_kernel(const float* __restrict__ part, float* __restrict__ out,
+                   const float* __restrict__ part2, float* __restrict__ out2, int nb, int N) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float sh[2][RED_GROUPS][RED_COLS];
+  const int cl = threadIdx.x % RED_COLS, g = threadIdx.x / RED_COLS;
+  const int n = blockIdx.x * RED_COLS + cl;
+  float s = 0.f, s2 = 0.f;
+  if (n < N) {
+    for (int b = g; b < nb; b += RED_GROUPS) {
+      s += part[(int64_t)b * N + n];
+      if (part2) s2 += part2[(int64_t)b * N + n];
+    }
+  }
+  sh[0][g][cl] = s;
+  sh[1][g][cl] = s2;
+  __syncthreads();
+  if (g == 0 && n < N) {
+    float t = 0.f, t2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < RED_GROUPS; ++k) {
+      t += sh[0][k][cl];
+      t2 += sh[1][k][cl];
+    }
+    out[n] += t;
+    if (part2) out2[n] += t2;
   }
 }
 
 template <typename T>
 __global__ void add_into_kernel(const T* __restrict__ a, const float* __restrict__ b,
                                 T* __restrict__ out, int64_t n) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     float v = b[i];
     if (a) v += ld_elem(a, i);
     st_elem(out, i, v);
   }
+}
+
+template <int NV>
+cudaError_t ln_fwd_reg_launch(const void* x, const void* gamma, const void* beta, void* u,
+                              float* mean, float* rstd, int M, int H, float eps, cudaStream_t st) {
+  return launch_pdl(ln_fwd_bf16_reg<NV>, dim3((M + WARPS - 1) / WARPS), dim3(WARPS * 32), 0, st,
+                    (const __nv_bfloat16*)x, (const __nv_bfloat16*)gamma,
+                    (const __nv_bfloat16*)beta, (__nv_bfloat16*)u, mean, rstd, M, H, eps);
+}
+
+template <typename T>
+cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const float* rstd,
+                     const void* gamma, const void* dres, void* dx, float* part_g, float* part_b,
+                     float2* stat, float* dgamma, float* dbeta, int M, int H, cudaStream_t st) {
+  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
+  cudaError_t e = launch_pdl(ln_bwd_rowstat<T>, dim3((M + WARPS - 1) / WARPS), dim3(WARPS * 32),
+                             0, st, du, (const T*)x, mean, rstd, (const T*)gamma, stat, M, H);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(ln_bwd_colpass<T>, dim3((H + COLS_PER_CTA - 1) / COLS_PER_CTA, nb),
+                 dim3(COL_THREADS), 0, st, du, (const T*)x, mean, rstd, (const float2*)stat,
+                 (const T*)gamma, (const T*)dres, (T*)dx, part_g, part_b, M, H);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(part_reduce_kernel, dim3((H + RED_COLS - 1) / RED_COLS),
+                    dim3(RED_COLS * RED_GROUPS), 0, st, (const float*)part_g, dgamma,
+                    (const float*)part_b, dbeta, nb, H);
 }
 
 }  // namespace
@@ -145,57 +313,54 @@ cudaError_t layer_norm_fwd(const void* x, const void* gamma, const void* beta, v
                            float* mean, float* rstd, int M, int H, float eps, DType t,
                            cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  const int grid = (M + WARPS - 1) / WARPS;
+  const dim3 grid((M + WARPS - 1) / WARPS), block(WARPS * 32);
+  if (t == DType::BF16 && H % 256 == 0 && H / 256 <= 16) {
+    switch (H / 256) {
+#define OASES_LN_CASE(n) \
+  case n: return ln_fwd_reg_launch<n>(x, gamma, beta, u, mean, rstd, M, H, eps, st);
+      OASES_LN_CASE(1) OASES_LN_CASE(2) OASES_LN_CASE(3) OASES_LN_CASE(4) OASES_LN_CASE(5)
+      OASES_LN_CASE(6) OASES_LN_CASE(7) OASES_LN_CASE(8) OASES_LN_CASE(9) OASES_LN_CASE(10)
+      OASES_LN_CASE(11) OASES_LN_CASE(12) OASES_LN_CASE(13) OASES_LN_CASE(14) OASES_LN_CASE(15)
+      OASES_LN_CASE(16)
+#undef OASES_LN_CASE
+    }
+  }
   if (t == DType::F32)
-    ln_fwd_kernel<float><<<grid, WARPS * 32, 0, st>>>(
-        (const float*)x, (const float*)gamma, (const float*)beta, (float*)u, mean, rstd, M, H, eps);
-  else
-    ln_fwd_kernel<__nv_bfloat16><<<grid, WARPS * 32, 0, st>>>(
-        (const __nv_bfloat16*)x, (const __nv_bfloat16*)gamma, (const __nv_bfloat16*)beta,
-        (__nv_bfloat16*)u, mean, rstd, M, H, eps);
-  OASES_COUNT_LAUNCH();
-  return cudaGetLastError();
+    return launch_pdl(ln_fwd_kernel<float>, grid, block, 0, st, (const float*)x,
+                      (const float*)gamma, (const float*)beta, (float*)u, mean, rstd, M, H, eps);
+  return launch_pdl(ln_fwd_kernel<__nv_bfloat16>, grid, block, 0, st, (const __nv_bfloat16*)x,
+                    (const __nv_bfloat16*)gamma, (const __nv_bfloat16*)beta, (__nv_bfloat16*)u,
+                    mean, rstd, M, H, eps);
 }
 
 cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, const float* rstd,
                            const void* gamma, const void* dres, void* dx, float* part_g,
-                           float* part_b, float* dgamma, float* dbeta, int M, int H, DType t,
-                           cudaStream_t st) {
+                           float* part_b, float2* stat, float* dgamma, float* dbeta, int M, int H,
+                           DType t, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  const int grid = (M + WARPS - 1) / WARPS;
-  const int nb = ln_bwd_blocks(M);
-  dim3 pgrid((H + 255) / 256, nb);
-  if (t == DType::F32) {
-    ln_bwd_dx_kernel<float><<<grid, WARPS * 32, 0, st>>>(du, (const float*)x, mean, rstd,
-                                                         (const float*)gamma, (const float*)dres,
-                                                         (float*)dx, M, H);
-    ln_bwd_param_part_kernel<float><<<pgrid, 256, 0, st>>>(du, (const float*)x, mean, rstd,
-                                                           part_g, part_b, M, H);
-  } else {
-    ln_bwd_dx_kernel<__nv_bfloat16><<<grid, WARPS * 32, 0, st>>>(
-        du, (const __nv_bfloat16*)x, mean, rstd, (const __nv_bfloat16*)gamma,
-        (const __nv_bfloat16*)dres, (__nv_bfloat16*)dx, M, H);
-    ln_bwd_param_part_kernel<__nv_bfloat16><<<pgrid, 256, 0, st>>>(
-        du, (const __nv_bfloat16*)x, mean, rstd, part_g, part_b, M, H);
-  }
-  part_reduce_kernel<<<(H + 255) / 256, 256, 0, st>>>(part_g, dgamma, part_b, dbeta, nb, H);
-  g_launch_count += 3;
-  return cudaGetLastError();
+  if (t == DType::F32)
+    return ln_bwd_t<float>(du, x, mean, rstd, gamma, dres, dx, part_g, part_b, stat, dgamma,
+                           dbeta, M, H, st);
+  return ln_bwd_t<__nv_bfloat16>(du, x, mean, rstd, gamma, dres, dx, part_g, part_b, stat,
+                                 dgamma, dbeta, M, H, st);
 }
 
 cudaError_t colsum_accum(const void* in, int64_t ld, int M, int N, DType t, float* part,
                          float* out, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   const int nb = colsum_blocks(M);
-  dim3 pgrid((N + 255) / 256, nb);
+  const dim3 pgrid((N + COLS_PER_CTA - 1) / COLS_PER_CTA, nb);
+  cudaError_t e;
   if (t == DType::F32)
-    colsum_part_kernel<float><<<pgrid, 256, 0, st>>>((const float*)in, ld, M, N, part);
+    e = launch_pdl(colsum_part_kernel<float>, pgrid, dim3(COL_THREADS), 0, st, (const float*)in,
+                   ld, M, N, part);
   else
-    colsum_part_kernel<__nv_bfloat16><<<pgrid, 256, 0, st>>>((const __nv_bfloat16*)in, ld, M,
-                                                             N, part);
-  part_reduce_kernel<<<(N + 255) / 256, 256, 0, st>>>(part, out, nullptr, nullptr, nb, N);
-  g_launch_count += 2;
-  return cudaGetLastError();
+    e = launch_pdl(colsum_part_kernel<__nv_bfloat16>, pgrid, dim3(COL_THREADS), 0, st,
+                   (const __nv_bfloat16*)in, ld, M, N, part);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(part_reduce_kernel, dim3((N + RED_COLS - 1) / RED_COLS),
+                    dim3(RED_COLS * RED_GROUPS), 0, st, (const float*)part, out,
+                    (const float*)nullptr, (float*)nullptr, nb, N);
 }
 
 cudaError_t add_into(const void* a, const float* b, void* out, int64_t n, DType t,
@@ -203,12 +368,10 @@ cudaError_t add_into(const void* a, const float* b, void* out, int64_t n, DType 
   if (n == 0) return cudaSuccess;
   const int grid = (int)std::min<int64_t>((n + 255) / 256, 152 * 16);
   if (t == DType::F32)
-    add_into_kernel<float><<<grid, 256, 0, st>>>((const float*)a, b, (float*)out, n);
-  else
-    add_into_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)a, b,
-                                                         (__nv_bfloat16*)out, n);
-  OASES_COUNT_LAUNCH();
-  return cudaGetLastError();
+    return launch_pdl(add_into_kernel<float>, dim3(grid), dim3(256), 0, st, (const float*)a, b,
+                      (float*)out, n);
+  return launch_pdl(add_into_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
+                    (const __nv_bfloat16*)a, b, (__nv_bfloat16*)out, n);
 }
 
 }  // namespace oases
