@@ -37,6 +37,20 @@ oases_status oases_debug_gemm(int M, int N, int K, int in_dtype, const void *A, 
                               void *C, int64_t ldc, int c_dtype, void *C2, const void *bias,
                               const void *aux, int64_t ld_aux, int path, void *stream);
 
+/* Bias gradient of a linear layer, as the block takes it: by Oases §IV,
+ * Eq. (1) every shard's partial receives the same output gradient dY, and the
+ * row-parallel bias (added once after the shard sum) gets
+ *   out[n] += sum_{m < M} in[m * ld + n],   n < N,
+ * (also used for the column-parallel bias with in = dA).  Deterministic:
+ * blocks of 32 rows are summed into partial rows in scratch, then the partial
+ * rows are added in order.  in: device, type dtype (oases_dtype), leading
+ * dimension ld >= N.  out: device fp32 [N], accumulated.  scratch: device,
+ * at least oases_debug_bias_grad_scratch_bytes(M, N) bytes, owned by the
+ * caller.  Asynchronous on stream. */
+size_t oases_debug_bias_grad_scratch_bytes(int M, int N);
+oases_status oases_debug_bias_grad(const void *in, int64_t ld, int M, int N, int dtype, float *out,
+                                   void *scratch, size_t scratch_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,6 +37,7 @@ namespace oases {
 thread_local int g_launch_count = 0;
 }
 
+
 namespace {
 using namespace oases;
 
@@ -828,6 +829,30 @@ extern "C" oases_status oases_debug_gemm(int M, int N, int K, int in_dtype, cons
   } else {
     e = gemm(g, st);
   }
+  t_last_launches = g_launch_count;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
+extern "C" size_t oases_debug_bias_grad_scratch_bytes(int M, int N) {
+  if (M < 0 || N < 0) return 0;
+  return (size_t)oases::colsum_blocks(M) * (size_t)N * sizeof(float);
+}
+
+extern "C" oases_status oases_debug_bias_grad(const void* in, int64_t ld, int M, int N, int dtype,
+                                              float* out, void* scratch, size_t scratch_bytes,
+                                              void* stream) {
+  using namespace oases;
+  t_last_error.clear();
+  g_launch_count = 0;
+  if (M < 0 || N < 0 || dtype < 0 || dtype > 1 || ld < N) return OASES_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return OASES_OK;
+  if (!in || !out) return OASES_ERR_INVALID_ARG;
+  if (!scratch || scratch_bytes < oases_debug_bias_grad_scratch_bytes(M, N))
+    return OASES_ERR_WORKSPACE;
+  cudaError_t e = colsum_accum(in, ld, M, N, static_cast<DType>(dtype),
+                               static_cast<float*>(scratch), out,
+                               static_cast<cudaStream_t>(stream));
   t_last_launches = g_launch_count;
   if (e != cudaSuccess) return cuda_fail(e);
   return OASES_OK;
