@@ -51,6 +51,32 @@ size_t oases_debug_bias_grad_scratch_bytes(int M, int N);
 oases_status oases_debug_bias_grad(const void *in, int64_t ld, int M, int N, int dtype, float *out,
                                    void *scratch, size_t scratch_bytes, void *stream);
 
+/* The bias-gradient sum above for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for callers such
+ * as a plugin inside a host framework that owns every device allocation, a
+ * real-time loop where cudaMalloc's implicit device synchronisation is not
+ * acceptable, or code that must not grow its memory footprint after start-up.
+ *
+ * Same arguments and result as oases_debug_bias_grad, without the scratch
+ * argument: the partial rows live in a static device array of
+ * OASES_NOALLOC_SCRATCH_FLOATS fp32 values (4 MiB) that every GPU which loads
+ * the library keeps until the process exits.  Sizes whose partial rows do not
+ * fit, ceil(M / 32) * N > OASES_NOALLOC_SCRATCH_FLOATS, are rejected with
+ * OASES_ERR_UNSUPPORTED before anything is enqueued (oases_last_error() says
+ * how many floats were needed).  Nothing is allocated or freed, by this call
+ * or by any library routine it uses.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls on a device share the one array, which keeps
+ * the previous call's contents (every value it reads is written first by the
+ * same call): calls whose executions overlap on the GPU (for instance on two
+ * streams without ordering between them) race on the array and give wrong
+ * results.  Asynchronous on stream. */
+#define OASES_NOALLOC_SCRATCH_FLOATS (1u << 20)
+oases_status oases_bias_grad_noalloc(const void *in, int64_t ld, int M, int N, int dtype,
+                                     float *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

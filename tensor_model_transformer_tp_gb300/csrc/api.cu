@@ -37,6 +37,13 @@ namespace oases {
 thread_local int g_launch_count = 0;
 }
 
+namespace oases {
+// Entry-point bookkeeping shared with the other translation units that define
+// extern "C" functions: reset per call, record a CUDA or argument error.
+void api_begin();
+void api_set_error(const char* what);
+oases_status api_end(cudaError_t e);
+}
 
 namespace {
 using namespace oases;
@@ -696,6 +703,19 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
 }
 
 }  // namespace
+
+namespace oases {
+void api_begin() {
+  t_last_error.clear();
+  g_launch_count = 0;
+}
+void api_set_error(const char* what) { t_last_error = what; }
+oases_status api_end(cudaError_t e) {
+  t_last_launches = g_launch_count;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+}  // namespace oases
 
 extern "C" {
 
