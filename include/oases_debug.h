@@ -37,6 +37,25 @@ oases_status oases_debug_gemm(int M, int N, int K, int in_dtype, const void *A, 
                               void *C, int64_t ldc, int c_dtype, void *C2, const void *bias,
                               const void *aux, int64_t ld_aux, int path, void *stream);
 
+/* Causal softmax attention of the attention segment's F_i (Oases §IV-A: the
+ * column-parallel attention layer; each shard owns heads, and heads are
+ * independent, so all shards' heads run in one call):
+ *   O_h = softmax(Q_h K_h^T / sqrt(d) + mask) V_h, LSE_h = log sum exp
+ * per sequence and head, mask: key j visible from query i iff j <= i when
+ * causal.  qkv: device [batch*seq, 3*heads*head_dim], rows of one sequence
+ * contiguous, Q of head h at column h*d, K at H + h*d, V at 2H + h*d
+ * (H = heads*head_dim).  o: [batch*seq, H]; lse: fp32 [heads, batch*seq].
+ * backward = 1: from d_o ([batch*seq, H]) and the forward's o and lse, writes
+ * delta (fp32 [heads, batch*seq], rowsum(d_o * o)) and dqkv ([batch*seq, 3H],
+ * gradients of Q, K, V in qkv's layout).  dtype: oases_dtype of qkv, o, d_o,
+ * dqkv.  path: 0 = the block's choice, 1 = CUDA-core kernels, 2 = tensor-core
+ * kernels (bf16, head_dim 128; OASES_ERR_UNSUPPORTED otherwise).
+ * Asynchronous on stream. */
+oases_status oases_debug_attention(const void *qkv, void *o, float *lse, const void *d_o,
+                                   float *delta, void *dqkv, int batch, int seq, int heads,
+                                   int head_dim, int causal, int dtype, int backward, int path,
+                                   void *stream);
+
 /* Bias gradient of a linear layer, as the block takes it: by Oases §IV,
  * Eq. (1) every shard's partial receives the same output gradient dY, and the
  * row-parallel bias (added once after the shard sum) gets

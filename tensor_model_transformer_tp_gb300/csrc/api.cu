@@ -792,9 +792,9 @@ int oases_last_launch_count(void) { return t_last_launches; }
 oases_status oases_check_device(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
-  const int v = gemm_read_and_clear_error();
-  if (v < 0) return cuda_fail(cudaGetLastError());
-  return v ? OASES_ERR_TIMEOUT : OASES_OK;
+  const int v = gemm_read_and_clear_error(), w = attention_read_and_clear_error();
+  if (v < 0 || w < 0) return cuda_fail(cudaGetLastError());
+  return (v || w) ? OASES_ERR_TIMEOUT : OASES_OK;
 }
 
 }  // extern "C"
@@ -873,6 +873,48 @@ extern "C" oases_status oases_debug_bias_grad(const void* in, int64_t ld, int M,
   cudaError_t e = colsum_accum(in, ld, M, N, static_cast<DType>(dtype),
                                static_cast<float*>(scratch), out,
                                static_cast<cudaStream_t>(stream));
+  t_last_launches = g_launch_count;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
+extern "C" oases_status oases_debug_attention(const void* qkv, void* o, float* lse, const void* d_o,
+                                              float* delta, void* dqkv, int batch, int seq,
+                                              int heads, int head_dim, int causal, int dtype,
+                                              int backward, int path, void* stream) {
+  using namespace oases;
+  t_last_error.clear();
+  g_launch_count = 0;
+  if (batch < 0 || seq < 0 || heads <= 0 || head_dim <= 0 || dtype < 0 || dtype > 1 ||
+      path < 0 || path > 2)
+    return OASES_ERR_INVALID_ARG;
+  if (head_dim > 128 || head_dim % 8 != 0) return OASES_ERR_UNSUPPORTED;
+  AttnArgs a;
+  a.batch = batch;
+  a.seq = seq;
+  a.heads = heads;
+  a.head_dim = head_dim;
+  a.hidden = heads * head_dim;
+  a.causal = causal != 0;
+  a.t = static_cast<DType>(dtype);
+  a.qkv = qkv;
+  a.o = o;
+  a.lse = lse;
+  a.d_o = d_o;
+  a.delta = delta;
+  a.dqkv = dqkv;
+  if ((int64_t)batch * seq > 0 && (!qkv || !o || !lse)) return OASES_ERR_INVALID_ARG;
+  if (backward && (int64_t)batch * seq > 0 && (!d_o || !delta || !dqkv))
+    return OASES_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (!backward) {
+    if (path == 2 && !attention_tc_supported(a)) return OASES_ERR_UNSUPPORTED;
+    e = path == 1 ? attention_fwd_simt(a, st) : path == 2 ? attention_fwd_tc(a, st)
+                                                        : attention_fwd(a, st);
+  } else {
+    e = path == 1 ? attention_bwd_simt(a, st) : attention_bwd(a, st);
+  }
   t_last_launches = g_launch_count;
   if (e != cudaSuccess) return cuda_fail(e);
   return OASES_OK;

@@ -330,7 +330,10 @@ cudaError_t attention_bwd_simt(const AttnArgs& a, cudaStream_t st) {
 
 namespace oases {
 
-cudaError_t attention_fwd(const AttnArgs& a, cudaStream_t st) { return attention_fwd_simt(a, st); }
+cudaError_t attention_fwd(const AttnArgs& a, cudaStream_t st) {
+  if (attention_tc_supported(a)) return attention_fwd_tc(a, st);
+  return attention_fwd_simt(a, st);
+}
 cudaError_t attention_bwd(const AttnArgs& a, cudaStream_t st) { return attention_bwd_simt(a, st); }
 
 }  // namespace oases

@@ -170,6 +170,10 @@ struct AttnArgs {
 cudaError_t attention_fwd(const AttnArgs& a, cudaStream_t st);
 cudaError_t attention_bwd(const AttnArgs& a, cudaStream_t st);
 cudaError_t attention_fwd_simt(const AttnArgs& a, cudaStream_t st);
+// Tensor-core forward (bf16, head dimension 128); see attn_tc.cu.
+bool attention_tc_supported(const AttnArgs& a);
+cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st);
+int attention_read_and_clear_error();
 cudaError_t attention_bwd_simt(const AttnArgs& a, cudaStream_t st);
 
 // Reads and clears the error word the tensor-core kernels set when a bounded
