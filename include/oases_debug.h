@@ -56,6 +56,16 @@ oases_status oases_debug_attention(const void *qkv, void *o, float *lse, const v
                                    int head_dim, int causal, int dtype, int backward, int path,
                                    void *stream);
 
+/* Debugging aids for the tensor-core attention kernels.
+ * oases_debug_attention_progress: host_mapped is a device-accessible host
+ * buffer of 768 ints (pinned) or NULL; when set, thread 0 of CTA c of kernel k
+ * (0 forward, 1 dQ, 2 dK/dV) writes its current stage to host_mapped[256k + c]
+ * as it goes, which lets a host watchdog see where a stalled kernel stands.
+ * oases_debug_attention_error_word: reads and clears the code of the first
+ * bounded wait that gave up (kernel * 100 + site; 0 = none, -1 = unreadable). */
+oases_status oases_debug_attention_progress(int *host_mapped);
+int oases_debug_attention_error_word(void);
+
 /* Bias gradient of a linear layer, as the block takes it: by Oases §IV,
  * Eq. (1) every shard's partial receives the same output gradient dY, and the
  * row-parallel bias (added once after the shard sum) gets

@@ -919,3 +919,13 @@ extern "C" oases_status oases_debug_attention(const void* qkv, void* o, float* l
   if (e != cudaSuccess) return cuda_fail(e);
   return OASES_OK;
 }
+
+extern "C" oases_status oases_debug_attention_progress(int* host_mapped) {
+  cudaError_t e = oases::attention_set_progress(host_mapped);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
+extern "C" int oases_debug_attention_error_word(void) {
+  return oases::attention_read_and_clear_error();
+}

@@ -334,6 +334,10 @@ cudaError_t attention_fwd(const AttnArgs& a, cudaStream_t st) {
   if (attention_tc_supported(a)) return attention_fwd_tc(a, st);
   return attention_fwd_simt(a, st);
 }
-cudaError_t attention_bwd(const AttnArgs& a, cudaStream_t st) { return attention_bwd_simt(a, st); }
+cudaError_t attention_bwd(const AttnArgs& a, cudaStream_t st) {
+  if (attention_tc_supported(a) && !(((uintptr_t)a.d_o | (uintptr_t)a.dqkv) & 15))
+    return attention_bwd_tc(a, st);
+  return attention_bwd_simt(a, st);
+}
 
 }  // namespace oases

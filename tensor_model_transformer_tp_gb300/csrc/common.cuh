@@ -173,7 +173,11 @@ cudaError_t attention_fwd_simt(const AttnArgs& a, cudaStream_t st);
 // Tensor-core forward (bf16, head dimension 128); see attn_tc.cu.
 bool attention_tc_supported(const AttnArgs& a);
 cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st);
+cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st);
 int attention_read_and_clear_error();
+// Debugging aid: host-mapped int[768] that the attention kernels' thread 0
+// fills with progress markers (nullptr switches them off).
+cudaError_t attention_set_progress(int* p);
 cudaError_t attention_bwd_simt(const AttnArgs& a, cudaStream_t st);
 
 // Reads and clears the error word the tensor-core kernels set when a bounded

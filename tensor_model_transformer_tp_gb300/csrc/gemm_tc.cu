@@ -274,7 +274,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int t = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
       const int buf = t & 1;
-      if (!ptx::mbar_wait(tfull(buf), ((uint32_t)t >> 1) & 1u)) {
+      // the decision is warp-uniform: tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull(buf), ((uint32_t)t >> 1) & 1u))) {
         if (lane == 0) atomicExch(&g_gemm_error, 3);
         break;
       }

@@ -30,27 +30,32 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// One bounded probe of the phase: the thread may be suspended for at most
+// about 20 microseconds (suspend-time hint) before the answer comes back.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
-// Waits for the phase of the given parity to complete.  Gives up after
-// limit_ns nanoseconds and returns false (the caller records the error and
-// leaves its loop, so that no wait can hang the GPU).
+// Waits for the phase of the given parity to complete.  Gives up after about
+// limit_cycles SM clock cycles (2^32 cycles is about 2 s at 2 GHz; the clock
+// is checked on every probe) or 2^24 probes, whichever comes first, and
+// returns false: the caller records the error and leaves its loop, so that no
+// wait can hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          uint64_t limit_cycles = 1ull << 32) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
+  const uint64_t c0 = clock64();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && globaltimer() - t0 > limit_ns) return false;
+    if ((uint64_t)(clock64() - c0) > limit_cycles) return false;
   }
+  return false;
 }
 
 // 2-D TMA tile load into shared memory, completion signalled on an mbarrier.

@@ -93,7 +93,8 @@ def test_tc_forward(L, B, S, nh, causal):
     assert np.all(np.isfinite(tc["o"]))
 
 
-@pytest.mark.parametrize("B,S,nh,causal", [(2, 200, 2, True), (1, 128, 1, False)])
+@pytest.mark.parametrize("B,S,nh,causal", [(2, 200, 2, True), (1, 128, 1, False), (1, 77, 3, True),
+                                           (2, 300, 1, False), (1, 1, 1, True), (1, 320, 2, True)])
 def test_backward(L, B, S, nh, causal):
     d = 128
     g = torch.Generator().manual_seed(11 + S)
@@ -102,5 +103,21 @@ def test_backward(L, B, S, nh, causal):
     ref = ref_attention(qkv.double().numpy(), B, S, nh, d, causal, d_o.double().numpy())
     got = run(L, qkv.cuda(), B, S, nh, d, causal, path=0, d_o=d_o.cuda())
     H = nh * d
+    scale = np.linalg.norm(ref["dqkv"])
     for part, sl in (("dq", slice(0, H)), ("dk", slice(H, 2 * H)), ("dv", slice(2 * H, 3 * H))):
-        assert rel(got["dqkv"][:, sl], ref["dqkv"][:, sl]) < 2e-2, part
+        a, b = got["dqkv"][:, sl], ref["dqkv"][:, sl]
+        if np.linalg.norm(b) < 1e-9 * scale:
+            # exactly zero in exact arithmetic (one-token sequences: dS = P (dP - delta) = 0)
+            assert np.linalg.norm(a) <= 1e-4 * scale, part
+        else:
+            assert rel(a, b) < 2e-2, part
+
+
+def test_tc_backward_matches_cuda_core_backward(L):
+    B, S, nh, d = 2, 192, 2, 128
+    g = torch.Generator().manual_seed(5)
+    qkv = torch.randn(B * S, 3 * nh * d, generator=g).bfloat16().cuda()
+    d_o = torch.randn(B * S, nh * d, generator=g).bfloat16().cuda()
+    tc = run(L, qkv, B, S, nh, d, True, path=0, d_o=d_o)
+    simt = run(L, qkv, B, S, nh, d, True, path=1, d_o=d_o)
+    assert rel(tc["dqkv"], simt["dqkv"]) < 1e-2
