@@ -64,6 +64,11 @@ oases_status oases_debug_attention(const void *qkv, void *o, float *lse, const v
  * oases_debug_attention_error_word: reads and clears the code of the first
  * bounded wait that gave up (kernel * 100 + site; 0 = none, -1 = unreadable). */
 oases_status oases_debug_attention_progress(int *host_mapped);
+/* Timeline of the tensor-core GEMM (debugging aid): device_buffer holds 16
+ * uint64 %globaltimer stamps per CTA of every following launch (entry,
+ * prologue done, first stage landed, then per local tile t < 5 its MMAs done
+ * and its epilogue done, exit); NULL switches it off. */
+oases_status oases_debug_gemm_timeline(unsigned long long *device_buffer);
 int oases_debug_attention_error_word(void);
 
 /* Bias gradient of a linear layer, as the block takes it: by Oases §IV,

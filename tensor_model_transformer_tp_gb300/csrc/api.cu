@@ -929,3 +929,12 @@ extern "C" oases_status oases_debug_attention_progress(int* host_mapped) {
 extern "C" int oases_debug_attention_error_word(void) {
   return oases::attention_read_and_clear_error();
 }
+
+namespace oases {
+cudaError_t gemm_set_timeline(unsigned long long* p);
+}
+extern "C" oases_status oases_debug_gemm_timeline(unsigned long long* device_buffer) {
+  cudaError_t e = oases::gemm_set_timeline(device_buffer);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}

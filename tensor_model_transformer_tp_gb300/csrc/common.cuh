@@ -67,14 +67,41 @@ __device__ __forceinline__ void store_any(void* p, DType t, int64_t i, float v) 
 }
 
 // GeLU in its exact form a * Phi(a), Phi the standard normal CDF, and its
-// derivative Phi(a) + a * phi(a).  erff / expf are CUDA's own.
+// derivative Phi(a) + a * phi(a), phi the standard normal density.
+//
+// Phi is evaluated through erf with formula 7.1.26 of Abramowitz & Stegun,
+// Handbook of Mathematical Functions: for x >= 0,
+//   erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2) + e(x),
+//   t = 1 / (1 + p x),  |e(x)| <= 1.5e-7,
+//   p = 0.3275911, a1..a5 = 0.254829592, -0.284496736, 1.421413741,
+//   -1.453152027, 1.061405429,
+// and erf(-x) = -erf(x).  With x = |a| / sqrt(2), exp(-x^2) = exp(-a^2 / 2) is
+// also the Gaussian density's exponential, so GeLU' costs one more FMA.  One
+// reciprocal, one exp2 and a handful of FMAs, no branch.
+__device__ __forceinline__ void gelu_cdf_pdf(float a, float& cdf, float& pdf) {
+  const float x = fabsf(a) * 0.70710678118654752f;
+  float t, e;
+  // hardware reciprocal and base-2 exponential (relative error ~2^-22; an
+  // exponential that underflows is flushed to 0, i.e. erf = 1 exactly)
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.0f)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-x * x * 1.4426950408889634f));  // exp(-a^2/2)
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f),
+                       -0.284496736f),
+               0.254829592f);
+  const float erf_abs = fmaf(-poly, e, 1.0f);
+  cdf = 0.5f + 0.5f * copysignf(erf_abs, a);
+  pdf = 0.39894228040143268f * e;
+}
 __device__ __forceinline__ float gelu_f(float a) {
-  return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+  float cdf, pdf;
+  gelu_cdf_pdf(a, cdf, pdf);
+  return a * cdf;
 }
 __device__ __forceinline__ float gelu_grad_f(float a) {
-  const float cdf = 0.5f * (1.0f + erff(a * 0.70710678118654752f));
-  const float pdf = 0.39894228040143268f * expf(-0.5f * a * a);
-  return cdf + a * pdf;
+  float cdf, pdf;
+  gelu_cdf_pdf(a, cdf, pdf);
+  return fmaf(a, pdf, cdf);
 }
 
 // ---------------------------------------------------------------------------
@@ -111,6 +138,7 @@ struct GemmArgs {
   const void* aux = nullptr;   // [M, N] with leading dim ld_aux, type aux_t
   int64_t ld_aux = 0;
   DType aux_t = DType::BF16;
+  int tma_store = 0;  // set by the tensor-core path: outputs leave through TMA stores
 };
 
 // Returns cudaSuccess or the launch error.  Picks the tensor-core kernel when

@@ -37,6 +37,11 @@
 namespace oases {
 
 __device__ int g_gemm_error;
+// Optional timeline (debugging aid, off when null): per CTA 16 globaltimer
+// stamps: [0] entry, [1] after the prologue, [2] first stage landed (MMA
+// thread), [3 + 2t] MMAs of local tile t done, [4 + 2t] its epilogue done
+// (t < 5), [15] exit.
+__device__ unsigned long long* g_gemm_timeline;
 
 namespace {
 
@@ -51,8 +56,10 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * BKE * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int EPI_OFF = STAGES * STAGE;        // per epilogue warp: 32 rows x 128 B
+  static constexpr int EPI_BYTES = 8 * 32 * 128;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8;
-  static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE + EPI_BYTES + BAR_BYTES + 1024;
   static constexpr int TMEM_COLS = 2 * BN;
 };
 
@@ -145,17 +152,106 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int n, float
   }
 }
 
-template <int BN, bool A_K, bool B_K>
+// Epilogue through shared memory and TMA: the warp's 32 rows x CW columns
+// (CW * element size = 128 bytes) are written into its 128-byte-swizzled
+// staging buffer, one row per lane, then lane 0 stores the box with one TMA
+// store (or fp32 reduce-add for Accum).  The TMA unit clips rows >= M and
+// columns >= N.  v holds this lane's CW accumulator values for row m.
+template <int CW>
+__device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorMap* tmC,
+                                              const CUtensorMap* tmC2, uint8_t* stg,
+                                              uint32_t stg_s, int m, int mw, int n, int lane,
+                                              float (&v)[CW]) {
+  const bool bf = g.c_t == DType::BF16;
+  if (g.epi == Epi::Bias || g.epi == Epi::BiasGelu || g.epi == Epi::BiasResid) {
+    const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(g.bias) + n;
+    if (n + CW <= g.N) {
+#pragma unroll
+      for (int i = 0; i < CW / 8; ++i) {
+        float t[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(b) + i), t);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[8 * i + k] += t[k];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < CW; ++i)
+        if (n + i < g.N) v[i] += __bfloat162float(b[i]);
+    }
+  }
+  if ((g.epi == Epi::BiasResid || g.epi == Epi::GeluBwd) && m < g.M) {
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(g.aux) + (int64_t)m * g.ld_aux + n;
+    float t[CW];
+    if (n + CW <= g.N) {
+#pragma unroll
+      for (int i = 0; i < CW / 8; ++i) unpack8(__ldg(reinterpret_cast<const uint4*>(x) + i), t + 8 * i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < CW; ++i) t[i] = n + i < g.N ? __bfloat162float(x[i]) : 0.f;
+    }
+    if (g.epi == Epi::BiasResid) {
+#pragma unroll
+      for (int i = 0; i < CW; ++i) v[i] += t[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < CW; ++i) v[i] *= gelu_grad_f(t[i]);
+    }
+  }
+  // one staged store of v (as stored in C's type) to the box at (n, mw)
+  auto stage_and_store = [&](const CUtensorMap* tm, bool reduce) {
+    if (lane == 0) ptx::bulk_wait_read0();  // the previous store has read the buffer
+    __syncwarp();
+    uint8_t* row = stg + lane * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint4 w;
+      if (bf) {
+        w = make_uint4(pack_bf16(v[8 * u], v[8 * u + 1]), pack_bf16(v[8 * u + 2], v[8 * u + 3]),
+                       pack_bf16(v[8 * u + 4], v[8 * u + 5]), pack_bf16(v[8 * u + 6], v[8 * u + 7]));
+      } else {
+        w = make_uint4(__float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]),
+                       __float_as_uint(v[4 * u + 2]), __float_as_uint(v[4 * u + 3]));
+      }
+      *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) = w;
+    }
+    ptx::fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce)
+        ptx::tma_reduce_add_2d(tm, stg_s, n, mw);
+      else
+        ptx::tma_store_2d(tm, stg_s, n, mw);
+      ptx::bulk_commit();
+    }
+  };
+  if (g.epi == Epi::BiasGelu) {
+    if (g.C2) stage_and_store(tmC2, false);
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = gelu_f(v[i]);
+  }
+  stage_and_store(tmC, g.epi == Epi::Accum);
+}
+
+// CL = 1: one CTA per 128 x BN tile.  CL = 2: a cluster of two CTAs takes a
+// 256 x BN tile; CTA r computes rows [128 r, 128 r + 128), loads its own A rows
+// and half r of the B tile, multicasting that half into both CTAs' shared
+// memory, so each CTA moves A + B/2 per stage instead of A + B.  A stage is
+// refilled only after both CTAs' MMAs have released it (the empty barriers
+// count two commits, multicast by each CTA's MMA thread).
+template <int BN, bool A_K, bool B_K, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                const GemmArgs g) {
   using C = TcCfg<BN>;
   constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, !A_K, !B_K);
+  unsigned long long* tl = g_gemm_timeline ? g_gemm_timeline + 16 * blockIdx.x : nullptr;
+  if (tl && threadIdx.x == 0) tl[0] = ptx::globaltimer();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + C::STAGES * C::STAGE;
+  const uint32_t bars = base + C::EPI_OFF + C::EPI_BYTES;
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
   auto tfull = [&](int b) { return bars + 8u * (2 * C::STAGES + b); };
@@ -164,13 +260,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tslot = bars + 8u * (2 * C::STAGES + 5);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = CL > 1 ? (int)ptx::cluster_rank() : 0;
   const int num_m = (g.M + BM - 1) / BM, num_n = (g.N + BN - 1) / BN;
-  const int tiles = num_m * num_n, nkb = (g.K + BKE - 1) / BKE;
+  const int num_mp = (num_m + CL - 1) / CL;  // row blocks of CL * 128 rows
+  const int tiles = num_mp * num_n, nkb = (g.K + BKE - 1) / BKE;
+  const int first = blockIdx.x / CL, stride = gridDim.x / CL;
+  auto tile_m0 = [&](int t) { return ((t % num_mp) * CL + rank) * BM; };
+  auto tile_n0 = [&](int t) { return (t / num_mp) * BN; };
+  constexpr uint16_t MASK = (1u << CL) - 1u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(full(s), 1);
-      ptx::mbar_init(empty(s), 1);
+      ptx::mbar_init(empty(s), CL);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull(b), 1);
@@ -186,15 +288,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    if (g.tma_store) {
+      ptx::prefetch_tmap(&tmC);
+      if (g.C2) ptx::prefetch_tmap(&tmC2);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
+  if (CL > 1) ptx::cluster_sync();  // partner's barriers initialised before any multicast
   // Everything above touched only shared memory, TMEM and kernel parameters, so
   // it overlapped the previous kernel on the stream; global memory from here on.
   pdl_wait();
   pdl_trigger();
+  if (tl && threadIdx.x == 0) tl[1] = ptx::globaltimer();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -203,8 +311,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s has a load outstanding at some phase
       uint32_t iphase = 0;  // bit s: parity of the last load issued into stage s
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+      for (int tile = first; tile < tiles && ok; tile += stride) {
+        const int m0 = tile_m0(tile), n0 = tile_n0(tile);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!ptx::mbar_wait(empty(stage), phase ^ 1u)) { ok = false; break; }
           const uint32_t fb = full(stage);
@@ -217,11 +325,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::tma_load_2d(sa, &tmA, fb, m0, k0);
             ptx::tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
           }
-          if (B_K) {
-            ptx::tma_load_2d(sb, &tmB, fb, k0, n0);
-          } else {
+          if (CL == 1) {
+            if (B_K) {
+              ptx::tma_load_2d(sb, &tmB, fb, k0, n0);
+            } else {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) ptx::tma_load_2d(sb + c * 8192, &tmB, fb, n0 + 64 * c, k0);
+              for (int c = 0; c < BN / 64; ++c)
+                ptx::tma_load_2d(sb + c * 8192, &tmB, fb, n0 + 64 * c, k0);
+            }
+          } else if (B_K) {  // rows [rank * BN/CL, ...) of the B tile, to both CTAs
+            ptx::tma_load_2d_mc(sb + rank * (BN / CL) * 128, &tmB, fb, k0, n0 + rank * (BN / CL),
+                                MASK);
+          } else {  // 64-wide N chunks rank * (BN/64/CL) ..., to both CTAs
+#pragma unroll
+            for (int c = 0; c < BN / 64 / CL; ++c) {
+              const int cc = rank * (BN / 64 / CL) + c;
+              ptx::tma_load_2d_mc(sb + cc * 8192, &tmB, fb, n0 + 64 * cc, k0, MASK);
+            }
           }
           issued |= 1u << stage;
           iphase = (iphase & ~(1u << stage)) | (phase << stage);
@@ -240,7 +360,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t phase = 0;
       bool ok = true;
       int t = 0;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++t) {
+      for (int tile = first; tile < tiles && ok; tile += stride, ++t) {
         const int buf = t & 1;
         if (!ptx::mbar_wait(tempty(buf), (((uint32_t)t >> 1) & 1u) ^ 1u)) { ok = false; break; }
         ptx::tc_fence_after();
@@ -248,6 +368,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = 0; kb < nkb; ++kb) {
           if (!ptx::mbar_wait(full(stage), phase)) { ok = false; break; }
           ptx::tc_fence_after();
+          if (tl && t == 0 && kb == 0) tl[2] = ptx::globaltimer();
           const uint32_t sa = base + stage * C::STAGE, sb = sa + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BKE / 16; ++kk) {
@@ -257,11 +378,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                     : ptx::smem_desc_sw128(sb + kk * 2048, 8192, 1024);
             ptx::mma_bf16(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(empty(stage));
+          if (CL == 1)
+            ptx::mma_commit(empty(stage));
+          else
+            ptx::mma_commit_mc(empty(stage), MASK);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         ptx::mma_commit(tfull(buf));
+        if (tl && t < 5) tl[3 + 2 * t] = ptx::globaltimer();
       }
       // Drain: all MMAs issued by this thread are complete before TMEM is freed.
       ptx::mma_commit(drain);
@@ -272,7 +397,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;  // which half of the BN columns
     int t = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
+    for (int tile = first; tile < tiles; tile += stride, ++t) {
       const int buf = t & 1;
       // the decision is warp-uniform: tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull(buf), ((uint32_t)t >> 1) & 1u))) {
@@ -280,18 +405,43 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         break;
       }
       ptx::tc_fence_after();
-      const int m = (tile % num_m) * BM + q * 32 + lane;
-      const int nb0 = (tile / num_m) * BN;
+      const int mw = tile_m0(tile) + q * 32, m = mw + lane;
+      const int nb0 = tile_n0(tile);
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (g.tma_store && g.c_t == DType::BF16) {
+        uint8_t* stg = gbase + C::EPI_OFF + (warp - 2) * 4096;
+        const uint32_t stg_s = base + C::EPI_OFF + (warp - 2) * 4096;
 #pragma unroll 1
-      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(trow + c0, v);
-        if (m < g.M && nb0 + c0 < g.N) epi_chunk(g, m, nb0 + c0, v);
+        for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64) {
+          float v[64];
+          ptx::tmem_ld32(trow + c0, *reinterpret_cast<float(*)[32]>(v));
+          ptx::tmem_ld32(trow + c0 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+          if (mw < g.M && nb0 + c0 < g.N)
+            epi_tma_chunk<64>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, lane, v);
+        }
+      } else if (g.tma_store) {
+        uint8_t* stg = gbase + C::EPI_OFF + (warp - 2) * 4096;
+        const uint32_t stg_s = base + C::EPI_OFF + (warp - 2) * 4096;
+#pragma unroll 1
+        for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
+          float v[32];
+          ptx::tmem_ld32(trow + c0, v);
+          if (mw < g.M && nb0 + c0 < g.N)
+            epi_tma_chunk<32>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, lane, v);
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
+          float v[32];
+          ptx::tmem_ld32(trow + c0, v);
+          if (m < g.M && nb0 + c0 < g.N) epi_chunk(g, m, nb0 + c0, v);
+        }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty(buf));
+      if (tl && t < 5 && warp == 2 && lane == 0) tl[4 + 2 * t] = ptx::globaltimer();
     }
+    if (g.tma_store && lane == 0) ptx::bulk_wait0();  // stores performed before the CTA retires
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -299,6 +449,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // neither CTA leaves while its partner may still multicast into it or
+  // arrive on its barriers
+  if (CL > 1) ptx::cluster_sync();
+  if (tl && threadIdx.x == 0) tl[15] = ptx::globaltimer();
 }
 
 // ---- host side -------------------------------------------------------------
@@ -345,10 +499,10 @@ struct MapKeyHash {
 // dimension ld (elements), box [box_outer, box_inner], 128-byte swizzle,
 // out-of-bounds elements read as zero.  Cached by its arguments.
 bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer, bool f32 = false) {
   static std::mutex mu;
   static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-  const MapKey key{(uintptr_t)ptr, inner, outer, ld, box_inner, box_outer};
+  const MapKey key{(uintptr_t)ptr | (f32 ? 1u : 0u), inner, outer, ld, box_inner, box_outer};
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -358,11 +512,12 @@ bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint64_t strides[1] = {ld * (f32 ? 4 : 2)};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
-  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  if (fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+         const_cast<void*>(ptr), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
@@ -383,32 +538,80 @@ int num_sms() {
   return n;
 }
 
-template <int BN, bool A_K, bool B_K>
+template <int BN, bool A_K, bool B_K, int CL>
 cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
   using C = TcCfg<BN>;
   CUtensorMap ma, mb;
   bool ok = A_K ? make_map(&ma, g.A, g.K, g.M, g.lda, BKE, BM)
                 : make_map(&ma, g.A, g.M, g.K, g.lda, 64, BKE);
-  ok = ok && (B_K ? make_map(&mb, g.B, g.K, g.N, g.ldb, BKE, BN)
+  ok = ok && (B_K ? make_map(&mb, g.B, g.K, g.N, g.ldb, BKE, BN / CL)
                   : make_map(&mb, g.B, g.N, g.K, g.ldb, 64, BKE));
   if (!ok) return cudaErrorInvalidValue;
-  auto kern = gemm_tc_kernel<BN, A_K, B_K>;
+  // outputs through TMA stores when C (and C2) rows are 16-byte multiples
+  GemmArgs ga = g;
+  CUtensorMap mc = ma, mc2 = ma;
+  const bool f32c = g.c_t == DType::F32;
+  const int esz = f32c ? 4 : 2, cw = f32c ? 32 : 64;
+  const bool aligned = ((g.ldc * esz) % 16 == 0) && (((uintptr_t)g.C | (uintptr_t)g.C2) & 15) == 0 &&
+                       (((uintptr_t)g.bias | (uintptr_t)g.aux) & 15) == 0 &&
+                       (g.aux == nullptr || (g.ld_aux % 8 == 0 && g.aux_t == DType::BF16));
+  ga.tma_store = 0;
+  if (aligned && make_map(&mc, g.C, g.N, g.M, g.ldc, cw, 32, f32c) &&
+      (g.C2 == nullptr || make_map(&mc2, g.C2, g.N, g.M, g.ldc, cw, 32, f32c)))
+    ga.tma_store = 1;
+  auto kern = gemm_tc_kernel<BN, A_K, B_K, CL>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_pdl(kern, dim3(grid), dim3(NTHREADS), C::SMEM, st, ma, mb, g);
+  const int num_mp = ((g.M + BM - 1) / BM + CL - 1) / CL;
+  const int tiles = num_mp * ((g.N + BN - 1) / BN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  // persistent grid: as many clusters as can be resident at once
+  static int slots = 0;
+  if (slots == 0) {
+    slots = num_sms() / CL;
+    if (CL > 1) {
+      cudaLaunchAttribute ca[1];
+      ca[0].id = cudaLaunchAttributeClusterDimension;
+      ca[0].val.clusterDim.x = CL;
+      ca[0].val.clusterDim.y = 1;
+      ca[0].val.clusterDim.z = 1;
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(num_sms() / CL * CL);
+      q.attrs = ca;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) == cudaSuccess && n > 0 && n < slots)
+        slots = n;
+      cudaGetLastError();
+    }
+  }
+  const int grid = (tiles < slots ? tiles : slots) * CL;
+  cfg.gridDim = dim3(grid);
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = CL;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
+  ++g_launch_count;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, mc2, ga);
 }
 
-template <int BN>
+template <int BN, int CL>
 cudaError_t dispatch_major(const GemmArgs& g, cudaStream_t st) {
   if (g.a_kmajor)
-    return g.b_kmajor ? launch_tc<BN, true, true>(g, st) : launch_tc<BN, true, false>(g, st);
-  return g.b_kmajor ? launch_tc<BN, false, true>(g, st) : launch_tc<BN, false, false>(g, st);
+    return g.b_kmajor ? launch_tc<BN, true, true, CL>(g, st) : launch_tc<BN, true, false, CL>(g, st);
+  return g.b_kmajor ? launch_tc<BN, false, true, CL>(g, st) : launch_tc<BN, false, false, CL>(g, st);
 }
 
 }  // namespace
@@ -425,14 +628,20 @@ bool gemm_tc_supported(const GemmArgs& g) {
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
   const int tiles256 = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
-  if (g.N <= 128 || tiles256 < num_sms()) return dispatch_major<128>(g, st);
-  return dispatch_major<256>(g, st);
+  const bool pair = g.M > BM;  // a second row block exists for the cluster partner
+  if (g.N <= 128 || tiles256 < num_sms())
+    return pair ? dispatch_major<128, 2>(g, st) : dispatch_major<128, 1>(g, st);
+  return pair ? dispatch_major<256, 2>(g, st) : dispatch_major<256, 1>(g, st);
 }
 
 cudaError_t gemm(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (gemm_tc_supported(g)) return gemm_tc(g, st);
   return gemm_simt(g, st);
+}
+
+cudaError_t gemm_set_timeline(unsigned long long* p) {
+  return cudaMemcpyToSymbol(g_gemm_timeline, &p, sizeof(p));
 }
 
 int gemm_read_and_clear_error() {

@@ -129,3 +129,32 @@ def test_tensor_core_matches_simt_bf16(L):
 
 def test_no_timeout_recorded(L):
     oz.oases_check_device(None)
+
+
+def test_gelu_accuracy_against_float64(L):
+    """GeLU and GeLU' of the epilogues (erf via Abramowitz & Stegun 7.1.26,
+    |error| <= 1.5e-7) against float64, through an fp32 K=1 product C = a * 1."""
+    from scipy.special import erf
+    a = np.concatenate([np.linspace(-9, 9, 4001), np.random.default_rng(0).normal(0, 2, 4000)])
+    M = a.size
+    A = torch.tensor(a, dtype=torch.float32).reshape(M, 1).cuda()
+    B = torch.ones(1, 1, dtype=torch.float32, device="cuda")
+    bias = torch.zeros(1, dtype=torch.float32, device="cuda")
+    a32 = A.double().cpu().numpy()[:, 0]
+    cdf = 0.5 * (1 + erf(a32 / np.sqrt(2)))
+    pdf = np.exp(-0.5 * a32 * a32) / np.sqrt(2 * np.pi)
+    C = torch.zeros(M, 1, dtype=torch.float32, device="cuda")
+    assert L.oases_debug_gemm(M, 1, 1, 0, A.data_ptr(), 1, 1, B.data_ptr(), 1, 1, 2, C.data_ptr(), 1,
+                              0, None, bias.data_ptr(), None, 0, 1, None) == 0
+    aux = A.clone()
+    D = torch.zeros(M, 1, dtype=torch.float32, device="cuda")
+    # GeLU': C = 1 * gelu'(aux)
+    ones = torch.ones(M, 1, dtype=torch.float32, device="cuda")
+    assert L.oases_debug_gemm(M, 1, 1, 0, ones.data_ptr(), 1, 1, B.data_ptr(), 1, 1, 4, D.data_ptr(), 1,
+                              0, None, None, aux.data_ptr(), 1, 1, None) == 0
+    torch.cuda.synchronize()
+    g = C.double().cpu().numpy()[:, 0]
+    d = D.double().cpu().numpy()[:, 0]
+    assert np.max(np.abs(g - a32 * cdf)) <= 1e-6 * np.maximum(1, np.abs(a32)).max()
+    assert np.max(np.abs(g - a32 * cdf) / np.maximum(1, np.abs(a32))) <= 3e-7
+    assert np.max(np.abs(d - (cdf + a32 * pdf)) / np.maximum(1, np.abs(a32))) <= 4e-7
