@@ -71,6 +71,17 @@ oases_status oases_debug_attention_progress(int *host_mapped);
 oases_status oases_debug_gemm_timeline(unsigned long long *device_buffer);
 int oases_debug_attention_error_word(void);
 
+/* Per-operator timeline of the block scheduler (debugging aid).  With
+ * tracing on, every following block call records a timing event before and
+ * after each scheduled step (Algorithm 1 operator of one sub-batch) on that
+ * sub-batch's stream.  oases_debug_trace_read synchronizes those events and
+ * writes 6 doubles per step into out: event, operator, segment, sub-batch,
+ * start and end in microseconds from the first step's start; it returns the
+ * number of steps of the last call (entries beyond cap are not written), or
+ * -1 on a CUDA error.  Tracing adds two event records per step. */
+void oases_debug_trace_enable(int on);
+int oases_debug_trace_read(double *out, int cap);
+
 /* Bias gradient of a linear layer, as the block takes it: by Oases §IV,
  * Eq. (1) every shard's partial receives the same output gradient dY, and the
  * row-parallel bias (added once after the shard sum) gets

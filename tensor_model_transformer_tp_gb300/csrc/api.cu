@@ -51,6 +51,15 @@ using namespace oases;
 thread_local std::string t_last_error;
 thread_local int t_last_launches = 0;
 
+// Optional per-operator event timeline of the last call (debugging aid).
+struct TraceRec {
+  int ev, op, seg, sb;
+  cudaEvent_t e0, e1;
+};
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_trace_events;  // reused across calls
+
 enum Ev { EV_F = 0, EV_R = 1, EV_B = 2, EV_CF = 3, EV_CR = 4, EV_CB = 5, EV_SYNC = 6 };
 enum OpN { OP_LN = 0, OP_F = 1, OP_COL = 2, OP_ROW = 3, OP_G = 4 };
 enum SegKind { SEG_FFN = 0, SEG_ATTN = 1 };
@@ -686,9 +695,28 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
     ex.ok(cudaEventRecord(ev_in, ex.st[0]));
     ex.ok(cudaStreamWaitEvent(ex.st[1], ev_in, 0));
   }
+  g_trace.clear();
+  size_t tev = 0;
   if (s.M > 0)
     for (const Step& st : steps) {
+      TraceRec tr{st.ev, st.op, st.seg, st.sb, nullptr, nullptr};
+      if (g_trace_on) {
+        while (g_trace_events.size() < tev + 2) {
+          cudaEvent_t e;
+          if (cudaEventCreate(&e) != cudaSuccess) break;
+          g_trace_events.push_back(e);
+        }
+        if (g_trace_events.size() >= tev + 2) {
+          tr.e0 = g_trace_events[tev++];
+          tr.e1 = g_trace_events[tev++];
+          ex.ok(cudaEventRecord(tr.e0, ex.stream(st.sb)));
+        }
+      }
       ex.run(st);
+      if (tr.e1) {
+        ex.ok(cudaEventRecord(tr.e1, ex.stream(st.sb)));
+        g_trace.push_back(tr);
+      }
       if (ex.err != cudaSuccess) break;
     }
   if (two) {
@@ -937,4 +965,28 @@ extern "C" oases_status oases_debug_gemm_timeline(unsigned long long* device_buf
   cudaError_t e = oases::gemm_set_timeline(device_buffer);
   if (e != cudaSuccess) return cuda_fail(e);
   return OASES_OK;
+}
+
+extern "C" void oases_debug_trace_enable(int on) { g_trace_on = on != 0; }
+
+extern "C" int oases_debug_trace_read(double* out, int cap) {
+  if (g_trace.empty()) return 0;
+  for (const TraceRec& r : g_trace)
+    if (cudaEventSynchronize(r.e1) != cudaSuccess) return -1;
+  const cudaEvent_t t0 = g_trace.front().e0;
+  const int n = (int)g_trace.size();
+  for (int i = 0; i < n && i < cap; ++i) {
+    const TraceRec& r = g_trace[i];
+    float a = 0.f, b = 0.f;
+    cudaEventElapsedTime(&a, t0, r.e0);
+    cudaEventElapsedTime(&b, t0, r.e1);
+    double* o = out + 6 * i;
+    o[0] = r.ev;
+    o[1] = r.op;
+    o[2] = r.seg;
+    o[3] = r.sb;
+    o[4] = a * 1e3;
+    o[5] = b * 1e3;
+  }
+  return n;
 }

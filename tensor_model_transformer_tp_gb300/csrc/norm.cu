@@ -14,7 +14,7 @@
 namespace oases {
 namespace {
 
-constexpr int ROWS_PER_PART = 32;
+constexpr int ROWS_PER_PART = 8;  // rows per partial row of a column sum
 constexpr int WARPS = 8;
 constexpr int COLS_PER_THREAD = 2;
 constexpr int COL_THREADS = 256;
@@ -212,6 +212,118 @@ ln_bwd_colpass(const float* __restrict__ du, const T* __restrict__ x,
     }
 }
 
+// 4 consecutive elements as fp32 (16-byte fp32 or 8-byte bf16 access).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// LayerNorm backward for one block of ROWS_PER_PART rows (H % 4 == 0):
+//   phase 1, warp w: m1 = mean(du * gamma), m2 = mean(du * gamma * xhat) of row w;
+//   phase 2, threads over 4-column groups, rows in order:
+//     dx = rstd * (du * gamma - m1 - xhat * m2) (+ dres), and the block's
+//     partial column sums pg = sum du * xhat, pb = sum du.
+template <typename T>
+__global__ void __launch_bounds__(ROWS_PER_PART * 32)
+ln_bwd_fused(const float* __restrict__ du, const T* __restrict__ x, const float* __restrict__ mean,
+             const float* __restrict__ rstd, const T* __restrict__ gamma,
+             const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ pg,
+             float* __restrict__ pb, int M, int H) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float m1s[ROWS_PER_PART], m2s[ROWS_PER_PART];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int m0 = blockIdx.x * ROWS_PER_PART;
+  {
+    const int row = m0 + warp;
+    float s1 = 0.f, s2 = 0.f;
+    if (row < M) {
+      const float mu = mean[row], rs = rstd[row];
+      const float* dr = du + (int64_t)row * H;
+      const T* xr = x + (int64_t)row * H;
+#pragma unroll 4
+      for (int c = lane * 4; c < H; c += 128) {
+        const float4 d = ld4(dr + c), xv = ld4(xr + c), gv = ld4(gamma + c);
+        const float g0 = d.x * gv.x, g1 = d.y * gv.y, g2 = d.z * gv.z, g3 = d.w * gv.w;
+        s1 += (g0 + g1) + (g2 + g3);
+        s2 = fmaf(g0, (xv.x - mu) * rs, s2);
+        s2 = fmaf(g1, (xv.y - mu) * rs, s2);
+        s2 = fmaf(g2, (xv.z - mu) * rs, s2);
+        s2 = fmaf(g3, (xv.w - mu) * rs, s2);
+      }
+    }
+    s1 = warp_sum(s1);
+    s2 = warp_sum(s2);
+    if (lane == 0) {
+      m1s[warp] = s1 / H;
+      m2s[warp] = s2 / H;
+    }
+  }
+  __syncthreads();
+  const int rows = min(ROWS_PER_PART, M - m0);
+  for (int c = tid * 4; c < H; c += ROWS_PER_PART * 32 * 4) {
+    const float4 gv = ld4(gamma + c);
+    float4 ag = make_float4(0.f, 0.f, 0.f, 0.f), ab = ag;
+#pragma unroll 8
+    for (int r = 0; r < rows; ++r) {
+      const int row = m0 + r;
+      const float mu = mean[row], rs = rstd[row], a1 = m1s[r], a2 = m2s[r];
+      const int64_t o = (int64_t)row * H + c;
+      const float4 d = ld4(du + o), xv = ld4(x + o);
+      float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (dres) res = ld4(dres + o);
+      const float h0 = (xv.x - mu) * rs, h1 = (xv.y - mu) * rs, h2 = (xv.z - mu) * rs,
+                  h3 = (xv.w - mu) * rs;
+      st4(dx + o, make_float4(fmaf(rs, d.x * gv.x - a1 - h0 * a2, res.x),
+                              fmaf(rs, d.y * gv.y - a1 - h1 * a2, res.y),
+                              fmaf(rs, d.z * gv.z - a1 - h2 * a2, res.z),
+                              fmaf(rs, d.w * gv.w - a1 - h3 * a2, res.w)));
+      ag.x = fmaf(d.x, h0, ag.x);
+      ag.y = fmaf(d.y, h1, ag.y);
+      ag.z = fmaf(d.z, h2, ag.z);
+      ag.w = fmaf(d.w, h3, ag.w);
+      ab.x += d.x;
+      ab.y += d.y;
+      ab.z += d.z;
+      ab.w += d.w;
+    }
+    st4(pg + (int64_t)blockIdx.x * H + c, ag);
+    st4(pb + (int64_t)blockIdx.x * H + c, ab);
+  }
+}
+
+// Column sums of a block of ROWS_PER_PART rows, 4 columns per thread (N % 4 == 0).
+template <typename T>
+__global__ void __launch_bounds__(COL_THREADS)
+colsum_vec_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
+  const int c = (blockIdx.x * COL_THREADS + threadIdx.x) * 4;
+  if (c >= N) return;
+  const int m0 = blockIdx.y * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int m = m0; m < m1; ++m) {
+    const float4 v = ld4(in + (int64_t)m * ld + c);
+    a.x += v.x;
+    a.y += v.y;
+    a.z += v.z;
+    a.w += v.w;
+  }
+  st4(part + (int64_t)blockIdx.y * N + c, a);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(COL_THREADS)
 colsum_part_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __restrict__ part) {
@@ -233,9 +345,9 @@ colsum_part_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __
 }
 
 // out[n] += sum_b part[b, n] over b = 0 .. nb-1 in a fixed order: thread group g
-// (of 4) sums b = g, g+4, ... and the four group sums are added in order 0..3.
+// (of 8) sums b = g, g+8, ... and the eight group sums are added in order 0..7.
 // A second (part2, out2) pair is reduced by the same launch when given.
-constexpr int RED_COLS = 64, RED_GROUPS = 4;
+constexpr int RED_COLS = 32, RED_GROUPS = 8;
 __global__ void __launch_bounds__(RED_COLS * RED_GROUPS)
 part_reduce_kernel(const float* __restrict__ part, float* __restrict__ out,
                    const float* __restrict__ part2, float* __restrict__ out2, int nb, int N) {
@@ -264,6 +376,61 @@ part_reduce_kernel(const float* __restrict__ part, float* __restrict__ out,
     out[n] += t;
     if (part2) out2[n] += t2;
   }
+}
+
+// Two-level fixed-order column sum of nb partial rows [nb, N] (and optionally
+// a second array).  Level 1: CTA (x, g) sums rows 16g .. 16g+15 of each column
+// (four independent accumulators, combined in a fixed order) and writes the
+// result over row 16g — every row of the group is read before that write by
+// the same thread, so the update is in place.  Level 2 adds rows 0, 16, 32, ...
+// in order into out.
+constexpr int RED_ROWS = 16;
+__global__ void __launch_bounds__(256)
+part_reduce_l1(float* __restrict__ part, float* __restrict__ part2, int nb, int N) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = blockIdx.x * 256 + threadIdx.x;
+  if (n >= N) return;
+  const int r0 = blockIdx.y * RED_ROWS, r1 = min(nb, r0 + RED_ROWS);
+  for (int a = 0; a < (part2 ? 2 : 1); ++a) {
+    float* p = a == 0 ? part : part2;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int r = r0;
+    for (; r + 4 <= r1; r += 4) {
+      s0 += p[(int64_t)r * N + n];
+      s1 += p[(int64_t)(r + 1) * N + n];
+      s2 += p[(int64_t)(r + 2) * N + n];
+      s3 += p[(int64_t)(r + 3) * N + n];
+    }
+    for (; r < r1; ++r) s0 += p[(int64_t)r * N + n];
+    p[(int64_t)r0 * N + n] = (s0 + s1) + (s2 + s3);
+  }
+}
+__global__ void __launch_bounds__(256)
+part_reduce_l2(const float* __restrict__ part, float* __restrict__ out,
+               const float* __restrict__ part2, float* __restrict__ out2, int nb, int N) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = blockIdx.x * 256 + threadIdx.x;
+  if (n >= N) return;
+  float s = 0.f, s2 = 0.f;
+#pragma unroll 4
+  for (int r = 0; r < nb; r += RED_ROWS) {
+    s += part[(int64_t)r * N + n];
+    if (part2) s2 += part2[(int64_t)r * N + n];
+  }
+  out[n] += s;
+  if (part2) out2[n] += s2;
+}
+
+cudaError_t reduce_parts(float* part, float* out, float* part2, float* out2, int nb, int N,
+                         cudaStream_t st) {
+  const int gx = (N + 255) / 256;
+  cudaError_t e = launch_pdl(part_reduce_l1, dim3(gx, (nb + RED_ROWS - 1) / RED_ROWS), dim3(256),
+                             0, st, part, part2, nb, N);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(part_reduce_l2, dim3(gx), dim3(256), 0, st, (const float*)part, out,
+                    (const float*)part2, out2, nb, N);
 }
 
 template <typename T>
@@ -338,6 +505,24 @@ cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, co
                            float* part_b, float2* stat, float* dgamma, float* dbeta, int M, int H,
                            DType t, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
+  const bool vec = H % 4 == 0 && (((uintptr_t)du | (uintptr_t)x | (uintptr_t)gamma |
+                                   (uintptr_t)dres | (uintptr_t)dx) & 7) == 0 &&
+                   (t == DType::BF16 || ((uintptr_t)du | (uintptr_t)x | (uintptr_t)gamma |
+                                         (uintptr_t)dres | (uintptr_t)dx) % 16 == 0);
+  if (vec) {
+    const int nb = ln_bwd_blocks(M);
+    cudaError_t e;
+    if (t == DType::F32)
+      e = launch_pdl(ln_bwd_fused<float>, dim3(nb), dim3(ROWS_PER_PART * 32), 0, st, du,
+                     (const float*)x, mean, rstd, (const float*)gamma, (const float*)dres,
+                     (float*)dx, part_g, part_b, M, H);
+    else
+      e = launch_pdl(ln_bwd_fused<__nv_bfloat16>, dim3(nb), dim3(ROWS_PER_PART * 32), 0, st, du,
+                     (const __nv_bfloat16*)x, mean, rstd, (const __nv_bfloat16*)gamma,
+                     (const __nv_bfloat16*)dres, (__nv_bfloat16*)dx, part_g, part_b, M, H);
+    if (e != cudaSuccess) return e;
+    return reduce_parts(part_g, dgamma, part_b, dbeta, nb, H, st);
+  }
   if (t == DType::F32)
     return ln_bwd_t<float>(du, x, mean, rstd, gamma, dres, dx, part_g, part_b, stat, dgamma,
                            dbeta, M, H, st);
@@ -351,16 +536,23 @@ cudaError_t colsum_accum(const void* in, int64_t ld, int M, int N, DType t, floa
   const int nb = colsum_blocks(M);
   const dim3 pgrid((N + COLS_PER_CTA - 1) / COLS_PER_CTA, nb);
   cudaError_t e;
-  if (t == DType::F32)
+  const size_t esz = t == DType::F32 ? 4 : 2;
+  if (N % 4 == 0 && ld % 4 == 0 && ((uintptr_t)in % (4 * esz)) == 0) {
+    const dim3 vgrid((N + 4 * COL_THREADS - 1) / (4 * COL_THREADS), nb);
+    if (t == DType::F32)
+      e = launch_pdl(colsum_vec_kernel<float>, vgrid, dim3(COL_THREADS), 0, st, (const float*)in,
+                     ld, M, N, part);
+    else
+      e = launch_pdl(colsum_vec_kernel<__nv_bfloat16>, vgrid, dim3(COL_THREADS), 0, st,
+                     (const __nv_bfloat16*)in, ld, M, N, part);
+  } else if (t == DType::F32)
     e = launch_pdl(colsum_part_kernel<float>, pgrid, dim3(COL_THREADS), 0, st, (const float*)in,
                    ld, M, N, part);
   else
     e = launch_pdl(colsum_part_kernel<__nv_bfloat16>, pgrid, dim3(COL_THREADS), 0, st,
                    (const __nv_bfloat16*)in, ld, M, N, part);
   if (e != cudaSuccess) return e;
-  return launch_pdl(part_reduce_kernel, dim3((N + RED_COLS - 1) / RED_COLS),
-                    dim3(RED_COLS * RED_GROUPS), 0, st, (const float*)part, out,
-                    (const float*)nullptr, (float*)nullptr, nb, N);
+  return reduce_parts(part, out, nullptr, nullptr, nb, N, st);
 }
 
 cudaError_t add_into(const void* a, const float* b, void* out, int64_t n, DType t,
