@@ -41,20 +41,20 @@ constexpr int BQ = 128, BKV = 128;     // query rows per CTA, keys per block
 constexpr int BOX = 128 * 64 * 2;      // one TMA box: 128 rows x 64 bf16 (16 KB)
 constexpr int TILE = 2 * BOX;          // 128 rows x 128 bf16 (32 KB)
 constexpr int KV_STAGES = 2;
-// shared-memory map (offsets from a 1024-aligned base)
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;                  // KV_STAGES tiles
-constexpr int OFF_V = OFF_K + KV_STAGES * TILE;      // KV_STAGES tiles
-constexpr int OFF_P = OFF_V + KV_STAGES * TILE;      // 2 tiles (double-buffered P)
-constexpr int OFF_BAR = OFF_P + 2 * TILE;
-constexpr int NBAR = 1 + 2 * KV_STAGES + 2 + 2 + 1;  // q, K full, V full, s, pv, drain
-constexpr int FWD_SMEM = OFF_BAR + 8 * NBAR + 16 + 1024;
 constexpr int NT = 128;
 
 // S = Q K^T: M = 128 queries, N = 128 keys, both operands K-major (over d).
 constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BQ, BKV, false, false);
 // O = P V: M = 128 queries, N = 128 dims; P K-major (over keys), V MN-major.
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BQ, D, false, true);
+
+// 2^x on the hardware unit (relative error ~2^-22); results below the
+// normal range, including 2^-inf for masked keys, are flushed to 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -93,20 +93,32 @@ struct FwdArgs {
   float scale_log2;    // log2(e) / sqrt(d)
 };
 
+// Forward shared-memory map: Q, two K stages, three V stages, one P tile.
+constexpr int F_KST = 2, F_VST = 3;
+constexpr int F_OFF_Q = 0, F_OFF_K = TILE, F_OFF_V = F_OFF_K + F_KST * TILE;
+constexpr int F_OFF_P = F_OFF_V + F_VST * TILE, F_OFF_BAR = F_OFF_P + TILE;
+constexpr int F_NBAR = 1 + F_KST + F_VST + 2 + 2 + 1;  // q, K, V, s, pv, drain
+constexpr int FWD_SMEM = F_OFF_BAR + 8 * F_NBAR + 16 + 1024;
+// A row's reference maximum (log2 units) is raised only when the running
+// maximum exceeds it by more than this: P = exp2(s - m_ref) <= 256 stays exact
+// in fp32 and representable in bf16, and O (accumulated in TMEM) is rescaled
+// only on those rare occasions.
+constexpr float RESCALE_LOG2 = 8.f;
+
 __global__ void __launch_bounds__(NT, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + OFF_BAR;
+  const uint32_t bars = base + F_OFF_BAR;
   const uint32_t bar_q = bars;
   auto bar_k = [&](int s) { return bars + 8u * (1 + s); };
-  auto bar_v = [&](int s) { return bars + 8u * (1 + KV_STAGES + s); };
-  auto bar_s = [&](int i) { return bars + 8u * (1 + 2 * KV_STAGES + i); };
-  auto bar_pv = [&](int i) { return bars + 8u * (3 + 2 * KV_STAGES + i); };
-  const uint32_t bar_drain = bars + 8u * (5 + 2 * KV_STAGES);
-  const uint32_t tslot = bars + 8u * NBAR;
+  auto bar_v = [&](int s) { return bars + 8u * (1 + F_KST + s); };
+  auto bar_s = [&](int i) { return bars + 8u * (1 + F_KST + F_VST + i); };
+  auto bar_pv = [&](int i) { return bars + 8u * (3 + F_KST + F_VST + i); };
+  const uint32_t bar_drain = bars + 8u * (5 + F_KST + F_VST);
+  const uint32_t tslot = bars + 8u * F_NBAR;
 
   const int tid = threadIdx.x, warp = tid / 32;
   const int tile = gridDim.x - 1 - blockIdx.x;  // heavy (late) query tiles first
@@ -119,10 +131,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
 
   if (tid == 0) {
     ptx::mbar_init(bar_q, 1);
-    for (int s = 0; s < KV_STAGES; ++s) {
-      ptx::mbar_init(bar_k(s), 1);
-      ptx::mbar_init(bar_v(s), 1);
-    }
+    for (int s = 0; s < F_KST; ++s) ptx::mbar_init(bar_k(s), 1);
+    for (int s = 0; s < F_VST; ++s) ptx::mbar_init(bar_v(s), 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar_s(i), 1);
       ptx::mbar_init(bar_pv(i), 1);
@@ -140,37 +150,36 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
   const uint32_t t_s[2] = {tmem, tmem + 128};
-  const uint32_t t_pv[2] = {tmem + 256, tmem + 384};
+  const uint32_t t_o = tmem + 256;
   progress(0, 2);
   pdl_wait();
   pdl_trigger();
   progress(0, 3);
 
-  // Thread 0 issues every TMA load and MMA.  Loads in flight per stage are
-  // tracked (bit s of k_issued / v_issued, parity in k_par / v_par) so that a
-  // CTA that stops early can wait for them before it exits.
+  // Thread 0 issues every TMA load and MMA; loads in flight per stage are
+  // tracked (issued bit, parity) so that a CTA that stops early waits for them.
   bool ok = true;
   uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
   auto load_k = [&](int j) {
-    const int s = j % KV_STAGES;
+    const int s = j % F_KST;
     ptx::mbar_arrive_expect_tx(bar_k(s), TILE);
-    const uint32_t kt = base + OFF_K + s * TILE;
+    const uint32_t kt = base + F_OFF_K + s * TILE;
     ptx::tma_load_2d(kt, &tm, bar_k(s), col_k, row0 + j * BKV);
     ptx::tma_load_2d(kt + BOX, &tm, bar_k(s), col_k + 64, row0 + j * BKV);
     k_issued |= 1u << s;
-    k_par = (k_par & ~(1u << s)) | ((uint32_t)((j / KV_STAGES) & 1) << s);
+    k_par = (k_par & ~(1u << s)) | ((uint32_t)((j / F_KST) & 1) << s);
   };
   auto load_v = [&](int j) {
-    const int s = j % KV_STAGES;
+    const int s = j % F_VST;
     ptx::mbar_arrive_expect_tx(bar_v(s), TILE);
-    const uint32_t vt = base + OFF_V + s * TILE;
+    const uint32_t vt = base + F_OFF_V + s * TILE;
     ptx::tma_load_2d(vt, &tm, bar_v(s), col_v, row0 + j * BKV);
     ptx::tma_load_2d(vt + BOX, &tm, bar_v(s), col_v + 64, row0 + j * BKV);
     v_issued |= 1u << s;
-    v_par = (v_par & ~(1u << s)) | ((uint32_t)((j / KV_STAGES) & 1) << s);
+    v_par = (v_par & ~(1u << s)) | ((uint32_t)((j / F_VST) & 1) << s);
   };
   auto issue_s = [&](int j) {  // K_j must have landed
-    const uint32_t qt = base + OFF_Q, kt = base + OFF_K + (j % KV_STAGES) * TILE;
+    const uint32_t qt = base + F_OFF_Q, kt = base + F_OFF_K + (j % F_KST) * TILE;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       ptx::mma_bf16(t_s[j & 1], kmajor_desc(qt, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
@@ -179,12 +188,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
 
   if (tid == 0) {
     ptx::mbar_arrive_expect_tx(bar_q, TILE);
-    ptx::tma_load_2d(base + OFF_Q, &tm, bar_q, col_q, row0 + q0);
-    ptx::tma_load_2d(base + OFF_Q + BOX, &tm, bar_q, col_q + 64, row0 + q0);
-    for (int j = 0; j < KV_STAGES && j < nkv; ++j) {
-      load_k(j);
-      load_v(j);
-    }
+    ptx::tma_load_2d(base + F_OFF_Q, &tm, bar_q, col_q, row0 + q0);
+    ptx::tma_load_2d(base + F_OFF_Q + BOX, &tm, bar_q, col_q + 64, row0 + q0);
+    for (int j = 0; j < F_KST && j < nkv; ++j) load_k(j);
+    for (int j = 0; j < F_VST && j < nkv; ++j) load_v(j);
     ok = ptx::mbar_wait(bar_q, 0) && ptx::mbar_wait(bar_k(0), 0);
     if (ok) {
       ptx::tc_fence_after();
@@ -193,71 +200,78 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   }
 
   const int qi = q0 + tid;  // this thread's query position
-  float O[D];
-#pragma unroll
-  for (int c = 0; c < D; ++c) O[c] = 0.f;
-  float m2 = -INFINITY, l = 0.f, corr_prev = 1.f;
+  float m_ref = -INFINITY, l = 0.f;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   bool done_all = true;
 
   for (int j = 0; j < nkv; ++j) {
     // (1) S_{j+1} overlaps this block's softmax
     if (tid == 0 && ok && j + 1 < nkv) {
-      ok = ptx::mbar_wait(bar_k((j + 1) % KV_STAGES), ((j + 1) / KV_STAGES) & 1);
+      ok = ptx::mbar_wait(bar_k((j + 1) % F_KST), ((j + 1) / F_KST) & 1);
       if (ok) {
         ptx::tc_fence_after();
         issue_s(j + 1);
       }
     }
-    // (2) row max of S_j; afterwards K stage j % 2 is free for K_{j+2}
+    // (2) S_j ready.  In issue order S_j follows PV_{j-2}, so PV_{j-2} is done:
+    //     K stage j % 2 (S_j) and V stage (j-2) % 3 (PV_{j-2}) are free.
     if (!ptx::mbar_wait(bar_s(j & 1), (j >> 1) & 1)) ok = false;
     ptx::tc_fence_after();
-    if (tid == 0 && ok && j + 2 < nkv) load_k(j + 2);
+    if (tid == 0 && ok) {
+      if (j + 2 < nkv) load_k(j + 2);
+      if (j + 1 < nkv && j + 1 >= F_VST) load_v(j + 1);
+    }
     const int kbase = j * BKV;
+    float sv[BKV];
+#pragma unroll
+    for (int c0 = 0; c0 < BKV; c0 += 32)
+      ptx::tmem_ld32(t_s[j & 1] + lane_off + c0, *reinterpret_cast<float(*)[32]>(sv + c0));
     float mx = -INFINITY;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BKV; c0 += 32) {
-      float v[32];
-      ptx::tmem_ld32(t_s[j & 1] + lane_off + c0, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int key = kbase + c0 + i;
-        const bool valid = key < a.S && (!a.causal || key <= qi);
-        if (valid) mx = fmaxf(mx, v[i] * a.scale_log2);
+    for (int i = 0; i < BKV; ++i) {
+      const int key = kbase + i;
+      const bool valid = key < a.S && (!a.causal || key <= qi);
+      sv[i] = valid ? sv[i] * a.scale_log2 : -INFINITY;
+      mx = fmaxf(mx, sv[i]);
+    }
+    const float m_new = fmaxf(m_ref, mx);
+    // (3) reference maximum
+    if (j == 0) {
+      m_ref = m_new;
+    } else {
+      const bool need = m_new > m_ref + RESCALE_LOG2;
+      if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are collective
+        if (!ptx::mbar_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
+        ptx::tc_fence_after();
+        const float f = need ? exp2f(m_ref - m_new) : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float v[32];
+          ptx::tmem_ld32(t_o + lane_off + c0, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= f;
+          ptx::tmem_st32(t_o + lane_off + c0, v);
+        }
+        if (need) {
+          l *= f;
+          m_ref = m_new;
+        }
       }
     }
-    const float m_new = fmaxf(m2, mx);
-    const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m2 - m_new);
-    // (3) PV_{j-1} complete: fold it into O; its V stage takes V_{j+1}
-    if (j >= 1) {
-      if (!ptx::mbar_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
-      ptx::tc_fence_after();
-      if (tid == 0 && ok && j + 1 < nkv) load_v(j + 1);
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(t_pv[(j - 1) & 1] + lane_off + c0, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) O[c0 + i] = fmaf(O[c0 + i], corr_prev, v[i]);
-      }
-    }
-    // (4) P_j = exp2(s - m_new) as bf16 into the swizzled P buffer (j & 1)
+    // (4) P_j = exp2(s - m_ref) into the P buffer, free once PV_{j-1} is done
+    if (j >= 1 && !ptx::mbar_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
     float rs = 0.f;
-    const uint32_t pbuf = OFF_P + (j & 1) * TILE;
-#pragma unroll 1
+    const bool live = m_ref != -INFINITY;
+#pragma unroll
     for (int c0 = 0; c0 < BKV; c0 += 32) {
       float v[32];
-      ptx::tmem_ld32(t_s[j & 1] + lane_off + c0, v);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int key = kbase + c0 + i;
-        const bool valid = key < a.S && (!a.causal || key <= qi) && m_new != -INFINITY;
-        const float p = valid ? exp2f(v[i] * a.scale_log2 - m_new) : 0.f;
+        const float p = live ? fast_exp2(sv[c0 + i] - m_ref) : 0.f;  // masked keys: exp2(-inf) = 0
         v[i] = p;
         rs += p;
       }
-      // 32 keys = 4 16-byte units of this row in chunk c0 / 64
-      uint8_t* rowp = gbase + pbuf + (c0 >> 6) * BOX + tid * 128;
+      uint8_t* rowp = gbase + F_OFF_P + (c0 >> 6) * BOX + tid * 128;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int unit = ((c0 & 63) >> 3) + u;
@@ -267,10 +281,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         *reinterpret_cast<uint4*>(rowp + ((unit ^ (tid & 7)) << 4)) = w;
       }
     }
-    l = l * corr + rs;
-    m2 = m_new;
-    corr_prev = corr;
-    // (5) make P visible to the tensor core; all threads decide together
+    l += rs;
+    // (5) make P (and any rescaled O) visible to the tensor core; all threads decide together
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     ptx::tc_fence_before();
     if (__syncthreads_or(!ok)) {
@@ -278,49 +290,49 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
       break;
     }
     if (tid == 0) {
-      ok = ptx::mbar_wait(bar_v(j % KV_STAGES), (j / KV_STAGES) & 1);
+      ok = ptx::mbar_wait(bar_v(j % F_VST), (j / F_VST) & 1);
       if (ok) {
         ptx::tc_fence_after();
-        const uint32_t pt = base + pbuf, vt = base + OFF_V + (j % KV_STAGES) * TILE;
+        const uint32_t pt = base + F_OFF_P, vt = base + F_OFF_V + (j % F_VST) * TILE;
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          ptx::mma_bf16(t_pv[j & 1], kmajor_desc(pt, kk), mnmajor_desc(vt, kk), IDESC_PV, kk > 0);
+          ptx::mma_bf16(t_o, kmajor_desc(pt, kk), mnmajor_desc(vt, kk), IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar_pv(j & 1));
       }
     }
   }
-  if (done_all && nkv >= 1) {  // fold the last PV
+  if (done_all && nkv >= 1) {
     const int j = nkv - 1;
     if (!ptx::mbar_wait(bar_pv(j & 1), (j >> 1) & 1)) ok = false;
     ptx::tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const bool store = ok && qi < a.S;
+    uint4* orow = reinterpret_cast<uint4*>(a.o + (int64_t)(row0 + qi) * a.H + h * D);
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       float v[32];
-      ptx::tmem_ld32(t_pv[j & 1] + lane_off + c0, v);
+      ptx::tmem_ld32(t_o + lane_off + c0, v);  // every lane: warp-collective
+      if (store) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) O[c0 + i] = fmaf(O[c0 + i], corr_prev, v[i]);
+        for (int u = 0; u < 4; ++u)
+          orow[c0 / 8 + u] = make_uint4(pack2(v[8 * u] * inv, v[8 * u + 1] * inv),
+                                        pack2(v[8 * u + 2] * inv, v[8 * u + 3] * inv),
+                                        pack2(v[8 * u + 4] * inv, v[8 * u + 5] * inv),
+                                        pack2(v[8 * u + 6] * inv, v[8 * u + 7] * inv));
+      }
     }
-  }
-  if (done_all && ok && qi < a.S) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint4* orow = reinterpret_cast<uint4*>(a.o + (int64_t)(row0 + qi) * a.H + h * D);
-#pragma unroll
-    for (int u = 0; u < D / 8; ++u)
-      orow[u] = make_uint4(pack2(O[8 * u] * inv, O[8 * u + 1] * inv),
-                           pack2(O[8 * u + 2] * inv, O[8 * u + 3] * inv),
-                           pack2(O[8 * u + 4] * inv, O[8 * u + 5] * inv),
-                           pack2(O[8 * u + 6] * inv, O[8 * u + 7] * inv));
-    a.lse[(int64_t)h * a.M + row0 + qi] = (m2 + log2f(l)) * 0.69314718055994531f;
+    if (store) a.lse[(int64_t)h * a.M + row0 + qi] = (m_ref + log2f(l)) * 0.69314718055994531f;
   }
   if (!(done_all && ok)) atomicExch(&g_attn_error, 1);
   if (tid == 0) {
     // drain: issued MMAs complete and issued loads land before the CTA exits
     ptx::mma_commit(bar_drain);
     bool dr = ptx::mbar_wait(bar_drain, 0);
-    for (int s = 0; s < KV_STAGES; ++s) {
+    for (int s = 0; s < F_KST; ++s)
       if ((k_issued >> s) & 1u) dr = ptx::mbar_wait(bar_k(s), (k_par >> s) & 1u) && dr;
+    for (int s = 0; s < F_VST; ++s)
       if ((v_issued >> s) & 1u) dr = ptx::mbar_wait(bar_v(s), (v_par >> s) & 1u) && dr;
-    }
     dr = ptx::mbar_wait(bar_q, 0) && dr;
     if (!dr) atomicExch(&g_attn_error, 2);
   }
@@ -478,7 +490,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       for (int i = 0; i < 32; ++i) {
         const int key = kbase + c0 + i;
         const bool valid = valid_q && key < a.S && (!a.causal || key <= qi);
-        const float p = valid ? exp2f(v[i] * a.scale_log2 - lse2) : 0.f;
+        const float p = valid ? fast_exp2(v[i] * a.scale_log2 - lse2) : 0.f;
         v[i] = p * (w[i] - dlt);
       }
       uint8_t* rowp = gbase + DQ_OFF_DS + (c0 >> 6) * BOX + tid * 128;
@@ -710,7 +722,7 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
       for (int c = 0; c < 32; ++c) {
         const int q = i * QB + c0 + c;
         const bool valid = valid_k && q < a.S && (!a.causal || kj <= q);
-        const float p = valid ? exp2f(v[c] * a.scale_log2 - lse_s[c0 + c]) : 0.f;
+        const float p = valid ? fast_exp2(v[c] * a.scale_log2 - lse_s[c0 + c]) : 0.f;
         v[c] = p;
         w[c] = p * (w[c] - dl_s[c0 + c]);
       }
