@@ -227,15 +227,18 @@ def dominant_kernel_roofline(blk, shape, pk, torch):
 
     for _ in range(5):
         launch()
-    times = []
+    # enqueue every (flush, start, kernel, end) first and synchronize once, so
+    # each event pair brackets GPU time only, not the host's submission
+    evs = []
     for _ in range(20):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
         launch()
         e1.record(st)
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1) * 1e-3)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    times = [a.elapsed_time(b) * 1e-3 for a, b in evs]
     t = sum(times) / len(times)
     fl = 2.0 * Ms * N * H
     achieved = fl / t / 1e12
@@ -261,6 +264,7 @@ def main():
     ap.add_argument("--recompute", default="fine", choices=["fine", "full", "none"])
     ap.add_argument("--sub-batches", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the step directly, not as a CUDA graph")
     args = ap.parse_args()
     from synth import SHAPES
     shape = SHAPES[args.workload]
@@ -298,16 +302,35 @@ def main():
     for _ in range(max(3, args.warmup)):
         blk.step(x, g, y, dx)
     launches = oases_last_launch_count()
+    # The timed step replays a CUDA graph captured from one oases_stack_step
+    # call: the same kernels, stream fork/join and programmatic dependencies,
+    # without the per-launch host cost.  Weight gradients keep accumulating.
+    graph = None
+    if not args.no_graph:
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        cap = blk.s0
+        with torch.cuda.stream(cap):
+            graph.capture_begin(capture_error_mode="relaxed")
+            blk.step(x, g, y, dx)
+            graph.capture_end()
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
     barrier()
     with ClockSampler(local) as clk:
         evs = []
         for _ in range(args.steps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(blk.s0)
-            blk.step(x, g, y, dx)
+            if graph is not None:
+                with torch.cuda.stream(blk.s0):
+                    graph.replay()
+            else:
+                blk.step(x, g, y, dx)
             e1.record(blk.s0)
             evs.append((e0, e1))
-            flush.zero_()
+            with torch.cuda.stream(blk.s0):
+                flush.zero_()
         barrier()
     t_step = sum(a.elapsed_time(b) for a, b in evs) * 1e-3 / args.steps
     if world > 1:
@@ -345,6 +368,7 @@ def main():
                       "heads": shape.heads, "w": shape.w, "sub_batches": shape.sub_batches,
                       "n_layers": shape.n_layers, "recompute": args.recompute,
                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                      "launch": "cuda-graph" if not args.no_graph else "direct",
                       "l2": "flushed between timed steps (256 MiB write)"},
            "pct_bf16_peak": 100.0 * value / world / pk["bf16_tflops_sustained"],
            "e2e": {"value": fl / t_e2e / 1e12 * world, "unit": "TFLOP/s",
