@@ -265,6 +265,8 @@ def main():
     ap.add_argument("--sub-batches", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the step directly, not as a CUDA graph")
+    ap.add_argument("--reduce", default="fused", choices=["fused", "separate"],
+                    help="shard sums fused into the GEMMs or as separate reduction kernels")
     args = ap.parse_args()
     from synth import SHAPES
     shape = SHAPES[args.workload]
@@ -288,7 +290,7 @@ def main():
     build_library()
     inp = block_inputs(shape, seed=0)
     blk = DeviceBlock(shape, inp["layers"], recompute=args.recompute,
-                      device="cuda:%d" % local)
+                      device="cuda:%d" % local, reduce=args.reduce)
     x, g = blk.tensor(inp["x"]), blk.tensor(inp["g"])
     y, dx = blk.empty_like_io(), blk.empty_like_io()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -367,6 +369,7 @@ def main():
                       "seq": shape.seq, "hidden": shape.hidden, "ffn": shape.ffn,
                       "heads": shape.heads, "w": shape.w, "sub_batches": shape.sub_batches,
                       "n_layers": shape.n_layers, "recompute": args.recompute,
+                      "reduce": args.reduce,
                       "parallelism": "replicas" if world > 1 else "single-gpu",
                       "launch": "cuda-graph" if not args.no_graph else "direct",
                       "l2": "flushed between timed steps (256 MiB write)"},

@@ -77,6 +77,16 @@ typedef enum { OASES_F32 = 0, OASES_BF16 = 1 } oases_dtype;
  *       part only: C_i(R) and the row GEMM feeding it are not recomputed
  *       (Oases §IV, Eq. (1), Fig. 4d). */
 typedef enum { OASES_RECOMPUTE_NONE = 0, OASES_RECOMPUTE_FULL = 1, OASES_RECOMPUTE_FINE = 2 } oases_recompute;
+/* How the shard sums C_i(F) (and C_i(R)) and C_i(B) are formed (Oases §IV,
+ * Eq. (1): y = sum_k P_k over the w shards).
+ * FUSED:    the row GEMM contracts over every shard's K-slice into one TMEM
+ *           accumulator (and the input-gradient GEMM likewise), so the sum
+ *           never leaves the chip.
+ * SEPARATE: each shard's partial P_k (its own K-slice only) is written to HBM
+ *           as fp32, and a separate memory-bound reduction kernel forms the
+ *           sum at the communication step — the on-device analogue of the
+ *           AllReduce, which one sub-batch runs while the other computes. */
+typedef enum { OASES_REDUCE_FUSED = 0, OASES_REDUCE_SEPARATE = 1 } oases_reduce;
 
 typedef struct {
   int32_t kind;         /* oases_block_kind */
@@ -92,6 +102,7 @@ typedef struct {
   int32_t residual;     /* 1: y = segment(x) + x */
   int32_t causal;       /* 1: causal attention mask (key j visible from query i iff j <= i) */
   int32_t recompute;    /* oases_recompute */
+  int32_t reduce;       /* oases_reduce */
   float ln_eps;         /* LayerNorm epsilon (biased variance) */
 } oases_block_desc;
 

@@ -24,6 +24,7 @@ STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA"
 KIND = {"ffn": 0, "attn": 1, "layer": 2}
 DTYPE = {"f32": 0, "bf16": 1}
 RECOMPUTE = {"none": 0, "full": 1, "fine": 2}
+REDUCE = {"fused": 0, "separate": 1}
 EVENTS = ["F", "R", "B", "C(F)", "C(R)", "C(B)", "Sync"]
 OPS = ["ln", "f", "col", "row", "g"]
 PARAM_NAMES = ("ln1_g", "ln1_b", "wqkv", "bqkv", "wo", "bo",
@@ -39,7 +40,7 @@ class OasesError(RuntimeError):
 class BlockDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kind", "dtype", "batch", "seq", "hidden", "ffn", "heads", "w", "sub_batches",
-                 "pre_ln", "residual", "causal", "recompute")] + [("ln_eps", ctypes.c_float)]
+                 "pre_ln", "residual", "causal", "recompute", "reduce")] + [("ln_eps", ctypes.c_float)]
 
 
 class Weights(ctypes.Structure):
@@ -111,17 +112,19 @@ def _check(st: int) -> None:
 def make_desc(kind: str, dtype: str, batch: int, seq: int, hidden: int, ffn: int = 0,
               heads: int = 0, w: int = 1, sub_batches: int = 2, pre_ln: bool = True,
               residual: bool = True, causal: bool = True, recompute: str = "fine",
-              eps: float = 1e-5) -> BlockDesc:
+              eps: float = 1e-5, reduce: str = "fused") -> BlockDesc:
     return BlockDesc(KIND[kind], DTYPE[dtype], batch, seq, hidden, ffn, heads, w, sub_batches,
-                     int(pre_ln), int(residual), int(causal), RECOMPUTE[recompute], eps)
+                     int(pre_ln), int(residual), int(causal), RECOMPUTE[recompute], REDUCE[reduce],
+                     eps)
 
 
-def desc_from_shape(shape, recompute: str = "fine", sub_batches: Optional[int] = None) -> BlockDesc:
+def desc_from_shape(shape, recompute: str = "fine", sub_batches: Optional[int] = None,
+                    reduce: str = "fused") -> BlockDesc:
     """BlockDesc from any object with the BlockShape attributes."""
     return make_desc(shape.kind, shape.dtype, shape.batch, shape.seq, shape.hidden, shape.ffn,
                      shape.heads, shape.w,
                      shape.sub_batches if sub_batches is None else sub_batches,
-                     shape.pre_ln, shape.residual, shape.causal, recompute, shape.eps)
+                     shape.pre_ln, shape.residual, shape.causal, recompute, shape.eps, reduce)
 
 
 def weights_struct(params: Dict) -> Weights:

@@ -71,7 +71,7 @@ struct Step {
 };
 
 struct Shape {
-  int kind, B, S, H, F, nh, d, w, nsb, pre_ln, residual, causal, mode;
+  int kind, B, S, H, F, nh, d, w, nsb, pre_ln, residual, causal, mode, reduce;
   DType t;
   float eps;
   int64_t M, Ms;
@@ -90,6 +90,7 @@ oases_status validate(const oases_block_desc* d, int n_layers, Shape* s) {
     return OASES_ERR_INVALID_ARG;
   if (d->batch % d->sub_batches != 0) return OASES_ERR_INVALID_ARG;
   if (d->recompute < 0 || d->recompute > 2) return OASES_ERR_INVALID_ARG;
+  if (d->reduce < 0 || d->reduce > 1) return OASES_ERR_INVALID_ARG;
   if (!(d->ln_eps >= 0.f)) return OASES_ERR_INVALID_ARG;
   const bool has_ffn = d->kind != OASES_BLOCK_ATTN, has_attn = d->kind != OASES_BLOCK_FFN;
   if (has_ffn && (d->ffn <= 0 || d->ffn % d->w != 0)) return OASES_ERR_INVALID_ARG;
@@ -118,6 +119,7 @@ oases_status validate(const oases_block_desc* d, int n_layers, Shape* s) {
   s->residual = d->residual != 0;
   s->causal = d->causal != 0;
   s->mode = d->recompute;
+  s->reduce = d->reduce;
   s->t = d->dtype == OASES_F32 ? DType::F32 : DType::BF16;
   s->eps = d->ln_eps;
   s->M = M;
@@ -137,7 +139,8 @@ inline size_t up(size_t v) { return (v + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct ActSet {  // offsets relative to the workspace base
   size_t u = 0, mu = 0, rstd = 0, a = 0, h = 0, qkv = 0, o = 0, lse = 0, delta = 0, d_o = 0,
-         dqkv = 0, du = 0, cpart = 0, lpart_g = 0, lpart_b = 0, lstat = 0;
+         dqkv = 0, du = 0, cpart = 0, lpart_g = 0, lpart_b = 0, lstat = 0,
+         red = 0;  // separate-reduction partials, fp32 [w][M][H]
 };
 
 struct Layout {
@@ -191,6 +194,7 @@ Layout make_layout(const Shape& s) {
     a.lpart_g = take(s.nsb * L.lpart_n * 4);
     a.lpart_b = take(s.nsb * L.lpart_n * 4);
     a.lstat = take(M * 8);
+    if (s.reduce == OASES_REDUCE_SEPARATE) a.red = take((size_t)s.w * M * s.H * 4);
     return a;
   };
   L.act.resize(s.nseg);
@@ -428,6 +432,62 @@ struct Exec {
     ok(gemm(g, stream(b)));
   }
 
+  // SEPARATE mode: shard k's partial of sub-batch b, fp32 [Ms, H] rows of [w][M][H].
+  float* red_part(int seg, int k, int b) const {
+    return at<float>(L.act[seg].red) + ((size_t)k * s.M + (size_t)b * s.Ms) * s.H;
+  }
+  // P_k = hin[:, slice k] W_row[:, slice k]^T for every shard k (its K-slice
+  // only): one split-contraction launch over all shards where the tensor-core
+  // path takes it, else one GEMM per shard.
+  void row_partials(int seg, int b) {
+    const ActSet& a = L.act[seg];
+    const bool ffn = s.seg_kind(seg) == SEG_FFN;
+    const int Kin = ffn ? s.F : s.H, Kw = Kin / s.w;
+    const uint8_t* hin = reinterpret_cast<const uint8_t*>(
+        ffn ? rowp(at(a.h), b, s.F, s.esz) : rowp(at(a.o), b, s.H, s.esz));
+    const uint8_t* wr = reinterpret_cast<const uint8_t*>(sp[seg].wr);
+    GemmArgs all = base_gemm();
+    all.M = (int)s.Ms;
+    all.N = s.H;
+    all.K = Kw;
+    all.A = hin;
+    all.lda = Kin;
+    all.B = wr;
+    all.ldb = Kin;
+    all.epi = Epi::Store;
+    all.C = red_part(seg, 0, b);
+    all.c_t = DType::F32;
+    all.ldc = s.H;
+    all.splits = s.w;
+    all.k_extent = Kin;
+    all.c_split_rows = s.M;
+    if (gemm_tc_supported(all)) {
+      ok(gemm(all, stream(b)));
+      return;
+    }
+    for (int k = 0; k < s.w; ++k) {
+      GemmArgs g = base_gemm();
+      g.M = (int)s.Ms;
+      g.N = s.H;
+      g.K = Kw;
+      g.A = hin + (size_t)k * Kw * s.esz;
+      g.lda = Kin;
+      g.B = wr + (size_t)k * Kw * s.esz;
+      g.ldb = Kin;
+      g.epi = Epi::Store;
+      g.C = red_part(seg, k, b);
+      g.c_t = DType::F32;
+      g.ldc = s.H;
+      ok(gemm(g, stream(b)));
+    }
+  }
+  // y = sum_k P_k + bias (+ x): the C(F) / C(R) step in SEPARATE mode.
+  void reduce_rows(int seg, int b, void* out) {
+    ok(shard_sum(red_part(seg, 0, b), (int64_t)s.M * s.H, s.w, sp[seg].br,
+                 s.residual ? rowp(seg_in(seg), b, s.H, s.esz) : nullptr,
+                 rowp(out, b, s.H, s.esz), s.t, s.t, (int)s.Ms, s.H, stream(b)));
+  }
+
   float* cpart(int seg, int b) const {
     return at<float>(L.act[seg].cpart) + (size_t)b * L.cpart_n;
   }
@@ -539,6 +599,10 @@ struct Exec {
 
   // C_i(B): du = sum over shards of dcol_k W_col_k = dcol W_col (full-K contraction), fp32.
   void comm_bwd(int seg, int b) {
+    if (s.reduce == OASES_REDUCE_SEPARATE) {
+      comm_bwd_separate(seg, b);
+      return;
+    }
     const ActSet& a = L.act[seg];
     const bool ffn = s.seg_kind(seg) == SEG_FFN;
     const int Nc = ffn ? s.F : 3 * s.H;
@@ -556,6 +620,59 @@ struct Exec {
     g.c_t = DType::F32;
     g.ldc = s.H;
     ok(gemm(g, stream(b)));
+  }
+
+  // SEPARATE mode: du_k = dcol[:, cols of shard k] W_col[rows of shard k, :] in
+  // fp32 partials, then du = sum_k du_k.  An attention shard's columns are three
+  // ranges (its Q, K and V heads), accumulated into the same partial.
+  void comm_bwd_separate(int seg, int b) {
+    const ActSet& a = L.act[seg];
+    const bool ffn = s.seg_kind(seg) == SEG_FFN;
+    const int Nc = ffn ? s.F : 3 * s.H;
+    const uint8_t* dcol = reinterpret_cast<const uint8_t*>(
+        ffn ? rowp(at(a.a), b, s.F, s.esz) : rowp(at(a.dqkv), b, 3 * s.H, s.esz));
+    const uint8_t* wc = reinterpret_cast<const uint8_t*>(sp[seg].wc);
+    const int parts = ffn ? 1 : 3, Kw = ffn ? s.F / s.w : s.H / s.w;
+    GemmArgs all = base_gemm();
+    all.M = (int)s.Ms;
+    all.N = s.H;
+    all.K = parts * Kw;
+    all.kpieces = parts;
+    all.kpiece_stride = s.H;  // attention: the Q, K and V column blocks
+    all.k_extent = Nc;
+    all.A = dcol;
+    all.lda = Nc;
+    all.B = wc;
+    all.ldb = s.H;
+    all.b_kmajor = false;
+    all.epi = Epi::Store;
+    all.C = red_part(seg, 0, b);
+    all.c_t = DType::F32;
+    all.ldc = s.H;
+    all.splits = s.w;
+    all.c_split_rows = s.M;
+    const bool one_launch = gemm_tc_supported(all);
+    if (one_launch) ok(gemm(all, stream(b)));
+    for (int k = 0; k < s.w && !one_launch; ++k)
+      for (int p = 0; p < parts; ++p) {
+        const size_t c0 = (ffn ? 0 : (size_t)p * s.H) + (size_t)k * Kw;  // first column / W row
+        GemmArgs g = base_gemm();
+        g.M = (int)s.Ms;
+        g.N = s.H;
+        g.K = Kw;
+        g.A = dcol + c0 * s.esz;
+        g.lda = Nc;
+        g.B = wc + c0 * s.H * s.esz;
+        g.ldb = s.H;
+        g.b_kmajor = false;
+        g.epi = p == 0 ? Epi::Store : Epi::Accum;
+        g.C = red_part(seg, k, b);
+        g.c_t = DType::F32;
+        g.ldc = s.H;
+        ok(gemm(g, stream(b)));
+      }
+    ok(shard_sum(red_part(seg, 0, b), (int64_t)s.M * s.H, s.w, nullptr, nullptr,
+                 rowp(at<float>(a.du), b, s.H, 4), DType::F32, s.t, (int)s.Ms, s.H, stream(b)));
   }
 
   void bwd_ln(int seg, int b) {
@@ -583,12 +700,24 @@ struct Exec {
       case EV_F:
         if (st_.op == OP_LN) ln_fwd(seg, b);
         else if (st_.op == OP_COL) col_fwd(seg, b, s.mode == OASES_RECOMPUTE_NONE);
-        else if (st_.op == OP_ROW) row_fwd(seg, b, seg_out(seg));
+        else if (st_.op == OP_ROW) {
+          if (s.reduce == OASES_REDUCE_SEPARATE) row_partials(seg, b);
+          else row_fwd(seg, b, seg_out(seg));
+        }
+        break;
+      case EV_CF:
+        if (s.reduce == OASES_REDUCE_SEPARATE) reduce_rows(seg, b, seg_out(seg));
         break;
       case EV_R:
         if (st_.op == OP_LN) ln_fwd(seg, b);
         else if (st_.op == OP_COL) col_fwd(seg, b, true);
-        else if (st_.op == OP_ROW) row_fwd(seg, b, at(L.yr));
+        else if (st_.op == OP_ROW) {
+          if (s.reduce == OASES_REDUCE_SEPARATE) row_partials(seg, b);
+          else row_fwd(seg, b, at(L.yr));
+        }
+        break;
+      case EV_CR:
+        if (s.reduce == OASES_REDUCE_SEPARATE) reduce_rows(seg, b, at(L.yr));
         break;
       case EV_B:
         if (st_.op == OP_G) bwd_g(seg, b);
@@ -599,7 +728,7 @@ struct Exec {
       case EV_CB:
         comm_bwd(seg, b);
         break;
-      default:  // C(F), C(R): fused into the row GEMM; Sync: stream order
+      default:  // Sync: stream order
         break;
     }
   }

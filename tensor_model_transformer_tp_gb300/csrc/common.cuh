@@ -139,6 +139,13 @@ struct GemmArgs {
   int64_t ld_aux = 0;
   DType aux_t = DType::BF16;
   int tma_store = 0;  // set by the tensor-core path: outputs leave through TMA stores
+  // Split contraction (tensor-core path only, Epi::Store): `splits` independent
+  // products in one launch.  Product s contracts over kpieces ranges of K
+  // coordinates, piece p covering [p * kpiece_stride + s * K / kpieces, + K / kpieces)
+  // of A's and B's K axis (k_extent wide), and writes rows [s * c_split_rows, + M)
+  // of C.  splits = 1, kpieces = 1 is the plain GEMM.
+  int splits = 1, kpieces = 1;
+  int64_t kpiece_stride = 0, k_extent = 0, c_split_rows = 0;
 };
 
 // Returns cudaSuccess or the launch error.  Picks the tensor-core kernel when
@@ -173,6 +180,12 @@ cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, co
 int colsum_blocks(int M);
 cudaError_t colsum_accum(const void* in, int64_t ld, int M, int N, DType t, float* part,
                          float* out, cudaStream_t st);
+// Shard sum of the separate-reduction mode: out[m, n] = sum_{k<w} part[k][m, n]
+// (+ bias[n]) (+ resid[m, n]); part fp32 with pstride floats between shards;
+// bias / resid of type in_t, out of type out_t.  Fixed order k = 0, 1, ...
+cudaError_t shard_sum(const float* part, int64_t pstride, int w, const void* bias,
+                      const void* resid, void* out, DType out_t, DType in_t, int M, int N,
+                      cudaStream_t st);
 // y = x + a elementwise (n elements, type t); used for the residual gradient
 // when there is no LayerNorm.
 cudaError_t add_into(const void* a, const float* b, void* out, int64_t n, DType t,

@@ -160,8 +160,8 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int n, float
 template <int CW>
 __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorMap* tmC,
                                               const CUtensorMap* tmC2, uint8_t* stg,
-                                              uint32_t stg_s, int m, int mw, int n, int lane,
-                                              float (&v)[CW]) {
+                                              uint32_t stg_s, int m, int mw, int n, int z,
+                                              int lane, float (&v)[CW]) {
   const bool bf = g.c_t == DType::BF16;
   if (g.epi == Epi::Bias || g.epi == Epi::BiasGelu || g.epi == Epi::BiasResid) {
     const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(g.bias) + n;
@@ -219,6 +219,8 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
     if (lane == 0) {
       if (reduce)
         ptx::tma_reduce_add_2d(tm, stg_s, n, mw);
+      else if (g.splits > 1)
+        ptx::tma_store_3d(tm, stg_s, n, mw, z);
       else
         ptx::tma_store_2d(tm, stg_s, n, mw);
       ptx::bulk_commit();
@@ -263,10 +265,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int rank = CL > 1 ? (int)ptx::cluster_rank() : 0;
   const int num_m = (g.M + BM - 1) / BM, num_n = (g.N + BN - 1) / BN;
   const int num_mp = (num_m + CL - 1) / CL;  // row blocks of CL * 128 rows
-  const int tiles = num_mp * num_n, nkb = (g.K + BKE - 1) / BKE;
+  // tiles of split s are [s * tiles1, (s + 1) * tiles1); K blocks walk the
+  // pieces of that split's contraction range in order
+  const int tiles1 = num_mp * num_n, tiles = tiles1 * g.splits;
+  const int kpl = g.K / g.kpieces, nkb_p = (kpl + BKE - 1) / BKE, nkb = nkb_p * g.kpieces;
   const int first = blockIdx.x / CL, stride = gridDim.x / CL;
-  auto tile_m0 = [&](int t) { return ((t % num_mp) * CL + rank) * BM; };
-  auto tile_n0 = [&](int t) { return (t / num_mp) * BN; };
+  auto tile_split = [&](int t) { return t / tiles1; };
+  auto tile_m0 = [&](int t) { return (((t % tiles1) % num_mp) * CL + rank) * BM; };
+  auto tile_n0 = [&](int t) { return ((t % tiles1) / num_mp) * BN; };
   constexpr uint16_t MASK = (1u << CL) - 1u;
 
   if (threadIdx.x == 0) {
@@ -312,13 +318,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t issued = 0;  // bit s: stage s has a load outstanding at some phase
       uint32_t iphase = 0;  // bit s: parity of the last load issued into stage s
       for (int tile = first; tile < tiles && ok; tile += stride) {
-        const int m0 = tile_m0(tile), n0 = tile_n0(tile);
+        const int m0 = tile_m0(tile), n0 = tile_n0(tile), ks = tile_split(tile) * kpl;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!ptx::mbar_wait(empty(stage), phase ^ 1u)) { ok = false; break; }
           const uint32_t fb = full(stage);
           ptx::mbar_arrive_expect_tx(fb, C::STAGE);
           const uint32_t sa = base + stage * C::STAGE, sb = sa + C::A_BYTES;
-          const int k0 = kb * BKE;
+          const int pc = kb / nkb_p;
+          const int k0 = (int)(pc * g.kpiece_stride) + ks + (kb - pc * nkb_p) * BKE;
           if (A_K) {
             ptx::tma_load_2d(sa, &tmA, fb, k0, m0);
           } else {
@@ -406,7 +413,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       ptx::tc_fence_after();
       const int mw = tile_m0(tile) + q * 32, m = mw + lane;
-      const int nb0 = tile_n0(tile);
+      const int nb0 = tile_n0(tile), z = tile_split(tile);
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
       if (g.tma_store && g.c_t == DType::BF16) {
         uint8_t* stg = gbase + C::EPI_OFF + (warp - 2) * 4096;
@@ -417,7 +424,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ptx::tmem_ld32(trow + c0, *reinterpret_cast<float(*)[32]>(v));
           ptx::tmem_ld32(trow + c0 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
           if (mw < g.M && nb0 + c0 < g.N)
-            epi_tma_chunk<64>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, lane, v);
+            epi_tma_chunk<64>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, z, lane, v);
         }
       } else if (g.tma_store) {
         uint8_t* stg = gbase + C::EPI_OFF + (warp - 2) * 4096;
@@ -427,7 +434,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           float v[32];
           ptx::tmem_ld32(trow + c0, v);
           if (mw < g.M && nb0 + c0 < g.N)
-            epi_tma_chunk<32>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, lane, v);
+            epi_tma_chunk<32>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, z, lane, v);
         }
       } else {
 #pragma unroll 1
@@ -477,11 +484,12 @@ EncodeTiledFn encode_fn() {
 
 struct MapKey {
   uintptr_t ptr;
-  uint64_t inner, outer, ld;
+  uint64_t inner, outer, ld, depth, ld2;
   uint32_t box_inner, box_outer;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && inner == o.inner && outer == o.outer && ld == o.ld &&
-           box_inner == o.box_inner && box_outer == o.box_outer;
+           depth == o.depth && ld2 == o.ld2 && box_inner == o.box_inner &&
+           box_outer == o.box_outer;
   }
 };
 struct MapKeyHash {
@@ -490,19 +498,25 @@ struct MapKeyHash {
     h ^= k.inner + 0x9E37 + (h << 6) + (h >> 2);
     h ^= k.outer + 0x79B9 + (h << 6) + (h >> 2);
     h ^= k.ld + (h << 6) + (h >> 2);
+    h ^= (k.depth * 0x100000001B3ull ^ k.ld2) + (h << 6) + (h >> 2);
     h ^= ((uint64_t)k.box_inner << 32 | k.box_outer) + (h << 6) + (h >> 2);
     return h;
   }
 };
 
-// 2-D bf16 tensor map over a row-major [outer, inner] matrix with leading
-// dimension ld (elements), box [box_outer, box_inner], 128-byte swizzle,
-// out-of-bounds elements read as zero.  Cached by its arguments.
+// 2-D bf16 (or fp32) tensor map over a row-major [outer, inner] matrix with
+// leading dimension ld (elements), box [box_outer, box_inner], 128-byte
+// swizzle, out-of-bounds elements read as zero.  depth > 1 adds a third
+// dimension of `depth` such matrices, ld2 elements apart (box depth 1).
+// Cached by its arguments.
 bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_inner, uint32_t box_outer, bool f32 = false) {
+              uint32_t box_inner, uint32_t box_outer, bool f32 = false, uint64_t depth = 1,
+              uint64_t ld2 = 0) {
   static std::mutex mu;
   static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-  const MapKey key{(uintptr_t)ptr | (f32 ? 1u : 0u), inner, outer, ld, box_inner, box_outer};
+  if (depth < 1) depth = 1;
+  const MapKey key{(uintptr_t)ptr | (f32 ? 1u : 0u), inner, outer, ld, depth,
+                   depth > 1 ? ld2 : 0, box_inner, box_outer};
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -511,12 +525,14 @@ bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {ld * (f32 ? 4 : 2)};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
+  const uint64_t esz = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {inner, outer, depth};
+  const cuuint64_t strides[2] = {ld * esz, ld2 * esz};
+  const cuuint32_t box[3] = {box_inner, box_outer, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
-  if (fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  if (fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+         depth > 1 ? 3u : 2u,
          const_cast<void*>(ptr), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -542,10 +558,11 @@ template <int BN, bool A_K, bool B_K, int CL>
 cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
   using C = TcCfg<BN>;
   CUtensorMap ma, mb;
-  bool ok = A_K ? make_map(&ma, g.A, g.K, g.M, g.lda, BKE, BM)
-                : make_map(&ma, g.A, g.M, g.K, g.lda, 64, BKE);
-  ok = ok && (B_K ? make_map(&mb, g.B, g.K, g.N, g.ldb, BKE, BN / CL)
-                  : make_map(&mb, g.B, g.N, g.K, g.ldb, 64, BKE));
+  const uint64_t kext = g.k_extent > 0 ? (uint64_t)g.k_extent : (uint64_t)g.K;
+  bool ok = A_K ? make_map(&ma, g.A, kext, g.M, g.lda, BKE, BM)
+                : make_map(&ma, g.A, g.M, kext, g.lda, 64, BKE);
+  ok = ok && (B_K ? make_map(&mb, g.B, kext, g.N, g.ldb, BKE, BN / CL)
+                  : make_map(&mb, g.B, g.N, kext, g.ldb, 64, BKE));
   if (!ok) return cudaErrorInvalidValue;
   // outputs through TMA stores when C (and C2) rows are 16-byte multiples
   GemmArgs ga = g;
@@ -556,9 +573,11 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
                        (((uintptr_t)g.bias | (uintptr_t)g.aux) & 15) == 0 &&
                        (g.aux == nullptr || (g.ld_aux % 8 == 0 && g.aux_t == DType::BF16));
   ga.tma_store = 0;
-  if (aligned && make_map(&mc, g.C, g.N, g.M, g.ldc, cw, 32, f32c) &&
+  if (aligned && make_map(&mc, g.C, g.N, g.M, g.ldc, cw, 32, f32c, (uint64_t)g.splits,
+                          (uint64_t)(g.c_split_rows * g.ldc)) &&
       (g.C2 == nullptr || make_map(&mc2, g.C2, g.N, g.M, g.ldc, cw, 32, f32c)))
     ga.tma_store = 1;
+  if (g.splits > 1 && !ga.tma_store) return cudaErrorNotSupported;  // slabs need the 3-D map
   auto kern = gemm_tc_kernel<BN, A_K, B_K, CL>;
   static bool attr = false;
   if (!attr) {
@@ -567,7 +586,7 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
     attr = true;
   }
   const int num_mp = ((g.M + BM - 1) / BM + CL - 1) / CL;
-  const int tiles = num_mp * ((g.N + BN - 1) / BN);
+  const int tiles = num_mp * ((g.N + BN - 1) / BN) * g.splits;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
@@ -622,12 +641,22 @@ bool gemm_tc_supported(const GemmArgs& g) {
   if (g.lda % 8 != 0 || g.ldb % 8 != 0) return false;
   if ((((uintptr_t)g.A) | ((uintptr_t)g.B)) & 15) return false;
   if (g.epi == Epi::Accum && g.c_t != DType::F32) return false;
+  if (g.splits < 1 || g.kpieces < 1 || g.K % g.kpieces != 0) return false;
+  if (g.splits > 1 || g.kpieces > 1) {
+    // every K block of a piece lies inside it; slabs are disjoint, 16-byte aligned
+    const int64_t kpl = g.K / g.kpieces, esz = g.c_t == DType::F32 ? 4 : 2;
+    if (g.epi != Epi::Store || kpl % BKE != 0 || g.k_extent <= 0) return false;
+    if ((g.kpieces - 1) * g.kpiece_stride + (int64_t)g.splits * kpl > g.k_extent) return false;
+    if (g.splits > 1 && (g.c_split_rows < g.M || (g.c_split_rows * g.ldc * esz) % 16 != 0 ||
+                         (g.ldc * esz) % 16 != 0 || ((uintptr_t)g.C & 15) != 0))
+      return false;
+  }
   return encode_fn() != nullptr;
 }
 
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
-  const int tiles256 = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
+  const int tiles256 = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256) * g.splits;
   const bool pair = g.M > BM;  // a second row block exists for the cluster partner
   if (g.N <= 128 || tiles256 < num_sms())
     return pair ? dispatch_major<128, 2>(g, st) : dispatch_major<128, 1>(g, st);
@@ -637,6 +666,7 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st) {
 cudaError_t gemm(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (gemm_tc_supported(g)) return gemm_tc(g, st);
+  if (g.splits != 1 || g.kpieces != 1) return cudaErrorNotSupported;  // tensor-core path only
   return gemm_simt(g, st);
 }
 

@@ -471,7 +471,83 @@ cudaError_t ln_bwd_t(const float* du, const void* x, const float* mean, const fl
                     (const float*)part_b, dbeta, nb, H);
 }
 
+// out[m, n] = sum_{k < w} part[k][m, n] (+ bias[n]) (+ resid[m, n]): the shard
+// sum of the separate-reduction mode, k in order 0, 1, ...; part fp32 with
+// pstride floats between shards and row pitch N; VEC = 4 or 1 columns per thread.
+template <typename TO, typename TI, int VEC>
+__global__ void __launch_bounds__(256)
+shard_sum_kernel(const float* __restrict__ part, int64_t pstride, int w,
+                 const TI* __restrict__ bias, const TI* __restrict__ resid, TO* __restrict__ out,
+                 int64_t n_vec, int N) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_vec;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i * VEC;
+    const int c = (int)(e % N);
+    if (VEC == 4) {
+      float4 a = ld4(part + e);
+      for (int k = 1; k < w; ++k) {
+        const float4 b = ld4(part + k * pstride + e);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      if (bias) {
+        const float4 b = ld4(bias + c);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      if (resid) {
+        const float4 b = ld4(resid + e);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      st4(out + e, a);
+    } else {
+      float a = part[e];
+      for (int k = 1; k < w; ++k) a += part[k * pstride + e];
+      if (bias) a += ld_elem(bias, c);
+      if (resid) a += ld_elem(resid, e);
+      st_elem(out, e, a);
+    }
+  }
+}
+
+template <typename TO, typename TI>
+cudaError_t shard_sum_t(const float* part, int64_t pstride, int w, const void* bias,
+                        const void* resid, void* out, int M, int N, cudaStream_t st) {
+  const int64_t n = (int64_t)M * N;
+  const bool vec = N % 4 == 0 && pstride % 4 == 0 &&
+                   (((uintptr_t)part | (uintptr_t)out | (uintptr_t)bias | (uintptr_t)resid) % 16) == 0;
+  if (vec) {
+    const int64_t nv = n / 4;
+    const int grid = (int)std::min<int64_t>((nv + 255) / 256, 152 * 8);
+    return launch_pdl(shard_sum_kernel<TO, TI, 4>, dim3(grid), dim3(256), 0, st, part, pstride, w,
+                      (const TI*)bias, (const TI*)resid, (TO*)out, nv, N);
+  }
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, 152 * 8);
+  return launch_pdl(shard_sum_kernel<TO, TI, 1>, dim3(grid), dim3(256), 0, st, part, pstride, w,
+                    (const TI*)bias, (const TI*)resid, (TO*)out, n, N);
+}
+
 }  // namespace
+
+cudaError_t shard_sum(const float* part, int64_t pstride, int w, const void* bias,
+                      const void* resid, void* out, DType out_t, DType in_t, int M, int N,
+                      cudaStream_t st) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  if (out_t == DType::F32)
+    return in_t == DType::F32 ? shard_sum_t<float, float>(part, pstride, w, bias, resid, out, M, N, st)
+                              : shard_sum_t<float, __nv_bfloat16>(part, pstride, w, bias, resid, out, M, N, st);
+  return in_t == DType::F32 ? shard_sum_t<__nv_bfloat16, float>(part, pstride, w, bias, resid, out, M, N, st)
+                            : shard_sum_t<__nv_bfloat16, __nv_bfloat16>(part, pstride, w, bias, resid, out, M, N, st);
+}
 
 int ln_bwd_blocks(int M) { return (M + ROWS_PER_PART - 1) / ROWS_PER_PART; }
 int colsum_blocks(int M) { return (M + ROWS_PER_PART - 1) / ROWS_PER_PART; }

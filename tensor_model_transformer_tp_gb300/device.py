@@ -25,12 +25,12 @@ class DeviceBlock:
 
     def __init__(self, shape, layers: Sequence[Dict], recompute: str = "fine",
                  sub_batches: Optional[int] = None, device: str = "cuda:0",
-                 streams: Optional[tuple] = None):
+                 streams: Optional[tuple] = None, reduce: str = "fused"):
         self.shape = shape
         self.device = torch.device(device)
         self.dtype = TORCH_DTYPE[shape.dtype]
         self.n_layers = len(layers)
-        self.desc = desc_from_shape(shape, recompute, sub_batches)
+        self.desc = desc_from_shape(shape, recompute, sub_batches, reduce)
         self.params: List[Dict[str, torch.Tensor]] = []
         self.grads: List[Dict[str, torch.Tensor]] = []
         for p in layers:

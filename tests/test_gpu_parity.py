@@ -35,8 +35,8 @@ def rel(a, b):
     return float(np.linalg.norm(a - b) / (n if n > 0 else 1.0))
 
 
-def run_gpu(shape, inp, mode="fine", sub_batches=None, api="stack"):
-    blk = DeviceBlock(shape, inp["layers"], recompute=mode, sub_batches=sub_batches)
+def run_gpu(shape, inp, mode="fine", sub_batches=None, api="stack", reduce="fused"):
+    blk = DeviceBlock(shape, inp["layers"], recompute=mode, sub_batches=sub_batches, reduce=reduce)
     x, g = blk.tensor(inp["x"]), blk.tensor(inp["g"])
     if api == "stack":
         y, dx = blk.step(x, g)
@@ -191,3 +191,40 @@ def test_host_buffers_through_stack_step():
     torch.cuda.synchronize()
     np.testing.assert_array_equal(yh.double().numpy(), dev["y"])
     np.testing.assert_array_equal(dxh.double().numpy(), dev["dx"])
+
+
+# ------------------------------------------------------------------ separate reduction
+@pytest.mark.parametrize("mode", ["fine", "full"])
+def test_separate_reduce_ffn_f32_h256(mode):
+    """Shard partials in HBM + reduction kernel (C(F), C(R), C(B)) at fp32 tolerance."""
+    shape = SHAPES["ffn_f32_h256"]
+    inp = block_inputs(shape, seed=0)
+    compare(shape, run_gpu(shape, inp, mode, reduce="separate"),
+            oracle.run_step(shape, inp, mode=mode))
+
+
+@pytest.mark.parametrize("kind", ["ffn", "attn", "layer"])
+def test_separate_reduce_bf16_matches_oracle_and_fused(kind):
+    shape = BlockShape(kind, "bf16", batch=2, seq=96, hidden=256, ffn=768, heads=2, w=2,
+                       n_layers=2 if kind == "layer" else 1)
+    inp = block_inputs(shape, seed=13, affine=True)
+    sep = run_gpu(shape, inp, reduce="separate")
+    compare(shape, sep, oracle.run_step(shape, inp, mode="fine"))
+    fused = run_gpu(shape, inp, reduce="fused")
+    assert rel(sep["y"], fused["y"]) < 1e-2 and rel(sep["dx"], fused["dx"]) < 1e-2
+
+
+def test_separate_reduce_w4_full_recompute():
+    shape = BlockShape("ffn", "bf16", batch=4, seq=64, hidden=256, ffn=1024, w=4)
+    inp = block_inputs(shape, seed=14, affine=True)
+    compare(shape, run_gpu(shape, inp, "full", reduce="separate"),
+            oracle.run_step(shape, inp, mode="full"))
+
+
+@pytest.mark.parametrize("kind", ["ffn", "layer"])
+def test_separate_reduce_ragged_sub_batch_rows(kind):
+    """200 rows per sub-batch: paired 128-row tiles with a ragged last pair, and
+    the shard slabs of the split launch clipped at the sub-batch's last row."""
+    shape = BlockShape(kind, "bf16", batch=2, seq=200, hidden=256, ffn=1024, heads=2, w=2)
+    inp = block_inputs(shape, seed=15, affine=True)
+    compare(shape, run_gpu(shape, inp, reduce="separate"), oracle.run_step(shape, inp, mode="fine"))
