@@ -4,7 +4,8 @@
 //   followed by the block's fused epilogue (bias, GeLU, residual, GeLU',
 //   fp32 accumulate).
 //
-// One CTA per SM, persistent over 128 x BN output tiles (BN = 128 or 256).
+// One CTA per SM, persistent over 128 x BN output tiles (BN = 128 or 256);
+// for M > 128, CTA pairs share 256 x BN tiles through cta_group::2 MMAs.
 // Warp roles (320 threads):
 //   warp 0      one thread issues TMA loads of A and B K-slices (64 bf16 =
 //               128 bytes deep, 128-byte swizzle) into a STAGES-deep ring;
@@ -48,14 +49,14 @@ namespace {
 constexpr int BM = 128;
 constexpr int BKE = 64;  // K elements per stage (128 bytes of bf16)
 constexpr int NTHREADS = 320;  // 2 control warps + 8 epilogue warps
-constexpr int EPI_THREADS = 256;
 
-template <int BN>
+// CL = 2: a CTA pair shares each MMA; a CTA holds BN / 2 rows of the B tile.
+template <int BN, int CL>
 struct TcCfg {
   static constexpr int A_BYTES = BM * BKE * 2;
-  static constexpr int B_BYTES = BN * BKE * 2;
+  static constexpr int B_BYTES = BN / CL * BKE * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int STAGES = (192 * 1024) / STAGE;
   static constexpr int EPI_OFF = STAGES * STAGE;        // per epilogue warp: 32 rows x 128 B
   static constexpr int EPI_BYTES = 8 * 32 * 128;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8;
@@ -234,19 +235,23 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
   stage_and_store(tmC, g.epi == Epi::Accum);
 }
 
-// CL = 1: one CTA per 128 x BN tile.  CL = 2: a cluster of two CTAs takes a
-// 256 x BN tile; CTA r computes rows [128 r, 128 r + 128), loads its own A rows
-// and half r of the B tile, multicasting that half into both CTAs' shared
-// memory, so each CTA moves A + B/2 per stage instead of A + B.  A stage is
-// refilled only after both CTAs' MMAs have released it (the empty barriers
-// count two commits, multicast by each CTA's MMA thread).
+// CL = 1: one CTA per 128 x BN tile.  CL = 2: a CTA pair (cluster of two)
+// takes a 256 x BN tile with M = 256 pair MMAs (cta_group::2) issued by the
+// even CTA: CTA r loads A rows [128 r, 128 r + 128) and B rows [r BN/2, (r+1) BN/2)
+// of the tile into its own shared memory and holds output rows 128 r .. in its
+// TMEM, so per stage each SM stores and reads A + B/2 instead of A + B.  Both
+// CTAs' loads complete on the even CTA's full barrier (it expects both byte
+// counts); its commits arrive on both CTAs' empty and accumulator-full
+// barriers; both CTAs' epilogue warps release an accumulator on the even CTA's
+// barrier.
 template <int BN, bool A_K, bool B_K, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                const GemmArgs g) {
-  using C = TcCfg<BN>;
-  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, !A_K, !B_K);
+  using C = TcCfg<BN, CL>;
+  constexpr int BNH = BN / CL;  // B rows of the tile held by this CTA
+  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM * CL, BN, !A_K, !B_K);
   unsigned long long* tl = g_gemm_timeline ? g_gemm_timeline + 16 * blockIdx.x : nullptr;
   if (tl && threadIdx.x == 0) tl[0] = ptx::globaltimer();
   extern __shared__ uint8_t smem_raw[];
@@ -278,18 +283,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(full(s), 1);
-      ptx::mbar_init(empty(s), CL);
+      ptx::mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull(b), 1);
-      ptx::mbar_init(tempty(b), EPI_THREADS);
+      ptx::mbar_init(tempty(b), 8 * CL);  // one arrival per epilogue warp of the pair
     }
     ptx::mbar_init(drain, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tslot, C::TMEM_COLS);
-    ptx::tmem_relinquish();
+    if (CL > 1) {
+      ptx::tmem_alloc_pair(tslot, C::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tslot, C::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
@@ -321,48 +331,45 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int m0 = tile_m0(tile), n0 = tile_n0(tile), ks = tile_split(tile) * kpl;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!ptx::mbar_wait(empty(stage), phase ^ 1u)) { ok = false; break; }
-          const uint32_t fb = full(stage);
-          ptx::mbar_arrive_expect_tx(fb, C::STAGE);
+          // the pair's loads complete on the even CTA's barrier, which expects both
+          const uint32_t fb = CL > 1 ? ptx::mapa(full(stage), 0) : full(stage);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full(stage), CL * C::STAGE);
+          auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
+            if (CL > 1)
+              ptx::tma_load_2d_pair(dst, tm, fb, x, y);
+            else
+              ptx::tma_load_2d(dst, tm, fb, x, y);
+          };
           const uint32_t sa = base + stage * C::STAGE, sb = sa + C::A_BYTES;
           const int pc = kb / nkb_p;
           const int k0 = (int)(pc * g.kpiece_stride) + ks + (kb - pc * nkb_p) * BKE;
           if (A_K) {
-            ptx::tma_load_2d(sa, &tmA, fb, k0, m0);
+            load(sa, &tmA, k0, m0);
           } else {
-            ptx::tma_load_2d(sa, &tmA, fb, m0, k0);
-            ptx::tma_load_2d(sa + 8192, &tmA, fb, m0 + 64, k0);
+            load(sa, &tmA, m0, k0);
+            load(sa + 8192, &tmA, m0 + 64, k0);
           }
-          if (CL == 1) {
-            if (B_K) {
-              ptx::tma_load_2d(sb, &tmB, fb, k0, n0);
-            } else {
+          const int nb = n0 + rank * BNH;  // this CTA's B rows
+          if (B_K) {
+            load(sb, &tmB, k0, nb);
+          } else {
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                ptx::tma_load_2d(sb + c * 8192, &tmB, fb, n0 + 64 * c, k0);
-            }
-          } else if (B_K) {  // rows [rank * BN/CL, ...) of the B tile, to both CTAs
-            ptx::tma_load_2d_mc(sb + rank * (BN / CL) * 128, &tmB, fb, k0, n0 + rank * (BN / CL),
-                                MASK);
-          } else {  // 64-wide N chunks rank * (BN/64/CL) ..., to both CTAs
-#pragma unroll
-            for (int c = 0; c < BN / 64 / CL; ++c) {
-              const int cc = rank * (BN / 64 / CL) + c;
-              ptx::tma_load_2d_mc(sb + cc * 8192, &tmB, fb, n0 + 64 * cc, k0, MASK);
-            }
+            for (int c = 0; c < BNH / 64; ++c) load(sb + c * 8192, &tmB, nb + 64 * c, k0);
           }
           issued |= 1u << stage;
           iphase = (iphase & ~(1u << stage)) | (phase << stage);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      // Drain: every TMA load this thread issued has landed before the CTA exits.
+      // Drain: every TMA load this thread issued has landed before the CTA exits
+      // (the odd CTA of a pair sees that through the release of each stage).
       for (int s = 0; s < C::STAGES; ++s)
         if ((issued >> s) & 1u)
-          if (!ptx::mbar_wait(full(s), (iphase >> s) & 1u)) ok = false;
+          if (!ptx::mbar_wait(rank == 0 ? full(s) : empty(s), (iphase >> s) & 1u)) ok = false;
       if (!ok) atomicExch(&g_gemm_error, 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {  // the even CTA issues the pair's MMAs
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -383,20 +390,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                     : ptx::smem_desc_sw128(sa + kk * 2048, 8192, 1024);
             const uint64_t bd = B_K ? ptx::smem_desc_sw128(sb + kk * 32, 16, 1024)
                                     : ptx::smem_desc_sw128(sb + kk * 2048, 8192, 1024);
-            ptx::mma_bf16(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            if (CL > 1)
+              ptx::mma_bf16_pair(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (CL == 1)
-            ptx::mma_commit(empty(stage));
+          if (CL > 1)
+            ptx::mma_commit_pair_mc(empty(stage), MASK);
           else
-            ptx::mma_commit_mc(empty(stage), MASK);
+            ptx::mma_commit(empty(stage));
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        ptx::mma_commit(tfull(buf));
+        if (CL > 1)
+          ptx::mma_commit_pair_mc(tfull(buf), MASK);
+        else
+          ptx::mma_commit(tfull(buf));
         if (tl && t < 5) tl[3 + 2 * t] = ptx::globaltimer();
       }
       // Drain: all MMAs issued by this thread are complete before TMEM is freed.
-      ptx::mma_commit(drain);
+      if (CL > 1)
+        ptx::mma_commit_pair(drain);
+      else
+        ptx::mma_commit(drain);
       if (!ptx::mbar_wait(drain, 0)) ok = false;
       if (!ok) atomicExch(&g_gemm_error, 2);
     }
@@ -445,19 +461,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty(buf));
+      __syncwarp();
+      if (lane == 0) {
+        if (CL > 1)
+          ptx::mbar_arrive_cluster(ptx::mapa(tempty(buf), 0));
+        else
+          ptx::mbar_arrive(tempty(buf));
+      }
       if (tl && t < 5 && warp == 2 && lane == 0) tl[4 + 2 * t] = ptx::globaltimer();
     }
     if (g.tma_store && lane == 0) ptx::bulk_wait0();  // stores performed before the CTA retires
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // the pair's MMAs (which write both CTAs' TMEM) and every cross-CTA arrival
+  // are complete before either CTA frees TMEM or leaves
+  if (CL > 1) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    if (CL > 1)
+      ptx::tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  // neither CTA leaves while its partner may still multicast into it or
-  // arrive on its barriers
   if (CL > 1) ptx::cluster_sync();
   if (tl && threadIdx.x == 0) tl[15] = ptx::globaltimer();
 }
@@ -556,7 +582,7 @@ int num_sms() {
 
 template <int BN, bool A_K, bool B_K, int CL>
 cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, CL>;
   CUtensorMap ma, mb;
   const uint64_t kext = g.k_extent > 0 ? (uint64_t)g.k_extent : (uint64_t)g.K;
   bool ok = A_K ? make_map(&ma, g.A, kext, g.M, g.lda, BKE, BM)
