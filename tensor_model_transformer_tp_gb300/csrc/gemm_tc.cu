@@ -684,7 +684,12 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
   const int tiles256 = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256) * g.splits;
   const bool pair = g.M > BM;  // a second row block exists for the cluster partner
-  if (g.N <= 128 || tiles256 < num_sms())
+  // Pair MMAs with N = 128 move 1.5x the operand bytes per FLOP of N = 256
+  // and run at about half its rate: the pair path takes 256-wide tiles unless
+  // that would leave more than half of the SMs idle.
+  const bool narrow = pair ? (g.N <= 128 || 2 * tiles256 < num_sms())
+                           : (g.N <= 128 || tiles256 < num_sms());
+  if (narrow)
     return pair ? dispatch_major<128, 2>(g, st) : dispatch_major<128, 1>(g, st);
   return pair ? dispatch_major<256, 2>(g, st) : dispatch_major<256, 1>(g, st);
 }
