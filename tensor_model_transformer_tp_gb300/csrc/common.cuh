@@ -104,6 +104,78 @@ __device__ __forceinline__ float gelu_grad_f(float a) {
   return fmaf(a, pdf, cdf);
 }
 
+// ---- two values at a time: packed fp32x2 arithmetic (sm_100 family) --------
+// Each lane of a packed fma / mul / add rounds exactly like the scalar
+// operation, so the pair forms below return the same bits as gelu_f,
+// gelu_grad_f and scalar adds while issuing about half the instructions.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  return (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(b) << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_splat(float a) { return f2_pack(a, a); }
+// (a0, a1) += (b0, b1)
+__device__ __forceinline__ void add2_inplace(float& a0, float& a1, float b0, float b1) {
+  const uint64_t r = f2_add(f2_pack(a0, a1), f2_pack(b0, b1));
+  a0 = f2_lo(r);
+  a1 = f2_hi(r);
+}
+// Phi and phi of a pair, the operations of gelu_cdf_pdf in the same order.
+__device__ __forceinline__ void gelu_cdf_pdf2(uint64_t a, uint64_t& cdf, uint64_t& pdf) {
+  constexpr uint64_t ABS = 0x7fffffff7fffffffull, SIGN = 0x8000000080000000ull;
+  const uint64_t x = f2_mul(a & ABS, f2_splat(0.70710678118654752f));
+  const uint64_t den = f2_fma(f2_splat(0.3275911f), x, f2_splat(1.0f));
+  const uint64_t arg = f2_mul(f2_mul(x, x), f2_splat(-1.4426950408889634f));
+  float t0, t1, e0, e1;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t0) : "f"(f2_lo(den)));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t1) : "f"(f2_hi(den)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(f2_lo(arg)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(f2_hi(arg)));
+  const uint64_t t = f2_pack(t0, t1), e = f2_pack(e0, e1);
+  uint64_t poly = f2_fma(t, f2_splat(1.061405429f), f2_splat(-1.453152027f));
+  poly = f2_fma(t, poly, f2_splat(1.421413741f));
+  poly = f2_fma(t, poly, f2_splat(-0.284496736f));
+  poly = f2_fma(t, poly, f2_splat(0.254829592f));
+  poly = f2_mul(t, poly);
+  const uint64_t erf_abs = f2_fma(poly ^ SIGN, e, f2_splat(1.0f));
+  const uint64_t erf_s = (erf_abs & ABS) | (a & SIGN);  // copysign(erf_abs, a)
+  cdf = f2_fma(f2_splat(0.5f), erf_s, f2_splat(0.5f));
+  pdf = f2_mul(f2_splat(0.39894228040143268f), e);
+}
+// (a0, a1) = (gelu(a0), gelu(a1))
+__device__ __forceinline__ void gelu2_inplace(float& a0, float& a1) {
+  const uint64_t a = f2_pack(a0, a1);
+  uint64_t cdf, pdf;
+  gelu_cdf_pdf2(a, cdf, pdf);
+  const uint64_t r = f2_mul(a, cdf);
+  a0 = f2_lo(r);
+  a1 = f2_hi(r);
+}
+// (v0, v1) *= (gelu'(a0), gelu'(a1))
+__device__ __forceinline__ void mul_gelu_grad2_inplace(float& v0, float& v1, float a0, float a1) {
+  const uint64_t a = f2_pack(a0, a1);
+  uint64_t cdf, pdf;
+  gelu_cdf_pdf2(a, cdf, pdf);
+  const uint64_t r = f2_mul(f2_pack(v0, v1), f2_fma(a, pdf, cdf));
+  v0 = f2_lo(r);
+  v1 = f2_hi(r);
+}
+
 // ---------------------------------------------------------------------------
 // GEMM description shared by the SIMT and the tensor-core kernels.
 //   D[m, n] = sum_k A(m, k) * B(n, k), m < M, n < N, k < K.

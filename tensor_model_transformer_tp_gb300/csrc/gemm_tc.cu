@@ -172,7 +172,7 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
         float t[8];
         unpack8(__ldg(reinterpret_cast<const uint4*>(b) + i), t);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[8 * i + k] += t[k];
+        for (int k = 0; k < 8; k += 2) add2_inplace(v[8 * i + k], v[8 * i + k + 1], t[k], t[k + 1]);
       }
     } else {
 #pragma unroll
@@ -192,10 +192,10 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
     }
     if (g.epi == Epi::BiasResid) {
 #pragma unroll
-      for (int i = 0; i < CW; ++i) v[i] += t[i];
+      for (int i = 0; i < CW; i += 2) add2_inplace(v[i], v[i + 1], t[i], t[i + 1]);
     } else {
 #pragma unroll
-      for (int i = 0; i < CW; ++i) v[i] *= gelu_grad_f(t[i]);
+      for (int i = 0; i < CW; i += 2) mul_gelu_grad2_inplace(v[i], v[i + 1], t[i], t[i + 1]);
     }
   }
   // one staged store of v (as stored in C's type) to the box at (n, mw)
@@ -230,7 +230,7 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
   if (g.epi == Epi::BiasGelu) {
     if (g.C2) stage_and_store(tmC2, false);
 #pragma unroll
-    for (int i = 0; i < CW; ++i) v[i] = gelu_f(v[i]);
+    for (int i = 0; i < CW; i += 2) gelu2_inplace(v[i], v[i + 1]);
   }
   stage_and_store(tmC, g.epi == Epi::Accum);
 }
