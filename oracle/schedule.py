@@ -41,6 +41,12 @@ Recompute modes:
           since its output reaches only that dropped AllReduce and no Backward
           operation of the sequence reads it.  Backward order per segment pair
           is (R_j, B_j, R_i, B_i, C_i(B)) with j the later segment.
+  "selective": the selective recomputation the pages compare against in
+          §VI ("Megatron SS"): every activation is kept except the output of
+          the attention operation, which is recomputed (operator "attn": the
+          causal softmax attention of each shard's heads from the stored Q, K,
+          V) before the attention segment's Backward.  FFN segments keep
+          everything, as in "none".
 
 Weight gradients are summed (the loss is a sum) and accumulated in sub-batch
 order 0, 1, ...
@@ -128,6 +134,10 @@ class _Segment:
             QKV = [u @ wc[r].T + bc[r] for r in self.qkv_rows]
             a[(self.s, "QKV")] = QKV
             a[(self.s, "H")] = [self._attn_shard(q) for q in QKV]
+
+    def attn_fwd(self, a):
+        """The attention operation alone, from the stored Q, K, V of every shard."""
+        a[(self.s, "H")] = [self._attn_shard(q) for q in a[(self.s, "QKV")]]
 
     def row_fwd(self, a):
         wr = self.p[self.names["wr"]]
@@ -230,10 +240,13 @@ def build_operator_sequence(n_segments: int) -> List[Op]:
     return O
 
 
-def recompute_ops(seq: List[Op], mode: str) -> List[Op]:
-    """Operators re-run by the Recompute phase of one saved sequence."""
+def recompute_ops(seq: List[Op], mode: str, kind: str = None) -> List[Op]:
+    """Operators re-run by the Recompute phase of one saved sequence (kind:
+    the segment's "ffn" or "attn", needed by the selective mode)."""
     if mode == "none":
         return []
+    if mode == "selective":
+        return [Op("attn", seq[0].seg, "compute")] if kind == "attn" else []
     if mode == "full":
         return list(seq)                       # as the forward ran it, incl. C(R)
     # fine: communication dropped; the row operator's output only feeds the
@@ -249,7 +262,7 @@ def run_step(shape, inputs, mode: str = "fine", sub_batches: int = None, w: int 
     {name: float64 array}), trace (Trace) and saved_bytes (activation bytes
     held between the forward and the backward, all sub-batches, excluding y).
     """
-    assert mode in ("none", "full", "fine"), mode
+    assert mode in ("none", "full", "fine", "selective"), mode
     n_sb = shape.sub_batches if sub_batches is None else sub_batches
     w = shape.w if w is None else w
     layers = [{k: np.asarray(v, dtype=np.float64) for k, v in p.items()} for p in inputs["layers"]]
@@ -298,7 +311,12 @@ def run_step(shape, inputs, mode: str = "fine", sub_batches: int = None, w: int 
 
     # Saved recompute sequences: one per segment, first input x_s stored.
     seqs = [[op for op in O if op.seg == s] for s in range(nS)]
-    if mode != "none":
+    if mode == "selective":
+        for a in acts:
+            for s in range(nS):
+                if segs[s].kind == "attn":
+                    del a[(s, "H")]              # the attention output, recomputed
+    elif mode != "none":
         for a in acts:
             for key in list(a.keys()):
                 if not (key == "y" or (isinstance(key, tuple) and key[1] == "x")):
@@ -317,7 +335,7 @@ def run_step(shape, inputs, mode: str = "fine", sub_batches: int = None, w: int 
     # Per sub-batch stream of (phase, op); it is cut after every C(B) StartAsync.
     stream: List[Tuple[str, Op]] = []
     for seq in reversed(seqs):
-        stream += [("R", op) for op in recompute_ops(seq, mode)]
+        stream += [("R", op) for op in recompute_ops(seq, mode, segs[seq[0].seg].kind)]
         stream += [("B", op) for op in reversed(seq)]
     bruns: List[List[Tuple[str, Op]]] = [[]]
     for item in stream:

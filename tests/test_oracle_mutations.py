@@ -173,3 +173,17 @@ def test_row_gemm_uses_neighbour_shard_columns(monkeypatch):
                             for k, Hk in enumerate(a[(self.s, "H")])]
     monkeypatch.setattr(osch._Segment, "row_fwd", bad)
     assert _caught(SHARD)
+
+
+def test_selective_recompute_of_attention_drops_the_mask(monkeypatch):
+    """A selective recompute that re-runs the attention operation without the
+    causal mask: the mode no longer matches "none"."""
+    def bad(self, a):
+        shape = self.shape
+        self.shape = shape.replace(causal=False)
+        try:
+            a[(self.s, "H")] = [self._attn_shard(q) for q in a[(self.s, "QKV")]]
+        finally:
+            self.shape = shape
+    monkeypatch.setattr(osch._Segment, "attn_fwd", bad)
+    assert _caught(lambda: pins.test_recompute_modes_bit_identical("attn"))

@@ -140,13 +140,13 @@ def test_w1_is_the_textbook_mlp():
             assert abs(y[m, i] - acc) <= 1e-13 * max(1, abs(acc))
 
 
-# ------------------------------------------------ check 2: fine == full == none
+# ------------------------------------ check 2: fine == full == selective == none
 @pytest.mark.parametrize("kind", ["ffn", "attn", "layer"])
 def test_recompute_modes_bit_identical(kind):
     s = tiny(kind, n_layers=2)
     inp = block_inputs(s, seed=7, affine=True)
-    r = {m: oracle.run_step(s, inp, mode=m) for m in ("none", "full", "fine")}
-    for m in ("full", "fine"):
+    r = {m: oracle.run_step(s, inp, mode=m) for m in ("none", "full", "fine", "selective")}
+    for m in ("full", "fine", "selective"):
         np.testing.assert_array_equal(r[m]["y"], r["none"]["y"])
         np.testing.assert_array_equal(r[m]["dx"], r["none"]["dx"])
         for gl, gn in zip(r[m]["grads"], r["none"]["grads"]):
@@ -295,6 +295,31 @@ def test_recompute_stores_only_segment_inputs():
     one = s.rows * s.hidden * 8
     assert r["fine"] == r["full"] == 4 * one      # x_s for 4 segments
     assert r["none"] > r["fine"]
+
+
+def test_selective_recomputes_only_the_attention_operation():
+    """Selective recomputation (§VI, "Megatron SS"): no communication is
+    re-run, only the attention operation of attention segments is recomputed,
+    once per sub-batch, before that segment's Backward; the forward keeps every
+    activation but the attention output (rows x hidden per attention segment)."""
+    s = tiny("layer", n_layers=2)
+    inp = block_inputs(s, seed=16)
+    res = oracle.run_step(s, inp, mode="selective")
+    t = res["trace"]
+    rec = [e for e in t if e[0] == "R"]
+    assert sorted(rec) == sorted(("R", "attn", seg, b) for seg in (0, 2)
+                                 for b in range(s.sub_batches))
+    assert t.count_event("C(R)") == 0
+    for seg in (0, 2):
+        for b in range(s.sub_batches):
+            assert t.index(("R", "attn", seg, b)) < t.index(("B", "row", seg, b))
+    none = oracle.run_step(s, inp, mode="none")["saved_bytes"]
+    assert none - res["saved_bytes"] == 2 * s.rows * s.hidden * 8
+    f = tiny("ffn")
+    fi = block_inputs(f, seed=17)
+    assert (oracle.run_step(f, fi, mode="selective")["saved_bytes"] ==
+            oracle.run_step(f, fi, mode="none")["saved_bytes"])
+    assert oracle.run_step(f, fi, mode="selective")["trace"].count_event("R") == 0
 
 
 def test_empty_batch():
