@@ -44,14 +44,25 @@ METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300"
 NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
 
 
-def flops_fine(shape) -> float:
+def flops_fine(shape, mode="fine") -> float:
+    """Algorithmic FLOPs of one step, counted for the FINE schedule: FFN
+    fwd 4MHF + recompute 2MHF + bwd 8MHF; attention fwd 8MH^2 + 2BS^2H,
+    recompute 6MH^2 + 2BS^2H, bwd 16MH^2 + 5BS^2H (causal; x2 without the
+    mask).  NONE and SELECTIVE are credited only with what they execute (no
+    recompute; SELECTIVE recomputes the attention operation); FULL's extra
+    work is not credited."""
     M, H, B, S = shape.rows, shape.hidden, shape.batch, shape.seq
+    bs2h = B * S * S * H * (1.0 if shape.causal else 2.0)
     f = 0.0
     if shape.kind in ("ffn", "layer"):
-        f += 14.0 * M * H * shape.ffn
+        f += (12.0 if mode in ("none", "selective") else 14.0) * M * H * shape.ffn
     if shape.kind in ("attn", "layer"):
-        att = 9.0 * B * S * S * H * (1.0 if shape.causal else 2.0)
-        f += 30.0 * M * H * H + att
+        if mode == "none":
+            f += 24.0 * M * H * H + 7.0 * bs2h
+        elif mode == "selective":
+            f += 24.0 * M * H * H + 9.0 * bs2h
+        else:
+            f += 30.0 * M * H * H + 9.0 * bs2h
     return f * shape.n_layers
 
 
@@ -155,7 +166,7 @@ def run_reference(args, shape):
     for _ in range(args.steps):
         oracle.run_step(sample, inp, mode=args.recompute)
     dt = (time.perf_counter() - t0) / args.steps
-    value = flops_fine(sample) / dt / 1e12
+    value = flops_fine(sample, args.recompute) / dt / 1e12
     cores = len(os.sched_getaffinity(0))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
@@ -186,7 +197,7 @@ def cpu_baseline(shape, recompute):
         dt = time.perf_counter() - t0
         if dt >= 10.0 or reps >= 50:
             break
-    return {"value": flops_fine(sample) * reps / dt / 1e12, "unit": "TFLOP/s",
+    return {"value": flops_fine(sample, recompute) * reps / dt / 1e12, "unit": "TFLOP/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": "%d steps on %d of %d sequences (%.1f s, fp64 numpy)" % (
                 reps, nb, shape.batch, dt)}
@@ -261,7 +272,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_bf16_h1024")
-    ap.add_argument("--recompute", default="fine", choices=["fine", "full", "none"])
+    ap.add_argument("--recompute", default="fine", choices=["fine", "full", "none", "selective"])
     ap.add_argument("--sub-batches", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the step directly, not as a CUDA graph")
@@ -339,7 +350,7 @@ def main():
         tt = torch.tensor([t_step], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         t_step = float(tt.item())
-    fl = flops_fine(shape)
+    fl = flops_fine(shape, args.recompute)
     value = fl * world / t_step / 1e12
 
     # end to end: host (pinned) buffers through the same C-ABI call

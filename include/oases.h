@@ -75,8 +75,18 @@ typedef enum { OASES_F32 = 0, OASES_BF16 = 1 } oases_dtype;
  *       row GEMM and its reduction (Oases §IV-A, Fig. 4a, the default schedule).
  * FINE: keep only segment inputs; recompute LayerNorm and the column-parallel
  *       part only: C_i(R) and the row GEMM feeding it are not recomputed
- *       (Oases §IV, Eq. (1), Fig. 4d). */
-typedef enum { OASES_RECOMPUTE_NONE = 0, OASES_RECOMPUTE_FULL = 1, OASES_RECOMPUTE_FINE = 2 } oases_recompute;
+ *       (Oases §IV, Eq. (1), Fig. 4d).
+ * SELECTIVE: keep every activation except the output of the attention
+ *       operation (O and its log-sum-exp), which is recomputed from the kept
+ *       Q, K, V before the attention segment's backward: the selective
+ *       recomputation the pages compare against (§VI, "Megatron SS").  FFN
+ *       segments keep everything, as in NONE. */
+typedef enum {
+  OASES_RECOMPUTE_NONE = 0,
+  OASES_RECOMPUTE_FULL = 1,
+  OASES_RECOMPUTE_FINE = 2,
+  OASES_RECOMPUTE_SELECTIVE = 3
+} oases_recompute;
 /* How the shard sums C_i(F) (and C_i(R)) and C_i(B) are formed (Oases §IV,
  * Eq. (1): y = sum_k P_k over the w shards).
  * FUSED:    the row GEMM contracts over every shard's K-slice into one TMEM
@@ -176,7 +186,8 @@ const char *oases_version(void);
  *   event  = e & 0xF         0 F, 1 R, 2 B (compute operations),
  *                            3 C(F), 4 C(R), 5 C(B) (communication started),
  *                            6 Sync (the sub-batch waits for its communication)
- *   op     = (e >> 4) & 0xF  0 ln, 1 f, 2 col, 3 row, 4 g
+ *   op     = (e >> 4) & 0xF  0 ln, 1 f, 2 col, 3 row, 4 g, 5 attn (the attention
+ *                            operation alone, recomputed in SELECTIVE mode)
  *   sub    = (e >> 8) & 0xFF sub-batch
  *   seg    = e >> 16         segment (layer * segments_per_layer + index)
  * On one GPU a "communication" is the on-chip shard sum; Sync is the event

@@ -23,10 +23,10 @@ STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA"
           6: "INJECTED"}
 KIND = {"ffn": 0, "attn": 1, "layer": 2}
 DTYPE = {"f32": 0, "bf16": 1}
-RECOMPUTE = {"none": 0, "full": 1, "fine": 2}
+RECOMPUTE = {"none": 0, "full": 1, "fine": 2, "selective": 3}
 REDUCE = {"fused": 0, "separate": 1}
 EVENTS = ["F", "R", "B", "C(F)", "C(R)", "C(B)", "Sync"]
-OPS = ["ln", "f", "col", "row", "g"]
+OPS = ["ln", "f", "col", "row", "g", "attn"]
 PARAM_NAMES = ("ln1_g", "ln1_b", "wqkv", "bqkv", "wo", "bo",
                "ln2_g", "ln2_b", "w1", "b1", "w2", "b2")
 

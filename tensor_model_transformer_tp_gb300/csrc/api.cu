@@ -61,7 +61,7 @@ std::vector<TraceRec> g_trace;
 std::vector<cudaEvent_t> g_trace_events;  // reused across calls
 
 enum Ev { EV_F = 0, EV_R = 1, EV_B = 2, EV_CF = 3, EV_CR = 4, EV_CB = 5, EV_SYNC = 6 };
-enum OpN { OP_LN = 0, OP_F = 1, OP_COL = 2, OP_ROW = 3, OP_G = 4 };
+enum OpN { OP_LN = 0, OP_F = 1, OP_COL = 2, OP_ROW = 3, OP_G = 4, OP_ATTN = 5 };
 enum SegKind { SEG_FFN = 0, SEG_ATTN = 1 };
 // Weight-gradient groups of one segment, each accumulated in sub-batch order.
 enum Grp { GRP_BR = 0, GRP_WR = 1, GRP_BC = 2, GRP_WC = 3, GRP_LN = 4, GRP_N = 5 };
@@ -89,7 +89,7 @@ oases_status validate(const oases_block_desc* d, int n_layers, Shape* s) {
   if (d->batch < 0 || d->seq < 0 || d->hidden <= 0 || d->w < 1 || d->sub_batches < 1)
     return OASES_ERR_INVALID_ARG;
   if (d->batch % d->sub_batches != 0) return OASES_ERR_INVALID_ARG;
-  if (d->recompute < 0 || d->recompute > 2) return OASES_ERR_INVALID_ARG;
+  if (d->recompute < 0 || d->recompute > 3) return OASES_ERR_INVALID_ARG;
   if (d->reduce < 0 || d->reduce > 1) return OASES_ERR_INVALID_ARG;
   if (!(d->ln_eps >= 0.f)) return OASES_ERR_INVALID_ARG;
   const bool has_ffn = d->kind != OASES_BLOCK_ATTN, has_attn = d->kind != OASES_BLOCK_FFN;
@@ -172,7 +172,11 @@ Layout make_layout(const Shape& s) {
   const size_t maxN = (size_t)std::max<int64_t>(std::max(s.H, s.F), 3 * (int64_t)s.H);
   L.cpart_n = (size_t)colsum_blocks((int)s.Ms) * maxN;
   L.lpart_n = (size_t)ln_bwd_blocks((int)s.Ms) * s.H;
-  auto make_set = [&](int kind) {
+  // A segment's buffers.  `share` (the first set of the same kind, or null)
+  // supplies the backward scratch, which sub-batch streams use one segment
+  // at a time, and, in SELECTIVE mode, the attention output O and its LSE,
+  // which that mode recomputes before each attention segment's backward.
+  auto make_set = [&](int kind, const ActSet* share) {
     ActSet a;
     const size_t M = (size_t)s.M;
     if (s.pre_ln) a.u = take(M * s.H * s.esz);
@@ -183,8 +187,27 @@ Layout make_layout(const Shape& s) {
       a.h = take(M * s.F * s.esz);
     } else {
       a.qkv = take(M * 3 * s.H * s.esz);
-      a.o = take(M * s.H * s.esz);
-      a.lse = take(M * s.nh * 4);
+      if (share && s.mode == OASES_RECOMPUTE_SELECTIVE) {
+        a.o = share->o;
+        a.lse = share->lse;
+      } else {
+        a.o = take(M * s.H * s.esz);
+        a.lse = take(M * s.nh * 4);
+      }
+    }
+    if (share) {
+      a.delta = share->delta;
+      a.d_o = share->d_o;
+      a.dqkv = share->dqkv;
+      a.du = share->du;
+      a.cpart = share->cpart;
+      a.lpart_g = share->lpart_g;
+      a.lpart_b = share->lpart_b;
+      a.lstat = share->lstat;
+      a.red = share->red;
+      return a;
+    }
+    if (kind == SEG_ATTN) {
       a.delta = take(M * s.nh * 4);
       a.d_o = take(M * s.H * s.esz);
       a.dqkv = take(M * 3 * s.H * s.esz);
@@ -198,15 +221,21 @@ Layout make_layout(const Shape& s) {
     return a;
   };
   L.act.resize(s.nseg);
-  if (s.mode == OASES_RECOMPUTE_NONE) {
-    for (int i = 0; i < s.nseg; ++i) L.act[i] = make_set(s.seg_kind(i));
+  if (s.mode == OASES_RECOMPUTE_NONE || s.mode == OASES_RECOMPUTE_SELECTIVE) {
+    // activations kept per segment, scratch per kind
+    int first[2] = {-1, -1};
+    for (int i = 0; i < s.nseg; ++i) {
+      const int k = s.seg_kind(i);
+      L.act[i] = make_set(k, first[k] >= 0 ? &L.act[first[k]] : nullptr);
+      if (first[k] < 0) first[k] = i;
+    }
   } else {
     ActSet per_kind[2];
     bool made[2] = {false, false};
     for (int i = 0; i < s.nseg; ++i) {
       const int k = s.seg_kind(i);
       if (!made[k]) {
-        per_kind[k] = make_set(k);
+        per_kind[k] = make_set(k, nullptr);
         made[k] = true;
       }
       L.act[i] = per_kind[k];
@@ -239,7 +268,9 @@ std::vector<Step> schedule(const Shape& s, int phase) {
         out.push_back({EV_SYNC, OP_F, seg + 1, b});
         out.push_back({EV_B, OP_LN, seg + 1, b});
       }
-      if (s.mode != OASES_RECOMPUTE_NONE) {
+      if (s.mode == OASES_RECOMPUTE_SELECTIVE) {
+        if (s.seg_kind(seg) == SEG_ATTN) out.push_back({EV_R, OP_ATTN, seg, b});
+      } else if (s.mode != OASES_RECOMPUTE_NONE) {
         out.push_back({EV_R, OP_LN, seg, b});
         out.push_back({EV_R, OP_COL, seg, b});
         if (s.mode == OASES_RECOMPUTE_FULL) {
@@ -391,19 +422,28 @@ struct Exec {
       g.C = rowp(at(a.qkv), b, 3 * s.H, s.esz);
       g.ldc = 3 * s.H;
       ok(gemm(g, stream(b)));
-      AttnArgs at_;
-      at_.batch = s.B / s.nsb;
-      at_.seq = s.S;
-      at_.heads = s.nh;
-      at_.head_dim = s.d;
-      at_.hidden = s.H;
-      at_.causal = s.causal;
-      at_.t = s.t;
-      at_.qkv = g.C;
-      at_.o = rowp(at(a.o), b, s.H, s.esz);
-      at_.lse = at<float>(a.lse) + (size_t)b * s.nh * s.Ms;
-      ok(attention_fwd(at_, stream(b)));
+      ok(attention_fwd(attn_args(seg, b), stream(b)));
     }
+  }
+
+  // Causal attention of sub-batch b over the segment's kept Q, K, V.
+  AttnArgs attn_args(int seg, int b) const {
+    const ActSet& a = L.act[seg];
+    AttnArgs at_;
+    at_.batch = s.B / s.nsb;
+    at_.seq = s.S;
+    at_.heads = s.nh;
+    at_.head_dim = s.d;
+    at_.hidden = s.H;
+    at_.causal = s.causal;
+    at_.t = s.t;
+    at_.qkv = rowp(at(a.qkv), b, 3 * s.H, s.esz);
+    at_.o = rowp(at(a.o), b, s.H, s.esz);
+    at_.lse = at<float>(a.lse) + (size_t)b * s.nh * s.Ms;
+    at_.d_o = rowp(at(a.d_o), b, s.H, s.esz);
+    at_.delta = at<float>(a.delta) + (size_t)b * s.nh * s.Ms;
+    at_.dqkv = rowp(at(a.dqkv), b, 3 * s.H, s.esz);
+    return at_;
   }
 
   // Row GEMM with the shard sum fused (C_i(F)); out = seg output or recompute scratch.
@@ -557,20 +597,7 @@ struct Exec {
     if (ffn) {
       dcol = rowp(at(a.a), b, s.F, s.esz);  // dA
     } else {
-      AttnArgs at_;
-      at_.batch = s.B / s.nsb;
-      at_.seq = s.S;
-      at_.heads = s.nh;
-      at_.head_dim = s.d;
-      at_.hidden = s.H;
-      at_.causal = s.causal;
-      at_.t = s.t;
-      at_.qkv = rowp(at(a.qkv), b, 3 * s.H, s.esz);
-      at_.o = rowp(at(a.o), b, s.H, s.esz);
-      at_.lse = at<float>(a.lse) + (size_t)b * s.nh * s.Ms;
-      at_.d_o = rowp(at(a.d_o), b, s.H, s.esz);
-      at_.delta = at<float>(a.delta) + (size_t)b * s.nh * s.Ms;
-      at_.dqkv = rowp(at(a.dqkv), b, 3 * s.H, s.esz);
+      const AttnArgs at_ = attn_args(seg, b);
       ok(attention_bwd(at_, stream(b)));
       dcol = at_.dqkv;
     }
@@ -699,7 +726,8 @@ struct Exec {
     switch (st_.ev) {
       case EV_F:
         if (st_.op == OP_LN) ln_fwd(seg, b);
-        else if (st_.op == OP_COL) col_fwd(seg, b, s.mode == OASES_RECOMPUTE_NONE);
+        else if (st_.op == OP_COL)
+          col_fwd(seg, b, s.mode == OASES_RECOMPUTE_NONE || s.mode == OASES_RECOMPUTE_SELECTIVE);
         else if (st_.op == OP_ROW) {
           if (s.reduce == OASES_REDUCE_SEPARATE) row_partials(seg, b);
           else row_fwd(seg, b, seg_out(seg));
@@ -710,6 +738,7 @@ struct Exec {
         break;
       case EV_R:
         if (st_.op == OP_LN) ln_fwd(seg, b);
+        else if (st_.op == OP_ATTN) ok(attention_fwd(attn_args(seg, b), stream(b)));
         else if (st_.op == OP_COL) col_fwd(seg, b, true);
         else if (st_.op == OP_ROW) {
           if (s.reduce == OASES_REDUCE_SEPARATE) row_partials(seg, b);

@@ -119,7 +119,7 @@ def _oracle_trace(shape, mode, n_sb):
 
 @pytest.mark.parametrize("kind,n_layers", [("ffn", 1), ("attn", 1), ("layer", 1), ("layer", 2),
                                            ("ffn", 3)])
-@pytest.mark.parametrize("mode", ["none", "full", "fine"])
+@pytest.mark.parametrize("mode", ["none", "full", "fine", "selective"])
 @pytest.mark.parametrize("n_sb", [1, 2, 4])
 def test_schedule_matches_oracle_algorithm1(L, kind, n_layers, mode, n_sb):
     """The library enqueues operators in exactly the oracle's Algorithm 1 order."""
@@ -137,3 +137,13 @@ def test_schedule_counts_per_mode(L):
         assert sum(e[0] == "C(R)" for e in t) == cr
         assert sum(e[0] == "C(B)" for e in t) == 2
         assert sum(e[0] == "R" for e in t) == {"none": 0, "full": 6, "fine": 4}[m]
+
+
+def test_selective_workspace_between_fine_and_none(L):
+    """SELECTIVE keeps what NONE keeps except each attention segment's output O
+    and its LSE, which all attention segments share."""
+    d = {m: _desc(kind="layer", heads=2, recompute=m) for m in ("none", "fine", "selective")}
+    n = {m: oz.oases_workspace_bytes(d[m], 2) for m in d}
+    assert n["fine"] < n["selective"] < n["none"]
+    f = {m: oz.oases_workspace_bytes(_desc(recompute=m), 2) for m in ("none", "selective")}
+    assert f["none"] == f["selective"]          # FFN only: nothing to recompute

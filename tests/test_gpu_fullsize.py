@@ -105,9 +105,10 @@ def test_layer_full_batch_sub_batch_split_and_modes():
     one = run_gpu(full.replace(sub_batches=1), inp, "fine")
     np.testing.assert_array_equal(two["y"], one["y"])
     np.testing.assert_array_equal(two["dx"], one["dx"])
-    none = run_gpu(full, inp, "none")
-    np.testing.assert_array_equal(two["y"], none["y"])
-    np.testing.assert_array_equal(two["dx"], none["dx"])
-    for gf, gn in zip(two["grads"], none["grads"]):
-        for k in gf:
-            np.testing.assert_array_equal(gf[k], gn[k])
+    for mode in ("none", "selective"):
+        other = run_gpu(full, inp, mode)
+        np.testing.assert_array_equal(two["y"], other["y"])
+        np.testing.assert_array_equal(two["dx"], other["dx"])
+        for gf, gn in zip(two["grads"], other["grads"]):
+            for k in gf:
+                np.testing.assert_array_equal(gf[k], gn[k])

@@ -102,9 +102,10 @@ def test_ffn_bf16_h1024_full_size():
 def test_ffn_bf16_modes_bit_identical():
     shape = BlockShape("ffn", "bf16", batch=4, seq=96, hidden=256, ffn=512, w=2)
     inp = block_inputs(shape, seed=3, affine=True)
-    r = {m: run_gpu(shape, inp, m) for m in ("none", "full", "fine")}
+    r = {m: run_gpu(shape, inp, m) for m in ("none", "full", "fine", "selective")}
     assert_identical(r["fine"], r["none"])
     assert_identical(r["full"], r["none"])
+    assert_identical(r["selective"], r["none"])
 
 
 def test_ffn_bf16_sub_batch_split():
@@ -228,3 +229,23 @@ def test_separate_reduce_ragged_sub_batch_rows(kind):
     shape = BlockShape(kind, "bf16", batch=2, seq=200, hidden=256, ffn=1024, heads=2, w=2)
     inp = block_inputs(shape, seed=15, affine=True)
     compare(shape, run_gpu(shape, inp, reduce="separate"), oracle.run_step(shape, inp, mode="fine"))
+
+
+# ------------------------------------------------------------------ selective recompute
+def test_layer_stack_selective_recompute():
+    """SELECTIVE (the attention operation recomputed from kept Q, K, V; both
+    layers' attention share one O/LSE buffer): against the oracle, and bit for
+    bit equal to keeping everything."""
+    shape = BlockShape("layer", "bf16", batch=2, seq=96, hidden=256, ffn=768, heads=2, w=2,
+                       n_layers=2)
+    inp = block_inputs(shape, seed=16, affine=True)
+    sel = run_gpu(shape, inp, "selective")
+    compare(shape, sel, oracle.run_step(shape, inp, mode="selective"))
+    assert_identical(sel, run_gpu(shape, inp, "none"))
+    assert_identical(sel, run_gpu(shape, inp, "fine"))
+
+
+def test_attn_f32_selective_recompute():
+    shape = BlockShape("attn", "f32", batch=2, seq=40, hidden=128, heads=4, w=2)
+    inp = block_inputs(shape, seed=17, affine=True)
+    compare(shape, run_gpu(shape, inp, "selective"), oracle.run_step(shape, inp, mode="selective"))
