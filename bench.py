@@ -39,9 +39,22 @@ sys.path.insert(0, ROOT)
 METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300"
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel (the fused column GEMM + bias + GeLU of the FFN, one sub-batch), with
-# the sha256 of the kernel source it was measured on; traffic is reported only
-# while the source is unchanged.
-NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+# the sha256 of the kernel sources it was measured on (kernel_source_sha);
+# traffic is reported only while those sources are unchanged.
+NCU_TRAFFIC = {"source_sha256": "aeb1ae55ef11388730dbabf1ac1fe0a5869d4c873916c1eda78024b3785ab1dc",
+               "bytes_per_launch": 12668928 + 10496}  # dram read + write, one launch
+
+
+GEMM_SOURCES = ("gemm_tc.cu", "common.cuh", "epilogue.cuh", "sm100_ptx.cuh")
+
+
+def kernel_source_sha() -> str:
+    """sha256 over the sources the tensor-core GEMM kernel is compiled from."""
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "tensor_model_transformer_tp_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def flops_fine(shape, mode="fine") -> float:
@@ -254,8 +267,7 @@ def dominant_kernel_roofline(blk, shape, pk, torch):
     fl = 2.0 * Ms * N * H
     achieved = fl / t / 1e12
     traffic = None
-    src = os.path.join(ROOT, "tensor_model_transformer_tp_gb300", "csrc", "gemm_tc.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = kernel_source_sha()
     if NCU_TRAFFIC["source_sha256"] == sha:
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     return {"kernel": "gemm_tc_kernel (column GEMM + bias + GeLU, %dx%dx%d)" % (Ms, N, H),
