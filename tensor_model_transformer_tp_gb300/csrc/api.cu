@@ -1112,6 +1112,12 @@ extern "C" oases_status oases_debug_attention_progress(int* host_mapped) {
   return OASES_OK;
 }
 
+extern "C" oases_status oases_debug_attention_timeline(unsigned long long* device_buffer) {
+  cudaError_t e = oases::attention_set_timeline(device_buffer);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
 extern "C" int oases_debug_attention_error_word(void) {
   return oases::attention_read_and_clear_error();
 }

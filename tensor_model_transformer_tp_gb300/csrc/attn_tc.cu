@@ -33,6 +33,13 @@ __device__ int g_attn_error;
 // Optional progress markers (debugging aid, off when null): thread 0 of CTA c
 // of kernel k writes its current stage to g_attn_progress[k * 256 + c].
 __device__ int* g_attn_progress;
+// Optional timeline of the backward kernels (debugging aid, off when null),
+// %globaltimer stamps: entry and exit of every CTA (dq kernel at
+// [2 c], dK/dV kernel at [8192 + 2 c], c = linear CTA index < 4096), and per
+// block j < 64 of CTA 0 (dq at 16384 + 4 j, dK/dV at 16640 + 4 j): [0] S, dP
+// MMAs issued, [1] accumulation MMAs issued, [2] compute warp 2 saw S, dP,
+// [3] compute warp 2 handed over its dS (and P) rows.
+__device__ unsigned long long* g_attn_timeline;
 
 namespace {
 
@@ -40,7 +47,6 @@ constexpr int D = 128;                 // head dimension
 constexpr int BQ = 128, BKV = 128;     // query rows per CTA, keys per block
 constexpr int BOX = 128 * 64 * 2;      // one TMA box: 128 rows x 64 bf16 (16 KB)
 constexpr int TILE = 2 * BOX;          // 128 rows x 128 bf16 (32 KB)
-constexpr int KV_STAGES = 2;
 constexpr int NT = 128;
 
 // S = Q K^T: M = 128 queries, N = 128 keys, both operands K-major (over d).
@@ -82,6 +88,20 @@ __device__ __forceinline__ void progress(int kid, int code) {
     }
   }
 }
+__device__ __forceinline__ int linear_cta() {
+  return blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+}
+// kid 1 = dq, 2 = dK/dV; what 0 = entry, 1 = exit (thread 0)
+__device__ __forceinline__ void tl_cta(int kid, int what) {
+  unsigned long long* t = g_attn_timeline;
+  const int c = linear_cta();
+  if (t != nullptr && c < 4096) t[(kid - 1) * 8192 + 2 * c + what] = ptx::globaltimer();
+}
+__device__ __forceinline__ void tl_block(int kid, int j, int what) {
+  unsigned long long* t = g_attn_timeline;
+  if (t != nullptr && linear_cta() == 0 && j < 64)
+    t[16384 + (kid - 1) * 256 + 4 * j + what] = ptx::globaltimer();
+}
 // Records the first failed wait site (kernel * 100 + site) in g_attn_error.
 __device__ __forceinline__ void wait_failed(int code) { atomicCAS(&g_attn_error, 0, code); }
 
@@ -121,8 +141,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   const uint32_t tslot = bars + 8u * F_NBAR;
 
   const int tid = threadIdx.x, warp = tid / 32;
-  const int tile = gridDim.x - 1 - blockIdx.x;  // heavy (late) query tiles first
-  const int h = blockIdx.y, b = blockIdx.z;
+  // grid (heads, batch, tiles): the slowest index runs heavy (late) query tiles first
+  const int tile = gridDim.z - 1 - blockIdx.z;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int q0 = tile * BQ;
   const int row0 = b * a.S;
   const int nkv_all = (a.S + BKV - 1) / BKV;
@@ -350,8 +371,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
 //   dP = dO V^T,  dS = P * (dP - delta),
 //   dQ = dS K / sqrt(d),  dK = dS^T Q / sqrt(d),  dV = P^T dO.
 // Two kernels own disjoint outputs, so there are no atomics:
-//   dq kernel   one CTA per 128 queries, loops over key blocks (thread = query)
-//   dkv kernel  one CTA per 128 keys, loops over 64-query blocks (thread = key)
+//   dq kernel   one CTA per 128 queries, loops over 64-key blocks (row = query)
+//   dkv kernel  one CTA per 128 keys, loops over 64-query blocks (row = key)
 // ---------------------------------------------------------------------------
 struct BwdArgs {
   const float* lse;
@@ -362,47 +383,116 @@ struct BwdArgs {
   float scale;       // 1 / sqrt(d)
 };
 
-// dq kernel shared-memory map
-constexpr int DQ_OFF_Q = 0, DQ_OFF_DO = TILE, DQ_OFF_K = 2 * TILE;
-constexpr int DQ_OFF_V = DQ_OFF_K + KV_STAGES * TILE, DQ_OFF_DS = DQ_OFF_V + KV_STAGES * TILE;
-constexpr int DQ_OFF_BAR = DQ_OFF_DS + TILE;
-constexpr int DQ_NBAR = 1 + KV_STAGES + 1 + 1 + 1;  // q+dO, kv, s+dP, final, drain
-constexpr int DQ_SMEM = DQ_OFF_BAR + 8 * DQ_NBAR + 16 + 1024;
+// Both backward kernels are warp-specialised pipelines over blocks of 64
+// keys (dq kernel) or 64 queries (dkv kernel), 320 threads:
+//   warp 0      TMA loads (a ring of operand stages);
+//   warp 1      TMEM allocation; one thread issues the MMAs;
+//   warps 2..9  element-wise work: warp w owns TMEM lanes 32 (w % 4) .. + 31
+//               (one row each) and half (w - 2) / 4 of the block's 64 columns.
+// S and dP of a block land in one of two TMEM buffers, dS (and P) in one of
+// two shared-memory buffers, so while the element-wise warps turn block j into
+// dS the tensor core computes S, dP of block j + 1 and the accumulation of
+// block j - 1.  MMA issue order: SdP_0, then SdP_j, ACC_{j-1} for j >= 1,
+// then ACC_{n-1}.
+constexpr int BWD_NT = 320;
+constexpr int BK = 64;                  // keys or queries per block
+constexpr int BOX64 = 64 * 64 * 2;      // one TMA box: 64 rows x 64 bf16 (8 KB)
+constexpr int T64 = 2 * BOX64;          // 64 rows x 128 dims (16 KB)
+constexpr int PB = 128 * 64 * 2;        // 128 rows x 64 bf16, one box width (16 KB)
+constexpr uint64_t BWD_WAIT = 1ull << 29;  // cycles before a wait gives up (~0.25 s)
+// S = Q K_j^T and dP = dO V_j^T (dq), S^T = K Q_i^T and dP^T = V dO_i^T (dkv):
+// M = 128 rows, N = 64 block columns, both operands K-major over d.
+constexpr uint32_t IDESC_N64 = ptx::idesc_bf16_f32(128, BK, false, false);
+// dQ += dS K_j, dV += P^T dO_i, dK += dS^T Q_i: M = 128, N = 128 dims, A
+// K-major over the 64 block columns, B MN-major.
+constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(128, D, false, true);
 
-__global__ void __launch_bounds__(NT, 1)
-attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-                      const BwdArgs a) {
+// [64 rows][128 cols] K-major tile stored as two 64-column boxes, k-step kk of 8.
+__device__ __forceinline__ uint64_t kmajor64_desc(uint32_t tile, int kk) {
+  return ptx::smem_desc_sw128(tile + (kk >> 2) * BOX64 + (kk & 3) * 32, 16, 1024);
+}
+// [64 k-rows][128 n-cols] MN-major tile stored as two 64-column boxes, k-step kk of 4.
+__device__ __forceinline__ uint64_t mnmajor64_desc(uint32_t tile, int kk) {
+  return ptx::smem_desc_sw128(tile + kk * 2048, BOX64, 1024);
+}
+// [128 rows][64 cols] K-major buffer (one box width), k-step kk of 4.
+__device__ __forceinline__ uint64_t kmajor_blk_desc(uint32_t buf, int kk) {
+  return ptx::smem_desc_sw128(buf + kk * 32, 16, 1024);
+}
+// Writes this thread's 32 values (columns 32 half .. + 31 of its row) as bf16
+// into a [128 rows][64 cols] 128-byte-swizzled buffer.
+__device__ __forceinline__ void store_row_half(uint8_t* buf, int row, int half, const float (&v)[32]) {
+  uint8_t* r = buf + row * 128;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<uint4*>(r + (((half * 4 + u) ^ (row & 7)) << 4)) =
+        make_uint4(pack2(v[8 * u], v[8 * u + 1]), pack2(v[8 * u + 2], v[8 * u + 3]),
+                   pack2(v[8 * u + 4], v[8 * u + 5]), pack2(v[8 * u + 6], v[8 * u + 7]));
+}
+// Warp-uniform bounded wait (every lane waits; the warp agrees on the outcome).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, BWD_WAIT));
+}
+
+// dq kernel shared-memory map: Q, dO, four K/V stages of 64 keys (a stage is
+// refilled only after the block's dQ MMA, so the ring must cover the load
+// latency), two dS buffers.
+constexpr int DQ_KST = 4;
+constexpr int DQ_OFF_Q = 0, DQ_OFF_DO = TILE, DQ_OFF_K = 2 * TILE;
+constexpr int DQ_OFF_V = DQ_OFF_K + DQ_KST * T64, DQ_OFF_DS = DQ_OFF_V + DQ_KST * T64;
+constexpr int DQ_OFF_BAR = DQ_OFF_DS + 2 * PB;
+// q+dO, kv_full[3], kv_empty[3], sdp_full[2], sdp_empty[2], ds_full[2], ds_empty[2], fin
+constexpr int DQ_NBAR = 1 + 2 * DQ_KST + 8 + 1;
+constexpr int DQ_SMEM = DQ_OFF_BAR + 8 * DQ_NBAR + 16 + 1024;
+static_assert(DQ_SMEM <= 232448, "dq kernel: more than 227 KB of shared memory");
+
+__global__ void __launch_bounds__(BWD_NT, 1)
+attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_constant__ CUtensorMap tq64,
+                      const __grid_constant__ CUtensorMap tdo128, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + DQ_OFF_BAR;
   const uint32_t bar_qdo = bars;
-  auto bar_kv = [&](int s) { return bars + 8u * (1 + s); };
-  const uint32_t bar_sdp = bars + 8u * (1 + KV_STAGES);
-  const uint32_t bar_fin = bars + 8u * (2 + KV_STAGES);
-  const uint32_t bar_drain = bars + 8u * (3 + KV_STAGES);
+  auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bars + 8u * (1 + DQ_KST + s); };
+  auto sdp_full = [&](int b) { return bars + 8u * (1 + 2 * DQ_KST + b); };
+  auto sdp_empty = [&](int b) { return bars + 8u * (3 + 2 * DQ_KST + b); };
+  auto ds_full = [&](int b) { return bars + 8u * (5 + 2 * DQ_KST + b); };
+  auto ds_empty = [&](int b) { return bars + 8u * (7 + 2 * DQ_KST + b); };
+  const uint32_t bar_fin = bars + 8u * (9 + 2 * DQ_KST);
   const uint32_t tslot = bars + 8u * DQ_NBAR;
 
-  const int tid = threadIdx.x, warp = tid / 32;
-  const int tile = gridDim.x - 1 - blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int q0 = tile * BQ, row0 = b * a.S;
-  const int nkv_all = (a.S + BKV - 1) / BKV;
-  const int n = a.causal ? min(tile + 1, nkv_all) : nkv_all;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // grid (heads, batch, tiles): the slowest index runs longest causal rows first
+  const int tile = gridDim.z - 1 - blockIdx.z;
+  const int h = blockIdx.x, bb = blockIdx.y;
+  const int q0 = tile * BQ, row0 = bb * a.S;
+  const int nkv_all = (a.S + BK - 1) / BK;
+  const int n = a.causal ? min(2 * tile + 2, nkv_all) : nkv_all;
   const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
+  if (tid == 0) tl_cta(1, 0);
 
   if (tid == 0) {
     ptx::mbar_init(bar_qdo, 1);
-    for (int s2 = 0; s2 < KV_STAGES; ++s2) ptx::mbar_init(bar_kv(s2), 1);
-    ptx::mbar_init(bar_sdp, 1);
+    for (int s = 0; s < DQ_KST; ++s) {
+      ptx::mbar_init(kv_full(s), 1);
+      ptx::mbar_init(kv_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(sdp_full(b), 1);
+      ptx::mbar_init(sdp_empty(b), 8);
+      ptx::mbar_init(ds_full(b), 8);
+      ptx::mbar_init(ds_empty(b), 1);
+    }
     ptx::mbar_init(bar_fin, 1);
-    ptx::mbar_init(bar_drain, 1);
     ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tq);
-    ptx::prefetch_tmap(&tdo);
+    ptx::prefetch_tmap(&tq128);
+    ptx::prefetch_tmap(&tq64);
+    ptx::prefetch_tmap(&tdo128);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tmem_alloc(tslot, 512);
     ptx::tmem_relinquish();
   }
@@ -410,191 +500,174 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
-  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256;
+  auto t_s = [&](int b) { return tmem + (uint32_t)(b * 128); };
+  auto t_dp = [&](int b) { return tmem + (uint32_t)(b * 128 + 64); };
+  const uint32_t t_dq = tmem + 256;
   progress(1, 2);
   pdl_wait();
   pdl_trigger();
   progress(1, 3);
-
   bool ok = true;
-  uint32_t kv_issued = 0, kv_par = 0;
-  auto load_kv = [&](int j) {
-    const int st = j % KV_STAGES;
-    ptx::mbar_arrive_expect_tx(bar_kv(st), 2 * TILE);
-    const uint32_t kt = base + DQ_OFF_K + st * TILE, vt = base + DQ_OFF_V + st * TILE;
-    const int r = row0 + j * BKV;
-    ptx::tma_load_2d(kt, &tq, bar_kv(st), col_k, r);
-    ptx::tma_load_2d(kt + BOX, &tq, bar_kv(st), col_k + 64, r);
-    ptx::tma_load_2d(vt, &tq, bar_kv(st), col_v, r);
-    ptx::tma_load_2d(vt + BOX, &tq, bar_kv(st), col_v + 64, r);
-    kv_issued |= 1u << st;
-    kv_par = (kv_par & ~(1u << st)) | ((uint32_t)((j / KV_STAGES) & 1) << st);
-  };
-  auto issue_sdp = [&](int j) {  // S = Q K_j^T, dP = dO V_j^T
-    const uint32_t kt = base + DQ_OFF_K + (j % KV_STAGES) * TILE;
-    const uint32_t vt = base + DQ_OFF_V + (j % KV_STAGES) * TILE;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      ptx::mma_bf16(t_s, kmajor_desc(base + DQ_OFF_Q, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      ptx::mma_bf16(t_dp, kmajor_desc(base + DQ_OFF_DO, kk), kmajor_desc(vt, kk), IDESC_S, kk > 0);
-    ptx::mma_commit(bar_sdp);
-  };
 
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(bar_qdo, 2 * TILE);
-    ptx::tma_load_2d(base + DQ_OFF_Q, &tq, bar_qdo, col_q, row0 + q0);
-    ptx::tma_load_2d(base + DQ_OFF_Q + BOX, &tq, bar_qdo, col_q + 64, row0 + q0);
-    ptx::tma_load_2d(base + DQ_OFF_DO, &tdo, bar_qdo, h * D, row0 + q0);
-    ptx::tma_load_2d(base + DQ_OFF_DO + BOX, &tdo, bar_qdo, h * D + 64, row0 + q0);
-    for (int j = 0; j < KV_STAGES && j < n; ++j) load_kv(j);
-    progress(1, 4);
-    ok = ptx::mbar_wait(bar_qdo, 0);
-    if (!ok) wait_failed(101);
-    ok = ok && ptx::mbar_wait(bar_kv(0), 0);
-    if (!ok) wait_failed(102);
-    if (ok) {
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(bar_qdo, 2 * TILE);
+      ptx::tma_load_2d(base + DQ_OFF_Q, &tq128, bar_qdo, col_q, row0 + q0);
+      ptx::tma_load_2d(base + DQ_OFF_Q + BOX, &tq128, bar_qdo, col_q + 64, row0 + q0);
+      ptx::tma_load_2d(base + DQ_OFF_DO, &tdo128, bar_qdo, h * D, row0 + q0);
+      ptx::tma_load_2d(base + DQ_OFF_DO + BOX, &tdo128, bar_qdo, h * D + 64, row0 + q0);
+      uint32_t issued = 0, par = 0;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % DQ_KST;
+        if (j >= DQ_KST && !ptx::mbar_wait(kv_empty(s), ((j / DQ_KST) & 1) ^ 1, BWD_WAIT)) {
+          ok = false;
+          wait_failed(101);
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(kv_full(s), 2 * T64);
+        const uint32_t kt = base + DQ_OFF_K + s * T64, vt = base + DQ_OFF_V + s * T64;
+        const int r = row0 + j * BK;
+        ptx::tma_load_2d(kt, &tq64, kv_full(s), col_k, r);
+        ptx::tma_load_2d(kt + BOX64, &tq64, kv_full(s), col_k + 64, r);
+        ptx::tma_load_2d(vt, &tq64, kv_full(s), col_v, r);
+        ptx::tma_load_2d(vt + BOX64, &tq64, kv_full(s), col_v + 64, r);
+        issued |= 1u << s;
+        par = (par & ~(1u << s)) | ((uint32_t)((j / DQ_KST) & 1) << s);
+      }
+      // every load issued has landed before the CTA may exit
+      bool dr = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
+      for (int s = 0; s < DQ_KST; ++s)
+        if ((issued >> s) & 1u) dr = ptx::mbar_wait(kv_full(s), (par >> s) & 1u, BWD_WAIT) && dr;
+      if (!dr) wait_failed(102);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      ok = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
+      if (!ok) wait_failed(103);
+      auto sdp = [&](int j) {  // S_j = Q K_j^T, dP_j = dO V_j^T into TMEM buffer j % 2
+        const int s = j % DQ_KST, b = j & 1;
+        if (!ptx::mbar_wait(kv_full(s), (j / DQ_KST) & 1, BWD_WAIT)) { wait_failed(104); return false; }
+        if (j >= 2 && !ptx::mbar_wait(sdp_empty(b), ((j / 2) & 1) ^ 1, BWD_WAIT)) {
+          wait_failed(105);
+          return false;
+        }
+        ptx::tc_fence_after();
+        const uint32_t kt = base + DQ_OFF_K + s * T64, vt = base + DQ_OFF_V + s * T64;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16(t_s(b), kmajor_desc(base + DQ_OFF_Q, kk), kmajor64_desc(kt, kk), IDESC_N64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16(t_dp(b), kmajor_desc(base + DQ_OFF_DO, kk), kmajor64_desc(vt, kk), IDESC_N64, kk > 0);
+        ptx::mma_commit(sdp_full(b));
+        tl_block(1, j, 0);
+        return true;
+      };
+      auto acc = [&](int j) {  // dQ += dS_j K_j
+        const int s = j % DQ_KST, b = j & 1;
+        if (!ptx::mbar_wait(ds_full(b), (j / 2) & 1, BWD_WAIT)) { wait_failed(106); return false; }
+        ptx::tc_fence_after();
+        const uint32_t kt = base + DQ_OFF_K + s * T64;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          ptx::mma_bf16(t_dq, kmajor_blk_desc(base + DQ_OFF_DS + b * PB, kk), mnmajor64_desc(kt, kk),
+                        IDESC_ACC, (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(ds_empty(b));
+        ptx::mma_commit(kv_empty(s));
+        tl_block(1, j, 1);
+        return true;
+      };
+      if (ok && n > 0) ok = sdp(0);
+      for (int j = 1; j < n && ok; ++j) ok = sdp(j) && acc(j - 1);
+      if (ok && n > 0) ok = acc(n - 1);
+      ptx::mma_commit(bar_fin);  // completes once every MMA issued above has
+      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(107); }
+    }
+  } else {
+    const int qq = warp & 3, half = (warp - 2) >> 2;
+    const int row = qq * 32 + lane, qi = q0 + row;
+    const bool valid_q = qi < a.S;
+    const float lse2 = valid_q ? a.lse[(int64_t)h * a.M + row0 + qi] * 1.4426950408889634f : 0.f;
+    const float dlt = valid_q ? a.delta[(int64_t)h * a.M + row0 + qi] : 0.f;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    for (int j = 0; j < n && ok; ++j) {
+      const int b = j & 1;
+      if (!warp_wait(sdp_full(b), (j / 2) & 1)) { ok = false; if (lane == 0) wait_failed(108); break; }
+      if (warp == 2 && lane == 0) tl_block(1, j, 2);
       ptx::tc_fence_after();
-      issue_sdp(0);
-    }
-    progress(1, 5);
-  }
-
-  const int qi = q0 + tid;
-  const bool valid_q = qi < a.S;
-  const float lse2 = valid_q ? a.lse[(int64_t)h * a.M + row0 + qi] * 1.4426950408889634f : 0.f;
-  const float dlt = valid_q ? a.delta[(int64_t)h * a.M + row0 + qi] : 0.f;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  bool done_all = true;
-
-  for (int j = 0; j < n; ++j) {
-    // (a) S_j, dP_j ready; dQ_{j-1} (issued before them) is complete too, so
-    //     the dS buffer and K/V stage (j-1) % 2 are free
-    progress(1, 10 + 10 * j);
-    if (!ptx::mbar_wait(bar_sdp, j & 1)) {
-      ok = false;
-      wait_failed(103);
-    }
-    ptx::tc_fence_after();
-    progress(1, 11 + 10 * j);
-    if (tid == 0 && ok && j + 1 < n && j + 1 >= KV_STAGES) load_kv(j + 1);
-    // (b) dS = P * (dP - delta) into the swizzled dS buffer
-    const int kbase = j * BKV;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BKV; c0 += 32) {
       float v[32], w[32];
-      ptx::tmem_ld32(t_s + lane_off + c0, v);
-      ptx::tmem_ld32(t_dp + lane_off + c0, w);
+      ptx::tmem_ld32(t_s(b) + lane_off + half * 32, v);
+      ptx::tmem_ld32(t_dp(b) + lane_off + half * 32, w);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sdp_empty(b));  // the TMEM buffer may be overwritten
+      const int kbase = j * BK + half * 32;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int key = kbase + c0 + i;
+        const int key = kbase + i;
         const bool valid = valid_q && key < a.S && (!a.causal || key <= qi);
         const float p = valid ? fast_exp2(v[i] * a.scale_log2 - lse2) : 0.f;
         v[i] = p * (w[i] - dlt);
       }
-      uint8_t* rowp = gbase + DQ_OFF_DS + (c0 >> 6) * BOX + tid * 128;
+      if (j >= 2 && !warp_wait(ds_empty(b), ((j / 2) & 1) ^ 1)) {
+        ok = false;
+        if (lane == 0) wait_failed(109);
+        break;
+      }
+      store_row_half(gbase + DQ_OFF_DS + b * PB, row, half, v);
+      ptx::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ds_full(b));
+      if (warp == 2 && lane == 0) tl_block(1, j, 3);
+    }
+    // the last accumulation is complete (or the MMA thread gave up)
+    const bool fin = warp_wait(bar_fin, 0);
+    ptx::tc_fence_after();
+    float v0[32], v1[32];  // tcgen05.ld is warp-collective: every lane loads
+    ptx::tmem_ld32(t_dq + lane_off + half * 64, v0);
+    ptx::tmem_ld32(t_dq + lane_off + half * 64 + 32, v1);
+    if (ok && fin && valid_q) {
+      uint4* out = reinterpret_cast<uint4*>(a.dqkv + (int64_t)(row0 + qi) * 3 * a.H + h * D + half * 64);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int unit = ((c0 & 63) >> 3) + u;
-        *reinterpret_cast<uint4*>(rowp + ((unit ^ (tid & 7)) << 4)) =
-            make_uint4(pack2(v[8 * u], v[8 * u + 1]), pack2(v[8 * u + 2], v[8 * u + 3]),
-                       pack2(v[8 * u + 4], v[8 * u + 5]), pack2(v[8 * u + 6], v[8 * u + 7]));
+        out[u] = make_uint4(pack2(v0[8 * u] * a.scale, v0[8 * u + 1] * a.scale),
+                            pack2(v0[8 * u + 2] * a.scale, v0[8 * u + 3] * a.scale),
+                            pack2(v0[8 * u + 4] * a.scale, v0[8 * u + 5] * a.scale),
+                            pack2(v0[8 * u + 6] * a.scale, v0[8 * u + 7] * a.scale));
+        out[4 + u] = make_uint4(pack2(v1[8 * u] * a.scale, v1[8 * u + 1] * a.scale),
+                                pack2(v1[8 * u + 2] * a.scale, v1[8 * u + 3] * a.scale),
+                                pack2(v1[8 * u + 4] * a.scale, v1[8 * u + 5] * a.scale),
+                                pack2(v1[8 * u + 6] * a.scale, v1[8 * u + 7] * a.scale));
       }
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    ptx::tc_fence_before();
-    if (__syncthreads_or(!ok)) {
-      done_all = false;
-      break;
-    }
-    // (d) dQ += dS K_j; then S_{j+1}, dP_{j+1}
-    progress(1, 12 + 10 * j);
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      const uint32_t kt = base + DQ_OFF_K + (j % KV_STAGES) * TILE;
-#pragma unroll
-      for (int kk = 0; kk < BKV / 16; ++kk)
-        ptx::mma_bf16(t_dq, kmajor_desc(base + DQ_OFF_DS, kk), mnmajor_desc(kt, kk), IDESC_PV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      if (j + 1 < n) {
-        ok = ptx::mbar_wait(bar_kv((j + 1) % KV_STAGES), ((j + 1) / KV_STAGES) & 1);
-        if (!ok) wait_failed(104);
-        if (ok) issue_sdp(j + 1);
-      }
-    }
-  }
-  progress(1, 900);
-  if (tid == 0) ptx::mma_commit(bar_fin);
-  if (!ptx::mbar_wait(bar_fin, 0)) {
-    ok = false;
-    wait_failed(105);
-  }
-  ptx::tc_fence_after();
-  progress(1, 950);
-  // tcgen05.ld is warp-collective: every thread loads, only valid rows store.
-  if (done_all && n > 0) {
-    const bool store = ok && valid_q;
-    uint4* out = reinterpret_cast<uint4*>(a.dqkv + (int64_t)(row0 + qi) * 3 * a.H + h * D);
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      float v[32];
-      ptx::tmem_ld32(t_dq + lane_off + c0, v);
-      if (store) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          out[c0 / 8 + u] = make_uint4(
-              pack2(v[8 * u] * a.scale, v[8 * u + 1] * a.scale),
-              pack2(v[8 * u + 2] * a.scale, v[8 * u + 3] * a.scale),
-              pack2(v[8 * u + 4] * a.scale, v[8 * u + 5] * a.scale),
-              pack2(v[8 * u + 6] * a.scale, v[8 * u + 7] * a.scale));
-      }
-    }
-  }
-  if (!(done_all && ok)) atomicExch(&g_attn_error, 3);
-  if (tid == 0) {
-    ptx::mma_commit(bar_drain);
-    bool dr = ptx::mbar_wait(bar_drain, 0);
-    for (int s2 = 0; s2 < KV_STAGES; ++s2)
-      if ((kv_issued >> s2) & 1u) dr = ptx::mbar_wait(bar_kv(s2), (kv_par >> s2) & 1u) && dr;
-    dr = ptx::mbar_wait(bar_qdo, 0) && dr;
-    if (!dr) wait_failed(106);
+    if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 3);
   }
   progress(1, 990);
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
   progress(1, 999);
+  if (tid == 0) tl_cta(1, 1);
 }
 
-// dkv kernel: 64-query blocks stored as two 64x64 boxes.
-constexpr int QB = 64;
-constexpr int BOX64 = 64 * 64 * 2;   // 8 KB
-constexpr int QTILE = 2 * BOX64;     // 64 rows x 128 dims
-constexpr int KV_OFF_K = 0, KV_OFF_V = TILE, KV_OFF_ST = 2 * TILE;  // stages: Q then dO
-constexpr int KV_STAGE = 2 * QTILE;
-constexpr int KV_OFF_PT = KV_OFF_ST + KV_STAGES * KV_STAGE;
-constexpr int KV_OFF_DST = KV_OFF_PT + 128 * QB * 2;
-constexpr int KV_OFF_STAT = KV_OFF_DST + 128 * QB * 2;  // lse2 / delta, [2][2][QB] floats
-constexpr int KV_OFF_BAR = KV_OFF_STAT + 4 * QB * 4;
-constexpr int KV_NBAR = 1 + KV_STAGES + 1 + 1 + 1;  // K+V, q+dO stages, st+dpt, final, drain
+// dkv kernel shared-memory map: K, V of the CTA's 128 keys, three Q/dO stages
+// of 64 queries with their LSE (log2 units) and delta, two P^T and two dS^T
+// buffers.
+constexpr int KV_QST = 3;
+constexpr int KV_OFF_K = 0, KV_OFF_V = TILE, KV_OFF_Q = 2 * TILE;
+constexpr int KV_OFF_DO = KV_OFF_Q + KV_QST * T64;
+constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + 2 * PB;
+constexpr int KV_OFF_STAT = KV_OFF_DST + 2 * PB;  // [stage][lse2[64] | delta[64]] fp32
+constexpr int KV_OFF_BAR = KV_OFF_STAT + KV_QST * 2 * BK * 4;
+// kv, q_full[2], q_empty[2], sdp_full[2], sdp_empty[2], pd_full[2], pd_empty[2], fin
+constexpr int KV_NBAR = 1 + 2 * KV_QST + 8 + 1;
 constexpr int KV_SMEM = KV_OFF_BAR + 8 * KV_NBAR + 16 + 1024;
-// S^T = K Q^T: M = 128 keys, N = 64 queries, both K-major (over d).
-constexpr uint32_t IDESC_ST = ptx::idesc_bf16_f32(128, QB, false, false);
-// dV = P^T dO, dK = dS^T Q: M = 128 keys, N = 128 dims; A K-major (over queries), B MN-major.
-constexpr uint32_t IDESC_DKV = ptx::idesc_bf16_f32(128, D, false, true);
+static_assert(KV_SMEM <= 232448, "dkv kernel: more than 227 KB of shared memory");
 
-__device__ __forceinline__ uint64_t kmajor64_desc(uint32_t tile, int kk) {  // [64 rows][128 cols]
-  return ptx::smem_desc_sw128(tile + (kk >> 2) * BOX64 + (kk & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mnmajor64_desc(uint32_t tile, int kk) {  // [64 k][128 n]
-  return ptx::smem_desc_sw128(tile + kk * 2048, BOX64, 1024);
-}
-
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(BWD_NT, 1)
 attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
                        const __grid_constant__ CUtensorMap tdo64, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -603,33 +676,45 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + KV_OFF_BAR;
   const uint32_t bar_kv = bars;
-  auto bar_qd = [&](int s) { return bars + 8u * (1 + s); };
-  const uint32_t bar_st = bars + 8u * (1 + KV_STAGES);
-  const uint32_t bar_fin = bars + 8u * (2 + KV_STAGES);
-  const uint32_t bar_drain = bars + 8u * (3 + KV_STAGES);
+  auto q_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto q_empty = [&](int s) { return bars + 8u * (1 + KV_QST + s); };
+  auto sdp_full = [&](int b) { return bars + 8u * (1 + 2 * KV_QST + b); };
+  auto sdp_empty = [&](int b) { return bars + 8u * (3 + 2 * KV_QST + b); };
+  auto pd_full = [&](int b) { return bars + 8u * (5 + 2 * KV_QST + b); };
+  auto pd_empty = [&](int b) { return bars + 8u * (7 + 2 * KV_QST + b); };
+  const uint32_t bar_fin = bars + 8u * (9 + 2 * KV_QST);
   const uint32_t tslot = bars + 8u * KV_NBAR;
-  float* stat = reinterpret_cast<float*>(gbase + KV_OFF_STAT);  // [buf][lse2 | delta][QB]
+  float* stat = reinterpret_cast<float*>(gbase + KV_OFF_STAT);
 
-  const int tid = threadIdx.x, warp = tid / 32;
-  const int ktile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int k0 = ktile * 128, row0 = b * a.S;
-  const int nq_all = (a.S + QB - 1) / QB;
-  const int i0 = a.causal ? k0 / QB : 0;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // grid (heads, batch, tiles): key tile 0 (the most query blocks) first
+  const int ktile = blockIdx.z, h = blockIdx.x, bb = blockIdx.y;
+  const int k0 = ktile * 128, row0 = bb * a.S;
+  const int nq_all = (a.S + BK - 1) / BK;
+  const int i0 = a.causal ? k0 / BK : 0;  // query blocks before the diagonal see none of these keys
   const int n = nq_all - i0;
   const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
+  if (tid == 0) tl_cta(2, 0);
 
   if (tid == 0) {
     ptx::mbar_init(bar_kv, 1);
-    for (int s2 = 0; s2 < KV_STAGES; ++s2) ptx::mbar_init(bar_qd(s2), 1);
-    ptx::mbar_init(bar_st, 1);
+    for (int s = 0; s < KV_QST; ++s) {
+      ptx::mbar_init(q_full(s), 1);
+      ptx::mbar_init(q_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(sdp_full(b), 1);
+      ptx::mbar_init(sdp_empty(b), 8);
+      ptx::mbar_init(pd_full(b), 8);
+      ptx::mbar_init(pd_empty(b), 1);
+    }
     ptx::mbar_init(bar_fin, 1);
-    ptx::mbar_init(bar_drain, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tkv);
     ptx::prefetch_tmap(&tq64);
     ptx::prefetch_tmap(&tdo64);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tmem_alloc(tslot, 512);
     ptx::tmem_relinquish();
   }
@@ -637,184 +722,180 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
-  const uint32_t t_st = tmem, t_dpt = tmem + 64, t_dv = tmem + 128, t_dk = tmem + 256;
+  auto t_st = [&](int b) { return tmem + (uint32_t)(b * 128); };
+  auto t_dpt = [&](int b) { return tmem + (uint32_t)(b * 128 + 64); };
+  const uint32_t t_dv = tmem + 256, t_dk = tmem + 384;
   progress(2, 2);
   pdl_wait();
   pdl_trigger();
   progress(2, 3);
-
   bool ok = true;
-  uint32_t qd_issued = 0, qd_par = 0;
-  auto load_qd = [&](int ii) {  // query block i0 + ii into stage ii % 2
-    const int st = ii % KV_STAGES;
-    const uint32_t qt = base + KV_OFF_ST + st * KV_STAGE, dt = qt + QTILE;
-    const int r = row0 + (i0 + ii) * QB;
-    ptx::mbar_arrive_expect_tx(bar_qd(st), KV_STAGE);
-    ptx::tma_load_2d(qt, &tq64, bar_qd(st), col_q, r);
-    ptx::tma_load_2d(qt + BOX64, &tq64, bar_qd(st), col_q + 64, r);
-    ptx::tma_load_2d(dt, &tdo64, bar_qd(st), h * D, r);
-    ptx::tma_load_2d(dt + BOX64, &tdo64, bar_qd(st), h * D + 64, r);
-    qd_issued |= 1u << st;
-    qd_par = (qd_par & ~(1u << st)) | ((uint32_t)((ii / KV_STAGES) & 1) << st);
-  };
-  auto issue_st = [&](int ii) {  // S^T = K Q_i^T, dP^T = V dO_i^T
-    const uint32_t qt = base + KV_OFF_ST + (ii % KV_STAGES) * KV_STAGE, dt = qt + QTILE;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      ptx::mma_bf16(t_st, kmajor_desc(base + KV_OFF_K, kk), kmajor64_desc(qt, kk), IDESC_ST, kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      ptx::mma_bf16(t_dpt, kmajor_desc(base + KV_OFF_V, kk), kmajor64_desc(dt, kk), IDESC_ST, kk > 0);
-    ptx::mma_commit(bar_st);
-  };
 
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(bar_kv, 2 * TILE);
-    ptx::tma_load_2d(base + KV_OFF_K, &tkv, bar_kv, col_k, row0 + k0);
-    ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, bar_kv, col_k + 64, row0 + k0);
-    ptx::tma_load_2d(base + KV_OFF_V, &tkv, bar_kv, col_v, row0 + k0);
-    ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, bar_kv, col_v + 64, row0 + k0);
-    for (int ii = 0; ii < KV_STAGES && ii < n; ++ii) load_qd(ii);
-    progress(2, 4);
-    ok = ptx::mbar_wait(bar_kv, 0);
-    if (!ok) wait_failed(201);
-    ok = ok && (n <= 0 || ptx::mbar_wait(bar_qd(0), 0));
-    if (!ok) wait_failed(202);
-    if (ok && n > 0) {
+  if (warp == 0) {
+    uint32_t issued = 0, par = 0;
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(bar_kv, 2 * TILE);
+      ptx::tma_load_2d(base + KV_OFF_K, &tkv, bar_kv, col_k, row0 + k0);
+      ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, bar_kv, col_k + 64, row0 + k0);
+      ptx::tma_load_2d(base + KV_OFF_V, &tkv, bar_kv, col_v, row0 + k0);
+      ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, bar_kv, col_v + 64, row0 + k0);
+    }
+    for (int ii = 0; ii < n; ++ii) {
+      const int s = ii % KV_QST, i = i0 + ii;
+      if (ii >= KV_QST && !warp_wait(q_empty(s), ((ii / KV_QST) & 1) ^ 1)) {
+        ok = false;
+        if (lane == 0) wait_failed(201);
+        break;
+      }
+      // the block's LSE (log2 units) and delta, written by the whole warp
+      float* st = stat + s * 2 * BK;
+      for (int t = lane; t < BK; t += 32) {
+        const int q = i * BK + t;
+        const bool vq = q < a.S;
+        st[t] = vq ? a.lse[(int64_t)h * a.M + row0 + q] * 1.4426950408889634f : 0.f;
+        st[BK + t] = vq ? a.delta[(int64_t)h * a.M + row0 + q] : 0.f;
+      }
+      __syncwarp();  // the warp's stores precede lane 0's arrive on the stage barrier
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(q_full(s), 2 * T64);
+        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+        const int r = row0 + i * BK;
+        ptx::tma_load_2d(qt, &tq64, q_full(s), col_q, r);
+        ptx::tma_load_2d(qt + BOX64, &tq64, q_full(s), col_q + 64, r);
+        ptx::tma_load_2d(dt, &tdo64, q_full(s), h * D, r);
+        ptx::tma_load_2d(dt + BOX64, &tdo64, q_full(s), h * D + 64, r);
+        issued |= 1u << s;
+        par = (par & ~(1u << s)) | ((uint32_t)((ii / KV_QST) & 1) << s);
+      }
+    }
+    if (lane == 0) {
+      bool dr = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
+      for (int s = 0; s < KV_QST; ++s)
+        if ((issued >> s) & 1u) dr = ptx::mbar_wait(q_full(s), (par >> s) & 1u, BWD_WAIT) && dr;
+      if (!dr) wait_failed(202);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      ok = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
+      if (!ok) wait_failed(203);
+      auto sdp = [&](int ii) {  // S^T = K Q_i^T, dP^T = V dO_i^T into TMEM buffer ii % 2
+        const int s = ii % KV_QST, b = ii & 1;
+        if (!ptx::mbar_wait(q_full(s), (ii / KV_QST) & 1, BWD_WAIT)) { wait_failed(204); return false; }
+        if (ii >= 2 && !ptx::mbar_wait(sdp_empty(b), ((ii / 2) & 1) ^ 1, BWD_WAIT)) {
+          wait_failed(205);
+          return false;
+        }
+        ptx::tc_fence_after();
+        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16(t_st(b), kmajor_desc(base + KV_OFF_K, kk), kmajor64_desc(qt, kk), IDESC_N64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16(t_dpt(b), kmajor_desc(base + KV_OFF_V, kk), kmajor64_desc(dt, kk), IDESC_N64, kk > 0);
+        ptx::mma_commit(sdp_full(b));
+        tl_block(2, ii, 0);
+        return true;
+      };
+      auto acc = [&](int ii) {  // dV += P^T dO_i, dK += dS^T Q_i
+        const int s = ii % KV_QST, b = ii & 1;
+        if (!ptx::mbar_wait(pd_full(b), (ii / 2) & 1, BWD_WAIT)) { wait_failed(206); return false; }
+        ptx::tc_fence_after();
+        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t accum = (ii > 0 || kk > 0) ? 1u : 0u;
+          ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT + b * PB, kk), mnmajor64_desc(dt, kk),
+                        IDESC_ACC, accum);
+          ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST + b * PB, kk), mnmajor64_desc(qt, kk),
+                        IDESC_ACC, accum);
+        }
+        ptx::mma_commit(pd_empty(b));
+        ptx::mma_commit(q_empty(s));
+        tl_block(2, ii, 1);
+        return true;
+      };
+      if (ok && n > 0) ok = sdp(0);
+      for (int ii = 1; ii < n && ok; ++ii) ok = sdp(ii) && acc(ii - 1);
+      if (ok && n > 0) ok = acc(n - 1);
+      ptx::mma_commit(bar_fin);
+      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(207); }
+    }
+  } else {
+    const int qq = warp & 3, half = (warp - 2) >> 2;
+    const int row = qq * 32 + lane, kj = k0 + row;
+    const bool valid_k = kj < a.S;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    for (int ii = 0; ii < n && ok; ++ii) {
+      const int s = ii % KV_QST, b = ii & 1, i = i0 + ii;
+      // this block's S^T, dP^T are in TMEM (which also means its stage has landed)
+      if (!warp_wait(sdp_full(b), (ii / 2) & 1) || !warp_wait(q_full(s), (ii / KV_QST) & 1)) {
+        ok = false;
+        if (lane == 0) wait_failed(208);
+        break;
+      }
+      if (warp == 2 && lane == 0) tl_block(2, ii, 2);
       ptx::tc_fence_after();
-      issue_st(0);
-    }
-    progress(2, 5);
-  }
-
-  const int kj = k0 + tid;
-  const bool valid_k = kj < a.S;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  bool done_all = true;
-
-  for (int ii = 0; ii < n; ++ii) {
-    const int i = i0 + ii;
-    float* lse_s = stat + (ii & 1) * 2 * QB;
-    float* dl_s = lse_s + QB;
-    if (tid < QB) {
-      const int q = i * QB + tid;
-      lse_s[tid] = q < a.S ? a.lse[(int64_t)h * a.M + row0 + q] * 1.4426950408889634f : 0.f;
-      dl_s[tid] = q < a.S ? a.delta[(int64_t)h * a.M + row0 + q] : 0.f;
-    }
-    __syncthreads();
-    // (a) S^T, dP^T of block i ready; dK/dV MMAs of block i-1 are complete, so
-    //     P^T / dS^T buffers and stage (ii-1) % 2 are free
-    progress(2, 10 + 10 * ii);
-    if (!ptx::mbar_wait(bar_st, ii & 1)) {
-      ok = false;
-      wait_failed(203);
-    }
-    ptx::tc_fence_after();
-    progress(2, 11 + 10 * ii);
-    if (tid == 0 && ok && ii + 1 < n && ii + 1 >= KV_STAGES) load_qd(ii + 1);
-    // (b) P^T and dS^T rows of this key
-#pragma unroll
-    for (int c0 = 0; c0 < QB; c0 += 32) {
       float v[32], w[32];
-      ptx::tmem_ld32(t_st + lane_off + c0, v);
-      ptx::tmem_ld32(t_dpt + lane_off + c0, w);
+      ptx::tmem_ld32(t_st(b) + lane_off + half * 32, v);
+      ptx::tmem_ld32(t_dpt(b) + lane_off + half * 32, w);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
+      const float* st = stat + s * 2 * BK + half * 32;
+      const int qbase = i * BK + half * 32;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const int q = i * QB + c0 + c;
+        const int q = qbase + c;
         const bool valid = valid_k && q < a.S && (!a.causal || kj <= q);
-        const float p = valid ? fast_exp2(v[c] * a.scale_log2 - lse_s[c0 + c]) : 0.f;
+        const float p = valid ? fast_exp2(v[c] * a.scale_log2 - st[c]) : 0.f;
         v[c] = p;
-        w[c] = p * (w[c] - dl_s[c0 + c]);
+        w[c] = p * (w[c] - st[BK + c]);
       }
-      uint8_t* prow = gbase + KV_OFF_PT + tid * 128;
-      uint8_t* drow = gbase + KV_OFF_DST + tid * 128;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int unit = (c0 >> 3) + u;
-        const int off = (unit ^ (tid & 7)) << 4;
-        *reinterpret_cast<uint4*>(prow + off) =
-            make_uint4(pack2(v[8 * u], v[8 * u + 1]), pack2(v[8 * u + 2], v[8 * u + 3]),
-                       pack2(v[8 * u + 4], v[8 * u + 5]), pack2(v[8 * u + 6], v[8 * u + 7]));
-        *reinterpret_cast<uint4*>(drow + off) =
-            make_uint4(pack2(w[8 * u], w[8 * u + 1]), pack2(w[8 * u + 2], w[8 * u + 3]),
-                       pack2(w[8 * u + 4], w[8 * u + 5]), pack2(w[8 * u + 6], w[8 * u + 7]));
+      if (ii >= 2 && !warp_wait(pd_empty(b), ((ii / 2) & 1) ^ 1)) {
+        ok = false;
+        if (lane == 0) wait_failed(209);
+        break;
       }
+      store_row_half(gbase + KV_OFF_PT + b * PB, row, half, v);
+      store_row_half(gbase + KV_OFF_DST + b * PB, row, half, w);
+      ptx::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(pd_full(b));
+      if (warp == 2 && lane == 0) tl_block(2, ii, 3);
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    ptx::tc_fence_before();
-    if (__syncthreads_or(!ok)) {
-      done_all = false;
-      break;
-    }
-    // (d) dV += P^T dO_i, dK += dS^T Q_i; then the next block's S^T, dP^T
-    progress(2, 12 + 10 * ii);
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      const uint32_t qt = base + KV_OFF_ST + (ii % KV_STAGES) * KV_STAGE, dt = qt + QTILE;
-#pragma unroll
-      for (int kk = 0; kk < QB / 16; ++kk) {
-        const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-        ptx::mma_bf16(t_dv, ptx::smem_desc_sw128(base + KV_OFF_PT + kk * 32, 16, 1024),
-                      mnmajor64_desc(dt, kk), IDESC_DKV, acc);
-        ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(base + KV_OFF_DST + kk * 32, 16, 1024),
-                      mnmajor64_desc(qt, kk), IDESC_DKV, acc);
-      }
-      if (ii + 1 < n) {
-        ok = ptx::mbar_wait(bar_qd((ii + 1) % KV_STAGES), ((ii + 1) / KV_STAGES) & 1);
-        if (!ok) wait_failed(204);
-        if (ok) issue_st(ii + 1);
-      }
-    }
-  }
-  progress(2, 900);
-  if (tid == 0) ptx::mma_commit(bar_fin);
-  if (!ptx::mbar_wait(bar_fin, 0)) {
-    ok = false;
-    wait_failed(205);
-  }
-  ptx::tc_fence_after();
-  progress(2, 950);
-  // tcgen05.ld is warp-collective: every thread loads, only valid rows store.
-  if (done_all) {
-    const bool store = ok && valid_k;
+    const bool fin = warp_wait(bar_fin, 0);
+    ptx::tc_fence_after();
     __nv_bfloat16* rowp = a.dqkv + (int64_t)(row0 + kj) * 3 * a.H;
-    uint4* dk_out = reinterpret_cast<uint4*>(rowp + a.H + h * D);
-    uint4* dv_out = reinterpret_cast<uint4*>(rowp + 2 * a.H + h * D);
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      float v[32], w[32];
-      ptx::tmem_ld32(t_dk + lane_off + c0, v);
-      ptx::tmem_ld32(t_dv + lane_off + c0, w);
-      if (store) {
+    for (int part = 0; part < 2; ++part) {  // dK (scaled), then dV
+      float v0[32], v1[32];  // tcgen05.ld is warp-collective: every lane loads
+      const uint32_t t = (part == 0 ? t_dk : t_dv) + lane_off + half * 64;
+      ptx::tmem_ld32(t, v0);
+      ptx::tmem_ld32(t + 32, v1);
+      const float sc = part == 0 ? a.scale : 1.f;
+      if (ok && fin && valid_k) {
+        uint4* out = reinterpret_cast<uint4*>(rowp + (part == 0 ? a.H : 2 * a.H) + h * D + half * 64);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          dk_out[c0 / 8 + u] = make_uint4(pack2(v[8 * u] * a.scale, v[8 * u + 1] * a.scale),
-                                          pack2(v[8 * u + 2] * a.scale, v[8 * u + 3] * a.scale),
-                                          pack2(v[8 * u + 4] * a.scale, v[8 * u + 5] * a.scale),
-                                          pack2(v[8 * u + 6] * a.scale, v[8 * u + 7] * a.scale));
-          dv_out[c0 / 8 + u] = make_uint4(pack2(w[8 * u], w[8 * u + 1]), pack2(w[8 * u + 2], w[8 * u + 3]),
-                                          pack2(w[8 * u + 4], w[8 * u + 5]), pack2(w[8 * u + 6], w[8 * u + 7]));
+          out[u] = make_uint4(pack2(v0[8 * u] * sc, v0[8 * u + 1] * sc), pack2(v0[8 * u + 2] * sc, v0[8 * u + 3] * sc),
+                              pack2(v0[8 * u + 4] * sc, v0[8 * u + 5] * sc), pack2(v0[8 * u + 6] * sc, v0[8 * u + 7] * sc));
+          out[4 + u] = make_uint4(pack2(v1[8 * u] * sc, v1[8 * u + 1] * sc), pack2(v1[8 * u + 2] * sc, v1[8 * u + 3] * sc),
+                                  pack2(v1[8 * u + 4] * sc, v1[8 * u + 5] * sc), pack2(v1[8 * u + 6] * sc, v1[8 * u + 7] * sc));
         }
       }
     }
-  }
-  if (!(done_all && ok)) atomicExch(&g_attn_error, 5);
-  if (tid == 0) {
-    ptx::mma_commit(bar_drain);
-    bool dr = ptx::mbar_wait(bar_drain, 0);
-    for (int s2 = 0; s2 < KV_STAGES; ++s2)
-      if ((qd_issued >> s2) & 1u) dr = ptx::mbar_wait(bar_qd(s2), (qd_par >> s2) & 1u) && dr;
-    dr = ptx::mbar_wait(bar_kv, 0) && dr;
-    if (!dr) wait_failed(206);
+    if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 5);
   }
   progress(2, 990);
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
   progress(2, 999);
+  if (tid == 0) tl_cta(2, 1);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -884,7 +965,9 @@ cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   fa.M = M;
   fa.causal = a.causal ? 1 : 0;
   fa.scale_log2 = 1.4426950408889634f / sqrtf((float)a.head_dim);
-  const dim3 grid((a.seq + BQ - 1) / BQ, a.heads, a.batch);
+  const int tiles = (a.seq + BQ - 1) / BQ;
+  if (tiles > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(a.heads, a.batch, tiles);
   return launch_pdl(attn_fwd_tc_kernel, grid, dim3(NT), FWD_SMEM, st, m, fa);
 }
 
@@ -925,15 +1008,20 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   ba.scale = 1.f / sqrtf((float)a.head_dim);
   ba.scale_log2 = 1.4426950408889634f * ba.scale;
   const int tiles = (a.seq + 127) / 128;
-  e = launch_pdl(attn_bwd_dq_tc_kernel, dim3(tiles, a.heads, a.batch), dim3(NT), DQ_SMEM, st,
-                 tq128, tdo128, ba);
+  if (tiles > 65535) return cudaErrorInvalidConfiguration;
+  e = launch_pdl(attn_bwd_dq_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(BWD_NT), DQ_SMEM, st,
+                 tq128, tq64, tdo128, ba);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(tiles, a.heads, a.batch), dim3(NT), KV_SMEM, st,
-                    tq128, tq64, tdo64, ba);
+  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(BWD_NT), KV_SMEM,
+                    st, tq128, tq64, tdo64, ba);
 }
 
 cudaError_t attention_set_progress(int* p) {
   return cudaMemcpyToSymbol(g_attn_progress, &p, sizeof(p));
+}
+
+cudaError_t attention_set_timeline(unsigned long long* p) {
+  return cudaMemcpyToSymbol(g_attn_timeline, &p, sizeof(p));
 }
 
 int attention_read_and_clear_error() {

@@ -291,6 +291,7 @@ int attention_read_and_clear_error();
 // Debugging aid: host-mapped int[768] that the attention kernels' thread 0
 // fills with progress markers (nullptr switches them off).
 cudaError_t attention_set_progress(int* p);
+cudaError_t attention_set_timeline(unsigned long long* p);
 cudaError_t attention_bwd_simt(const AttnArgs& a, cudaStream_t st);
 
 // Reads and clears the error word the tensor-core kernels set when a bounded
