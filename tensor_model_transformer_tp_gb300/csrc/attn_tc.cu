@@ -596,18 +596,31 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_co
       if (warp == 2 && lane == 0) tl_block(1, j, 2);
       ptx::tc_fence_after();
       float v[32], w[32];
-      ptx::tmem_ld32(t_s(b) + lane_off + half * 32, v);
-      ptx::tmem_ld32(t_dp(b) + lane_off + half * 32, w);
+      ptx::tmem_ld32x2(t_s(b) + lane_off + half * 32, t_dp(b) + lane_off + half * 32, v, w);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sdp_empty(b));  // the TMEM buffer may be overwritten
       const int kbase = j * BK + half * 32;
+      // a block wholly visible to every row of the tile needs no mask (CTA-uniform)
+      const bool full = q0 + BQ <= a.S && (j + 1) * BK <= a.S && (!a.causal || (j + 1) * BK <= q0 + 1);
+      if (full) {
+        const uint64_t sc = f2_splat(a.scale_log2), nl = f2_splat(-lse2), nd = f2_splat(-dlt);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int key = kbase + i;
-        const bool valid = valid_q && key < a.S && (!a.causal || key <= qi);
-        const float p = valid ? fast_exp2(v[i] * a.scale_log2 - lse2) : 0.f;
-        v[i] = p * (w[i] - dlt);
+        for (int i = 0; i < 32; i += 2) {
+          const uint64_t x = f2_fma(f2_pack(v[i], v[i + 1]), sc, nl);
+          const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
+          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[i], w[i + 1]), nd));
+          v[i] = f2_lo(ds);
+          v[i + 1] = f2_hi(ds);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = kbase + i;
+          const bool valid = valid_q && key < a.S && (!a.causal || key <= qi);
+          const float p = valid ? fast_exp2(v[i] * a.scale_log2 - lse2) : 0.f;
+          v[i] = p * (w[i] - dlt);
+        }
       }
       if (j >= 2 && !warp_wait(ds_empty(b), ((j / 2) & 1) ^ 1)) {
         ok = false;
@@ -837,20 +850,37 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
       if (warp == 2 && lane == 0) tl_block(2, ii, 2);
       ptx::tc_fence_after();
       float v[32], w[32];
-      ptx::tmem_ld32(t_st(b) + lane_off + half * 32, v);
-      ptx::tmem_ld32(t_dpt(b) + lane_off + half * 32, w);
+      ptx::tmem_ld32x2(t_st(b) + lane_off + half * 32, t_dpt(b) + lane_off + half * 32, v, w);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
       const float* st = stat + s * 2 * BK + half * 32;
       const int qbase = i * BK + half * 32;
+      // a query block that sees every key of the tile needs no mask (CTA-uniform)
+      const bool full = k0 + 128 <= a.S && (i + 1) * BK <= a.S && (!a.causal || i * BK >= k0 + 127);
+      if (full) {
+        const uint64_t sc = f2_splat(a.scale_log2);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int q = qbase + c;
-        const bool valid = valid_k && q < a.S && (!a.causal || kj <= q);
-        const float p = valid ? fast_exp2(v[c] * a.scale_log2 - st[c]) : 0.f;
-        v[c] = p;
-        w[c] = p * (w[c] - st[BK + c]);
+        for (int c = 0; c < 32; c += 2) {
+          const float2 l2 = *reinterpret_cast<const float2*>(st + c);       // LSE (log2 units)
+          const float2 dl = *reinterpret_cast<const float2*>(st + BK + c);  // delta
+          const uint64_t x = f2_fma(f2_pack(v[c], v[c + 1]), sc, f2_pack(-l2.x, -l2.y));
+          const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
+          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[c], w[c + 1]), f2_pack(-dl.x, -dl.y)));
+          v[c] = f2_lo(p);
+          v[c + 1] = f2_hi(p);
+          w[c] = f2_lo(ds);
+          w[c + 1] = f2_hi(ds);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int q = qbase + c;
+          const bool valid = valid_k && q < a.S && (!a.causal || kj <= q);
+          const float p = valid ? fast_exp2(v[c] * a.scale_log2 - st[c]) : 0.f;
+          v[c] = p;
+          w[c] = p * (w[c] - st[BK + c]);
+        }
       }
       if (ii >= 2 && !warp_wait(pd_empty(b), ((ii / 2) & 1) ^ 1)) {
         ok = false;
