@@ -21,9 +21,9 @@ extern "C" {
 /* D[m, n] = sum_k A(m, k) * B(n, k) for m < M, n < N, k < K, then epilogue:
  *   0 Store      C = D
  *   1 Bias       C = D + bias[n]
- *   2 BiasGelu   C2 = D + bias[n] (if C2 != NULL); C = gelu(D + bias[n])
+ *   2 BiasGelu   C = gelu(D + bias[n]); C2 = gelu'(D + bias[n]) (if C2 != NULL)
  *   3 BiasResid  C = D + bias[n] + aux[m * ld_aux + n]
- *   4 GeluBwd    C = D * gelu'(aux[m * ld_aux + n])
+ *   4 Mul        C = D * aux[m * ld_aux + n]  (GeLU backward: aux = the stored gelu')
  *   5 Accum      C (fp32) += D
  * A(m, k) = a_kmajor ? A[m * lda + k] : A[k * lda + m]; B(n, k) likewise with
  * b_kmajor / ldb.  A, B, bias and aux have type in_dtype (oases_dtype); C and

@@ -394,7 +394,9 @@ struct Exec {
     return s.pre_ln ? rowp(at(L.act[seg].u), b, s.H, s.esz) : rowp(seg_in(seg), b, s.H, s.esz);
   }
 
-  void col_fwd(int seg, int b, bool keep_preact) {
+  // Column GEMM F_i.  FFN: H = GeLU(u W1^T + b1), and with keep_grad also
+  // G = GeLU'(u W1^T + b1) (into the A buffer), all the GeLU backward needs.
+  void col_fwd(int seg, int b, bool keep_grad) {
     const ActSet& a = L.act[seg];
     const SegParams& p = sp[seg];
     const void* u = u_of(seg, b);
@@ -411,7 +413,7 @@ struct Exec {
       g.bias = p.bc;
       g.C = rowp(at(a.h), b, s.F, s.esz);
       g.ldc = s.F;
-      g.C2 = keep_preact ? rowp(at(a.a), b, s.F, s.esz) : nullptr;
+      g.C2 = keep_grad ? rowp(at(a.a), b, s.F, s.esz) : nullptr;
       ok(gemm(g, stream(b)));
     } else {
       g.N = 3 * s.H;
@@ -564,7 +566,8 @@ struct Exec {
     grad_wait(seg, GRP_WR, b);
     ok(gemm(w, stream(b)));
     grad_done(seg, GRP_WR, b);
-    // d(hin) = dy W_row; FFN: dA = dH * gelu'(A), written over A.
+    // d(hin) = dy W_row; FFN: dA = dH * G with G = gelu'(A) kept by the forward or the
+    // recompute, written over G.
     GemmArgs d = base_gemm();
     d.M = (int)s.Ms;
     d.N = Kin;
@@ -576,11 +579,11 @@ struct Exec {
     d.b_kmajor = false;
     d.ldc = Kin;
     if (ffn) {
-      void* A = rowp(at(a.a), b, s.F, s.esz);
-      d.epi = Epi::GeluBwd;
-      d.aux = A;
+      void* G = rowp(at(a.a), b, s.F, s.esz);  // GeLU'(A), overwritten by dA
+      d.epi = Epi::Mul;
+      d.aux = G;
       d.ld_aux = s.F;
-      d.C = A;
+      d.C = G;
     } else {
       d.epi = Epi::Store;
       d.C = rowp(at(a.d_o), b, s.H, s.esz);
@@ -1002,7 +1005,7 @@ extern "C" oases_status oases_debug_gemm(int M, int N, int K, int in_dtype, cons
   const Epi epi = static_cast<Epi>(epilogue);
   if ((epi == Epi::Bias || epi == Epi::BiasGelu || epi == Epi::BiasResid) && !bias)
     return OASES_ERR_INVALID_ARG;
-  if ((epi == Epi::BiasResid || epi == Epi::GeluBwd) && !aux) return OASES_ERR_INVALID_ARG;
+  if ((epi == Epi::BiasResid || epi == Epi::Mul) && !aux) return OASES_ERR_INVALID_ARG;
   if (epi == Epi::Accum && c_dtype != OASES_F32) return OASES_ERR_INVALID_ARG;
   GemmArgs g;
   g.M = M;

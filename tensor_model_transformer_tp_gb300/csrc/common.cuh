@@ -166,14 +166,16 @@ __device__ __forceinline__ void gelu2_inplace(float& a0, float& a1) {
   a0 = f2_lo(r);
   a1 = f2_hi(r);
 }
-// (v0, v1) *= (gelu'(a0), gelu'(a1))
-__device__ __forceinline__ void mul_gelu_grad2_inplace(float& v0, float& v1, float a0, float a1) {
+// (a0, a1) = (gelu(a0), gelu(a1)) and (d0, d1) = (gelu'(a0), gelu'(a1))
+__device__ __forceinline__ void gelu_and_grad2(float& a0, float& a1, float& d0, float& d1) {
   const uint64_t a = f2_pack(a0, a1);
   uint64_t cdf, pdf;
   gelu_cdf_pdf2(a, cdf, pdf);
-  const uint64_t r = f2_mul(f2_pack(v0, v1), f2_fma(a, pdf, cdf));
-  v0 = f2_lo(r);
-  v1 = f2_hi(r);
+  const uint64_t g = f2_mul(a, cdf), d = f2_fma(a, pdf, cdf);
+  a0 = f2_lo(g);
+  a1 = f2_hi(g);
+  d0 = f2_lo(d);
+  d1 = f2_hi(d);
 }
 
 // ---------------------------------------------------------------------------
@@ -186,9 +188,9 @@ __device__ __forceinline__ void mul_gelu_grad2_inplace(float& v0, float& v1, flo
 enum class Epi : int {
   Store = 0,      // C = acc
   Bias = 1,       // C = acc + bias[n]
-  BiasGelu = 2,   // C2 = acc + bias[n] (pre-activation, if C2), C = gelu(acc + bias[n])
+  BiasGelu = 2,   // C = gelu(acc + bias[n]); C2 (if given) = gelu'(acc + bias[n])
   BiasResid = 3,  // C = acc + bias[n] + aux[m, n]
-  GeluBwd = 4,    // C = acc * gelu'(aux[m, n])
+  Mul = 4,        // C = acc * aux[m, n] (the GeLU backward with aux = the stored gelu')
   Accum = 5,      // C (fp32) += acc
 };
 
@@ -205,7 +207,7 @@ struct GemmArgs {
   void* C = nullptr;
   int64_t ldc = 0;
   DType c_t = DType::BF16;
-  void* C2 = nullptr;  // BiasGelu pre-activation output, type c_t, leading dim ldc
+  void* C2 = nullptr;  // BiasGelu derivative output gelu'(acc + bias), type c_t, leading dim ldc
   const void* bias = nullptr;  // [N], type in_t
   const void* aux = nullptr;   // [M, N] with leading dim ld_aux, type aux_t
   int64_t ld_aux = 0;

@@ -16,7 +16,7 @@ __device__ __forceinline__ void epi_apply(const GemmArgs& g, int m, int n, float
       break;
     case Epi::BiasGelu: {
       const float a = acc + load_any(g.bias, g.in_t, n);
-      if (g.C2) store_any(g.C2, g.c_t, ci, a);
+      if (g.C2) store_any(g.C2, g.c_t, ci, gelu_grad_f(a));
       store_any(g.C, g.c_t, ci, gelu_f(a));
       break;
     }
@@ -25,9 +25,8 @@ __device__ __forceinline__ void epi_apply(const GemmArgs& g, int m, int n, float
                 acc + load_any(g.bias, g.in_t, n) +
                     load_any(g.aux, g.aux_t, (int64_t)m * g.ld_aux + n));
       break;
-    case Epi::GeluBwd:
-      store_any(g.C, g.c_t, ci,
-                acc * gelu_grad_f(load_any(g.aux, g.aux_t, (int64_t)m * g.ld_aux + n)));
+    case Epi::Mul:
+      store_any(g.C, g.c_t, ci, acc * load_any(g.aux, g.aux_t, (int64_t)m * g.ld_aux + n));
       break;
     case Epi::Accum: {
       float* c = static_cast<float*>(g.C);

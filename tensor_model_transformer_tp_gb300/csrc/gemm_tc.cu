@@ -122,23 +122,26 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int n, float
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] += t[i];
   }
-  if (g.epi == Epi::BiasResid || g.epi == Epi::GeluBwd) {
+  if (g.epi == Epi::BiasResid || g.epi == Epi::Mul) {
     load32_bf16(static_cast<const __nv_bfloat16*>(g.aux) + (int64_t)m * g.ld_aux + n, t);
     if (g.epi == Epi::BiasResid) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] += t[i];
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(t[i]);
+      for (int i = 0; i < 32; ++i) v[i] *= t[i];
     }
   }
   if (g.epi == Epi::BiasGelu) {
     if (g.C2) {
-      if (g.c_t == DType::BF16) store32_bf16(static_cast<__nv_bfloat16*>(g.C2) + ci, v);
+      float d[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) d[i] = gelu_grad_f(v[i]);
+      if (g.c_t == DType::BF16) store32_bf16(static_cast<__nv_bfloat16*>(g.C2) + ci, d);
       else {
         float4* c = reinterpret_cast<float4*>(static_cast<float*>(g.C2) + ci);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 8; ++i) c[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
       }
     }
 #pragma unroll
@@ -180,7 +183,7 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
         if (n + i < g.N) v[i] += __bfloat162float(b[i]);
     }
   }
-  if ((g.epi == Epi::BiasResid || g.epi == Epi::GeluBwd) && m < g.M) {
+  if ((g.epi == Epi::BiasResid || g.epi == Epi::Mul) && m < g.M) {
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(g.aux) + (int64_t)m * g.ld_aux + n;
     float t[CW];
     if (n + CW <= g.N) {
@@ -195,7 +198,11 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
       for (int i = 0; i < CW; i += 2) add2_inplace(v[i], v[i + 1], t[i], t[i + 1]);
     } else {
 #pragma unroll
-      for (int i = 0; i < CW; i += 2) mul_gelu_grad2_inplace(v[i], v[i + 1], t[i], t[i + 1]);
+      for (int i = 0; i < CW; i += 2) {
+        const uint64_t r = f2_mul(f2_pack(v[i], v[i + 1]), f2_pack(t[i], t[i + 1]));
+        v[i] = f2_lo(r);
+        v[i + 1] = f2_hi(r);
+      }
     }
   }
   // one staged store of v (as stored in C's type) to the box at (n, mw)
@@ -227,8 +234,35 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
       ptx::bulk_commit();
     }
   };
-  if (g.epi == Epi::BiasGelu) {
-    if (g.C2) stage_and_store(tmC2, false);
+  if (g.epi == Epi::BiasGelu && g.C2) {
+    // v becomes gelu(v); gelu'(v) is packed straight into the staging buffer
+    // 16 bytes at a time and stored through C2 before v is staged for C
+    if (lane == 0) ptx::bulk_wait_read0();  // the previous store has read the buffer
+    __syncwarp();
+    uint8_t* row = stg + lane * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      constexpr int E = CW / 8;  // elements per 16-byte unit
+      float d[E];
+#pragma unroll
+      for (int i = 0; i < E; i += 2) gelu_and_grad2(v[E * u + i], v[E * u + i + 1], d[i], d[i + 1]);
+      uint4 w;
+      if constexpr (E == 8) {  // bf16 output
+        w = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]), pack_bf16(d[4], d[5]),
+                       pack_bf16(d[6], d[7]));
+      } else {  // fp32 output
+        w = make_uint4(__float_as_uint(d[0]), __float_as_uint(d[1]), __float_as_uint(d[2]),
+                       __float_as_uint(d[3]));
+      }
+      *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) = w;
+    }
+    ptx::fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tmC2, stg_s, n, mw);
+      ptx::bulk_commit();
+    }
+  } else if (g.epi == Epi::BiasGelu) {
 #pragma unroll
     for (int i = 0; i < CW; i += 2) gelu2_inplace(v[i], v[i + 1]);
   }
