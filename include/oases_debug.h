@@ -114,7 +114,7 @@ oases_status oases_debug_bias_grad(const void *in, int64_t ld, int M, int N, int
  * argument: the partial rows live in a static device array of
  * OASES_NOALLOC_SCRATCH_FLOATS fp32 values (4 MiB) that every GPU which loads
  * the library keeps until the process exits.  Sizes whose partial rows do not
- * fit, ceil(M / 32) * N > OASES_NOALLOC_SCRATCH_FLOATS, are rejected with
+ * fit, ceil(M / 8) * N > OASES_NOALLOC_SCRATCH_FLOATS, are rejected with
  * OASES_ERR_UNSUPPORTED before anything is enqueued (oases_last_error() says
  * how many floats were needed).  Nothing is allocated or freed, by this call
  * or by any library routine it uses.

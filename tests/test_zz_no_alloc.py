@@ -38,7 +38,7 @@ def L():
 
 
 def test_noalloc_matches_scratch_entry_point_twice(L):
-    M, N = 2048, 512           # ceil(2048/32) * 512 = 32768 partial floats
+    M, N = 2048, 512           # ceil(2048/8) * 512 = 131072 partial floats
     gen = torch.Generator().manual_seed(7)
     stream = torch.cuda.current_stream().cuda_stream
     init = torch.randn(N, generator=gen)
@@ -61,7 +61,7 @@ def test_noalloc_matches_scratch_entry_point_twice(L):
 
 def test_noalloc_rejects_sizes_beyond_the_array(L):
     N = 4096
-    M = 32 * (NOALLOC_FLOATS // N) + 1   # one partial row too many
+    M = 8 * (NOALLOC_FLOATS // N) + 1    # one 8-row partial row too many
     out = torch.zeros(N, device="cuda")
     x = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
     st = L.oases_bias_grad_noalloc(x.data_ptr(), N, M, N, 1, out.data_ptr(), None)
