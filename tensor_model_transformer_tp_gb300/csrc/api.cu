@@ -377,6 +377,7 @@ struct Exec {
     g.in_t = s.t;
     g.c_t = s.t;
     g.aux_t = s.t;
+    g.concurrent = st[0] != st[1] && s.nsb > 1;  // the other sub-batch stream runs beside it
     return g;
   }
 

@@ -220,6 +220,10 @@ struct GemmArgs {
   // of C.  splits = 1, kpieces = 1 is the plain GEMM.
   int splits = 1, kpieces = 1;
   int64_t kpiece_stride = 0, k_extent = 0, c_split_rows = 0;
+  // 1 when another stream's work runs beside this GEMM (the two sub-batch
+  // streams): SMs that 256-wide tiles leave idle are then filled by the other
+  // stream, so the dispatcher always takes the faster 256-wide pair tiles.
+  int concurrent = 0;
 };
 
 // Returns cudaSuccess or the launch error.  Picks the tensor-core kernel when

@@ -671,7 +671,10 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
       cudaGetLastError();
     }
   }
-  const int grid = (tiles < slots ? tiles : slots) * CL;
+  // as few clusters as finish in the same number of tile rounds: the rest of
+  // the SMs stay free for other streams' kernels at no cost to this one
+  const int rounds = (tiles + slots - 1) / slots;
+  const int grid = ((tiles + rounds - 1) / rounds) * CL;
   cfg.gridDim = dim3(grid);
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -720,8 +723,8 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st) {
   const bool pair = g.M > BM;  // a second row block exists for the cluster partner
   // Pair MMAs with N = 128 move 1.5x the operand bytes per FLOP of N = 256
   // and run at about half its rate: the pair path takes 256-wide tiles unless
-  // that would leave more than half of the SMs idle.
-  const bool narrow = pair ? (g.N <= 128 || 2 * tiles256 < num_sms())
+  // that would leave more than half of the SMs idle with nothing else to run.
+  const bool narrow = pair ? (g.N <= 128 || (!g.concurrent && 2 * tiles256 < num_sms()))
                            : (g.N <= 128 || tiles256 < num_sms());
   if (narrow)
     return pair ? dispatch_major<128, 2>(g, st) : dispatch_major<128, 1>(g, st);
