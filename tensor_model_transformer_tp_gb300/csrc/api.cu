@@ -27,6 +27,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <string>
 #include <vector>
 
@@ -320,6 +321,25 @@ struct EventPool {
 EventPool& pool() {
   static EventPool p;
   return p;
+}
+
+// A non-blocking stream per device for host<->device staging copies, so they
+// overlap the compute streams (created once, kept for the process).
+cudaStream_t copy_stream() {
+  static std::mutex mu;
+  static std::unordered_map<int, cudaStream_t> m;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = m.find(dev);
+  if (it != m.end()) return it->second;
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  m[dev] = st;
+  return st;
 }
 
 struct SegParams {  // one segment's weights / grads, typed by role
@@ -829,7 +849,8 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   ex.sp.resize(s.nseg);
   for (int i = 0; i < s.nseg; ++i) ex.sp[i] = seg_params(s, i, w, gr);
   if (!params_ok(s, ex.sp, bwd)) return OASES_ERR_INVALID_ARG;
-  cudaError_t e = pool().ensure(ex.ev_base + (size_t)s.nseg * GRP_N);
+  const size_t ev_stage = ex.ev_base + (size_t)s.nseg * GRP_N;  // staging-copy events
+  cudaError_t e = pool().ensure(ev_stage + 6);
   if (e != cudaSuccess) return cuda_fail(e);
 
   // Host buffers (oases_stack_step only) are staged through the workspace.
@@ -850,13 +871,45 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   ex.dx = host[3] ? ex.at(ex.L.stage[3]) : dx;
 
   cudaEvent_t ev_in = pool().ev[0], ev_out = pool().ev[1];
+  cudaEvent_t ev_x = pool().ev[ev_stage], ev_g = pool().ev[ev_stage + 1];
+  cudaEvent_t ev_y[2] = {pool().ev[ev_stage + 2], pool().ev[ev_stage + 3]};
+  cudaEvent_t ev_end = pool().ev[ev_stage + 4], ev_cs = pool().ev[ev_stage + 5];
   const bool two = ex.st[0] != ex.st[1];
-  if (host[0] && MH) ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[0]), x, MH, cudaMemcpyHostToDevice, ex.st[0]));
-  if (host[1] && MH) ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[1]), g_host_or_dev, MH, cudaMemcpyHostToDevice, ex.st[0]));
-  if (two) {
-    ex.ok(cudaEventRecord(ev_in, ex.st[0]));
-    ex.ok(cudaStreamWaitEvent(ex.st[1], ev_in, 0));
+  // Staging copies of host buffers go on a copy stream when nothing is being
+  // captured: x first (the compute streams wait for it), then g (waited for
+  // only before each stream's first backward operator); y is copied back as
+  // soon as both streams finish the forward, dx at the end, and s0 joins the
+  // copy stream before the call returns.  Under capture they stay on s0.
+  const bool any_host = host[0] || host[1] || host[2] || host[3];
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (any_host) ex.ok(cudaStreamIsCapturing(ex.st[0], &cap));
+  cudaStream_t cs = (any_host && cap == cudaStreamCaptureStatusNone && MH > 0 && s.M > 0 && bwd)
+                        ? copy_stream() : nullptr;
+  if (cs) {
+    ex.ok(cudaEventRecord(ev_in, ex.st[0]));  // everything the caller enqueued before
+    ex.ok(cudaStreamWaitEvent(cs, ev_in, 0));
+    if (two) ex.ok(cudaStreamWaitEvent(ex.st[1], ev_in, 0));
+    if (host[0]) {
+      ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[0]), x, MH, cudaMemcpyHostToDevice, cs));
+      ex.ok(cudaEventRecord(ev_x, cs));
+      ex.ok(cudaStreamWaitEvent(ex.st[0], ev_x, 0));
+      if (two) ex.ok(cudaStreamWaitEvent(ex.st[1], ev_x, 0));
+    }
+    if (host[1]) {
+      ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[1]), g_host_or_dev, MH, cudaMemcpyHostToDevice, cs));
+      ex.ok(cudaEventRecord(ev_g, cs));
+    }
+  } else {
+    if (host[0] && MH) ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[0]), x, MH, cudaMemcpyHostToDevice, ex.st[0]));
+    if (host[1] && MH) ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[1]), g_host_or_dev, MH, cudaMemcpyHostToDevice, ex.st[0]));
+    if (two) {
+      ex.ok(cudaEventRecord(ev_in, ex.st[0]));
+      ex.ok(cudaStreamWaitEvent(ex.st[1], ev_in, 0));
+    }
   }
+  const int nstreams = two ? 2 : 1;
+  bool in_bwd[2] = {false, false};
+  int bwd_started = 0;
   g_trace.clear();
   size_t tev = 0;
   if (s.M > 0)
@@ -874,6 +927,18 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
           ex.ok(cudaEventRecord(tr.e0, ex.stream(st.sb)));
         }
       }
+      const int si = two ? (st.sb & 1) : 0;
+      if (cs && !in_bwd[si] && st.ev != EV_F && st.ev != EV_CF &&
+          !(st.ev == EV_SYNC && st.op == OP_G)) {
+        // this stream's forward is complete; its backward needs g
+        in_bwd[si] = true;
+        ex.ok(cudaEventRecord(ev_y[si], ex.st[si]));
+        if (host[1]) ex.ok(cudaStreamWaitEvent(ex.st[si], ev_g, 0));
+        if (++bwd_started == nstreams && host[2]) {
+          for (int k = 0; k < nstreams; ++k) ex.ok(cudaStreamWaitEvent(cs, ev_y[k], 0));
+          ex.ok(cudaMemcpyAsync(const_cast<void*>(y), ex.y, MH, cudaMemcpyDeviceToHost, cs));
+        }
+      }
       ex.run(st);
       if (tr.e1) {
         ex.ok(cudaEventRecord(tr.e1, ex.stream(st.sb)));
@@ -885,8 +950,23 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
     ex.ok(cudaEventRecord(ev_out, ex.st[1]));
     ex.ok(cudaStreamWaitEvent(ex.st[0], ev_out, 0));
   }
-  if (host[2] && MH) ex.ok(cudaMemcpyAsync(const_cast<void*>(y), ex.y, MH, cudaMemcpyDeviceToHost, ex.st[0]));
-  if (host[3] && MH) ex.ok(cudaMemcpyAsync(dx, ex.dx, MH, cudaMemcpyDeviceToHost, ex.st[0]));
+  if (cs) {
+    if (host[2] && bwd_started < nstreams) {  // no backward operator ran: copy y now
+      ex.ok(cudaEventRecord(ev_end, ex.st[0]));
+      ex.ok(cudaStreamWaitEvent(cs, ev_end, 0));
+      ex.ok(cudaMemcpyAsync(const_cast<void*>(y), ex.y, MH, cudaMemcpyDeviceToHost, cs));
+    }
+    if (host[3]) {
+      ex.ok(cudaEventRecord(ev_end, ex.st[0]));
+      ex.ok(cudaStreamWaitEvent(cs, ev_end, 0));
+      ex.ok(cudaMemcpyAsync(dx, ex.dx, MH, cudaMemcpyDeviceToHost, cs));
+    }
+    ex.ok(cudaEventRecord(ev_cs, cs));
+    ex.ok(cudaStreamWaitEvent(ex.st[0], ev_cs, 0));  // completion is signalled on s0
+  } else {
+    if (host[2] && MH) ex.ok(cudaMemcpyAsync(const_cast<void*>(y), ex.y, MH, cudaMemcpyDeviceToHost, ex.st[0]));
+    if (host[3] && MH) ex.ok(cudaMemcpyAsync(dx, ex.dx, MH, cudaMemcpyDeviceToHost, ex.st[0]));
+  }
   t_last_launches = g_launch_count;
   if (ex.err != cudaSuccess) return cuda_fail(ex.err);
   return OASES_OK;
