@@ -35,7 +35,8 @@
  *   Memory    The caller owns every buffer.  The library never allocates or
  *             frees device memory; it uses only the caller's workspace, whose
  *             size oases_workspace_bytes() returns.  Device pointers must be
- *             16-byte aligned.
+ *             16-byte aligned.  It keeps a small pool of CUDA events and, for
+ *             host-buffer steps, one copy stream per device.
  *   Streams   s0 and s1 are cudaStream_t (NULL = legacy default stream).  Calls
  *             are asynchronous: on return the work is enqueued.  s1 first waits
  *             for the work already enqueued on s0, and before returning s0 is
@@ -165,8 +166,13 @@ oases_status oases_block_recompute_bwd(const oases_block_desc *desc, const oases
  * per_layer: n_layers weight structs; per_layer_grads: n_layers grad structs.
  * x, g, y, dx: [batch*seq, hidden] in desc->dtype; each may be device memory or
  * host memory (pageable or pinned): host buffers are staged through the
- * workspace with cudaMemcpyAsync on s0 (y and dx are complete in host memory
- * once s0 completes). */
+ * workspace with cudaMemcpyAsync.  Outside stream capture the copies run on a
+ * copy stream the library creates once per device, ordered by events: x is
+ * uploaded before any compute, g before each stream's first backward
+ * operator, y is downloaded once the forward is done (overlapping the
+ * backward) and dx at the end.  While s0 is being captured into a CUDA graph
+ * they are issued on s0 instead.  Either way y and dx are complete in host
+ * memory once s0 completes. */
 oases_status oases_stack_step(const oases_block_desc *desc, int n_layers,
                               const oases_weights *per_layer, const void *x, const void *g,
                               void *y, void *dx, const oases_grads *per_layer_grads,

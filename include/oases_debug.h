@@ -74,8 +74,8 @@ oases_status oases_debug_attention_progress(int *host_mapped);
 oases_status oases_debug_attention_timeline(unsigned long long *device_buffer);
 /* Timeline of the tensor-core GEMM (debugging aid): device_buffer holds 16
  * uint64 %globaltimer stamps per CTA of every following launch (entry,
- * prologue done, first stage landed, then per local tile t < 5 its MMAs done
- * and its epilogue done, exit); NULL switches it off. */
+ * prologue done, first stage landed, then per local tile t < 5 its last MMA
+ * issued and its epilogue done, exit); NULL switches it off. */
 oases_status oases_debug_gemm_timeline(unsigned long long *device_buffer);
 int oases_debug_attention_error_word(void);
 
