@@ -150,6 +150,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest value over all ranks (the whole job's step time); the value
+    itself with one rank.  device: where the collective's tensor lives."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, t_step_max: float) -> float:
+    """Throughput of the whole job: every rank's replica does flops_per_rank per
+    step, and the job's step takes the slowest rank's time."""
+    return flops_per_rank * world / t_step_max / 1e12
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -358,12 +376,9 @@ def main():
                 flush.zero_()
         barrier()
     t_step = sum(a.elapsed_time(b) for a, b in evs) * 1e-3 / args.steps
-    if world > 1:
-        tt = torch.tensor([t_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_step = float(tt.item())
+    t_step = max_over_ranks(t_step, dev)
     fl = flops_fine(shape, args.recompute)
-    value = fl * world / t_step / 1e12
+    value = whole_job_tflops(fl, world, t_step)
 
     # end to end: host (pinned) buffers through the same C-ABI call
     xh = x.cpu().pin_memory()
@@ -379,7 +394,7 @@ def main():
         blk.step(xh, gh, yh, dxh)
     e1.record(blk.s0)
     barrier()
-    t_e2e = e0.elapsed_time(e1) * 1e-3 / args.steps
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, dev)
     io = shape.rows * shape.hidden * (2 if shape.dtype == "bf16" else 4)
 
     pk = peaks()
@@ -397,7 +412,7 @@ def main():
                       "launch": "cuda-graph" if not args.no_graph else "direct",
                       "l2": "flushed between timed steps (256 MiB write)"},
            "pct_bf16_peak": 100.0 * value / world / pk["bf16_tflops_sustained"],
-           "e2e": {"value": fl / t_e2e / 1e12 * world, "unit": "TFLOP/s",
+           "e2e": {"value": whole_job_tflops(fl, world, t_e2e), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": 2 * io, "d2h_bytes_per_step": 2 * io},
            "gpu_launches": launches * args.steps,
            "clocks": clk.summary(),

@@ -89,6 +89,15 @@ def test_invalid_descriptors_rejected(L, bad, status):
     assert _fwd_status(_desc(**bad)) == status
 
 
+@pytest.mark.parametrize("field,value", [("recompute", 4), ("recompute", -1), ("reduce", 2),
+                                         ("reduce", -1), ("kind", 3), ("dtype", 2)])
+def test_out_of_range_codes_rejected(L, field, value):
+    d = _desc()
+    setattr(d, field, value)
+    assert _fwd_status(d) == 1
+    assert oz.oases_workspace_bytes(d) == 0
+
+
 def test_null_and_small_workspace(L):
     d = _desc()
     assert _fwd_status(d, ws=None) == 3

@@ -1,0 +1,93 @@
+"""Host-side logic of bench.py on the CPU: the FLOP accounting behind the
+metric, the whole-job aggregation over ranks (two gloo ranks), and the
+reference arm's rank rule.  Nothing here needs a GPU."""
+import importlib.util
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from synth import SHAPES
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    m = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(m)
+    return m
+
+
+# Algorithmic FLOPs of one FINE step per workload, counted by hand from the
+# block's GEMMs and the causal attention products: FFN 14·M·H·F; attention
+# 30·M·H² + 9·B·S²·H (forward 8·M·H² + 2·B·S²·H, recompute 6·M·H² + 2·B·S²·H,
+# backward 16·M·H² + 5·B·S²·H).
+@pytest.mark.parametrize("name,gflop", [("ffn_bf16_h1024", 240.52), ("attn_bf16_h2048", 592.71),
+                                        ("layer_bf16_h4096", 12437.5), ("stack4_bf16_h2560", 40030.0)])
+def test_fine_flop_counts(name, gflop):
+    b = _bench()
+    assert b.flops_fine(SHAPES[name]) / 1e9 == pytest.approx(gflop, rel=2e-4)
+
+
+def test_modes_are_credited_with_what_they_execute():
+    b = _bench()
+    s = SHAPES["layer_bf16_h4096"]
+    M, H, F, B, S = s.rows, s.hidden, s.ffn, s.batch, s.seq
+    fine = b.flops_fine(s, "fine")
+    none = b.flops_fine(s, "none")
+    sel = b.flops_fine(s, "selective")
+    assert b.flops_fine(s, "full") == fine          # FULL's extra work is not credited
+    assert fine - none == 2 * M * H * F + 6 * M * H * H + 2 * B * S * S * H   # the recompute
+    assert sel - none == 2 * B * S * S * H          # the attention operation again
+    f = SHAPES["ffn_bf16_h1024"]
+    assert b.flops_fine(f, "selective") == b.flops_fine(f, "none")
+
+
+def test_whole_job_throughput_is_total_work_over_slowest_rank():
+    b = _bench()
+    assert b.whole_job_tflops(2e12, 4, 0.5) == pytest.approx(16.0)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        b = _bench()
+        t = b.max_over_ranks(0.010 * (rank + 1), "cpu")   # rank r took (r + 1) * 10 ms
+        out[rank] = b.whole_job_tflops(1e12, world, t)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_step():
+    world, port = 2, _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
+    # both ranks see the slowest rank's 20 ms: 2 replicas x 1 TFLOP / 0.02 s
+    assert out[0] == pytest.approx(100.0) and out[1] == pytest.approx(100.0)
+
+
+def test_single_process_max_is_the_value_itself():
+    assert _bench().max_over_ranks(0.25, "cpu") == 0.25
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    b = _bench()
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class Args:
+        steps, warmup, recompute, workload = 1, 0, "fine", "ffn_bf16_h1024"
+
+    assert b.run_reference(Args, SHAPES["ffn_bf16_h1024"]) is None
+    assert capsys.readouterr().out == ""   # no line from a non-zero rank
