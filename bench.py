@@ -295,6 +295,152 @@ def dominant_kernel_roofline(blk, shape, pk, torch):
             "algorithmic_flops_per_launch": fl, "avg_launch_s": t}
 
 
+def kernel_table(shape, pk, reps=20):
+    """Each kernel of one sub-batch's step, launched alone through the kernel
+    entry points (oases_debug.h) at the workload's per-sub-batch shape, L2
+    flushed before every launch, CUDA-event time averaged over reps launches.
+    HBM-bound kernels report algorithmic bytes / time against the measured HBM
+    copy bandwidth; tensor-core kernels algorithmic FLOPs / time against the
+    measured bf16 burst peak.  Returns one dict per kernel."""
+    import ctypes
+
+    import torch
+
+    import tensor_model_transformer_tp_gb300 as oz
+    L = oz.lib()
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    L.oases_debug_gemm.argtypes = [i32, i32, i32, i32, vp, i64, i32, vp, i64, i32, i32, vp, i64,
+                                   i32, vp, vp, vp, i64, i32, vp]
+    L.oases_debug_layer_norm.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp]
+    L.oases_debug_layer_norm_bwd_scratch_bytes.argtypes = [i32, i32]
+    L.oases_debug_layer_norm_bwd_scratch_bytes.restype = sz
+    L.oases_debug_layer_norm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp,
+                                             sz, vp]
+    L.oases_debug_bias_grad_scratch_bytes.argtypes = [i32, i32]
+    L.oases_debug_bias_grad_scratch_bytes.restype = sz
+    L.oases_debug_bias_grad.argtypes = [vp, i64, i32, i32, i32, vp, vp, sz, vp]
+    L.oases_debug_shard_sum.argtypes = [vp, i64, i32, vp, vp, vp, i32, i32, i32, vp]
+    L.oases_debug_attention.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, vp]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = torch.cuda.current_stream(dev)
+    sp = st.cuda_stream
+    bf = torch.bfloat16
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    Ms, H, w = shape.rows // shape.sub_batches, shape.hidden, shape.w
+    rows = []
+
+    def rnd(*dims, dtype=bf, scale=1.0):
+        return (torch.randn(*dims, device=dev) * scale).to(dtype)
+
+    def timed(name, dims, bound, work, launch):
+        status = launch()
+        assert status == 0, (name, status)
+        torch.cuda.synchronize(dev)
+        evs = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            launch()
+            e1.record(st)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        t = sum(a.elapsed_time(b) for a, b in evs) / reps * 1e-3
+        if bound == "hbm":
+            ach, peak, unit = work / t / 1e9, pk["hbm_gbs"], "GB/s"
+        else:
+            ach, peak, unit = work / t / 1e12, pk["bf16_tflops"], "TFLOP/s"
+        rows.append({"kernel": name, "shape": dims, "bound": bound, "avg_us": t * 1e6,
+                     "algorithmic": work, "achieved": ach, "unit": unit, "peak": peak,
+                     "frac": ach / peak})
+
+    def gemm(name, M, N, K, A, lda, ak, B, ldb, bk, epi, C, ldc, c_f32, C2=None, bias=None,
+             aux=None, ld_aux=0):
+        p = lambda t: t.data_ptr() if t is not None else None
+        timed(name, "%dx%dx%d" % (M, N, K), "tensor", 2.0 * M * N * K,
+              lambda: L.oases_debug_gemm(M, N, K, 1, p(A), lda, ak, p(B), ldb, bk, epi, p(C), ldc,
+                                         0 if c_f32 else 1, p(C2), p(bias), p(aux), ld_aux, 2, sp))
+
+    x = rnd(Ms, H)
+    gam, bet = rnd(H, scale=0.1) + 1, rnd(H, scale=0.1)
+    u = torch.empty_like(x)
+    mean = torch.empty(Ms, device=dev)
+    rstd = torch.empty(Ms, device=dev)
+    timed("ln_fwd", "%dx%d" % (Ms, H), "hbm", 4.0 * Ms * H + 4.0 * H + 8.0 * Ms,
+          lambda: L.oases_debug_layer_norm(x.data_ptr(), gam.data_ptr(), bet.data_ptr(),
+                                           u.data_ptr(), mean.data_ptr(), rstd.data_ptr(), Ms, H,
+                                           1e-5, 1, sp))
+    dy = rnd(Ms, H)
+    if shape.kind in ("ffn", "layer"):
+        F = shape.ffn
+        w1, b1 = rnd(F, H, scale=0.02), rnd(F, scale=0.02)
+        w2, b2 = rnd(H, F, scale=0.02), rnd(H, scale=0.02)
+        h, g_ = torch.empty(Ms, F, dtype=bf, device=dev), torch.empty(Ms, F, dtype=bf, device=dev)
+        y = torch.empty(Ms, H, dtype=bf, device=dev)
+        dw1 = torch.zeros(F, H, device=dev)
+        dw2 = torch.zeros(H, F, device=dev)
+        da = torch.empty(Ms, F, dtype=bf, device=dev)
+        du = torch.empty(Ms, H, device=dev)
+        gemm("col_gemm_bias_gelu (F_i fwd)", Ms, F, H, u, H, 1, w1, H, 1, 2, h, F, False, bias=b1)
+        gemm("col_gemm_bias_gelu+gelu' (R_i)", Ms, F, H, u, H, 1, w1, H, 1, 2, h, F, False, C2=g_,
+             bias=b1)
+        gemm("row_gemm_shard_sum_bias_resid (F_j + C_i(F))", Ms, H, F, h, F, 1, w2, F, 1, 3, y, H,
+             False, bias=b2, aux=x, ld_aux=H)
+        gemm("dW2 += dy^T h (fp32 reduce-add)", H, F, Ms, dy, H, 0, h, F, 0, 5, dw2, F, True)
+        gemm("dA = (dy W2) * gelu' (B_j)", Ms, F, H, dy, H, 1, w2, F, 0, 4, da, F, False, aux=g_,
+             ld_aux=F)
+        gemm("dW1 += dA^T u (fp32 reduce-add)", F, H, Ms, da, F, 0, u, H, 0, 5, dw1, H, True)
+        gemm("du = dA W1 (C_i(B), fp32)", Ms, H, F, da, F, 1, w1, H, 0, 0, du, H, True)
+        db = torch.zeros(F, device=dev)
+        nb = L.oases_debug_bias_grad_scratch_bytes(Ms, F)
+        scratch = torch.empty(nb, dtype=torch.uint8, device=dev)
+        timed("bias_grad db1 = colsum(dA)", "%dx%d" % (Ms, F), "hbm", 2.0 * Ms * F + 8.0 * F,
+              lambda: L.oases_debug_bias_grad(da.data_ptr(), F, Ms, F, 1, db.data_ptr(),
+                                              scratch.data_ptr(), nb, sp))
+        dx = torch.empty(Ms, H, dtype=bf, device=dev)
+        dgam, dbet = torch.zeros(H, device=dev), torch.zeros(H, device=dev)
+        nl = L.oases_debug_layer_norm_bwd_scratch_bytes(Ms, H)
+        lscr = torch.empty(nl, dtype=torch.uint8, device=dev)
+        du.normal_()
+        timed("ln_bwd (+ residual, dgamma, dbeta)", "%dx%d" % (Ms, H), "hbm",
+              (4.0 + 3 * 2.0) * Ms * H + 8.0 * Ms + 2.0 * H + 16.0 * H,
+              lambda: L.oases_debug_layer_norm_bwd(du.data_ptr(), x.data_ptr(), mean.data_ptr(),
+                                                   rstd.data_ptr(), gam.data_ptr(), dy.data_ptr(),
+                                                   dx.data_ptr(), dgam.data_ptr(), dbet.data_ptr(),
+                                                   Ms, H, 1, lscr.data_ptr(), nl, sp))
+        part = torch.randn(w, Ms, H, device=dev)
+        timed("shard_sum (separate C_i(F), w=%d)" % w, "%dx%d" % (Ms, H), "hbm",
+              4.0 * w * Ms * H + 2.0 * H + 4.0 * Ms * H,
+              lambda: L.oases_debug_shard_sum(part.data_ptr(), Ms * H, w, b2.data_ptr(),
+                                              x.data_ptr(), y.data_ptr(), Ms, H, 1, sp))
+        del w1, w2, h, g_, dw1, dw2, da, part
+    if shape.kind in ("attn", "layer"):
+        nh, d = shape.heads, H // shape.heads
+        Bs, S = shape.batch // shape.sub_batches, shape.seq
+        wqkv, bqkv = rnd(3 * H, H, scale=0.02), rnd(3 * H, scale=0.02)
+        qkv = torch.empty(Ms, 3 * H, dtype=bf, device=dev)
+        gemm("qkv_gemm_bias (F_i fwd)", Ms, 3 * H, H, u, H, 1, wqkv, H, 1, 1, qkv, 3 * H, False,
+             bias=bqkv)
+        qkv.normal_()
+        o = torch.empty(Ms, H, dtype=bf, device=dev)
+        lse = torch.empty(nh, Ms, device=dev)
+        do = rnd(Ms, H)
+        delta = torch.empty(nh, Ms, device=dev)
+        dqkv = torch.empty(Ms, 3 * H, dtype=bf, device=dev)
+        causal = 1.0 if shape.causal else 2.0
+        dims = "batch %d x seq %d, %d heads of %d" % (Bs, S, nh, d)
+        timed("attention fwd (tcgen05)", dims, "tensor", 2.0 * Bs * S * S * H * causal,
+              lambda: L.oases_debug_attention(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), None,
+                                              None, None, Bs, S, nh, d, int(shape.causal), 1, 0, 2,
+                                              sp))
+        timed("attention bwd (delta + dQ + dK/dV)", dims, "tensor", 5.0 * Bs * S * S * H * causal,
+              lambda: L.oases_debug_attention(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                              do.data_ptr(), delta.data_ptr(), dqkv.data_ptr(), Bs,
+                                              S, nh, d, int(shape.causal), 1, 1, 0, sp))
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -308,6 +454,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch the step directly, not as a CUDA graph")
     ap.add_argument("--reduce", default="fused", choices=["fused", "separate"],
                     help="shard sums fused into the GEMMs or as separate reduction kernels")
+    ap.add_argument("--kernels", action="store_true",
+                    help="instead of the step: time each kernel alone at the workload's "
+                         "per-sub-batch shape and print one JSON line per kernel")
     args = ap.parse_args()
     from synth import SHAPES
     shape = SHAPES[args.workload]
@@ -315,6 +464,20 @@ def main():
         shape = shape.replace(sub_batches=args.sub_batches)
     if args.impl == "reference":
         run_reference(args, shape)
+        return
+    if args.kernels:
+        import torch
+        from tensor_model_transformer_tp_gb300 import build_library
+        build_library()
+        torch.cuda.set_device(0)
+        pk = peaks()
+        with ClockSampler(0) as clk:
+            rows = kernel_table(shape, pk)
+        for r in rows:
+            r["workload"] = args.workload
+            r["peak_source"] = pk["source"]
+            print(json.dumps(r), flush=True)
+        print(json.dumps({"clocks": clk.summary()}), flush=True)
         return
 
     import torch

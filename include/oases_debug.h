@@ -104,6 +104,47 @@ size_t oases_debug_bias_grad_scratch_bytes(int M, int N);
 oases_status oases_debug_bias_grad(const void *in, int64_t ld, int M, int N, int dtype, float *out,
                                    void *scratch, size_t scratch_bytes, void *stream);
 
+/* LayerNorm forward of a pre-LN segment (the normalisation in front of F_i;
+ * under fine-grained recomputation it is part of R_i, Oases §IV-A, Fig. 4):
+ *   u[m, h] = (x[m, h] - mean[m]) * rstd[m] * gamma[h] + beta[h],
+ *   mean[m] = (1/H) sum_h x[m, h], rstd[m] = 1 / sqrt((1/H) sum_h (x[m, h] - mean[m])^2 + eps).
+ * x, u: device [M, H] row-major (pitch H), type dtype (oases_dtype); gamma,
+ * beta: device [H], type dtype; mean, rstd: device fp32 [M], written.  Every
+ * pointer 16-byte aligned (OASES_ERR_INVALID_ARG otherwise).  Asynchronous on
+ * stream. */
+oases_status oases_debug_layer_norm(const void *x, const void *gamma, const void *beta, void *u,
+                                    float *mean, float *rstd, int M, int H, float eps, int dtype,
+                                    void *stream);
+
+/* LayerNorm backward, the last step of the block's C_i(B) (Oases §IV-A,
+ * Fig. 4d: the input gradient of a segment flows through its LayerNorm):
+ * with xhat = (x - mean) * rstd and gg = du * gamma per row,
+ *   dx[m, h] = rstd[m] * (gg[m, h] - mean_h(gg) - xhat[m, h] * mean_h(gg * xhat)) (+ dres[m, h]),
+ *   dgamma[h] += sum_m du[m, h] * xhat[m, h],  dbeta[h] += sum_m du[m, h].
+ * du: device fp32 [M, H]; x, gamma, dres (NULL: no residual term), dx: type
+ * dtype; mean, rstd: the forward's fp32 [M]; dgamma, dbeta: device fp32 [H],
+ * accumulated in a fixed order (bit-reproducible).  scratch: device, at least
+ * oases_debug_layer_norm_bwd_scratch_bytes(M, H) bytes, owned by the caller
+ * (OASES_ERR_WORKSPACE otherwise).  Every pointer 16-byte aligned.
+ * Asynchronous on stream. */
+size_t oases_debug_layer_norm_bwd_scratch_bytes(int M, int H);
+oases_status oases_debug_layer_norm_bwd(const float *du, const void *x, const float *mean,
+                                        const float *rstd, const void *gamma, const void *dres,
+                                        void *dx, float *dgamma, float *dbeta, int M, int H,
+                                        int dtype, void *scratch, size_t scratch_bytes,
+                                        void *stream);
+
+/* The shard sum C_i(F) of the separate-reduction mode (Oases §IV, Eq. (1):
+ * the row-parallel output is the sum of the w shards' partial outputs):
+ *   out[m, n] = sum_{k < w} part[k * pstride + m * N + n] (+ bias[n]) (+ resid[m * N + n]),
+ * shards added in the order k = 0, 1, ..., then the bias, then the residual.
+ * part: device fp32, w slabs of [M, N] with pstride >= M * N floats between
+ * them; bias [N], resid [M, N] (either may be NULL) and out [M, N]: type
+ * dtype.  Every pointer 16-byte aligned.  Asynchronous on stream. */
+oases_status oases_debug_shard_sum(const float *part, int64_t pstride, int w, const void *bias,
+                                   const void *resid, void *out, int M, int N, int dtype,
+                                   void *stream);
+
 /* The bias-gradient sum above for callers that cannot allocate device memory.
  * The paper has no counterpart to this entry point; it exists for callers such
  * as a plugin inside a host framework that owns every device allocation, a

@@ -804,9 +804,18 @@ SegParams seg_params(const Shape& s, int seg, const oases_weights* w, const oase
   return p;
 }
 
+// Device pointers must be 16-byte aligned (TMA operands, 16-byte vector loads
+// and stores); NULL passes.
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
 bool params_ok(const Shape& s, const std::vector<SegParams>& sp, bool need_grads) {
   for (const SegParams& p : sp) {
     if (!p.wc || !p.bc || !p.wr || !p.br) return false;
+    for (const void* q : {(const void*)p.g, (const void*)p.b, (const void*)p.wc,
+                          (const void*)p.bc, (const void*)p.wr, (const void*)p.br,
+                          (const void*)p.dg, (const void*)p.db, (const void*)p.dwc,
+                          (const void*)p.dbc, (const void*)p.dwr, (const void*)p.dbr})
+      if (!aligned16(q)) return false;
     if (s.pre_ln && (!p.g || !p.b)) return false;
     if (need_grads) {
       if (!p.dwc || !p.dbc || !p.dwr || !p.dbr) return false;
@@ -849,6 +858,10 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   ex.sp.resize(s.nseg);
   for (int i = 0; i < s.nseg; ++i) ex.sp[i] = seg_params(s, i, w, gr);
   if (!params_ok(s, ex.sp, bwd)) return OASES_ERR_INVALID_ARG;
+  const void* io[4] = {x, dy, y, dx};  // device unless staged from host memory
+  if (!stage_host)
+    for (const void* p : io)
+      if (!aligned16(p)) return OASES_ERR_INVALID_ARG;
   const size_t ev_stage = ex.ev_base + (size_t)s.nseg * GRP_N;  // staging-copy events
   cudaError_t e = pool().ensure(ev_stage + 6);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -864,6 +877,8 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
       if (e != cudaSuccess) return cuda_fail(e);
       host[i] = at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
     }
+    for (int i = 0; i < 4; ++i)
+      if (!host[i] && !aligned16(io[i])) return OASES_ERR_INVALID_ARG;
   }
   ex.x = host[0] ? ex.at(ex.L.stage[0]) : x;
   ex.dy = host[1] ? ex.at(ex.L.stage[1]) : dy;
@@ -1143,6 +1158,83 @@ extern "C" oases_status oases_debug_bias_grad(const void* in, int64_t ld, int M,
   cudaError_t e = colsum_accum(in, ld, M, N, static_cast<DType>(dtype),
                                static_cast<float*>(scratch), out,
                                static_cast<cudaStream_t>(stream));
+  t_last_launches = g_launch_count;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
+namespace {
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+}  // namespace
+
+extern "C" oases_status oases_debug_layer_norm(const void* x, const void* gamma, const void* beta,
+                                               void* u, float* mean, float* rstd, int M, int H,
+                                               float eps, int dtype, void* stream) {
+  using namespace oases;
+  t_last_error.clear();
+  g_launch_count = 0;
+  if (M < 0 || H <= 0 || dtype < 0 || dtype > 1 || !(eps >= 0.f)) return OASES_ERR_INVALID_ARG;
+  if (M == 0) return OASES_OK;
+  if (!x || !gamma || !beta || !u || !mean || !rstd) return OASES_ERR_INVALID_ARG;
+  for (const void* p : {x, gamma, beta, (const void*)u, (const void*)mean, (const void*)rstd})
+    if (!aligned16(p)) return OASES_ERR_INVALID_ARG;
+  cudaError_t e = layer_norm_fwd(x, gamma, beta, u, mean, rstd, M, H, eps,
+                                 static_cast<DType>(dtype), static_cast<cudaStream_t>(stream));
+  t_last_launches = g_launch_count;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
+extern "C" size_t oases_debug_layer_norm_bwd_scratch_bytes(int M, int H) {
+  if (M < 0 || H < 0) return 0;
+  const size_t part = (size_t)oases::ln_bwd_blocks(M) * (size_t)H * sizeof(float);
+  return 2 * round256(part) + round256((size_t)M * 2 * sizeof(float));
+}
+
+extern "C" oases_status oases_debug_layer_norm_bwd(const float* du, const void* x, const float* mean,
+                                                   const float* rstd, const void* gamma,
+                                                   const void* dres, void* dx, float* dgamma,
+                                                   float* dbeta, int M, int H, int dtype,
+                                                   void* scratch, size_t scratch_bytes,
+                                                   void* stream) {
+  using namespace oases;
+  t_last_error.clear();
+  g_launch_count = 0;
+  if (M < 0 || H <= 0 || dtype < 0 || dtype > 1) return OASES_ERR_INVALID_ARG;
+  if (M == 0) return OASES_OK;
+  if (!du || !x || !mean || !rstd || !gamma || !dx || !dgamma || !dbeta)
+    return OASES_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)du, x, (const void*)mean, (const void*)rstd, gamma, dres,
+                        (const void*)dx, (const void*)dgamma, (const void*)dbeta})
+    if (!aligned16(p)) return OASES_ERR_INVALID_ARG;
+  if (!scratch || scratch_bytes < oases_debug_layer_norm_bwd_scratch_bytes(M, H) ||
+      !aligned16(scratch))
+    return OASES_ERR_WORKSPACE;
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  const size_t part = round256((size_t)ln_bwd_blocks(M) * (size_t)H * sizeof(float));
+  cudaError_t e = layer_norm_bwd(du, x, mean, rstd, gamma, dres, dx, reinterpret_cast<float*>(sc),
+                                 reinterpret_cast<float*>(sc + part),
+                                 reinterpret_cast<float2*>(sc + 2 * part), dgamma, dbeta, M, H,
+                                 static_cast<DType>(dtype), static_cast<cudaStream_t>(stream));
+  t_last_launches = g_launch_count;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
+extern "C" oases_status oases_debug_shard_sum(const float* part, int64_t pstride, int w,
+                                              const void* bias, const void* resid, void* out,
+                                              int M, int N, int dtype, void* stream) {
+  using namespace oases;
+  t_last_error.clear();
+  g_launch_count = 0;
+  if (M < 0 || N < 0 || w <= 0 || dtype < 0 || dtype > 1) return OASES_ERR_INVALID_ARG;
+  if ((int64_t)M * N == 0) return OASES_OK;
+  if (!part || !out || pstride < (int64_t)M * N) return OASES_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)part, bias, resid, (const void*)out})
+    if (!aligned16(p)) return OASES_ERR_INVALID_ARG;
+  const DType t = static_cast<DType>(dtype);
+  cudaError_t e = shard_sum(part, pstride, w, bias, resid, out, t, t, M, N,
+                            static_cast<cudaStream_t>(stream));
   t_last_launches = g_launch_count;
   if (e != cudaSuccess) return cuda_fail(e);
   return OASES_OK;

@@ -98,6 +98,20 @@ def test_out_of_range_codes_rejected(L, field, value):
     assert oz.oases_workspace_bytes(d) == 0
 
 
+def test_misaligned_device_pointers_rejected(L):
+    d = _desc()
+    w = _weights()
+    w.b1 = FAKE + 8          # 16-byte rule: refused before anything is enqueued
+    assert L.oases_block_fwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, FAKE, 1 << 40,
+                             None, None) == 1
+    assert L.oases_block_fwd(ctypes.byref(d), ctypes.byref(_weights()), FAKE + 4, FAKE, FAKE,
+                             1 << 40, None, None) == 1
+    g = _grads()
+    g.w2 = FAKE + 2
+    assert L.oases_block_recompute_bwd(ctypes.byref(d), ctypes.byref(_weights()), FAKE, FAKE, FAKE,
+                                       ctypes.byref(g), FAKE, 1 << 40, None, None) == 1
+
+
 def test_null_and_small_workspace(L):
     d = _desc()
     assert _fwd_status(d, ws=None) == 3
