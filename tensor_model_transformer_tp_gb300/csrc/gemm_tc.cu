@@ -48,6 +48,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BKE = 64;  // K elements per stage (128 bytes of bf16)
+constexpr int GROUP_M = 8;  // row blocks per group of the tile order when A is large
+constexpr int64_t A_L2_BYTES = 48ll << 20;  // A up to this size stays in L2 across tile rounds
 constexpr int NTHREADS = 320;  // 2 control warps + 8 epilogue warps
 
 // CL = 2: a CTA pair shares each MMA; a CTA holds BN / 2 rows of the B tile.
@@ -278,7 +280,7 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
 // counts); its commits arrive on both CTAs' empty and accumulator-full
 // barriers; both CTAs' epilogue warps release an accumulator on the even CTA's
 // barrier.
-template <int BN, bool A_K, bool B_K, int CL>
+template <int BN, bool A_K, bool B_K, int CL, bool GRP>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
@@ -309,9 +311,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int tiles1 = num_mp * num_n, tiles = tiles1 * g.splits;
   const int kpl = g.K / g.kpieces, nkb_p = (kpl + BKE - 1) / BKE, nkb = nkb_p * g.kpieces;
   const int first = blockIdx.x / CL, stride = gridDim.x / CL;
+  // Tile order within a split: the row block varies fastest.  Without GRP it
+  // does so over every row block: each round of tiles re-reads A from L2 and
+  // B comes from DRAM once, which holds while all of A fits in L2.  A larger
+  // A (dW1 += dA^T u: 64 row blocks, 128 MB) would then be streamed from DRAM
+  // again for every column block, so with GRP the tiles go in groups of
+  // GROUP_M row blocks: the tiles in flight share GROUP_M row blocks of A and
+  // a few column blocks of B, and B is read once per group.
   auto tile_split = [&](int t) { return t / tiles1; };
-  auto tile_m0 = [&](int t) { return (((t % tiles1) % num_mp) * CL + rank) * BM; };
-  auto tile_n0 = [&](int t) { return ((t % tiles1) / num_mp) * BN; };
+  auto tile_mb = [&](int t) {
+    const int r = t % tiles1;
+    if constexpr (!GRP) {
+      return r % num_mp;
+    } else {
+      const int q = r / (GROUP_M * num_n), gm = min(GROUP_M, num_mp - q * GROUP_M);
+      return q * GROUP_M + (r - q * GROUP_M * num_n) % gm;
+    }
+  };
+  auto tile_nb = [&](int t) {
+    const int r = t % tiles1;
+    if constexpr (!GRP) {
+      return r / num_mp;
+    } else {
+      const int q = r / (GROUP_M * num_n), gm = min(GROUP_M, num_mp - q * GROUP_M);
+      return (r - q * GROUP_M * num_n) / gm;
+    }
+  };
+  auto tile_m0 = [&](int t) { return (tile_mb(t) * CL + rank) * BM; };
+  auto tile_n0 = [&](int t) { return tile_nb(t) * BN; };
   constexpr uint16_t MASK = (1u << CL) - 1u;
 
   if (threadIdx.x == 0) {
@@ -614,7 +641,7 @@ int num_sms() {
   return n;
 }
 
-template <int BN, bool A_K, bool B_K, int CL>
+template <int BN, bool A_K, bool B_K, int CL, bool GRP = false>
 cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
   using C = TcCfg<BN, CL>;
   CUtensorMap ma, mb;
@@ -638,7 +665,7 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
       (g.C2 == nullptr || make_map(&mc2, g.C2, g.N, g.M, g.ldc, cw, 32, f32c)))
     ga.tma_store = 1;
   if (g.splits > 1 && !ga.tma_store) return cudaErrorNotSupported;  // slabs need the 3-D map
-  auto kern = gemm_tc_kernel<BN, A_K, B_K, CL>;
+  auto kern = gemm_tc_kernel<BN, A_K, B_K, CL, GRP>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -689,8 +716,24 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, mc2, ga);
 }
 
+// The grouped tile order (the kernel's GRP): CTA-pair 256-wide tiles over more
+// than GROUP_M row blocks, with an A operand too large to stay in L2.
+bool grouped_order(const GemmArgs& g) {
+  const int num_mp = ((g.M + BM - 1) / BM + 1) / 2;
+  return num_mp > GROUP_M && (int64_t)g.M * g.K * 2 > A_L2_BYTES;
+}
+
 template <int BN, int CL>
 cudaError_t dispatch_major(const GemmArgs& g, cudaStream_t st) {
+  if constexpr (BN == 256 && CL == 2) {
+    if (grouped_order(g)) {
+      if (g.a_kmajor)
+        return g.b_kmajor ? launch_tc<BN, true, true, CL, true>(g, st)
+                          : launch_tc<BN, true, false, CL, true>(g, st);
+      return g.b_kmajor ? launch_tc<BN, false, true, CL, true>(g, st)
+                        : launch_tc<BN, false, false, CL, true>(g, st);
+    }
+  }
   if (g.a_kmajor)
     return g.b_kmajor ? launch_tc<BN, true, true, CL>(g, st) : launch_tc<BN, true, false, CL>(g, st);
   return g.b_kmajor ? launch_tc<BN, false, true, CL>(g, st) : launch_tc<BN, false, false, CL>(g, st);

@@ -99,7 +99,12 @@ def test_tensor_core_gemm_layouts_and_epilogues(L, a_k, b_k, epi):
     assert r is not None, "tensor-core path refused a supported case"
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (8, 8, 8), (264, 136, 1000), (2048, 1024, 512)])
+# 4736 rows = 19 pair row blocks.  K = 192: A is small, tiles run row block
+# fastest over all 19 (x 9 column blocks = 171 tiles, several per CTA pair).
+# K = 5376: A is 51 MB, tiles run in row-block groups of 8, 8 and 3 (x 7
+# column blocks, the last one 8 columns wide).
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (8, 8, 8), (264, 136, 1000), (2048, 1024, 512),
+                                   (4736, 2304, 192), (4736, 1544, 5376)])
 def test_tensor_core_gemm_shapes(L, M, N, K):
     assert run_case(L, M, N, K, True, True, "bias", "bf16", path=2) is not None
     assert run_case(L, M, N, K, False, False, "accum", "bf16", path=2) is not None
