@@ -38,10 +38,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300"
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel (the fused column GEMM + bias + GeLU of the FFN, one sub-batch), with
-# the sha256 of the kernel sources it was measured on (kernel_source_sha);
-# traffic is reported only while those sources are unchanged.
-NCU_TRAFFIC = {"source_sha256": "e9769cf1c8a6418971c838c4a060c25836205aa198bd41fa13c1f4e1c512d5e0",
+# kernel of one workload (the fused column GEMM + bias + GeLU of the FFN, one
+# sub-batch), with the sha256 of the kernel sources it was measured on
+# (kernel_source_sha); traffic is reported for that workload only, and only
+# while those sources are unchanged.
+NCU_TRAFFIC = {"workload": "ffn_bf16_h1024", "source_sha256": "e9769cf1c8a6418971c838c4a060c25836205aa198bd41fa13c1f4e1c512d5e0",
                "bytes_per_launch": 12668160 + 3072}  # dram read + write, one launch
 
 
@@ -55,6 +56,14 @@ def kernel_source_sha() -> str:
         with open(os.path.join(ROOT, "tensor_model_transformer_tp_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the ncu capture, for
+    the captured workload while the GEMM sources are unchanged; else None."""
+    if NCU_TRAFFIC["workload"] == workload and NCU_TRAFFIC["source_sha256"] == kernel_source_sha():
+        return NCU_TRAFFIC["bytes_per_launch"]
+    return None
 
 
 def flops_fine(shape, mode="fine") -> float:
@@ -234,7 +243,7 @@ def cpu_baseline(shape, recompute):
                 reps, nb, shape.batch, dt)}
 
 
-def dominant_kernel_roofline(blk, shape, pk, torch):
+def dominant_kernel_roofline(blk, shape, pk, torch, workload):
     """Average duration of the fused column GEMM (+bias+GeLU) at the step's
     per-sub-batch shape, timed with CUDA events on its launch stream."""
     import ctypes
@@ -284,10 +293,7 @@ def dominant_kernel_roofline(blk, shape, pk, torch):
     t = sum(times) / len(times)
     fl = 2.0 * Ms * N * H
     achieved = fl / t / 1e12
-    traffic = None
-    sha = kernel_source_sha()
-    if NCU_TRAFFIC["source_sha256"] == sha:
-        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    traffic = recorded_traffic(workload)
     return {"kernel": "gemm_tc_kernel (column GEMM + bias + GeLU, %dx%dx%d)" % (Ms, N, H),
             "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
@@ -561,7 +567,7 @@ def main():
     io = shape.rows * shape.hidden * (2 if shape.dtype == "bf16" else 4)
 
     pk = peaks()
-    roof = dominant_kernel_roofline(blk, shape, pk, torch)
+    roof = dominant_kernel_roofline(blk, shape, pk, torch, args.workload)
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t_step * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -47,6 +47,17 @@ def test_modes_are_credited_with_what_they_execute():
     assert b.flops_fine(f, "selective") == b.flops_fine(f, "none")
 
 
+def test_traffic_is_reported_only_for_the_captured_workload():
+    b = _bench()
+    for name in SHAPES:
+        t = b.recorded_traffic(name)
+        if name != b.NCU_TRAFFIC["workload"]:
+            assert t is None, name
+        else:   # the capture's bytes while the GEMM sources hash to the captured ones
+            assert t in (None, b.NCU_TRAFFIC["bytes_per_launch"])
+            assert (t is None) == (b.kernel_source_sha() != b.NCU_TRAFFIC["source_sha256"])
+
+
 def test_whole_job_throughput_is_total_work_over_slowest_rank():
     b = _bench()
     assert b.whole_job_tflops(2e12, 4, 0.5) == pytest.approx(16.0)
