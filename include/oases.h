@@ -35,8 +35,12 @@
  *   Memory    The caller owns every buffer.  The library never allocates or
  *             frees device memory; it uses only the caller's workspace, whose
  *             size oases_workspace_bytes() returns.  Device pointers must be
- *             16-byte aligned.  It keeps a small pool of CUDA events and, for
- *             host-buffer steps, one copy stream per device.
+ *             16-byte aligned.  It keeps a small pool of CUDA events per host
+ *             thread and device and, for host-buffer steps, one copy stream
+ *             per device.
+ *   Threads   Calls from several host threads may run concurrently on
+ *             different workspaces and streams, on one device or several; a
+ *             workspace must not be used by two calls whose work overlaps.
  *   Streams   s0 and s1 are cudaStream_t (NULL = legacy default stream).  Calls
  *             are asynchronous: on return the work is enqueued.  s1 first waits
  *             for the work already enqueued on s0, and before returning s0 is

@@ -80,13 +80,14 @@ oases_status oases_debug_gemm_timeline(unsigned long long *device_buffer);
 int oases_debug_attention_error_word(void);
 
 /* Per-operator timeline of the block scheduler (debugging aid).  With
- * tracing on, every following block call records a timing event before and
- * after each scheduled step (Algorithm 1 operator of one sub-batch) on that
- * sub-batch's stream.  oases_debug_trace_read synchronizes those events and
- * writes 6 doubles per step into out: event, operator, segment, sub-batch,
- * start and end in microseconds from the first step's start; it returns the
- * number of steps of the last call (entries beyond cap are not written), or
- * -1 on a CUDA error.  Tracing adds two event records per step. */
+ * tracing on (a process-wide switch), every following block call records a
+ * timing event before and after each scheduled step (Algorithm 1 operator of
+ * one sub-batch) on that sub-batch's stream.  oases_debug_trace_read
+ * synchronizes the events of the calling thread's last block call and writes
+ * 6 doubles per step into out: event, operator, segment, sub-batch, start and
+ * end in microseconds from the first step's start; it returns the number of
+ * steps of that call (entries beyond cap are not written), or -1 on a CUDA
+ * error.  Tracing adds two event records per step. */
 void oases_debug_trace_enable(int on);
 int oases_debug_trace_read(double *out, int cap);
 
@@ -95,7 +96,7 @@ int oases_debug_trace_read(double *out, int cap);
  * row-parallel bias (added once after the shard sum) gets
  *   out[n] += sum_{m < M} in[m * ld + n],   n < N,
  * (also used for the column-parallel bias with in = dA).  Deterministic:
- * blocks of 32 rows are summed into partial rows in scratch, then the partial
+ * blocks of 8 rows are summed into partial rows in scratch, then the partial
  * rows are added in order.  in: device, type dtype (oases_dtype), leading
  * dimension ld >= N.  out: device fp32 [N], accumulated.  scratch: device,
  * at least oases_debug_bias_grad_scratch_bytes(M, N) bytes, owned by the

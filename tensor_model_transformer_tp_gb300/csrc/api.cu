@@ -52,14 +52,21 @@ using namespace oases;
 thread_local std::string t_last_error;
 thread_local int t_last_launches = 0;
 
-// Optional per-operator event timeline of the last call (debugging aid).
+// Optional per-operator event timeline of this thread's last call (debugging
+// aid); its events are kept per device and reused across calls.
 struct TraceRec {
   int ev, op, seg, sb;
   cudaEvent_t e0, e1;
 };
-bool g_trace_on = false;
-std::vector<TraceRec> g_trace;
-std::vector<cudaEvent_t> g_trace_events;  // reused across calls
+struct TraceEvents {
+  std::vector<cudaEvent_t> ev;
+  ~TraceEvents() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+};
+std::atomic<bool> g_trace_on{false};
+thread_local std::vector<TraceRec> g_trace;
+thread_local std::unordered_map<int, TraceEvents> g_trace_events;
 
 enum Ev { EV_F = 0, EV_R = 1, EV_B = 2, EV_CF = 3, EV_CR = 4, EV_CB = 5, EV_SYNC = 6 };
 enum OpN { OP_LN = 0, OP_F = 1, OP_COL = 2, OP_ROW = 3, OP_G = 4, OP_ATTN = 5 };
@@ -305,10 +312,11 @@ bool injected(const std::vector<Step>& steps) {
 // Execution.
 // ---------------------------------------------------------------------------
 struct EventPool {
-  std::mutex mu;
   std::vector<cudaEvent_t> ev;
+  ~EventPool() {  // at thread exit; an event with pending work is released when it completes
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
   cudaError_t ensure(size_t n) {
-    std::lock_guard<std::mutex> lock(mu);
     while (ev.size() < n) {
       cudaEvent_t e;
       cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
@@ -318,9 +326,14 @@ struct EventPool {
     return cudaSuccess;
   }
 };
+// The events of this host thread's calls on the current device.  Per thread,
+// so concurrent calls from several threads never share an event (calls from
+// one thread are enqueued in order, and a wait captures an event's state when
+// it is enqueued, so reuse across that thread's calls is safe); per device,
+// because an event can be recorded only on streams of its own device.
 EventPool& pool() {
-  static EventPool p;
-  return p;
+  thread_local std::unordered_map<int, EventPool> pools;
+  return pools[current_device()];
 }
 
 // A non-blocking stream per device for host<->device staging copies, so they
@@ -358,7 +371,8 @@ struct Exec {
   const void* dy;             // gradient w.r.t. y
   void* dx;                   // gradient w.r.t. x
   cudaError_t err = cudaSuccess;
-  size_t ev_base = 2;  // pool()[0], [1]: call entry / exit joins
+  EventPool* P = nullptr;  // this thread's events on the call's device
+  size_t ev_base = 2;      // P->ev[0], [1]: call entry / exit joins
 
   template <typename T = void>
   T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
@@ -384,7 +398,7 @@ struct Exec {
   }
 
   // Weight-gradient ordering across sub-batches on different streams.
-  cudaEvent_t gev(int seg, int grp) const { return pool().ev[ev_base + seg * GRP_N + grp]; }
+  cudaEvent_t gev(int seg, int grp) const { return P->ev[ev_base + seg * GRP_N + grp]; }
   void grad_wait(int seg, int grp, int b) {
     if (b > 0 && st[0] != st[1]) ok(cudaStreamWaitEvent(stream(b), gev(seg, grp), 0));
   }
@@ -863,7 +877,8 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
     for (const void* p : io)
       if (!aligned16(p)) return OASES_ERR_INVALID_ARG;
   const size_t ev_stage = ex.ev_base + (size_t)s.nseg * GRP_N;  // staging-copy events
-  cudaError_t e = pool().ensure(ev_stage + 6);
+  ex.P = &pool();
+  cudaError_t e = ex.P->ensure(ev_stage + 6);
   if (e != cudaSuccess) return cuda_fail(e);
 
   // Host buffers (oases_stack_step only) are staged through the workspace.
@@ -885,10 +900,11 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   ex.y = host[2] ? ex.at(ex.L.stage[2]) : y;
   ex.dx = host[3] ? ex.at(ex.L.stage[3]) : dx;
 
-  cudaEvent_t ev_in = pool().ev[0], ev_out = pool().ev[1];
-  cudaEvent_t ev_x = pool().ev[ev_stage], ev_g = pool().ev[ev_stage + 1];
-  cudaEvent_t ev_y[2] = {pool().ev[ev_stage + 2], pool().ev[ev_stage + 3]};
-  cudaEvent_t ev_end = pool().ev[ev_stage + 4], ev_cs = pool().ev[ev_stage + 5];
+  const std::vector<cudaEvent_t>& pev = ex.P->ev;
+  cudaEvent_t ev_in = pev[0], ev_out = pev[1];
+  cudaEvent_t ev_x = pev[ev_stage], ev_g = pev[ev_stage + 1];
+  cudaEvent_t ev_y[2] = {pev[ev_stage + 2], pev[ev_stage + 3]};
+  cudaEvent_t ev_end = pev[ev_stage + 4], ev_cs = pev[ev_stage + 5];
   const bool two = ex.st[0] != ex.st[1];
   // Staging copies of host buffers go on a copy stream when nothing is being
   // captured: x first (the compute streams wait for it), then g (waited for
@@ -925,20 +941,22 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   const int nstreams = two ? 2 : 1;
   bool in_bwd[2] = {false, false};
   int bwd_started = 0;
+  const bool tracing = g_trace_on.load(std::memory_order_relaxed);
   g_trace.clear();
+  std::vector<cudaEvent_t>* tevs = tracing ? &g_trace_events[current_device()].ev : nullptr;
   size_t tev = 0;
   if (s.M > 0)
     for (const Step& st : steps) {
       TraceRec tr{st.ev, st.op, st.seg, st.sb, nullptr, nullptr};
-      if (g_trace_on) {
-        while (g_trace_events.size() < tev + 2) {
+      if (tracing) {
+        while (tevs->size() < tev + 2) {
           cudaEvent_t e;
           if (cudaEventCreate(&e) != cudaSuccess) break;
-          g_trace_events.push_back(e);
+          tevs->push_back(e);
         }
-        if (g_trace_events.size() >= tev + 2) {
-          tr.e0 = g_trace_events[tev++];
-          tr.e1 = g_trace_events[tev++];
+        if (tevs->size() >= tev + 2) {
+          tr.e0 = (*tevs)[tev++];
+          tr.e1 = (*tevs)[tev++];
           ex.ok(cudaEventRecord(tr.e0, ex.stream(st.sb)));
         }
       }

@@ -979,13 +979,12 @@ cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   CUtensorMap m;
   const int M = a.batch * a.seq;
   if (!qkv_map(&m, a.qkv, M, a.hidden)) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static DeviceOnce attr;
+  const cudaError_t ea = attr.run([] {
+    return cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FWD_SMEM);
+  });
+  if (ea != cudaSuccess) return ea;
   FwdArgs fa;
   fa.o = static_cast<__nv_bfloat16*>(a.o);
   fa.lse = a.lse;
@@ -1014,16 +1013,15 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
       !map2d(&tdo128, a.d_o, a.hidden, M, a.hidden, 128) ||
       !map2d(&tdo64, a.d_o, a.hidden, M, a.hidden, 64))
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
+  static DeviceOnce attr;
+  const cudaError_t ea = attr.run([] {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KV_SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    return cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                KV_SMEM);
+  });
+  if (ea != cudaSuccess) return ea;
   cudaError_t e = attention_delta(a, st);
   if (e != cudaSuccess) return e;
   BwdArgs ba;

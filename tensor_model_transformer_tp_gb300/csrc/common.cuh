@@ -6,9 +6,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace oases {
+
+// ---- host: per-device state for a process that drives several GPUs -------
+inline int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess ? d : 0;
+}
+// Runs a per-device setup step (a kernel attribute, say) once per device:
+// run(f) calls f until it succeeds on the current device, then skips it
+// there.  Safe from several threads (f may run more than once concurrently,
+// so it must be idempotent).  Device ordinals >= 64 run f on every call.
+struct DeviceOnce {
+  std::atomic<uint64_t> done{0};
+  template <typename F>
+  cudaError_t run(F&& f) {
+    const int dev = current_device();
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = f();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+};
 
 enum class DType : int { F32 = 0, BF16 = 1 };
 

@@ -630,14 +630,17 @@ bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
   return true;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+int num_sms() {  // of the current device, cached per device
+  static std::atomic<int> cache[64];
+  const int dev = current_device();
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -666,20 +669,21 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
     ga.tma_store = 1;
   if (g.splits > 1 && !ga.tma_store) return cudaErrorNotSupported;  // slabs need the 3-D map
   auto kern = gemm_tc_kernel<BN, A_K, B_K, CL, GRP>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static DeviceOnce attr;
+  cudaError_t ea = attr.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (ea != cudaSuccess) return ea;
   const int num_mp = ((g.M + BM - 1) / BM + CL - 1) / CL;
   const int tiles = num_mp * ((g.N + BN - 1) / BN) * g.splits;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
-  // persistent grid: as many clusters as can be resident at once
-  static int slots = 0;
+  // persistent grid: as many clusters as can be resident at once (per device)
+  static std::atomic<int> slots_by_dev[64];
+  const int dev = current_device();
+  int slots = dev < 64 ? slots_by_dev[dev].load(std::memory_order_relaxed) : 0;
   if (slots == 0) {
     slots = num_sms() / CL;
     if (CL > 1) {
@@ -697,6 +701,7 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
         slots = n;
       cudaGetLastError();
     }
+    if (dev < 64) slots_by_dev[dev].store(slots, std::memory_order_relaxed);
   }
   // as few clusters as finish in the same number of tile rounds: the rest of
   // the SMs stay free for other streams' kernels at no cost to this one

@@ -129,6 +129,41 @@ def test_deterministic():
     assert_identical(run_gpu(shape, inp), run_gpu(shape, inp))
 
 
+def test_concurrent_calls_from_two_host_threads():
+    """Two host threads, each with its own block, workspace and streams, step
+    at the same time; each gets the bits it gets when run alone."""
+    import threading
+    shape = BlockShape("layer", "bf16", batch=2, seq=64, hidden=256, ffn=512, heads=2, w=2)
+    inps = [block_inputs(shape, seed=s, affine=True) for s in (21, 22)]
+    alone = [run_gpu(shape, inp) for inp in inps]
+    blks = [DeviceBlock(shape, inp["layers"]) for inp in inps]
+    io = [(b.tensor(i["x"]), b.tensor(i["g"])) for b, i in zip(blks, inps)]
+    torch.cuda.synchronize()
+    outs, errs = [None, None], []
+    start = threading.Barrier(2)
+
+    def work(k):
+        try:
+            start.wait(timeout=60)
+            for _ in range(4):
+                blks[k].zero_grads()
+                y, dx = blks[k].step(*io[k])
+            torch.cuda.synchronize()
+            outs[k] = {"y": to_numpy(y), "dx": to_numpy(dx), "grads": blks[k].grads_numpy()}
+        except Exception as e:  # reported below, on the test's thread
+            errs.append(e)
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not errs, errs
+    oases_check_device(None)
+    for k in range(2):
+        assert_identical(outs[k], alone[k])
+
+
 def test_block_api_equals_stack_step():
     shape = BlockShape("layer", "bf16", batch=2, seq=64, hidden=256, ffn=512, heads=2, w=2)
     inp = block_inputs(shape, seed=6, affine=True)
