@@ -343,15 +343,16 @@ def kernel_table(shape, pk, reps=20):
         status = launch()
         assert status == 0, (name, status)
         torch.cuda.synchronize(dev)
-        evs = []
+        evs, bad = [], 0
         for _ in range(reps):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
-            launch()
+            bad += launch() != 0
             e1.record(st)
             evs.append((e0, e1))
         torch.cuda.synchronize(dev)
+        assert bad == 0, (name, "failed launches", bad)
         t = sum(a.elapsed_time(b) for a, b in evs) / reps * 1e-3
         if bound == "hbm":
             ach, peak, unit = work / t / 1e9, pk["hbm_gbs"], "GB/s"
