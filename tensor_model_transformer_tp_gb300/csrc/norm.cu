@@ -303,6 +303,171 @@ ln_bwd_fused(const float* __restrict__ du, const T* __restrict__ x, const float*
   }
 }
 
+// LayerNorm backward for one block of ROWS_PER_PART rows, H % 4 == 0 and
+// H <= 4096, reading every input once.  Each row is spread over the CTA's 256
+// threads: thread t owns the 4-column chunks t, t + 256, ... (NCH of them).
+// RB rows are loaded at a time (RB * NCH <= 4 chunks in flight per thread,
+// which keeps two CTAs per SM within 128 registers a thread);
+// their two row means m1 = mean(du * gamma), m2 = mean(du * gamma * xhat) are
+// summed within each warp, then over the 8 warps in a fixed order through
+// shared memory, so the result does not depend on timing.  Then
+//   dx = rstd * (du * gamma - m1 - xhat * m2) (+ dres)
+// and the block's partial column sums pg = sum du * xhat, pb = sum du, added
+// over the rows in order, are written as one partial row.
+constexpr int LNB_THREADS = 256;
+// 4 elements of T as loaded (bf16: 8 bytes, kept packed until used)
+template <typename T> struct Raw4 { using type = float4; };
+template <> struct Raw4<__nv_bfloat16> { using type = uint2; };
+__device__ __forceinline__ float4 raw_ld(const float* p) { return ld4(p); }
+__device__ __forceinline__ uint2 raw_ld(const __nv_bfloat16* p) {
+  return *reinterpret_cast<const uint2*>(p);
+}
+__device__ __forceinline__ float4 raw_f4(float4 v) { return v; }
+__device__ __forceinline__ float4 raw_f4(uint2 u) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+template <typename R> __device__ __forceinline__ R raw_zero();
+template <> __device__ __forceinline__ float4 raw_zero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+template <> __device__ __forceinline__ uint2 raw_zero<uint2>() { return make_uint2(0u, 0u); }
+
+template <typename T, int NCH, int RB>
+__global__ void __launch_bounds__(LNB_THREADS, 2)
+ln_bwd_rows(const float* __restrict__ du, const T* __restrict__ x, const float* __restrict__ mean,
+            const float* __restrict__ rstd, const T* __restrict__ gamma,
+            const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ pg,
+            float* __restrict__ pb, int M, int H) {
+  static_assert(ROWS_PER_PART % RB == 0, "whole row groups per block");
+  constexpr int NW = LNB_THREADS / 32;
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[2][NW][2 * RB];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int m0 = blockIdx.x * ROWS_PER_PART;
+  float4 gv[NCH], ag[NCH], ab[NCH];
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int c = (tid + LNB_THREADS * j) * 4;
+    gv[j] = c < H ? ld4(gamma + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ag[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    ab[j] = ag[j];
+  }
+#pragma unroll 1
+  for (int it = 0; it < ROWS_PER_PART / RB; ++it) {
+    const int par = it & 1;
+    using R = typename Raw4<T>::type;
+    float4 d[RB][NCH];
+    R xv[RB][NCH], rv[RB][NCH];
+    float mu[RB], rs[RB], s1[RB], s2[RB];
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      const int row = m0 + it * RB + i;
+      const bool ok = row < M;
+      mu[i] = ok ? mean[row] : 0.f;
+      rs[i] = ok ? rstd[row] : 0.f;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int c = (tid + LNB_THREADS * j) * 4;
+        const int64_t o = (int64_t)row * H + c;
+        const bool in = ok && c < H;
+        d[i][j] = in ? ld4(du + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xv[i][j] = in ? raw_ld(x + o) : raw_zero<R>();
+        rv[i][j] = (in && dres) ? raw_ld(dres + o) : raw_zero<R>();
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      float a = 0.f, b = 0.f;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const float4 dd = d[i][j], xx = raw_f4(xv[i][j]), g = gv[j];
+        const float g0 = dd.x * g.x, g1 = dd.y * g.y, g2 = dd.z * g.z, g3 = dd.w * g.w;
+        a += (g0 + g1) + (g2 + g3);
+        b = fmaf(g0, (xx.x - mu[i]) * rs[i], b);
+        b = fmaf(g1, (xx.y - mu[i]) * rs[i], b);
+        b = fmaf(g2, (xx.z - mu[i]) * rs[i], b);
+        b = fmaf(g3, (xx.w - mu[i]) * rs[i], b);
+      }
+      s1[i] = warp_sum(a);
+      s2[i] = warp_sum(b);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < RB; ++i) {
+        red[par][warp][2 * i] = s1[i];
+        red[par][warp][2 * i + 1] = s2[i];
+      }
+    }
+    __syncthreads();  // (the other parity's slots are free: every thread has passed it)
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      float a = 0.f, b = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        a += red[par][w][2 * i];
+        b += red[par][w][2 * i + 1];
+      }
+      const float a1 = a / H, a2 = b / H;
+      const int row = m0 + it * RB + i;
+      if (row >= M) continue;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int c = (tid + LNB_THREADS * j) * 4;
+        if (c >= H) continue;
+        const float4 dd = d[i][j], xx = raw_f4(xv[i][j]), rr = raw_f4(rv[i][j]), g = gv[j];
+        const float h0 = (xx.x - mu[i]) * rs[i], h1 = (xx.y - mu[i]) * rs[i],
+                    h2 = (xx.z - mu[i]) * rs[i], h3 = (xx.w - mu[i]) * rs[i];
+        st4(dx + (int64_t)row * H + c,
+            make_float4(fmaf(rs[i], dd.x * g.x - a1 - h0 * a2, rr.x),
+                        fmaf(rs[i], dd.y * g.y - a1 - h1 * a2, rr.y),
+                        fmaf(rs[i], dd.z * g.z - a1 - h2 * a2, rr.z),
+                        fmaf(rs[i], dd.w * g.w - a1 - h3 * a2, rr.w)));
+        ag[j].x = fmaf(dd.x, h0, ag[j].x);
+        ag[j].y = fmaf(dd.y, h1, ag[j].y);
+        ag[j].z = fmaf(dd.z, h2, ag[j].z);
+        ag[j].w = fmaf(dd.w, h3, ag[j].w);
+        ab[j].x += dd.x;
+        ab[j].y += dd.y;
+        ab[j].z += dd.z;
+        ab[j].w += dd.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int c = (tid + LNB_THREADS * j) * 4;
+    if (c < H) {
+      st4(pg + (int64_t)blockIdx.x * H + c, ag[j]);
+      st4(pb + (int64_t)blockIdx.x * H + c, ab[j]);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t ln_bwd_rows_launch(const float* du, const void* x, const float* mean, const float* rstd,
+                               const void* gamma, const void* dres, void* dx, float* pg,
+                               float* pb, int M, int H, cudaStream_t st) {
+  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
+  const int nch = (H / 4 + LNB_THREADS - 1) / LNB_THREADS;  // 1 .. 4
+  const T *xt = (const T*)x, *gt = (const T*)gamma, *rt = (const T*)dres;
+  T* dt = (T*)dx;
+  switch (nch) {
+    case 1:
+      return launch_pdl(ln_bwd_rows<T, 1, 4>, dim3(nb), dim3(LNB_THREADS), 0, st, du, xt, mean,
+                        rstd, gt, rt, dt, pg, pb, M, H);
+    case 2:
+      return launch_pdl(ln_bwd_rows<T, 2, 2>, dim3(nb), dim3(LNB_THREADS), 0, st, du, xt, mean,
+                        rstd, gt, rt, dt, pg, pb, M, H);
+    case 3:
+      return launch_pdl(ln_bwd_rows<T, 3, 1>, dim3(nb), dim3(LNB_THREADS), 0, st, du, xt, mean,
+                        rstd, gt, rt, dt, pg, pb, M, H);
+    default:
+      return launch_pdl(ln_bwd_rows<T, 4, 1>, dim3(nb), dim3(LNB_THREADS), 0, st, du, xt, mean,
+                        rstd, gt, rt, dt, pg, pb, M, H);
+  }
+}
+
 // Column sums of a block of ROWS_PER_PART rows, 4 columns per thread (N % 4 == 0).
 template <typename T>
 __global__ void __launch_bounds__(COL_THREADS)
@@ -581,10 +746,22 @@ cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, co
                            float* part_b, float2* stat, float* dgamma, float* dbeta, int M, int H,
                            DType t, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  const bool vec = H % 4 == 0 && (((uintptr_t)du | (uintptr_t)x | (uintptr_t)gamma |
-                                   (uintptr_t)dres | (uintptr_t)dx) & 7) == 0 &&
-                   (t == DType::BF16 || ((uintptr_t)du | (uintptr_t)x | (uintptr_t)gamma |
-                                         (uintptr_t)dres | (uintptr_t)dx) % 16 == 0);
+  // du is fp32 (16-byte vector loads); x, gamma, dres, dx 8-byte (bf16) or
+  // 16-byte (fp32) vectors of 4 elements
+  const bool vec = H % 4 == 0 && ((uintptr_t)du & 15) == 0 &&
+                   (((uintptr_t)x | (uintptr_t)gamma | (uintptr_t)dres | (uintptr_t)dx) &
+                    (t == DType::BF16 ? 7 : 15)) == 0 &&
+                   ((uintptr_t)part_g & 15) == 0 && ((uintptr_t)part_b & 15) == 0;
+  if (vec && H <= 4 * LNB_THREADS * 4) {
+    const int nb = ln_bwd_blocks(M);
+    cudaError_t e = t == DType::F32
+                        ? ln_bwd_rows_launch<float>(du, x, mean, rstd, gamma, dres, dx, part_g,
+                                                    part_b, M, H, st)
+                        : ln_bwd_rows_launch<__nv_bfloat16>(du, x, mean, rstd, gamma, dres, dx,
+                                                            part_g, part_b, M, H, st);
+    if (e != cudaSuccess) return e;
+    return reduce_parts(part_g, dgamma, part_b, dbeta, nb, H, st);
+  }
   if (vec) {
     const int nb = ln_bwd_blocks(M);
     cudaError_t e;

@@ -114,8 +114,11 @@ def test_layer_norm_forward(L, M, H, dtype):
     _close(_np(u), ru, dtype)
 
 
+# 4-column chunks per thread 1 (H <= 1024), 2, 3 and 4 (H <= 4096), H % 4 != 0
+# (scalar kernels), H > 4096 (two-phase kernel), ragged row blocks, M = 0
 LN_BWD_CASES = [(37, 1024, "bf16", True), (9, 256, "f32", False), (50, 302, "bf16", True),
-                (1, 2560, "bf16", False), (4096, 4096, "bf16", True), (0, 256, "f32", True)]
+                (1, 2560, "bf16", False), (4096, 4096, "bf16", True), (0, 256, "f32", True),
+                (13, 1028, "bf16", True), (19, 4096, "f32", True), (5, 5120, "bf16", True)]
 
 
 @pytest.mark.parametrize("M,H,dtype,resid", LN_BWD_CASES)
