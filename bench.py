@@ -36,7 +36,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300"
+METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300; % of dense BF16 peak"
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel of one workload (the fused column GEMM + bias + GeLU of the FFN, one
 # sub-batch), with the sha256 of the kernel sources it was measured on
@@ -582,6 +582,8 @@ def main():
                       "launch": "cuda-graph" if not args.no_graph else "direct",
                       "l2": "flushed between timed steps (256 MiB write)"},
            "pct_bf16_peak": 100.0 * value / world / pk["bf16_tflops_sustained"],
+           "pct_bf16_peak_of": "%s sustained bf16 GEMM rate, %.1f TFLOP/s per GPU" % (
+               pk["source"], pk["bf16_tflops_sustained"]),
            "e2e": {"value": whole_job_tflops(fl, world, t_e2e), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": 2 * io, "d2h_bytes_per_step": 2 * io},
            "gpu_launches": launches * args.steps,
