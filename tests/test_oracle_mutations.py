@@ -187,3 +187,49 @@ def test_selective_recompute_of_attention_drops_the_mask(monkeypatch):
             self.shape = shape
     monkeypatch.setattr(osch._Segment, "attn_fwd", bad)
     assert _caught(lambda: pins.test_recompute_modes_bit_identical("attn"))
+
+
+def test_gelu_tanh_approximation(monkeypatch):
+    """The tanh form of GeLU is a different function (off by up to ~1e-3)."""
+    def bad(a):
+        return 0.5 * a * (1 + np.tanh(np.sqrt(2 / np.pi) * (a + 0.044715 * a ** 3)))
+    monkeypatch.setattr(oops, "gelu", bad)
+    assert _caught(pins.test_gelu_against_normal_table)
+
+
+def test_layer_norm_gamma_gradient_without_normalisation(monkeypatch):
+    """dgamma must use xhat = (x - mean) * rstd, not the centred x alone."""
+    orig = oops.layer_norm_backward
+
+    def bad(du, x, mean, rstd, gamma):
+        dx, _, db = orig(du, x, mean, rstd, gamma)
+        return dx, (du * (x - mean[:, None])).sum(0), db
+    monkeypatch.setattr(osch, "layer_norm_backward", bad)
+    assert _caught(FD_FFN)
+
+
+def test_attention_backward_without_the_row_term(monkeypatch):
+    """dS = P * (dP - rowsum(dP * P)); dropping the row term breaks dQ and dK."""
+    import math
+
+    def bad(do, q, k, v, p):
+        scale = 1.0 / math.sqrt(q.shape[1])
+        dv = p.T @ do
+        ds = p * (do @ v.T)
+        return (ds @ k) * scale, (ds.T @ q) * scale, dv
+    monkeypatch.setattr(osch, "attention_head_backward", bad)
+    assert _caught(FD_ATTN)
+
+
+def test_weight_gradient_overwritten_per_sub_batch(monkeypatch):
+    """Gradients of the sub-batches are summed; keeping only the last one is a
+    plausible slip (two sub-batches in every tiny shape)."""
+    def bad(self, a, grads):
+        wr = self.p[self.names["wr"]]
+        dH = []
+        for Hk, dPk, c in zip(a[(self.s, "H")], a[(self.s, "dP")], self.cols):
+            grads[self.names["wr"]][:, c] = dPk.T @ Hk
+            dH.append(dPk @ wr[:, c])
+        a[(self.s, "dH")] = dH
+    monkeypatch.setattr(osch._Segment, "row_bwd", bad)
+    assert _caught(FD_FFN, lambda: pins.test_sub_batch_split_invariance("ffn"))
