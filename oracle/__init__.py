@@ -22,7 +22,10 @@ equation or algorithm:
     reverse-order Recompute then Backward).
 The block internals (pre-LayerNorm, erf GeLU, causal softmax attention,
 residual, row-parallel bias added once after the shard sum) are not on the
-pages; they follow the textbook definitions of these layers.
+pages; they follow the textbook definitions of these layers.  ``oracle.fp8``
+(E4M3 rounding and MX block-scaled GEMMs, for an FP8 form of the block's
+GEMMs that the pages do not describe) follows the published format
+definitions cited in its header.
 
 Everything is float64 numpy.  Parity status of each function is stated in its
 docstring; every function here is pinned by a test in tests/test_oracle_*.py.

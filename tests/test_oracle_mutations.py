@@ -233,3 +233,51 @@ def test_weight_gradient_overwritten_per_sub_batch(monkeypatch):
         a[(self.s, "dH")] = dH
     monkeypatch.setattr(osch._Segment, "row_bwd", bad)
     assert _caught(FD_FFN, lambda: pins.test_sub_batch_split_invariance("ffn"))
+
+
+# ---- FP8 E4M3 / MX oracle (oracle/fp8.py) ----
+import oracle.fp8 as ofp8
+import test_oracle_fp8 as fp8pins
+
+
+def test_fp8_ties_away_from_zero(monkeypatch):
+    orig_pos = ofp8._POS
+
+    def bad(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.minimum(np.abs(x), ofp8.E4M3_MAX)
+        hi = np.clip(np.searchsorted(orig_pos, a, side="left"), 0, len(orig_pos) - 1)
+        lo = np.maximum(hi - 1, 0)
+        code = np.where(orig_pos[hi] - a <= a - orig_pos[lo], hi, lo).astype(np.int64)
+        code = np.where(np.signbit(x), code | 0x80, code)
+        return np.where(np.isnan(x), 0x7F, code).astype(np.uint8)
+    monkeypatch.setattr(ofp8, "e4m3_encode", bad)
+    assert _caught(fp8pins.test_ties_go_to_the_even_code)
+
+
+def test_fp8_overflow_to_nan_instead_of_saturating(monkeypatch):
+    orig = ofp8.e4m3_encode
+
+    def bad(x):
+        x = np.asarray(x, dtype=np.float64)
+        return np.where(np.abs(x) > ofp8.E4M3_MAX, 0x7F, orig(x)).astype(np.uint8)
+    monkeypatch.setattr(ofp8, "e4m3_encode", bad)
+    assert _caught(fp8pins.test_saturation_and_underflow)
+
+
+def test_fp8_mx_scale_exponent_off_by_one(monkeypatch):
+    monkeypatch.setattr(ofp8, "EMAX_ELEM", 7)
+    assert _caught(lambda: fp8pins.test_mx_scale_is_the_block_exponent_minus_8(0))
+
+
+def test_fp8_mx_gemm_drops_the_b_scale(monkeypatch):
+    def bad(A, B, block=32):
+        PA, XA = ofp8.mx_quantize(A, block)
+        PB, _ = ofp8.mx_quantize(B, block)
+        D = np.zeros((A.shape[0], B.shape[0]))
+        for b in range((A.shape[1] + block - 1) // block):
+            s = slice(b * block, (b + 1) * block)
+            D += XA[:, b:b + 1] * (PA[:, s] @ PB[:, s].T)
+        return D
+    monkeypatch.setattr(ofp8, "mx_gemm", bad)
+    assert _caught(fp8pins.test_mx_gemm_exact_on_representable_inputs)
