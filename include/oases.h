@@ -66,7 +66,7 @@ extern "C" {
 typedef enum {
   OASES_OK = 0,
   OASES_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, inconsistent shape */
-  OASES_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  OASES_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement */
   OASES_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than oases_workspace_bytes() */
   OASES_ERR_CUDA = 4,         /* a CUDA call failed; see oases_last_error() */
   OASES_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up */
