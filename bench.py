@@ -184,22 +184,69 @@ def dist_env():
     return rank, world, local
 
 
-def run_reference(args, shape):
-    """The oracle as it stands, on this host's cores, on a bounded sample."""
-    import numpy as np
+def oracle_rate(shape, recompute) -> float:
+    """The oracle's FLOP/s on a small calibration sample of the workload (one
+    sequence per sub-batch, at most 64 tokens).  Fixed costs weigh more on so
+    small a sample, so the rate errs low and the samples sized from it small."""
+    import oracle
+    from synth import block_inputs
+    cal = shape.replace(batch=shape.sub_batches, seq=min(shape.seq, 64))
+    inp = block_inputs(cal, seed=0)
+    t0 = time.perf_counter()
+    oracle.run_step(cal, inp, mode=recompute)
+    return flops_fine(cal, recompute) / max(time.perf_counter() - t0, 1e-6)
 
+
+def oracle_sample(shape, recompute, seconds: float, rate: float):
+    """The largest sample of the workload whose oracle step should take at most
+    `seconds` at `rate` FLOP/s: its first sequences, a multiple of the
+    sub-batch count; when one sequence per sub-batch is already too much, those
+    sequences shortened (halved down to 8 tokens; the FFN is row-wise, the
+    attention per sequence, so a shorter sequence is a smaller instance)."""
+    fits = lambda s: flops_fine(s, recompute) / rate <= seconds
+    s = shape.replace(batch=shape.sub_batches)
+    while s.seq > 8 and not fits(s):
+        s = s.replace(seq=max(8, s.seq // 2))
+    nsb = shape.sub_batches
+    while (s.seq == shape.seq and s.batch + nsb <= shape.batch
+           and fits(s.replace(batch=s.batch + nsb))):
+        s = s.replace(batch=s.batch + nsb)
+    return s
+
+
+def sample_text(sample, shape) -> str:
+    return "%d of %d sequences, %d of %d tokens each" % (sample.batch, shape.batch, sample.seq,
+                                                          shape.seq)
+
+
+REFERENCE_SECONDS = 150.0  # the whole --impl reference run (warm-up and timed steps)
+
+
+def run_reference(args, shape):
+    """The oracle as it stands, on this host's cores, each step on a bounded
+    sample sized so that all warm-up and timed steps take about
+    REFERENCE_SECONDS."""
     import oracle
     from synth import block_inputs
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    # sample: the first sequences of the workload (the FFN is row-wise, the
-    # attention per sequence), sized to a few seconds of fp64 work per step
-    per_seq = flops_fine(shape.replace(batch=1))
-    nb = max(shape.sub_batches, int(20e9 // max(per_seq, 1.0)))
-    nb = min(shape.batch, nb - nb % shape.sub_batches or shape.sub_batches)
-    sample = shape.replace(batch=nb)
+    per_step = REFERENCE_SECONDS / max(args.steps + args.warmup, 1)
+    sample = oracle_sample(shape, args.recompute, per_step, oracle_rate(shape, args.recompute))
     inp = block_inputs(sample, seed=0)
+    # the calibration rate can be off for the sample taken: time one step of it
+    # (untimed, like the warm-up) and shrink it while it runs well over budget
+    while True:
+        t0 = time.perf_counter()
+        oracle.run_step(sample, inp, mode=args.recompute)
+        if time.perf_counter() - t0 <= 1.25 * per_step or (
+                sample.batch == shape.sub_batches and sample.seq <= 8):
+            break
+        if sample.batch > shape.sub_batches:
+            sample = sample.replace(batch=sample.batch - shape.sub_batches)
+        else:
+            sample = sample.replace(seq=max(8, sample.seq // 2))
+        inp = block_inputs(sample, seed=0)
     for _ in range(args.warmup):
         oracle.run_step(sample, inp, mode=args.recompute)
     t0 = time.perf_counter()
@@ -212,23 +259,22 @@ def run_reference(args, shape):
             "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded normal inputs, seed 0)",
-            "config": {"workload": args.workload, "batch_sample": nb, "recompute": args.recompute},
+            "config": {"workload": args.workload, "batch_sample": sample.batch,
+                       "seq_sample": sample.seq, "recompute": args.recompute},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": "%d of %d sequences per step" % (nb, shape.batch)},
+                             "sample": sample_text(sample, shape) + " per step"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def cpu_baseline(shape, recompute):
-    """Oracle timed on a bounded sample (rank 0, N = 1 only): whole steps on the
-    first sequences of the workload, repeated until about 10 s of host work."""
+    """Oracle timed on a bounded sample (rank 0, N = 1 only): whole steps on a
+    sample of the workload of about 5 s each, repeated until about 10 s of host
+    work."""
     import oracle
     from synth import block_inputs
-    per_seq = flops_fine(shape.replace(batch=1))
-    nb = max(shape.sub_batches, int(60e9 // max(per_seq, 1.0)))
-    nb = min(shape.batch, nb - nb % shape.sub_batches or shape.sub_batches)
-    sample = shape.replace(batch=nb)
+    sample = oracle_sample(shape, recompute, 5.0, oracle_rate(shape, recompute))
     inp = block_inputs(sample, seed=0)
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -239,8 +285,8 @@ def cpu_baseline(shape, recompute):
             break
     return {"value": flops_fine(sample, recompute) * reps / dt / 1e12, "unit": "TFLOP/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": "%d steps on %d of %d sequences (%.1f s, fp64 numpy)" % (
-                reps, nb, shape.batch, dt)}
+            "sample": "%d steps on %s (%.1f s, fp64 numpy)" % (
+                reps, sample_text(sample, shape), dt)}
 
 
 def dominant_kernel_roofline(blk, shape, pk, torch, workload):

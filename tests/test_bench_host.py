@@ -58,6 +58,25 @@ def test_traffic_is_reported_only_for_the_captured_workload():
             assert (t is None) == (b.kernel_source_sha() != b.NCU_TRAFFIC["source_sha256"])
 
 
+@pytest.mark.parametrize("name", sorted(SHAPES))
+@pytest.mark.parametrize("seconds", [0.01, 0.5, 5.0, 1e6])
+def test_oracle_sample_is_the_largest_that_fits(name, seconds):
+    b = _bench()
+    shape, rate = SHAPES[name], 2e11
+    s = b.oracle_sample(shape, "fine", seconds, rate)
+    s.validate()
+    assert s.batch % shape.sub_batches == 0 and s.batch <= shape.batch and s.seq <= shape.seq
+    cost = lambda t: b.flops_fine(t) / rate
+    if s.seq > 8:
+        assert cost(s) <= seconds
+    if s.seq < shape.seq:     # halved from a length that did not fit, one sub-batch's worth
+        assert s.batch == shape.sub_batches and cost(s.replace(seq=2 * s.seq)) > seconds
+    elif s.batch < shape.batch:
+        assert cost(s.replace(batch=s.batch + shape.sub_batches)) > seconds
+    if seconds == 1e6:
+        assert s == shape
+
+
 def test_whole_job_throughput_is_total_work_over_slowest_rank():
     b = _bench()
     assert b.whole_job_tflops(2e12, 4, 0.5) == pytest.approx(16.0)
