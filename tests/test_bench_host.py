@@ -121,3 +121,29 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 
     assert b.run_reference(Args, SHAPES["ffn_bf16_h1024"]) is None
     assert capsys.readouterr().out == ""   # no line from a non-zero rank
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference end to end (the oracle on this host): one JSON
+    line with the contract's keys, the oracle's own numbers in value, e2e and
+    cpu_baseline."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "ffn_f32_h256", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT,
+                       env={**os.environ, "RANK": "0", "WORLD_SIZE": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "ffn_f32_h256" and d["steps"] == 2
