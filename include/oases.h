@@ -212,6 +212,21 @@ int oases_schedule_trace(const oases_block_desc *desc, int n_layers, int phase,
 /* Number of kernel launches the last call on this thread enqueued. */
 int oases_last_launch_count(void);
 
+/* Releases the host-side state the library keeps between calls: the copy
+ * stream it made per device for host-buffer staging, the calling thread's
+ * CUDA events (per device), the event timeline of the trace aid and the host
+ * caches of tensor maps and device addresses.  Work already enqueued is not
+ * waited for: CUDA frees a stream or event once its pending work completes.
+ * No device memory is involved (the library never allocates any).  Events
+ * that other host threads made are released when those threads exit.  Call it
+ * while no other thread is inside a library call, and before cudaDeviceReset
+ * (state of a context that no longer exists is dropped, not reused, either
+ * way).  Any later call makes what it needs again.  Returns OASES_ERR_CUDA if
+ * destroying a stream or event failed (everything is released regardless).
+ * The pages fix no API; this is the release half of the executor's cached
+ * state (Oases §IV, the runtime executor). */
+oases_status oases_shutdown(void);
+
 /* Synchronizes the stream, then reports whether a bounded device-side wait of
  * a tensor-core kernel expired since the last check (OASES_ERR_TIMEOUT; the
  * error word is cleared), or a CUDA error occurred (OASES_ERR_CUDA). */

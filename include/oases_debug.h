@@ -163,7 +163,10 @@ oases_status oases_debug_shard_sum(const float *part, int64_t pstride, int w, co
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls on a device share the one array, which keeps
+ * any stream capture.  The address is kept per device together with the CUDA
+ * context it belongs to: after a cudaDeviceReset (or after oases_shutdown())
+ * the next call looks it up again, so that call too should come before any
+ * capture.  All calls on a device share the one array, which keeps
  * the previous call's contents (every value it reads is written first by the
  * same call): calls whose executions overlap on the GPU (for instance on two
  * streams without ordering between them) race on the array and give wrong

@@ -78,6 +78,8 @@ def lib():
         L.oases_last_launch_count.restype = i32
         L.oases_check_device.argtypes = [vp]
         L.oases_check_device.restype = i32
+        L.oases_shutdown.argtypes = []
+        L.oases_shutdown.restype = i32
         _lib = L
     return _lib
 
@@ -184,6 +186,12 @@ def oases_check_device(stream=None) -> None:
     _check(lib().oases_check_device(_stream(stream)))
 
 
+def oases_shutdown() -> None:
+    """Release the library's cached host-side state (copy streams, this
+    thread's events, tensor-map cache); later calls make it again."""
+    _check(lib().oases_shutdown())
+
+
 def oases_status_str(st: int) -> str:
     return lib().oases_status_str(st).decode()
 
@@ -205,5 +213,5 @@ def _nbytes(t) -> int:
 __all__ = ["BlockDesc", "Weights", "Grads", "OasesError", "build_library", "lib", "make_desc",
            "desc_from_shape", "weights_struct", "grads_struct", "oases_workspace_bytes",
            "oases_block_fwd", "oases_block_recompute_bwd", "oases_stack_step",
-           "oases_schedule_trace", "oases_last_launch_count", "oases_check_device",
+           "oases_schedule_trace", "oases_last_launch_count", "oases_check_device", "oases_shutdown",
            "oases_status_str", "oases_version", "PARAM_NAMES"]

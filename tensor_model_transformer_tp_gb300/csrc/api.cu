@@ -21,6 +21,7 @@
 // cross-stream dependencies are the weight-gradient accumulations, which are
 // chained sub-batch 0 -> 1 -> ... per (segment, parameter) with events so the
 // sums are taken in a fixed order.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -36,7 +37,37 @@
 
 namespace oases {
 thread_local int g_launch_count = 0;
+
+uint64_t current_ctx_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS) return 0;
+  if (!c) {
+    // no context bound to this thread yet: cudaSetDevice binds (and, if need
+    // be, creates) the current device's primary context
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || cudaSetDevice(d) != cudaSuccess) return 0;
+    if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  }
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? (uint64_t)id : 0;
 }
+}  // namespace oases
 
 namespace oases {
 // Entry-point bookkeeping shared with the other translation units that define
@@ -44,6 +75,9 @@ namespace oases {
 void api_begin();
 void api_set_error(const char* what);
 oases_status api_end(cudaError_t e);
+// Host caches of the other translation units, emptied by oases_shutdown().
+void gemm_release_host_caches();
+void noalloc_release_host_caches();
 }
 
 namespace {
@@ -59,10 +93,13 @@ struct TraceRec {
   cudaEvent_t e0, e1;
 };
 struct TraceEvents {
+  uint64_t ctx = 0;  // context the events belong to
   std::vector<cudaEvent_t> ev;
-  ~TraceEvents() {
+  void release() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    ev.clear();
   }
+  ~TraceEvents() { release(); }
 };
 std::atomic<bool> g_trace_on{false};
 thread_local std::vector<TraceRec> g_trace;
@@ -312,10 +349,14 @@ bool injected(const std::vector<Step>& steps) {
 // Execution.
 // ---------------------------------------------------------------------------
 struct EventPool {
+  uint64_t ctx = 0;  // context the events belong to
   std::vector<cudaEvent_t> ev;
-  ~EventPool() {  // at thread exit; an event with pending work is released when it completes
+  // an event with pending work is released when that work completes
+  void release() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    ev.clear();
   }
+  ~EventPool() { release(); }  // at thread exit
   cudaError_t ensure(size_t n) {
     while (ev.size() < n) {
       cudaEvent_t e;
@@ -330,28 +371,42 @@ struct EventPool {
 // so concurrent calls from several threads never share an event (calls from
 // one thread are enqueued in order, and a wait captures an event's state when
 // it is enqueued, so reuse across that thread's calls is safe); per device,
-// because an event can be recorded only on streams of its own device.
+// because an event can be recorded only on streams of its own device.  Events
+// made under a context that has since been destroyed are dropped, not used.
+thread_local std::unordered_map<int, EventPool> t_pools;
 EventPool& pool() {
-  thread_local std::unordered_map<int, EventPool> pools;
-  return pools[current_device()];
+  EventPool& p = t_pools[current_device()];
+  const uint64_t id = current_ctx_id();
+  if (p.ctx != id) {
+    p.ev.clear();  // the old context took its events with it
+    p.ctx = id;
+  }
+  return p;
 }
 
 // A non-blocking stream per device for host<->device staging copies, so they
-// overlap the compute streams (created once, kept for the process).
+// overlap the compute streams (created on first use, kept until
+// oases_shutdown() or until the device's context is destroyed).
+struct CopyStream {
+  uint64_t ctx = 0;
+  cudaStream_t st = nullptr;
+};
+std::mutex g_copy_mu;
+std::unordered_map<int, CopyStream> g_copy;
+
 cudaStream_t copy_stream() {
-  static std::mutex mu;
-  static std::unordered_map<int, cudaStream_t> m;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = m.find(dev);
-  if (it != m.end()) return it->second;
+  const uint64_t id = current_ctx_id();
+  std::lock_guard<std::mutex> lock(g_copy_mu);
+  auto it = g_copy.find(dev);
+  if (it != g_copy.end() && it->second.ctx == id && id != 0) return it->second.st;
   cudaStream_t st = nullptr;
   if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
-  m[dev] = st;
+  g_copy[dev] = CopyStream{id, st};
   return st;
 }
 
@@ -943,7 +998,16 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   int bwd_started = 0;
   const bool tracing = g_trace_on.load(std::memory_order_relaxed);
   g_trace.clear();
-  std::vector<cudaEvent_t>* tevs = tracing ? &g_trace_events[current_device()].ev : nullptr;
+  std::vector<cudaEvent_t>* tevs = nullptr;
+  if (tracing) {
+    TraceEvents& te = g_trace_events[current_device()];
+    const uint64_t id = current_ctx_id();
+    if (te.ctx != id) {
+      te.ev.clear();  // events of a destroyed context
+      te.ctx = id;
+    }
+    tevs = &te.ev;
+  }
   size_t tev = 0;
   if (s.M > 0)
     for (const Step& st : steps) {
@@ -1091,6 +1155,48 @@ int oases_schedule_trace(const oases_block_desc* desc, int n_layers, int phase, 
 }
 
 int oases_last_launch_count(void) { return t_last_launches; }
+
+oases_status oases_shutdown(void) {
+  t_last_error.clear();
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) cur = -1;
+  cudaError_t first = cudaSuccess;
+  auto note = [&](cudaError_t e) {
+    if (first == cudaSuccess && e != cudaSuccess) first = e;
+  };
+  // Streams and events of a live context are destroyed with that context's
+  // device current (pending work completes first, then CUDA frees them); those
+  // of a context that no longer exists are only forgotten.
+  auto on_device = [&](int dev, uint64_t ctx, auto&& destroy) {
+    if (ctx == 0 || cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    if (current_ctx_id() == ctx) destroy();
+  };
+  {
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    for (auto& kv : g_copy)
+      on_device(kv.first, kv.second.ctx, [&] { note(cudaStreamDestroy(kv.second.st)); });
+    g_copy.clear();
+  }
+  for (auto& kv : t_pools) {
+    on_device(kv.first, kv.second.ctx, [&] { kv.second.release(); });
+    kv.second.ev.clear();
+  }
+  t_pools.clear();
+  for (auto& kv : g_trace_events) {
+    on_device(kv.first, kv.second.ctx, [&] { kv.second.release(); });
+    kv.second.ev.clear();
+  }
+  g_trace_events.clear();
+  g_trace.clear();
+  if (cur >= 0) cudaSetDevice(cur);
+  gemm_release_host_caches();
+  noalloc_release_host_caches();
+  if (first != cudaSuccess) return cuda_fail(first);
+  return OASES_OK;
+}
 
 oases_status oases_check_device(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -16,19 +16,27 @@ inline int current_device() {
   int d = 0;
   return cudaGetDevice(&d) == cudaSuccess ? d : 0;
 }
-// Runs a per-device setup step (a kernel attribute, say) once per device:
-// run(f) calls f until it succeeds on the current device, then skips it
-// there.  Safe from several threads (f may run more than once concurrently,
-// so it must be idempotent).  Device ordinals >= 64 run f on every call.
+// Unique id of the calling thread's current CUDA context (the driver's
+// context id, never reused within the process), 0 if there is none yet.
+// Host caches of per-device state (events, streams, kernel attributes, device
+// addresses) keep the id they were made under and are remade when it changes,
+// so state of a context that was destroyed (cudaDeviceReset) is never reused.
+uint64_t current_ctx_id();
+
+// Runs a per-device setup step (a kernel attribute, say) once per device and
+// context: run(f) calls f until it succeeds on the current device, then skips
+// it there while the context stays the same.  Safe from several threads (f may
+// run more than once concurrently, so it must be idempotent).  Device ordinals
+// >= 64 run f on every call.
 struct DeviceOnce {
-  std::atomic<uint64_t> done{0};
+  std::atomic<uint64_t> ctx[64] = {};
   template <typename F>
   cudaError_t run(F&& f) {
     const int dev = current_device();
-    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
-    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const uint64_t id = current_ctx_id();
+    if (dev < 64 && id != 0 && ctx[dev].load(std::memory_order_acquire) == id) return cudaSuccess;
     const cudaError_t e = f();
-    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    if (e == cudaSuccess && dev < 64) ctx[dev].store(current_ctx_id(), std::memory_order_release);
     return e;
   }
 };

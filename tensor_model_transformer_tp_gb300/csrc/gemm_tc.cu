@@ -374,7 +374,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
-  if (CL > 1) ptx::cluster_sync();  // partner's barriers initialised before any multicast
+  if (CL > 1) ptx::cluster_sync();  // partner's barriers initialised before any cross-CTA arrival
   // Everything above touched only shared memory, TMEM and kernel parameters, so
   // it overlapped the previous kernel on the stream; global memory from here on.
   pdl_wait();
@@ -596,11 +596,14 @@ struct MapKeyHash {
 // swizzle, out-of-bounds elements read as zero.  depth > 1 adds a third
 // dimension of `depth` such matrices, ld2 elements apart (box depth 1).
 // Cached by its arguments.
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+
 bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
               uint32_t box_inner, uint32_t box_outer, bool f32 = false, uint64_t depth = 1,
               uint64_t ld2 = 0) {
-  static std::mutex mu;
-  static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+  std::mutex& mu = g_map_mu;
+  auto& cache = g_map_cache;
   if (depth < 1) depth = 1;
   const MapKey key{(uintptr_t)ptr | (f32 ? 1u : 0u), inner, outer, ld, depth,
                    depth > 1 ? ld2 : 0, box_inner, box_outer};
@@ -784,6 +787,11 @@ cudaError_t gemm(const GemmArgs& g, cudaStream_t st) {
   if (gemm_tc_supported(g)) return gemm_tc(g, st);
   if (g.splits != 1 || g.kpieces != 1) return cudaErrorNotSupported;  // tensor-core path only
   return gemm_simt(g, st);
+}
+
+void gemm_release_host_caches() {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  g_map_cache.clear();
 }
 
 cudaError_t gemm_set_timeline(unsigned long long* p) {

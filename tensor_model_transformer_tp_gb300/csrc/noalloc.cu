@@ -22,10 +22,16 @@ static __device__ __align__(256) float g_noalloc_scratch[OASES_NOALLOC_SCRATCH_F
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-float* g_dev_scratch[kMaxDevices] = {};
+struct Scratch {
+  uint64_t ctx = 0;  // context the address was looked up in
+  float* p = nullptr;
+};
+Scratch g_dev_scratch[kMaxDevices];
 
 // Device address of g_noalloc_scratch on the current device, looked up once per
-// device (with that device current).  Returns nullptr and sets *err on failure.
+// device and context (with that device current): a context created after a
+// cudaDeviceReset gets a new lookup, never the old address.  Returns nullptr
+// and sets *err on failure.
 float* scratch_for_current_device(cudaError_t* err) {
   int dev = 0;
   *err = cudaGetDevice(&dev);
@@ -34,17 +40,27 @@ float* scratch_for_current_device(cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  const uint64_t id = oases::current_ctx_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_dev_scratch[dev]) {
+  Scratch& s = g_dev_scratch[dev];
+  if (!s.p || s.ctx != id || id == 0) {
     void* p = nullptr;
     *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (*err != cudaSuccess) return nullptr;
-    g_dev_scratch[dev] = static_cast<float*>(p);
+    s.p = static_cast<float*>(p);
+    s.ctx = id;
   }
-  return g_dev_scratch[dev];
+  return s.p;
 }
 
 }  // namespace
+
+namespace oases {
+void noalloc_release_host_caches() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (Scratch& s : g_dev_scratch) s = Scratch{};
+}
+}  // namespace oases
 
 extern "C" oases_status oases_bias_grad_noalloc(const void* in, int64_t ld, int M, int N,
                                                 int dtype, float* out, void* stream) {

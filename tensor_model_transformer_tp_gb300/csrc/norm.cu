@@ -476,17 +476,21 @@ colsum_vec_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __r
   pdl_trigger();
   const int c = (blockIdx.x * COL_THREADS + threadIdx.x) * 4;
   if (c >= N) return;
-  const int m0 = blockIdx.y * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  // partial row p sums rows 8p .. 8p+7; CTA row y takes p = y, y + gridDim.y, ...
+  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
+  for (int p = blockIdx.y; p < nb; p += gridDim.y) {
+    const int m0 = p * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int m = m0; m < m1; ++m) {
-    const float4 v = ld4(in + (int64_t)m * ld + c);
-    a.x += v.x;
-    a.y += v.y;
-    a.z += v.z;
-    a.w += v.w;
+    for (int m = m0; m < m1; ++m) {
+      const float4 v = ld4(in + (int64_t)m * ld + c);
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    st4(part + (int64_t)p * N + c, a);
   }
-  st4(part + (int64_t)blockIdx.y * N + c, a);
 }
 
 template <typename T>
@@ -496,17 +500,20 @@ colsum_part_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __
   pdl_trigger();
   const int c0 = (blockIdx.x * COL_THREADS + threadIdx.x) * COLS_PER_THREAD;
   if (c0 >= N) return;
-  const int m0 = blockIdx.y * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
-  float s[COLS_PER_THREAD] = {};
+  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
+  for (int p = blockIdx.y; p < nb; p += gridDim.y) {
+    const int m0 = p * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
+    float s[COLS_PER_THREAD] = {};
 #pragma unroll 8
-  for (int m = m0; m < m1; ++m) {
+    for (int m = m0; m < m1; ++m) {
+#pragma unroll
+      for (int i = 0; i < COLS_PER_THREAD; ++i)
+        if (c0 + i < N) s[i] += ld_elem(in, (int64_t)m * ld + c0 + i);
+    }
 #pragma unroll
     for (int i = 0; i < COLS_PER_THREAD; ++i)
-      if (c0 + i < N) s[i] += ld_elem(in, (int64_t)m * ld + c0 + i);
+      if (c0 + i < N) part[(int64_t)p * N + c0 + i] = s[i];
   }
-#pragma unroll
-  for (int i = 0; i < COLS_PER_THREAD; ++i)
-    if (c0 + i < N) part[(int64_t)blockIdx.y * N + c0 + i] = s[i];
 }
 
 // out[n] += sum_b part[b, n] over b = 0 .. nb-1 in a fixed order: thread group g
@@ -556,19 +563,22 @@ part_reduce_l1(float* __restrict__ part, float* __restrict__ part2, int nb, int 
   pdl_trigger();
   const int n = blockIdx.x * 256 + threadIdx.x;
   if (n >= N) return;
-  const int r0 = blockIdx.y * RED_ROWS, r1 = min(nb, r0 + RED_ROWS);
-  for (int a = 0; a < (part2 ? 2 : 1); ++a) {
-    float* p = a == 0 ? part : part2;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    int r = r0;
-    for (; r + 4 <= r1; r += 4) {
-      s0 += p[(int64_t)r * N + n];
-      s1 += p[(int64_t)(r + 1) * N + n];
-      s2 += p[(int64_t)(r + 2) * N + n];
-      s3 += p[(int64_t)(r + 3) * N + n];
+  const int ngroups = (nb + RED_ROWS - 1) / RED_ROWS;
+  for (int grp = blockIdx.y; grp < ngroups; grp += gridDim.y) {
+    const int r0 = grp * RED_ROWS, r1 = min(nb, r0 + RED_ROWS);
+    for (int a = 0; a < (part2 ? 2 : 1); ++a) {
+      float* p = a == 0 ? part : part2;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      int r = r0;
+      for (; r + 4 <= r1; r += 4) {
+        s0 += p[(int64_t)r * N + n];
+        s1 += p[(int64_t)(r + 1) * N + n];
+        s2 += p[(int64_t)(r + 2) * N + n];
+        s3 += p[(int64_t)(r + 3) * N + n];
+      }
+      for (; r < r1; ++r) s0 += p[(int64_t)r * N + n];
+      p[(int64_t)r0 * N + n] = (s0 + s1) + (s2 + s3);
     }
-    for (; r < r1; ++r) s0 += p[(int64_t)r * N + n];
-    p[(int64_t)r0 * N + n] = (s0 + s1) + (s2 + s3);
   }
 }
 __global__ void __launch_bounds__(256)
@@ -591,7 +601,8 @@ part_reduce_l2(const float* __restrict__ part, float* __restrict__ out,
 cudaError_t reduce_parts(float* part, float* out, float* part2, float* out2, int nb, int N,
                          cudaStream_t st) {
   const int gx = (N + 255) / 256;
-  cudaError_t e = launch_pdl(part_reduce_l1, dim3(gx, (nb + RED_ROWS - 1) / RED_ROWS), dim3(256),
+  const int gy = std::min((nb + RED_ROWS - 1) / RED_ROWS, 65535);
+  cudaError_t e = launch_pdl(part_reduce_l1, dim3(gx, gy), dim3(256),
                              0, st, part, part2, nb, N);
   if (e != cudaSuccess) return e;
   return launch_pdl(part_reduce_l2, dim3(gx), dim3(256), 0, st, (const float*)part, out,
@@ -787,11 +798,14 @@ cudaError_t colsum_accum(const void* in, int64_t ld, int M, int N, DType t, floa
                          float* out, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   const int nb = colsum_blocks(M);
-  const dim3 pgrid((N + COLS_PER_CTA - 1) / COLS_PER_CTA, nb);
+  // gridDim.y is limited to 65535: beyond that each CTA row takes several
+  // partial rows (same partial sums, same order)
+  const int gy = std::min(nb, 65535);
+  const dim3 pgrid((N + COLS_PER_CTA - 1) / COLS_PER_CTA, gy);
   cudaError_t e;
   const size_t esz = t == DType::F32 ? 4 : 2;
   if (N % 4 == 0 && ld % 4 == 0 && ((uintptr_t)in % (4 * esz)) == 0) {
-    const dim3 vgrid((N + 4 * COL_THREADS - 1) / (4 * COL_THREADS), nb);
+    const dim3 vgrid((N + 4 * COL_THREADS - 1) / (4 * COL_THREADS), gy);
     if (t == DType::F32)
       e = launch_pdl(colsum_vec_kernel<float>, vgrid, dim3(COL_THREADS), 0, st, (const float*)in,
                      ld, M, N, part);

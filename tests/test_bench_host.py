@@ -47,15 +47,50 @@ def test_modes_are_credited_with_what_they_execute():
     assert b.flops_fine(f, "selective") == b.flops_fine(f, "none")
 
 
-def test_traffic_is_reported_only_for_the_captured_workload():
+def test_traffic_is_reported_only_for_a_captured_workload():
     b = _bench()
     for name in SHAPES:
         t = b.recorded_traffic(name)
-        if name != b.NCU_TRAFFIC["workload"]:
+        rec = b.NCU_TRAFFIC.get(name)
+        if rec is None:
             assert t is None, name
         else:   # the capture's bytes while the GEMM sources hash to the captured ones
-            assert t in (None, b.NCU_TRAFFIC["bytes_per_launch"])
-            assert (t is None) == (b.kernel_source_sha() != b.NCU_TRAFFIC["source_sha256"])
+            assert t in (None, rec["bytes_per_launch"])
+            assert (t is None) == (b.kernel_source_sha() != rec["source_sha256"])
+
+
+def test_roofline_entries_aggregate_the_gemm_launches():
+    b = _bench()
+    pk = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0, "source": "measured"}
+    rows = [{"kernel": "a", "shape": "1", "family": "gemm", "algorithmic": 2e12, "avg_us": 1e3,
+             "frac": 1.0},
+            {"kernel": "b", "shape": "2", "family": "gemm", "algorithmic": 1e12, "avg_us": 2e3,
+             "frac": 0.25},
+            {"kernel": "c", "shape": "3", "family": "attn_bwd", "algorithmic": 1e12,
+             "avg_us": 1e3, "frac": 0.5},
+            {"kernel": "d", "shape": "4", "family": "hbm", "algorithmic": 1e9, "avg_us": 1.0,
+             "frac": 0.1}]
+    out = b.roofline_entries(rows, pk, "no_such_workload")
+    r = out["roofline"]
+    assert r["achieved"] == pytest.approx(3e12 / 3e-3 / 1e12)   # 1000 TFLOP/s
+    assert r["frac"] == pytest.approx(0.5)
+    assert r["algorithmic_flops_per_launch"] == pytest.approx(1.5e12)
+    assert r["avg_launch_s"] == pytest.approx(1.5e-3)
+    assert r["traffic"] is None and r["bound"] == "tensor" and len(r["launches"]) == 2
+    assert out["roofline_attention_bwd"]["frac"] == pytest.approx(0.5)
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_regions():
+    b = _bench()
+    c = b.ClockSampler(0)
+    c.samples = [(1.0, 1000.0, 2070.0, 0x1), (2.0, 2000.0, 2070.0, 0x4), (3.0, 2050.0, 2070.0, 0x0),
+                 (4.0, 900.0, 2070.0, 0x20), (5.0, 1990.0, 2070.0, 0x0)]
+    c.windows = [[1.5, 3.5], [4.5, 5.5]]
+    sm = c.summary()
+    assert sm["samples"] == 3 and sm["sm_mhz"] == 2000.0
+    assert sm["reasons"] == ["sw_power_cap"]   # the thermal sample lies outside the regions
+    c.windows = [[10.0, 11.0]]
+    assert c.summary()["reasons"] == ["unsampled"]
 
 
 @pytest.mark.parametrize("name", sorted(SHAPES))

@@ -89,13 +89,14 @@ def test_full_shapes_one_sequence_and_batch_properties(name):
     for b in range(1, full.batch):
         gb = run_gpu(one, one_sequence(inp, full, b))
         np.testing.assert_array_equal(got["y"][b * S:(b + 1) * S], gb["y"])
+        np.testing.assert_array_equal(got["dx"][b * S:(b + 1) * S], gb["dx"])
         for la, lb in zip(acc, gb["grads"]):
             for k in la:
                 la[k] += lb[k]
     for la, lg in zip(acc, got["grads"]):
         for k in la:
             assert rel(lg[k], la[k]) <= 1e-5, k
-    assert all(np.isfinite(got["y"]).all() for _ in [0]) and np.isfinite(got["dx"]).all()
+    assert np.isfinite(got["y"]).all() and np.isfinite(got["dx"]).all()
 
 
 def test_layer_full_batch_sub_batch_split_and_modes():

@@ -229,6 +229,43 @@ def test_host_buffers_through_stack_step():
     np.testing.assert_array_equal(dxh.double().numpy(), dev["dx"])
 
 
+def test_shutdown_releases_state_and_next_calls_remake_it():
+    """oases_shutdown() drops the copy stream, this thread's events and the
+    host caches; the next calls (device and host buffers, traced) remake
+    them and give the same bits as before."""
+    from tensor_model_transformer_tp_gb300 import lib, oases_shutdown
+    import ctypes
+    shape = BlockShape("layer", "bf16", batch=2, seq=64, hidden=256, ffn=512, heads=2, w=2)
+    inp = block_inputs(shape, seed=13, affine=True)
+    before = run_gpu(shape, inp)
+    blk = DeviceBlock(shape, inp["layers"])
+    xh = blk.tensor(inp["x"]).cpu().pin_memory()
+    gh = blk.tensor(inp["g"]).cpu().pin_memory()
+    yh, dxh = torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()
+    blk.step(xh, gh, yh, dxh)  # makes the copy stream
+    torch.cuda.synchronize()
+    L = lib()
+    L.oases_debug_trace_enable.argtypes = [ctypes.c_int]
+    L.oases_debug_trace_enable(1)
+    try:
+        blk.zero_grads()
+        blk.step(xh, gh, yh, dxh)  # makes the trace events
+        torch.cuda.synchronize()
+        oases_shutdown()
+        oases_shutdown()  # a second call finds nothing to release
+        after = run_gpu(shape, inp)
+        assert_identical(after, before)
+        blk.zero_grads()
+        blk.step(xh, gh, yh, dxh)
+        torch.cuda.synchronize()
+    finally:
+        L.oases_debug_trace_enable(0)
+    np.testing.assert_array_equal(yh.double().numpy(), before["y"])
+    np.testing.assert_array_equal(dxh.double().numpy(), before["dx"])
+    for k, v in blk.grads_numpy()[0].items():
+        np.testing.assert_array_equal(v, before["grads"][0][k])
+
+
 # ------------------------------------------------------------------ separate reduction
 @pytest.mark.parametrize("mode", ["fine", "full"])
 def test_separate_reduce_ffn_f32_h256(mode):

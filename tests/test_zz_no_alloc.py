@@ -5,9 +5,11 @@ scratch is a static device array inside the library.
 
 This file is collected last on purpose.  It checks, through the C ABI, that
 the entry point gives the same result as oases_debug_bias_grad (which takes
-caller-owned scratch) on two calls in a row, and that a size whose partial rows
-do not fit the static array is refused.  It passes alone in a fresh process and
-after the other tests."""
+caller-owned scratch) on two calls in a row, that both agree with the column
+sums taken in float64 on the host, that a narrow input with more partial rows
+than a grid dimension allows is still summed, and that a size whose partial
+rows do not fit the static array is refused.  It passes alone in a fresh
+process and after the other tests."""
 import ctypes
 
 import numpy as np
@@ -46,6 +48,7 @@ def test_noalloc_matches_scratch_entry_point_twice(L):
     out_new = init.clone().cuda()
     nb = L.oases_debug_bias_grad_scratch_bytes(M, N)
     scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    expect = None
     for call in range(2):     # the second call sees the array the first one left
         x = torch.randn(M, N, generator=gen).to(torch.bfloat16).cuda()
         assert L.oases_debug_bias_grad(x.data_ptr(), N, M, N, 1, out_ref.data_ptr(),
@@ -57,6 +60,27 @@ def test_noalloc_matches_scratch_entry_point_twice(L):
         b = out_ref.double().cpu().numpy()
         np.testing.assert_allclose(a, b, rtol=1e-6, atol=0), call
         np.testing.assert_array_equal(a, b)   # same kernels, same summation order
+        # the plain definition: out += sum over rows, in float64 on the host
+        expect = expect + x.double().cpu().numpy().sum(axis=0) if call else \
+            init.double().numpy() + x.double().cpu().numpy().sum(axis=0)
+        scale = np.abs(x.double().cpu().numpy()).sum(axis=0) + np.abs(expect)
+        assert np.all(np.abs(a - expect) <= 1e-5 * scale), call
+
+
+def test_noalloc_narrow_input_with_many_partial_rows(L):
+    """N = 4 columns, 600000 rows: 75000 partial rows of 8, more than one grid
+    dimension holds (65535), within the static array (300000 floats)."""
+    M, N = 600000, 4
+    gen = torch.Generator().manual_seed(8)
+    xh = torch.randn(M, N, generator=gen).to(torch.bfloat16)
+    x = xh.cuda()
+    out = torch.zeros(N, device="cuda")
+    assert L.oases_bias_grad_noalloc(x.data_ptr(), N, M, N, 1, out.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    expect = xh.double().numpy().sum(axis=0)
+    scale = np.abs(xh.double().numpy()).sum(axis=0)
+    assert np.all(np.abs(out.double().cpu().numpy() - expect) <= 1e-5 * scale)
 
 
 def test_noalloc_rejects_sizes_beyond_the_array(L):
