@@ -41,13 +41,15 @@ struct DeviceOnce {
   }
 };
 
-enum class DType : int { F32 = 0, BF16 = 1 };
+// E4M3 (FP8, 1-4-3, bias 7) occurs only as a GEMM operand of the MX path,
+// with UE8M0 block scales beside it.
+enum class DType : int { F32 = 0, BF16 = 1, E4M3 = 2 };
 
 // Kernel launches issued by this host thread (read and reset by the scheduler).
 extern thread_local int g_launch_count;
 #define OASES_COUNT_LAUNCH() (++::oases::g_launch_count)
 
-inline size_t dtype_size(DType t) { return t == DType::F32 ? 4 : 2; }
+inline size_t dtype_size(DType t) { return t == DType::F32 ? 4 : t == DType::BF16 ? 2 : 1; }
 
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // programmatic stream serialization, so it may start while its predecessor on
@@ -255,6 +257,13 @@ struct GemmArgs {
   // streams): SMs that 256-wide tiles leave idle are then filled by the other
   // stream, so the dispatcher always takes the faster 256-wide pair tiles.
   int concurrent = 0;
+  // MX path (in_t == E4M3, both operands K-major): UE8M0 scales of A's and B's
+  // 32-element K blocks, in 512-byte tiles of 128 rows x 4 blocks; tile
+  // (row block rb, K group kg) at byte (rb * ceil(K / 128) + kg) * 512, row r
+  // of the tile, block j at byte (r % 32) * 16 + (r / 32) * 4 + j.  Bias and
+  // aux stay bf16.
+  const uint8_t* a_sf = nullptr;
+  const uint8_t* b_sf = nullptr;
 };
 
 // Returns cudaSuccess or the launch error.  Picks the tensor-core kernel when
@@ -265,6 +274,23 @@ cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st);
 // operands do not meet its alignment rules.
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st);
 bool gemm_tc_supported(const GemmArgs& g);
+// MX-FP8 path: E4M3 operands with block-32 UE8M0 scales (kind::mxf8f6f4).
+bool gemm_mx_supported(const GemmArgs& g);
+cudaError_t gemm_mx(const GemmArgs& g, cudaStream_t st);
+// Quantisers to the MX layout (E4M3 codes + scale tiles above).
+//   rows: q[r, k] = E4M3(x[r, k] / X[r, k / 32]) for x [R, K] (leading dim ld)
+//   cols: the same for the transpose x^T [C, R] of x [R, C]: q[c, r] with blocks
+//         of 32 along r (q has leading dim ldq, at least R)
+// X = 2^(floor(log2(max |block|)) - 8), clamped to the UE8M0 range; 1 for an
+// all-zero block.  Every byte of every scale tile is written (127 = 2^0 for
+// rows and blocks beyond the matrix).
+cudaError_t mx_quantize_rows(const void* x, int64_t ld, int R, int K, DType t, uint8_t* q,
+                             int64_t ldq, uint8_t* sf, cudaStream_t st);
+cudaError_t mx_quantize_cols(const void* x, int64_t ld, int R, int C, DType t, uint8_t* q,
+                             int64_t ldq, uint8_t* sf, cudaStream_t st);
+inline int64_t mx_sf_bytes(int rows, int K) {
+  return (int64_t)((rows + 127) / 128) * ((K + 127) / 128) * 512;
+}
 
 // ---------------------------------------------------------------------------
 // Row-wise LayerNorm and column reductions (norm.cu).

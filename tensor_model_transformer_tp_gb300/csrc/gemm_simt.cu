@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
 
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (g.in_t == DType::E4M3) return cudaErrorNotSupported;  // E4M3 runs on the MX path only
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   if (g.in_t == DType::F32) return launch_pdl(gemm_simt_kernel<float>, grid, dim3(NT), 0, st, g);

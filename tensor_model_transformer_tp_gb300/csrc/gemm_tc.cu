@@ -53,17 +53,27 @@ constexpr int64_t A_L2_BYTES = 48ll << 20;  // A up to this size stays in L2 acr
 constexpr int NTHREADS = 320;  // 2 control warps + 8 epilogue warps
 
 // CL = 2: a CTA pair shares each MMA; a CTA holds BN / 2 rows of the B tile.
-template <int BN, int CL>
+// MX: E4M3 operands (128 elements = 128 bytes of K per stage, the same bytes
+// as 64 bf16) and, per stage, the A and B scale tiles (128 rows x 4 K blocks,
+// 512 bytes each), which the MMA thread copies into TMEM columns
+// SF_COL0 + 8 * stage (A) and + 4 (B).
+template <int BN, int CL, bool MX = false>
 struct TcCfg {
-  static constexpr int A_BYTES = BM * BKE * 2;
-  static constexpr int B_BYTES = BN / CL * BKE * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int KE = MX ? 128 : BKE;  // K elements per stage
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN / CL * 128;
+  static constexpr int SF_BYTES = MX ? 512 + BN * 4 : 0;
+  static constexpr int STAGE = A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE;
   static constexpr int EPI_OFF = STAGES * STAGE;        // per epilogue warp: 32 rows x 128 B
   static constexpr int EPI_BYTES = 8 * 32 * 128;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8;
   static constexpr int SMEM = STAGES * STAGE + EPI_BYTES + BAR_BYTES + 1024;
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int SF_COL0 = 2 * BN;
+  static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
+  static_assert(!MX || (BN == 128 && CL == 1), "the MX path takes 128 x 128 single-CTA tiles");
+  static_assert(!MX || SF_COL0 + 8 * STAGES <= TMEM_COLS, "MX scale ring exceeds TMEM");
+  static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte alignment of swizzled tiles");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -280,14 +290,16 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
 // counts); its commits arrive on both CTAs' empty and accumulator-full
 // barriers; both CTAs' epilogue warps release an accumulator on the even CTA's
 // barrier.
-template <int BN, bool A_K, bool B_K, int CL, bool GRP>
+template <int BN, bool A_K, bool B_K, int CL, bool GRP, bool MX>
 __global__ void __launch_bounds__(NTHREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                const GemmArgs g) {
-  using C = TcCfg<BN, CL>;
+  using C = TcCfg<BN, CL, MX>;
   constexpr int BNH = BN / CL;  // B rows of the tile held by this CTA
-  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM * CL, BN, !A_K, !B_K);
+  constexpr uint32_t IDESC = MX ? ptx::idesc_mx_e4m3(BM, BN)
+                                : ptx::idesc_bf16_f32(BM * CL, BN, !A_K, !B_K);
+  static_assert(!MX || (A_K && B_K), "MX operands are K-major");
   unsigned long long* tl = g_gemm_timeline ? g_gemm_timeline + 16 * blockIdx.x : nullptr;
   if (tl && threadIdx.x == 0) tl[0] = ptx::globaltimer();
   extern __shared__ uint8_t smem_raw[];
@@ -309,7 +321,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // tiles of split s are [s * tiles1, (s + 1) * tiles1); K blocks walk the
   // pieces of that split's contraction range in order
   const int tiles1 = num_mp * num_n, tiles = tiles1 * g.splits;
-  const int kpl = g.K / g.kpieces, nkb_p = (kpl + BKE - 1) / BKE, nkb = nkb_p * g.kpieces;
+  const int kpl = g.K / g.kpieces, nkb_p = (kpl + C::KE - 1) / C::KE, nkb = nkb_p * g.kpieces;
   const int first = blockIdx.x / CL, stride = gridDim.x / CL;
   // Tile order within a split: the row block varies fastest.  Without GRP it
   // does so over every row block: each round of tiles re-reads A from L2 and
@@ -403,7 +415,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           };
           const uint32_t sa = base + stage * C::STAGE, sb = sa + C::A_BYTES;
           const int pc = kb / nkb_p;
-          const int k0 = (int)(pc * g.kpiece_stride) + ks + (kb - pc * nkb_p) * BKE;
+          const int k0 = (int)(pc * g.kpiece_stride) + ks + (kb - pc * nkb_p) * C::KE;
+          if constexpr (MX) {  // the stage's scale tiles (K group kb)
+            const uint32_t ssf = sb + C::B_BYTES;
+            ptx::bulk_load(ssf, g.a_sf + ((int64_t)(m0 / BM) * nkb + kb) * 512, 512, fb);
+            ptx::bulk_load(ssf + 512, g.b_sf + ((int64_t)(n0 / 128) * nkb + kb) * 512, 512, fb);
+          }
           if (A_K) {
             load(sa, &tmA, k0, m0);
           } else {
@@ -445,16 +462,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ptx::tc_fence_after();
           if (tl && t == 0 && kb == 0) tl[2] = ptx::globaltimer();
           const uint32_t sa = base + stage * C::STAGE, sb = sa + C::A_BYTES;
+          if constexpr (MX) {
+            // scale tiles -> TMEM (ordered before the MMAs below, which read them),
+            // then four K = 32 MMAs, each with its K block's scale byte
+            const uint32_t ssf = sb + C::B_BYTES;
+            const uint32_t tsa = tmem + (uint32_t)(C::SF_COL0 + 8 * stage), tsb = tsa + 4;
+            ptx::tmem_cp_32x128b_x4(tsa, ptx::smem_desc_noswz(ssf, 128, 128));
+            ptx::tmem_cp_32x128b_x4(tsb, ptx::smem_desc_noswz(ssf + 512, 128, 128));
 #pragma unroll
-          for (int kk = 0; kk < BKE / 16; ++kk) {
-            const uint64_t ad = A_K ? ptx::smem_desc_sw128(sa + kk * 32, 16, 1024)
-                                    : ptx::smem_desc_sw128(sa + kk * 2048, 8192, 1024);
-            const uint64_t bd = B_K ? ptx::smem_desc_sw128(sb + kk * 32, 16, 1024)
-                                    : ptx::smem_desc_sw128(sb + kk * 2048, 8192, 1024);
-            if (CL > 1)
-              ptx::mma_bf16_pair(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-            else
-              ptx::mma_bf16(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_mx(dt, ptx::smem_desc_sw128(sa + kk * 32, 16, 1024),
+                          ptx::smem_desc_sw128(sb + kk * 32, 16, 1024),
+                          IDESC | ptx::idesc_sf_ids(kk, kk), tsa, tsb, (kb | kk) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BKE / 16; ++kk) {
+              const uint64_t ad = A_K ? ptx::smem_desc_sw128(sa + kk * 32, 16, 1024)
+                                      : ptx::smem_desc_sw128(sa + kk * 2048, 8192, 1024);
+              const uint64_t bd = B_K ? ptx::smem_desc_sw128(sb + kk * 32, 16, 1024)
+                                      : ptx::smem_desc_sw128(sb + kk * 2048, 8192, 1024);
+              if (CL > 1)
+                ptx::mma_bf16_pair(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+              else
+                ptx::mma_bf16(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           if (CL > 1)
             ptx::mma_commit_pair_mc(empty(stage), MASK);
@@ -599,13 +630,16 @@ struct MapKeyHash {
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
 
+enum class MapT : uint32_t { BF16 = 0, F32 = 1, U8 = 2 };
+
 bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_inner, uint32_t box_outer, bool f32 = false, uint64_t depth = 1,
+              uint32_t box_inner, uint32_t box_outer, MapT mt = MapT::BF16, uint64_t depth = 1,
               uint64_t ld2 = 0) {
   std::mutex& mu = g_map_mu;
   auto& cache = g_map_cache;
   if (depth < 1) depth = 1;
-  const MapKey key{(uintptr_t)ptr | (f32 ? 1u : 0u), inner, outer, ld, depth,
+  // device pointers are 16-byte aligned: the low bits carry the element kind
+  const MapKey key{(uintptr_t)ptr | (uintptr_t)mt, inner, outer, ld, depth,
                    depth > 1 ? ld2 : 0, box_inner, box_outer};
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
@@ -615,14 +649,16 @@ bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const uint64_t esz = f32 ? 4 : 2;
+  const uint64_t esz = mt == MapT::F32 ? 4 : mt == MapT::BF16 ? 2 : 1;
   const cuuint64_t dims[3] = {inner, outer, depth};
   const cuuint64_t strides[2] = {ld * esz, ld2 * esz};
   const cuuint32_t box[3] = {box_inner, box_outer, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
-  if (fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-         depth > 1 ? 3u : 2u,
+  const CUtensorMapDataType dt = mt == MapT::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : mt == MapT::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (fn(&m, dt, depth > 1 ? 3u : 2u,
          const_cast<void*>(ptr), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -647,15 +683,21 @@ int num_sms() {  // of the current device, cached per device
   return n;
 }
 
-template <int BN, bool A_K, bool B_K, int CL, bool GRP = false>
+template <int BN, bool A_K, bool B_K, int CL, bool GRP = false, bool MX = false>
 cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
-  using C = TcCfg<BN, CL>;
+  using C = TcCfg<BN, CL, MX>;
   CUtensorMap ma, mb;
   const uint64_t kext = g.k_extent > 0 ? (uint64_t)g.k_extent : (uint64_t)g.K;
-  bool ok = A_K ? make_map(&ma, g.A, kext, g.M, g.lda, BKE, BM)
-                : make_map(&ma, g.A, g.M, kext, g.lda, 64, BKE);
-  ok = ok && (B_K ? make_map(&mb, g.B, kext, g.N, g.ldb, BKE, BN / CL)
-                  : make_map(&mb, g.B, g.N, kext, g.ldb, 64, BKE));
+  bool ok;
+  if constexpr (MX) {  // E4M3 codes: 128 elements (bytes) of K per box row
+    ok = make_map(&ma, g.A, kext, g.M, g.lda, C::KE, BM, MapT::U8) &&
+         make_map(&mb, g.B, kext, g.N, g.ldb, C::KE, BN, MapT::U8);
+  } else {
+    ok = A_K ? make_map(&ma, g.A, kext, g.M, g.lda, BKE, BM)
+             : make_map(&ma, g.A, g.M, kext, g.lda, 64, BKE);
+    ok = ok && (B_K ? make_map(&mb, g.B, kext, g.N, g.ldb, BKE, BN / CL)
+                    : make_map(&mb, g.B, g.N, kext, g.ldb, 64, BKE));
+  }
   if (!ok) return cudaErrorInvalidValue;
   // outputs through TMA stores when C (and C2) rows are 16-byte multiples
   GemmArgs ga = g;
@@ -666,12 +708,13 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
                        (((uintptr_t)g.bias | (uintptr_t)g.aux) & 15) == 0 &&
                        (g.aux == nullptr || (g.ld_aux % 8 == 0 && g.aux_t == DType::BF16));
   ga.tma_store = 0;
-  if (aligned && make_map(&mc, g.C, g.N, g.M, g.ldc, cw, 32, f32c, (uint64_t)g.splits,
+  const MapT ct = f32c ? MapT::F32 : MapT::BF16;
+  if (aligned && make_map(&mc, g.C, g.N, g.M, g.ldc, cw, 32, ct, (uint64_t)g.splits,
                           (uint64_t)(g.c_split_rows * g.ldc)) &&
-      (g.C2 == nullptr || make_map(&mc2, g.C2, g.N, g.M, g.ldc, cw, 32, f32c)))
+      (g.C2 == nullptr || make_map(&mc2, g.C2, g.N, g.M, g.ldc, cw, 32, ct)))
     ga.tma_store = 1;
   if (g.splits > 1 && !ga.tma_store) return cudaErrorNotSupported;  // slabs need the 3-D map
-  auto kern = gemm_tc_kernel<BN, A_K, B_K, CL, GRP>;
+  auto kern = gemm_tc_kernel<BN, A_K, B_K, CL, GRP, MX>;
   static DeviceOnce attr;
   cudaError_t ea = attr.run([&] {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -749,6 +792,24 @@ cudaError_t dispatch_major(const GemmArgs& g, cudaStream_t st) {
 
 }  // namespace
 
+bool gemm_mx_supported(const GemmArgs& g) {
+  if (g.in_t != DType::E4M3 || !g.a_kmajor || !g.b_kmajor) return false;
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || !g.a_sf || !g.b_sf) return false;
+  if (g.splits != 1 || g.kpieces != 1 || g.k_extent != 0) return false;
+  if (g.lda < g.K || g.ldb < g.K || g.lda % 16 != 0 || g.ldb % 16 != 0) return false;
+  if ((((uintptr_t)g.A) | ((uintptr_t)g.B) | ((uintptr_t)g.a_sf) | ((uintptr_t)g.b_sf)) & 15)
+    return false;
+  if (g.epi == Epi::Accum && g.c_t != DType::F32) return false;
+  if (g.c_t == DType::E4M3 || (g.aux && g.aux_t != DType::BF16)) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t gemm_mx(const GemmArgs& g, cudaStream_t st) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (!gemm_mx_supported(g)) return cudaErrorNotSupported;
+  return launch_tc<128, true, true, 1, false, true>(g, st);
+}
+
 bool gemm_tc_supported(const GemmArgs& g) {
   if (g.in_t != DType::BF16) return false;
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
@@ -784,6 +845,7 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t st) {
 
 cudaError_t gemm(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (g.in_t == DType::E4M3) return gemm_mx(g, st);  // the MX path or nothing
   if (gemm_tc_supported(g)) return gemm_tc(g, st);
   if (g.splits != 1 || g.kpieces != 1) return cudaErrorNotSupported;  // tensor-core path only
   return gemm_simt(g, st);

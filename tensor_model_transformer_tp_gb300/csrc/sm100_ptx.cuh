@@ -67,6 +67,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
+// Plain (non-tensor) bulk copy of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned) from global memory into this CTA's shared memory, completion
+// signalled on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
 // TMA tile store / fp32 reduce-add from shared memory (bulk-group tracked).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -220,6 +230,35 @@ __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_ma
       : "memory");
 }
 
+// D[tmem] (+)= sum over 32-element K blocks of SFA * SFB * (A[smem] B[smem]^T):
+// kind::mxf8f6f4 with block scaling, one UE8M0 scale per 32 K elements
+// (scale_vec::1X).  sfa / sfb are the TMEM addresses of the scale factors; the
+// instruction descriptor's scale-factor ids pick the byte of each 32-bit TMEM
+// column (the K block within a group of four).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Shared memory -> TMEM copy of a 32-row x 128-bit matrix into columns
+// taddr .. taddr+3 of lanes 0..31, repeated in each of the four 32-lane
+// quarters (row r -> lane r of every quarter).  Issued by one thread; ordered
+// with that thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Shared-memory matrix descriptor without swizzle: 8-row x 16-byte core
+// matrices, sbo bytes between core matrices along the rows (lbo along K).
+__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t start, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((start >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -294,6 +333,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | (1u << 10)                   // B format: bf16
          | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with E4M3 A/B, fp32 D, UE8M0 block
+// scales; the scale-factor ids (bits 29-30 for A, 4-5 for B) are or-ed in per
+// instruction.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N) {
+  return (0u << 7)                      // A format: E4M3
+         | (0u << 10)                   // B format: E4M3
+         | ((uint32_t)(N >> 3) << 17) | (1u << 23)  // scale type UE8M0
+         | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) {
+  return (a_id << 29) | (b_id << 4);
 }
 
 }  // namespace ptx
