@@ -346,7 +346,94 @@ def roofline_entries(rows, pk, workload):
     sel, fl, t = _launch_aggregate(rows, "attn_fwd")
     if sel:
         out["roofline_attention_fwd_frac"] = fl / t / 1e12 / pk["bf16_tflops"]
+    mx = [r for r in rows if r["family"] == "mx"]
+    if mx:
+        g = [r for r in mx if r["bound"] == "tensor"][0]
+        out["fp8_gemm"] = {
+            "kernel": "gemm_tc_kernel MX variant (tcgen05 kind::mxf8f6f4, block-32 UE8M0 "
+                      "scales): %s" % g["kernel"], "shape": g["shape"], "bound": "tensor",
+            "achieved": g["achieved"], "unit": "TFLOP/s", "peak": g["peak"], "frac": g["frac"],
+            "peak_source": pk["source"] + " bf16 burst x 2 (nominal dense FP8 / BF16 rate)",
+            "avg_launch_s": g["avg_us"] * 1e-6,
+            "quantize": [{"kernel": r["kernel"], "shape": r["shape"], "us": r["avg_us"],
+                          "GB/s": r["achieved"], "frac": r["frac"]} for r in mx
+                         if r["bound"] == "hbm"]}
     return out
+
+
+def mx_table(shape, pk, reps=20):
+    """The MX-FP8 GEMM variant at the workload's FFN column-GEMM shape (per
+    sub-batch): quantisers of the two operands (HBM-bound: read the bf16 rows,
+    write codes + scales) and the block-scaled GEMM with the bias + GeLU
+    epilogue, timed alone like kernel_table's rows.  The GEMM's peak is the
+    measured bf16 burst peak times 2, the ratio of the nominal dense FP8 and
+    BF16 tensor rates (4.5 / 2.25 PFLOP/s)."""
+    import ctypes
+
+    import torch
+
+    import tensor_model_transformer_tp_gb300 as oz
+    L = oz.lib()
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    L.oases_mx_scale_bytes.argtypes = [i32, i32]
+    L.oases_mx_scale_bytes.restype = sz
+    L.oases_mx_quantize.argtypes = [vp, i64, i32, i32, i32, i32, vp, i64, vp, vp]
+    L.oases_mx_gemm.argtypes = [i32, i32, i32, vp, i64, vp, vp, i64, vp, i32, vp, i64, i32, vp, vp,
+                                vp, i64, vp]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = torch.cuda.current_stream(dev)
+    sp = st.cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    Ms, H = shape.rows // shape.sub_batches, shape.hidden
+    N = shape.ffn if shape.kind in ("ffn", "layer") else 3 * H
+    u = torch.randn(Ms, H, device=dev).to(torch.bfloat16)
+    w = (torch.randn(N, H, device=dev) * 0.02).to(torch.bfloat16)
+    b = (torch.randn(N, device=dev) * 0.02).to(torch.bfloat16)
+    qa = torch.empty(Ms, H, dtype=torch.uint8, device=dev)
+    qb = torch.empty(N, H, dtype=torch.uint8, device=dev)
+    sfa = torch.empty(L.oases_mx_scale_bytes(Ms, H), dtype=torch.uint8, device=dev)
+    sfb = torch.empty(L.oases_mx_scale_bytes(N, H), dtype=torch.uint8, device=dev)
+    C = torch.empty(Ms, N, dtype=torch.bfloat16, device=dev)
+    rows = []
+
+    def timed(name, dims, bound, work, peak, launch):
+        assert launch() == 0, name
+        torch.cuda.synchronize(dev)
+        evs = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            assert launch() == 0, name
+            e1.record(st)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        t = sum(a.elapsed_time(c) for a, c in evs) / reps * 1e-3
+        unit = "GB/s" if bound == "hbm" else "TFLOP/s"
+        ach = work / t / (1e9 if bound == "hbm" else 1e12)
+        rows.append({"kernel": name, "shape": dims, "bound": bound, "family": "mx",
+                     "avg_us": t * 1e6, "algorithmic": work, "achieved": ach, "unit": unit,
+                     "peak": peak, "frac": ach / peak})
+
+    def qbytes(R, K):
+        return 2.0 * R * K + R * K + R * K / 32.0
+
+    timed("mx_quantize (transposed, for a weight gradient)", "%dx%d" % (H, Ms), "hbm",
+          qbytes(Ms, H), pk["hbm_gbs"],
+          lambda: L.oases_mx_quantize(u.data_ptr(), H, H, Ms, 1, 1, qa.data_ptr(), Ms,
+                                      sfa.data_ptr(), sp))
+    timed("mx_quantize (activation rows)", "%dx%d" % (Ms, H), "hbm", qbytes(Ms, H), pk["hbm_gbs"],
+          lambda: L.oases_mx_quantize(u.data_ptr(), H, Ms, H, 1, 0, qa.data_ptr(), H,
+                                      sfa.data_ptr(), sp))
+    timed("mx_quantize (weight rows)", "%dx%d" % (N, H), "hbm", qbytes(N, H), pk["hbm_gbs"],
+          lambda: L.oases_mx_quantize(w.data_ptr(), H, N, H, 1, 0, qb.data_ptr(), H,
+                                      sfb.data_ptr(), sp))
+    timed("mx_gemm column GEMM + bias + GeLU (E4M3 x E4M3, fp32 accumulate)",
+          "%dx%dx%d" % (Ms, N, H), "tensor", 2.0 * Ms * N * H, 2.0 * pk["bf16_tflops"],
+          lambda: L.oases_mx_gemm(Ms, N, H, qa.data_ptr(), H, sfa.data_ptr(), qb.data_ptr(), H,
+                                  sfb.data_ptr(), 2, C.data_ptr(), N, 1, None, b.data_ptr(),
+                                  None, 0, sp))
+    return rows
 
 
 def kernel_table(shape, pk, reps=20):
@@ -546,7 +633,7 @@ def main():
         torch.cuda.set_device(0)
         pk = peaks()
         with ClockSampler(0) as clk:
-            rows = kernel_table(shape, pk, reps=args.reps)
+            rows = kernel_table(shape, pk, reps=args.reps) + mx_table(shape, pk, reps=args.reps)
         for r in rows:
             r["workload"] = args.workload
             r["peak_source"] = pk["source"]
@@ -640,7 +727,7 @@ def main():
     io = shape.rows * shape.hidden * (2 if shape.dtype == "bf16" else 4)
 
     pk = peaks()
-    rows = kernel_table(shape, pk)
+    rows = kernel_table(shape, pk) + mx_table(shape, pk)
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t_step * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -78,6 +78,15 @@ def test_roofline_entries_aggregate_the_gemm_launches():
     assert r["avg_launch_s"] == pytest.approx(1.5e-3)
     assert r["traffic"] is None and r["bound"] == "tensor" and len(r["launches"]) == 2
     assert out["roofline_attention_bwd"]["frac"] == pytest.approx(0.5)
+    assert "fp8_gemm" not in out
+    rows.append({"kernel": "q", "shape": "5", "family": "mx", "bound": "hbm", "algorithmic": 1e9,
+                 "avg_us": 1.0, "achieved": 1e3, "frac": 0.2})
+    rows.append({"kernel": "mxg", "shape": "6", "family": "mx", "bound": "tensor",
+                 "algorithmic": 4e12, "avg_us": 1e3, "achieved": 4000.0, "peak": 4000.0,
+                 "frac": 1.0})
+    out = b.roofline_entries(rows, pk, "no_such_workload")
+    assert out["fp8_gemm"]["frac"] == 1.0 and len(out["fp8_gemm"]["quantize"]) == 1
+    assert out["roofline"]["frac"] == pytest.approx(0.5)   # the MX rows are not in the bf16 GEMM family
 
 
 def test_clock_summary_keeps_only_samples_inside_the_timed_regions():
