@@ -47,7 +47,6 @@ constexpr int D = 128;                 // head dimension
 constexpr int BQ = 128, BKV = 128;     // query rows per CTA, keys per block
 constexpr int BOX = 128 * 64 * 2;      // one TMA box: 128 rows x 64 bf16 (16 KB)
 constexpr int TILE = 2 * BOX;          // 128 rows x 128 bf16 (32 KB)
-constexpr int NT = 128;
 
 // S = Q K^T: M = 128 queries, N = 128 keys, both operands K-major (over d).
 constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BQ, BKV, false, false);
@@ -113,19 +112,43 @@ struct FwdArgs {
   float scale_log2;    // log2(e) / sqrt(d)
 };
 
-// Forward shared-memory map: Q, two K stages, three V stages, one P tile.
-constexpr int F_KST = 2, F_VST = 3;
-constexpr int F_OFF_Q = 0, F_OFF_K = TILE, F_OFF_V = F_OFF_K + F_KST * TILE;
-constexpr int F_OFF_P = F_OFF_V + F_VST * TILE, F_OFF_BAR = F_OFF_P + TILE;
-constexpr int F_NBAR = 1 + F_KST + F_VST + 2 + 2 + 1;  // q, K, V, s, pv, drain
+// Forward: one CTA per 256 queries of one (sequence, head), as two tiles of
+// 128 queries that share every K/V block, 320 threads:
+//   warp 0      TMA loads: Q of both tiles once, then K_j and V_j into
+//               two-stage rings;
+//   warp 1      TMEM allocation (512 columns); one thread issues the MMAs;
+//   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1: thread r
+//               (TMEM lane r of its warp's quarter) owns one query row.
+// TMEM: S_t (then P_t) in columns 128 t .. +127, O_t in 256 + 128 t .. +127.
+// Per tile t and key block j:
+//   S_t = Q_t K_j^T                 tcgen05.mma, A and B from shared memory
+//   P_t = exp2(s - m)               the softmax threads read S_t, keep the row
+//                                   maximum m and sum l in registers, and write
+//                                   P_t back over the first 64 columns of S_t
+//                                   as packed bf16
+//   O_t += P_t V_j                  tcgen05.mma, A = P_t from tensor memory,
+//                                   B = V_j (MN-major) from shared memory
+// The MMA thread issues, per block, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): while
+// one tile's softmax threads turn S into P, the tensor core works on the other
+// tile.  S_t(j+1) overwrites P_t(j); it is issued after PV_t(j), and MMAs of
+// one thread run in issue order.  The completion of S_t(j) therefore also
+// means PV_t(j-1) is complete, so the softmax threads may rescale their O row
+// in place before publishing P_t(j).  A row's reference maximum is raised only
+// when the running maximum exceeds it by more than 2^8 (RESCALE_LOG2), so P
+// stays <= 256 and O is rescaled rarely.  Key blocks past the diagonal are
+// skipped; keys past the diagonal inside it (and past the sequence end) get
+// weight 0.  LSE = m + log(l) per (head, row) for the backward.
+constexpr int F_NT = 320;
+constexpr int F_KST = 2, F_VST = 2;
+constexpr int F_OFF_Q = 0, F_OFF_K = 2 * TILE, F_OFF_V = F_OFF_K + F_KST * TILE;
+constexpr int F_OFF_BAR = F_OFF_V + F_VST * TILE;
+// q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full[2], drain
+constexpr int F_NBAR = 1 + 2 * F_KST + 2 * F_VST + 6 + 1;
 constexpr int FWD_SMEM = F_OFF_BAR + 8 * F_NBAR + 16 + 1024;
-// A row's reference maximum (log2 units) is raised only when the running
-// maximum exceeds it by more than this: P = exp2(s - m_ref) <= 256 stays exact
-// in fp32 and representable in bf16, and O (accumulated in TMEM) is rescaled
-// only on those rare occasions.
+static_assert(FWD_SMEM <= 232448, "attention forward: more than 227 KB of shared memory");
 constexpr float RESCALE_LOG2 = 8.f;
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(F_NT, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -133,36 +156,52 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + F_OFF_BAR;
   const uint32_t bar_q = bars;
-  auto bar_k = [&](int s) { return bars + 8u * (1 + s); };
-  auto bar_v = [&](int s) { return bars + 8u * (1 + F_KST + s); };
-  auto bar_s = [&](int i) { return bars + 8u * (1 + F_KST + F_VST + i); };
-  auto bar_pv = [&](int i) { return bars + 8u * (3 + F_KST + F_VST + i); };
-  const uint32_t bar_drain = bars + 8u * (5 + F_KST + F_VST);
+  auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bars + 8u * (1 + F_KST + s); };
+  auto v_full = [&](int s) { return bars + 8u * (1 + 2 * F_KST + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * F_KST + F_VST + s); };
+  auto s_full = [&](int t) { return bars + 8u * (1 + 2 * F_KST + 2 * F_VST + t); };
+  auto p_full = [&](int t) { return bars + 8u * (3 + 2 * F_KST + 2 * F_VST + t); };
+  auto o_full = [&](int t) { return bars + 8u * (5 + 2 * F_KST + 2 * F_VST + t); };
+  const uint32_t bar_drain = bars + 8u * (7 + 2 * F_KST + 2 * F_VST);
   const uint32_t tslot = bars + 8u * F_NBAR;
 
-  const int tid = threadIdx.x, warp = tid / 32;
-  // grid (heads, batch, tiles): the slowest index runs heavy (late) query tiles first
-  const int tile = gridDim.z - 1 - blockIdx.z;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // grid (heads, batch, pairs of tiles): the slowest index runs heavy (late) pairs first
+  const int pair = gridDim.z - 1 - blockIdx.z;
   const int h = blockIdx.x, b = blockIdx.y;
-  const int q0 = tile * BQ;
+  const int q0 = pair * 2 * BQ;
   const int row0 = b * a.S;
   const int nkv_all = (a.S + BKV - 1) / BKV;
-  const int nkv = a.causal ? min(tile + 1, nkv_all) : nkv_all;
+  int n[2];  // key blocks of each tile (0: the tile lies past the sequence end)
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = q0 + t * BQ;
+    n[t] = qt >= a.S ? 0 : (a.causal ? min(qt / BKV + 1, nkv_all) : nkv_all);
+  }
+  const int nmax = max(n[0], n[1]);
   const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
 
   if (tid == 0) {
     ptx::mbar_init(bar_q, 1);
-    for (int s = 0; s < F_KST; ++s) ptx::mbar_init(bar_k(s), 1);
-    for (int s = 0; s < F_VST; ++s) ptx::mbar_init(bar_v(s), 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(bar_s(i), 1);
-      ptx::mbar_init(bar_pv(i), 1);
+    for (int s = 0; s < F_KST; ++s) {
+      ptx::mbar_init(k_full(s), 1);
+      ptx::mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < F_VST; ++s) {
+      ptx::mbar_init(v_full(s), 1);
+      ptx::mbar_init(v_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(s_full(t), 1);
+      ptx::mbar_init(p_full(t), 4);  // one arrival per softmax warp of the tile
+      ptx::mbar_init(o_full(t), 1);
     }
     ptx::mbar_init(bar_drain, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tmem_alloc(tslot, 512);
     ptx::tmem_relinquish();
   }
@@ -170,196 +209,228 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
-  const uint32_t t_s[2] = {tmem, tmem + 128};
-  const uint32_t t_o = tmem + 256;
   progress(0, 2);
   pdl_wait();
   pdl_trigger();
   progress(0, 3);
-
-  // Thread 0 issues every TMA load and MMA; loads in flight per stage are
-  // tracked (issued bit, parity) so that a CTA that stops early waits for them.
   bool ok = true;
-  uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
-  auto load_k = [&](int j) {
-    const int s = j % F_KST;
-    ptx::mbar_arrive_expect_tx(bar_k(s), TILE);
-    const uint32_t kt = base + F_OFF_K + s * TILE;
-    ptx::tma_load_2d(kt, &tm, bar_k(s), col_k, row0 + j * BKV);
-    ptx::tma_load_2d(kt + BOX, &tm, bar_k(s), col_k + 64, row0 + j * BKV);
-    k_issued |= 1u << s;
-    k_par = (k_par & ~(1u << s)) | ((uint32_t)((j / F_KST) & 1) << s);
-  };
-  auto load_v = [&](int j) {
-    const int s = j % F_VST;
-    ptx::mbar_arrive_expect_tx(bar_v(s), TILE);
-    const uint32_t vt = base + F_OFF_V + s * TILE;
-    ptx::tma_load_2d(vt, &tm, bar_v(s), col_v, row0 + j * BKV);
-    ptx::tma_load_2d(vt + BOX, &tm, bar_v(s), col_v + 64, row0 + j * BKV);
-    v_issued |= 1u << s;
-    v_par = (v_par & ~(1u << s)) | ((uint32_t)((j / F_VST) & 1) << s);
-  };
-  auto issue_s = [&](int j) {  // K_j must have landed
-    const uint32_t qt = base + F_OFF_Q, kt = base + F_OFF_K + (j % F_KST) * TILE;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      ptx::mma_bf16(t_s[j & 1], kmajor_desc(qt, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
-    ptx::mma_commit(bar_s(j & 1));
-  };
 
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(bar_q, TILE);
-    ptx::tma_load_2d(base + F_OFF_Q, &tm, bar_q, col_q, row0 + q0);
-    ptx::tma_load_2d(base + F_OFF_Q + BOX, &tm, bar_q, col_q + 64, row0 + q0);
-    for (int j = 0; j < F_KST && j < nkv; ++j) load_k(j);
-    for (int j = 0; j < F_VST && j < nkv; ++j) load_v(j);
-    ok = ptx::mbar_wait(bar_q, 0) && ptx::mbar_wait(bar_k(0), 0);
-    if (ok) {
-      ptx::tc_fence_after();
-      issue_s(0);
-    }
-  }
-
-  const int qi = q0 + tid;  // this thread's query position
-  float m_ref = -INFINITY, l = 0.f;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  bool done_all = true;
-
-  for (int j = 0; j < nkv; ++j) {
-    // (1) S_{j+1} overlaps this block's softmax
-    if (tid == 0 && ok && j + 1 < nkv) {
-      ok = ptx::mbar_wait(bar_k((j + 1) % F_KST), ((j + 1) / F_KST) & 1);
-      if (ok) {
-        ptx::tc_fence_after();
-        issue_s(j + 1);
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
+      const int nq = n[1] > 0 ? 2 : 1;
+      ptx::mbar_arrive_expect_tx(bar_q, nq * TILE);
+      for (int t = 0; t < nq; ++t) {
+        const uint32_t qt = base + F_OFF_Q + t * TILE;
+        ptx::tma_load_2d(qt, &tm, bar_q, col_q, row0 + q0 + t * BQ);
+        ptx::tma_load_2d(qt + BOX, &tm, bar_q, col_q + 64, row0 + q0 + t * BQ);
       }
-    }
-    // (2) S_j ready.  In issue order S_j follows PV_{j-2}, so PV_{j-2} is done:
-    //     K stage j % 2 (S_j) and V stage (j-2) % 3 (PV_{j-2}) are free.
-    if (!ptx::mbar_wait(bar_s(j & 1), (j >> 1) & 1)) ok = false;
-    ptx::tc_fence_after();
-    if (tid == 0 && ok) {
-      if (j + 2 < nkv) load_k(j + 2);
-      if (j + 1 < nkv && j + 1 >= F_VST) load_v(j + 1);
-    }
-    const int kbase = j * BKV;
-    float sv[BKV];
-#pragma unroll
-    for (int c0 = 0; c0 < BKV; c0 += 32)
-      ptx::tmem_ld32(t_s[j & 1] + lane_off + c0, *reinterpret_cast<float(*)[32]>(sv + c0));
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < BKV; ++i) {
-      const int key = kbase + i;
-      const bool valid = key < a.S && (!a.causal || key <= qi);
-      sv[i] = valid ? sv[i] * a.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, sv[i]);
-    }
-    const float m_new = fmaxf(m_ref, mx);
-    // (3) reference maximum
-    if (j == 0) {
-      m_ref = m_new;
-    } else {
-      const bool need = m_new > m_ref + RESCALE_LOG2;
-      if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are collective
-        if (!ptx::mbar_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
-        ptx::tc_fence_after();
-        const float f = need ? exp2f(m_ref - m_new) : 1.f;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float v[32];
-          ptx::tmem_ld32(t_o + lane_off + c0, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= f;
-          ptx::tmem_st32(t_o + lane_off + c0, v);
+      for (int j = 0; j < nmax && ok; ++j) {
+        const int s = j % F_KST, r = row0 + j * BKV;
+        if (j >= F_KST && !ptx::mbar_wait(k_empty(s), ((j / F_KST) & 1) ^ 1)) {
+          ok = false;
+          wait_failed(11);
+          break;
         }
-        if (need) {
-          l *= f;
-          m_ref = m_new;
+        ptx::mbar_arrive_expect_tx(k_full(s), TILE);
+        const uint32_t kt = base + F_OFF_K + s * TILE;
+        ptx::tma_load_2d(kt, &tm, k_full(s), col_k, r);
+        ptx::tma_load_2d(kt + BOX, &tm, k_full(s), col_k + 64, r);
+        k_issued |= 1u << s;
+        k_par = (k_par & ~(1u << s)) | ((uint32_t)((j / F_KST) & 1) << s);
+        const int sv = j % F_VST;
+        if (j >= F_VST && !ptx::mbar_wait(v_empty(sv), ((j / F_VST) & 1) ^ 1)) {
+          ok = false;
+          wait_failed(12);
+          break;
         }
+        ptx::mbar_arrive_expect_tx(v_full(sv), TILE);
+        const uint32_t vt = base + F_OFF_V + sv * TILE;
+        ptx::tma_load_2d(vt, &tm, v_full(sv), col_v, r);
+        ptx::tma_load_2d(vt + BOX, &tm, v_full(sv), col_v + 64, r);
+        v_issued |= 1u << sv;
+        v_par = (v_par & ~(1u << sv)) | ((uint32_t)((j / F_VST) & 1) << sv);
       }
+      // every load issued has landed before the CTA may exit
+      bool dr = ptx::mbar_wait(bar_q, 0);
+      for (int s = 0; s < F_KST; ++s)
+        if ((k_issued >> s) & 1u) dr = ptx::mbar_wait(k_full(s), (k_par >> s) & 1u) && dr;
+      for (int s = 0; s < F_VST; ++s)
+        if ((v_issued >> s) & 1u) dr = ptx::mbar_wait(v_full(s), (v_par >> s) & 1u) && dr;
+      if (!dr) wait_failed(13);
     }
-    // (4) P_j = exp2(s - m_ref) into the P buffer, free once PV_{j-1} is done
-    if (j >= 1 && !ptx::mbar_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
-    float rs = 0.f;
-    const bool live = m_ref != -INFINITY;
-#pragma unroll
-    for (int c0 = 0; c0 < BKV; c0 += 32) {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p = live ? fast_exp2(sv[c0 + i] - m_ref) : 0.f;  // masked keys: exp2(-inf) = 0
-        v[i] = p;
-        rs += p;
-      }
-      uint8_t* rowp = gbase + F_OFF_P + (c0 >> 6) * BOX + tid * 128;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int unit = ((c0 & 63) >> 3) + u;
-        const uint4 w = make_uint4(pack2(v[8 * u], v[8 * u + 1]), pack2(v[8 * u + 2], v[8 * u + 3]),
-                                   pack2(v[8 * u + 4], v[8 * u + 5]),
-                                   pack2(v[8 * u + 6], v[8 * u + 7]));
-        *reinterpret_cast<uint4*>(rowp + ((unit ^ (tid & 7)) << 4)) = w;
-      }
-    }
-    l += rs;
-    // (5) make P (and any rescaled O) visible to the tensor core; all threads decide together
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    ptx::tc_fence_before();
-    if (__syncthreads_or(!ok)) {
-      done_all = false;
-      break;
-    }
-    if (tid == 0) {
-      ok = ptx::mbar_wait(bar_v(j % F_VST), (j / F_VST) & 1);
-      if (ok) {
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int k_have = -1, v_have = -1;  // K / V blocks already waited for
+      auto need_k = [&](int j) {
+        if (j <= k_have) return true;
+        k_have = j;
+        if (!ptx::mbar_wait(k_full(j % F_KST), (j / F_KST) & 1)) { wait_failed(14); return false; }
+        return true;
+      };
+      auto need_v = [&](int j) {
+        if (j <= v_have) return true;
+        v_have = j;
+        if (!ptx::mbar_wait(v_full(j % F_VST), (j / F_VST) & 1)) { wait_failed(15); return false; }
+        return true;
+      };
+      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+        if (!need_k(j)) return false;
         ptx::tc_fence_after();
-        const uint32_t pt = base + F_OFF_P, vt = base + F_OFF_V + (j % F_VST) * TILE;
+        const uint32_t qt = base + F_OFF_Q + t * TILE, kt = base + F_OFF_K + (j % F_KST) * TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16(tmem + 128u * t, kmajor_desc(qt, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
+        ptx::mma_commit(s_full(t));
+        return true;
+      };
+      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t read from tensor memory
+        if (!ptx::mbar_wait(p_full(t), j & 1)) { wait_failed(16); return false; }
+        if (!need_v(j)) return false;
+        ptx::tc_fence_after();
+        const uint32_t vt = base + F_OFF_V + (j % F_VST) * TILE;
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          ptx::mma_bf16(t_o, kmajor_desc(pt, kk), mnmajor_desc(vt, kk), IDESC_PV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(bar_pv(j & 1));
+          ptx::mma_bf16_ts(tmem + 256u + 128u * t, tmem + 128u * t + 8u * kk, mnmajor_desc(vt, kk),
+                           IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        return true;
+      };
+      ok = ptx::mbar_wait(bar_q, 0);
+      if (!ok) wait_failed(17);
+      for (int t = 0; t < 2 && ok; ++t)
+        if (n[t] > 0) ok = issue_s(t, 0);
+      if (ok && nmax > 0) ptx::mma_commit(k_empty(0));
+      for (int j = 0; j < nmax && ok; ++j) {
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n[t]) continue;
+          ok = issue_pv(t, j);
+          if (!ok) break;
+          if (j + 1 < n[t])
+            ok = issue_s(t, j + 1);
+          else
+            ptx::mma_commit(o_full(t));  // the tile's last PV
+        }
+        if (!ok) break;
+        ptx::mma_commit(v_empty(j % F_VST));                       // V_j read by both PVs
+        if (j + 1 < nmax) ptx::mma_commit(k_empty((j + 1) % F_KST));  // K_{j+1} by both S
+      }
+      ptx::mma_commit(bar_drain);  // completes once every MMA issued above has
+      if (!ptx::mbar_wait(bar_drain, 0)) {
+        ok = false;
+        wait_failed(18);
       }
     }
-  }
-  if (done_all && nkv >= 1) {
-    const int j = nkv - 1;
-    if (!ptx::mbar_wait(bar_pv(j & 1), (j >> 1) & 1)) ok = false;
-    ptx::tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const bool store = ok && qi < a.S;
-    uint4* orow = reinterpret_cast<uint4*>(a.o + (int64_t)(row0 + qi) * a.H + h * D);
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      float v[32];
-      ptx::tmem_ld32(t_o + lane_off + c0, v);  // every lane: warp-collective
-      if (store) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          orow[c0 / 8 + u] = make_uint4(pack2(v[8 * u] * inv, v[8 * u + 1] * inv),
-                                        pack2(v[8 * u + 2] * inv, v[8 * u + 3] * inv),
-                                        pack2(v[8 * u + 4] * inv, v[8 * u + 5] * inv),
-                                        pack2(v[8 * u + 6] * inv, v[8 * u + 7] * inv));
+  } else {
+    const int t = (warp - 2) >> 2, qq = warp & 3;
+    const int row = qq * 32 + lane, qi = q0 + t * BQ + row;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const uint32_t t_s = tmem + 128u * t + lane_off, t_o = tmem + 256u + 128u * t + lane_off;
+    const int qt0 = q0 + t * BQ;  // first query of the tile
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < n[t] && ok; ++j) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(s_full(t), j & 1))) {
+        ok = false;
+        if (lane == 0) wait_failed(19);
+        break;
       }
+      ptx::tc_fence_after();
+      float sv[BKV];
+      ptx::tmem_ld128(t_s, sv);
+      const int kbase = j * BKV;
+      // a block every row of the tile sees whole needs no mask (warp-uniform)
+      const bool full = (j + 1) * BKV <= a.S && (!a.causal || (j + 1) * BKV <= qt0 + 1);
+      float mx = -INFINITY;
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < BKV; ++i) {
+          sv[i] *= a.scale_log2;
+          mx = fmaxf(mx, sv[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < BKV; ++i) {
+          const int key = kbase + i;
+          const bool valid = key < a.S && (!a.causal || key <= qi);
+          sv[i] = valid ? sv[i] * a.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sv[i]);
+        }
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      if (j == 0) {
+        m_ref = m_new;
+      } else {
+        const bool need = m_new > m_ref + RESCALE_LOG2;
+        // S_t(j) complete => PV_t(j-1) complete: O_t may be rescaled in place
+        if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are collective
+          const float f = need ? exp2f(m_ref - m_new) : 1.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float v[32];
+            ptx::tmem_ld32(t_o + c0, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= f;
+            ptx::tmem_st32(t_o + c0, v);
+          }
+          if (need) {
+            l *= f;
+            m_ref = m_new;
+          }
+        }
+      }
+      // P = exp2(s - m_ref) as packed bf16 over S's first 64 columns; the
+      // packed word of keys (2i, 2i+1) goes to sv[i] (already consumed), so P
+      // needs no registers beyond S's
+      const bool live = m_ref != -INFINITY;
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < BKV / 2; ++i) {
+        const float p0 = live ? fast_exp2(sv[2 * i] - m_ref) : 0.f;
+        const float p1 = live ? fast_exp2(sv[2 * i + 1] - m_ref) : 0.f;
+        rs += p0 + p1;
+        sv[i] = __uint_as_float(pack2(p0, p1));
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(sv[32 * half + i]);
+        ptx::tmem_st32_nowait(t_s + 32u * half, w);
+      }
+      ptx::tmem_wait_st();
+      l += rs;
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_full(t));
     }
-    if (store) a.lse[(int64_t)h * a.M + row0 + qi] = (m_ref + log2f(l)) * 0.69314718055994531f;
+    if (n[t] > 0) {
+      // the tile's last PV is complete (or the MMA thread gave up)
+      const bool fin = __all_sync(0xffffffffu, ptx::mbar_wait(o_full(t), 0));
+      if (!fin && lane == 0) wait_failed(20);
+      ptx::tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = ok && fin && qi < a.S;
+      uint4* orow = reinterpret_cast<uint4*>(a.o + (int64_t)(row0 + qi) * a.H + h * D);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(t_o + c0, v);  // every lane: warp-collective
+        if (store) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            orow[c0 / 8 + u] = make_uint4(pack2(v[8 * u] * inv, v[8 * u + 1] * inv),
+                                          pack2(v[8 * u + 2] * inv, v[8 * u + 3] * inv),
+                                          pack2(v[8 * u + 4] * inv, v[8 * u + 5] * inv),
+                                          pack2(v[8 * u + 6] * inv, v[8 * u + 7] * inv));
+        }
+      }
+      if (store) a.lse[(int64_t)h * a.M + row0 + qi] = (m_ref + log2f(l)) * 0.69314718055994531f;
+      if (!(ok && fin)) ok = false;
+    }
   }
-  if (!(done_all && ok)) atomicExch(&g_attn_error, 1);
-  if (tid == 0) {
-    // drain: issued MMAs complete and issued loads land before the CTA exits
-    ptx::mma_commit(bar_drain);
-    bool dr = ptx::mbar_wait(bar_drain, 0);
-    for (int s = 0; s < F_KST; ++s)
-      if ((k_issued >> s) & 1u) dr = ptx::mbar_wait(bar_k(s), (k_par >> s) & 1u) && dr;
-    for (int s = 0; s < F_VST; ++s)
-      if ((v_issued >> s) & 1u) dr = ptx::mbar_wait(bar_v(s), (v_par >> s) & 1u) && dr;
-    dr = ptx::mbar_wait(bar_q, 0) && dr;
-    if (!dr) atomicExch(&g_attn_error, 2);
-  }
+  if (!ok) atomicExch(&g_attn_error, 1);
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
@@ -994,10 +1065,10 @@ cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   fa.M = M;
   fa.causal = a.causal ? 1 : 0;
   fa.scale_log2 = 1.4426950408889634f / sqrtf((float)a.head_dim);
-  const int tiles = (a.seq + BQ - 1) / BQ;
-  if (tiles > 65535) return cudaErrorInvalidConfiguration;
-  const dim3 grid(a.heads, a.batch, tiles);
-  return launch_pdl(attn_fwd_tc_kernel, grid, dim3(NT), FWD_SMEM, st, m, fa);
+  const int pairs = (a.seq + 2 * BQ - 1) / (2 * BQ);
+  if (pairs > 65535 || a.batch > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(a.heads, a.batch, pairs);
+  return launch_pdl(attn_fwd_tc_kernel, grid, dim3(F_NT), FWD_SMEM, st, m, fa);
 }
 
 cudaError_t attention_delta(const AttnArgs& a, cudaStream_t st);
