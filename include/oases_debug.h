@@ -64,13 +64,16 @@ oases_status oases_debug_attention(const void *qkv, void *o, float *lse, const v
  * oases_debug_attention_error_word: reads and clears the code of the first
  * bounded wait that gave up (kernel * 100 + site; 0 = none, -1 = unreadable). */
 oases_status oases_debug_attention_progress(int *host_mapped);
-/* Timeline of the attention backward kernels (debugging aid): device_buffer
- * holds 16896 uint64 %globaltimer stamps, written by every following backward
- * launch: entry and exit of each CTA c < 4096 at [2c] (dQ kernel) and
+/* Timeline of the tensor-core attention kernels (debugging aid): device_buffer
+ * holds uint64 %globaltimer stamps, written by every following launch.
+ * Backward: entry and exit of each CTA c < 4096 at [2c] (dQ kernel) and
  * [8192 + 2c] (dK/dV kernel); for CTA 0 and block j < 64, four stamps at
  * [16384 + 4j] (dQ) and [16640 + 4j] (dK/dV): S and dP MMAs issued,
  * accumulation MMAs issued, element-wise warp 2 saw S and dP, and handed over
- * its rows.  NULL switches it off. */
+ * its rows.  Forward: for CTA 0, query tile t (0, 1) and key block j < 64,
+ * eight stamps at [16896 + 8 (64 t + j)]: S_t(j) issued, the softmax warp of
+ * lane quarter 2 saw S_t(j), the warps of lane quarters 0..3 published P_t(j),
+ * PV_t(j) issued.  The buffer then holds 17920 stamps.  NULL switches it off. */
 oases_status oases_debug_attention_timeline(unsigned long long *device_buffer);
 /* Timeline of the tensor-core GEMM (debugging aid): device_buffer holds 16
  * uint64 %globaltimer stamps per CTA of every following launch (entry,

@@ -66,15 +66,23 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Shared-memory descriptors are formed once per tile and stepped per MMA: the
+// start-address field (bits 0..13) holds the address in 16-byte units, and
+// every shared address here is below 2^18, so adding byte offset d as d >> 4
+// cannot carry out of the field.  (Forming each descriptor from scratch cost
+// more issue time in the single MMA thread than the MMA itself takes.)
+__device__ __forceinline__ uint64_t desc_step(uint64_t base_desc, uint32_t byte_off) {
+  return base_desc + (uint64_t)(byte_off >> 4);
+}
 // Descriptor of a K-major operand tile [128 rows][128 cols] stored as two
 // 128-byte-swizzled 64-column boxes, for k-step kk (16 columns) of 8.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-  return ptx::smem_desc_sw128(tile + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024);
+  return desc_step(ptx::smem_desc_sw128(tile, 16, 1024), (kk >> 2) * BOX + (kk & 3) * 32);
 }
 // Descriptor of an MN-major operand [128 k-rows][128 n-cols] stored as two
 // boxes of 64 n-columns, for k-step kk (16 k-rows) of 8.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
-  return ptx::smem_desc_sw128(tile + kk * 2048, BOX, 1024);
+  return desc_step(ptx::smem_desc_sw128(tile, BOX, 1024), kk * 2048);
 }
 
 __device__ __forceinline__ void progress(int kid, int code) {
@@ -100,6 +108,13 @@ __device__ __forceinline__ void tl_block(int kid, int j, int what) {
   unsigned long long* t = g_attn_timeline;
   if (t != nullptr && linear_cta() == 0 && j < 64)
     t[16384 + (kid - 1) * 256 + 4 * j + what] = ptx::globaltimer();
+}
+// Forward, CTA 0, tile t, key block j < 64: [0] S_t(j) issued, [1] the
+// softmax warp of lane quarter 2 saw S_t(j), [2 + q] the warp of lane quarter
+// q published P_t(j), [6] PV_t(j) issued.
+__device__ __forceinline__ void tl_fwd(int t, int j, int what) {
+  unsigned long long* tb = g_attn_timeline;
+  if (tb != nullptr && linear_cta() == 0 && j < 64) tb[16896 + 8 * (64 * t + j) + what] = ptx::globaltimer();
 }
 // Records the first failed wait site (kernel * 100 + site) in g_attn_error.
 __device__ __forceinline__ void wait_failed(int code) { atomicCAS(&g_attn_error, 0, code); }
@@ -282,6 +297,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         for (int kk = 0; kk < D / 16; ++kk)
           ptx::mma_bf16(tmem + 128u * t, kmajor_desc(qt, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
         ptx::mma_commit(s_full(t));
+        tl_fwd(t, j, 0);
         return true;
       };
       auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t read from tensor memory
@@ -293,6 +309,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         for (int kk = 0; kk < BKV / 16; ++kk)
           ptx::mma_bf16_ts(tmem + 256u + 128u * t, tmem + 128u * t + 8u * kk, mnmajor_desc(vt, kk),
                            IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        tl_fwd(t, j, 6);
         return true;
       };
       ok = ptx::mbar_wait(bar_q, 0);
@@ -334,27 +351,28 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         break;
       }
       ptx::tc_fence_after();
+      if (qq == 2 && lane == 0) tl_fwd(t, j, 1);
       float sv[BKV];
       ptx::tmem_ld128(t_s, sv);
       const int kbase = j * BKV;
       // a block every row of the tile sees whole needs no mask (warp-uniform)
       const bool full = (j + 1) * BKV <= a.S && (!a.causal || (j + 1) * BKV <= qt0 + 1);
-      float mx = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int i = 0; i < BKV; ++i) {
-          sv[i] *= a.scale_log2;
-          mx = fmaxf(mx, sv[i]);
-        }
-      } else {
+      if (!full) {
 #pragma unroll
         for (int i = 0; i < BKV; ++i) {
           const int key = kbase + i;
-          const bool valid = key < a.S && (!a.causal || key <= qi);
-          sv[i] = valid ? sv[i] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sv[i]);
+          if (!(key < a.S && (!a.causal || key <= qi))) sv[i] = -INFINITY;
         }
       }
+      // row maximum of the raw scores in eight independent chains (the scale
+      // is positive, so it is applied to the maximum alone)
+      float pm[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) pm[c] = sv[c];
+#pragma unroll
+      for (int i = 8; i < BKV; ++i) pm[i % 8] = fmaxf(pm[i % 8], sv[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * a.scale_log2;
       const float m_new = fmaxf(m_ref, mx);
       if (j == 0) {
         m_ref = m_new;
@@ -377,16 +395,20 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
           }
         }
       }
-      // P = exp2(s - m_ref) as packed bf16 over S's first 64 columns; the
-      // packed word of keys (2i, 2i+1) goes to sv[i] (already consumed), so P
-      // needs no registers beyond S's
+      // P = exp2(s * scale - m_ref) as packed bf16 over S's first 64 columns.
+      // Scale and shift in one fp32x2 FMA per pair, the row sum in four fp32x2
+      // accumulators.
       const bool live = m_ref != -INFINITY;
-      float rs = 0.f;
+      const uint64_t sc2 = f2_splat(a.scale_log2), nm2 = f2_splat(-m_ref);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      // the packed word of keys (2i, 2i+1) goes to sv[i] (already consumed), so
+      // P needs no registers beyond S's
 #pragma unroll
       for (int i = 0; i < BKV / 2; ++i) {
-        const float p0 = live ? fast_exp2(sv[2 * i] - m_ref) : 0.f;
-        const float p1 = live ? fast_exp2(sv[2 * i + 1] - m_ref) : 0.f;
-        rs += p0 + p1;
+        const uint64_t x = f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), sc2, nm2);
+        float p0 = fast_exp2(f2_lo(x)), p1 = fast_exp2(f2_hi(x));
+        if (!live) p0 = p1 = 0.f;  // (a row with no visible key; x is NaN there)
+        acc[i % 4] = f2_add(acc[i % 4], f2_pack(p0, p1));
         sv[i] = __uint_as_float(pack2(p0, p1));
       }
 #pragma unroll
@@ -396,11 +418,14 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(sv[32 * half + i]);
         ptx::tmem_st32_nowait(t_s + 32u * half, w);
       }
+      const uint64_t acc2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+      const float rs = f2_lo(acc2) + f2_hi(acc2);
       ptx::tmem_wait_st();
       l += rs;
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(p_full(t));
+      if (lane == 0) tl_fwd(t, j, 2 + qq);
     }
     if (n[t] > 0) {
       // the tile's last PV is complete (or the MMA thread gave up)
@@ -480,15 +505,15 @@ constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(128, D, false, true);
 
 // [64 rows][128 cols] K-major tile stored as two 64-column boxes, k-step kk of 8.
 __device__ __forceinline__ uint64_t kmajor64_desc(uint32_t tile, int kk) {
-  return ptx::smem_desc_sw128(tile + (kk >> 2) * BOX64 + (kk & 3) * 32, 16, 1024);
+  return desc_step(ptx::smem_desc_sw128(tile, 16, 1024), (kk >> 2) * BOX64 + (kk & 3) * 32);
 }
 // [64 k-rows][128 n-cols] MN-major tile stored as two 64-column boxes, k-step kk of 4.
 __device__ __forceinline__ uint64_t mnmajor64_desc(uint32_t tile, int kk) {
-  return ptx::smem_desc_sw128(tile + kk * 2048, BOX64, 1024);
+  return desc_step(ptx::smem_desc_sw128(tile, BOX64, 1024), kk * 2048);
 }
 // [128 rows][64 cols] K-major buffer (one box width), k-step kk of 4.
 __device__ __forceinline__ uint64_t kmajor_blk_desc(uint32_t buf, int kk) {
-  return ptx::smem_desc_sw128(buf + kk * 32, 16, 1024);
+  return desc_step(ptx::smem_desc_sw128(buf, 16, 1024), kk * 32);
 }
 // Writes this thread's 32 values (columns 32 half .. + 31 of its row) as bf16
 // into a [128 rows][64 cols] 128-byte-swizzled buffer.

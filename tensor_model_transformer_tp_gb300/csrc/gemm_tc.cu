@@ -469,18 +469,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t tsa = tmem + (uint32_t)(C::SF_COL0 + 8 * stage), tsb = tsa + 4;
             ptx::tmem_cp_32x128b_x4(tsa, ptx::smem_desc_noswz(ssf, 128, 128));
             ptx::tmem_cp_32x128b_x4(tsb, ptx::smem_desc_noswz(ssf + 512, 128, 128));
+            const uint64_t ad0 = ptx::smem_desc_sw128(sa, 16, 1024), bd0 = ptx::smem_desc_sw128(sb, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              ptx::mma_mx(dt, ptx::smem_desc_sw128(sa + kk * 32, 16, 1024),
-                          ptx::smem_desc_sw128(sb + kk * 32, 16, 1024),
-                          IDESC | ptx::idesc_sf_ids(kk, kk), tsa, tsb, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)  // start address += 32 bytes per K = 32 step
+              ptx::mma_mx(dt, ad0 + 2 * kk, bd0 + 2 * kk, IDESC | ptx::idesc_sf_ids(kk, kk), tsa, tsb,
+                          (kb | kk) != 0 ? 1u : 0u);
           } else {
+            // descriptors formed once per stage; the start-address field (16-byte
+            // units, shared addresses < 2^18) is stepped per K = 16 MMA
+            const uint64_t ad0 = A_K ? ptx::smem_desc_sw128(sa, 16, 1024) : ptx::smem_desc_sw128(sa, 8192, 1024);
+            const uint64_t bd0 = B_K ? ptx::smem_desc_sw128(sb, 16, 1024) : ptx::smem_desc_sw128(sb, 8192, 1024);
 #pragma unroll
             for (int kk = 0; kk < BKE / 16; ++kk) {
-              const uint64_t ad = A_K ? ptx::smem_desc_sw128(sa + kk * 32, 16, 1024)
-                                      : ptx::smem_desc_sw128(sa + kk * 2048, 8192, 1024);
-              const uint64_t bd = B_K ? ptx::smem_desc_sw128(sb + kk * 32, 16, 1024)
-                                      : ptx::smem_desc_sw128(sb + kk * 2048, 8192, 1024);
+              const uint64_t ad = ad0 + (uint64_t)(A_K ? 2 * kk : 128 * kk);
+              const uint64_t bd = bd0 + (uint64_t)(B_K ? 2 * kk : 128 * kk);
               if (CL > 1)
                 ptx::mma_bf16_pair(dt, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
               else

@@ -555,7 +555,7 @@ part_reduce_kernel(const float* __restrict__ part, float* __restrict__ out,
 // (four independent accumulators, combined in a fixed order) and writes the
 // result over row 16g — every row of the group is read before that write by
 // the same thread, so the update is in place.  Level 2 adds rows 0, 16, 32, ...
-// in order into out.
+// into out in a fixed order (part_reduce_l2).
 constexpr int RED_ROWS = 16;
 __global__ void __launch_bounds__(256)
 part_reduce_l1(float* __restrict__ part, float* __restrict__ part2, int nb, int N) {
@@ -581,21 +581,38 @@ part_reduce_l1(float* __restrict__ part, float* __restrict__ part2, int nb, int 
     }
   }
 }
-__global__ void __launch_bounds__(256)
+// Level 2: out[n] += the level-1 rows 0, 16, 32, ... of column n.  A CTA
+// takes 32 columns with 8 thread groups; group g adds the rows 16 (g + 8 i)
+// in order of i, then group sums are added in order 0..7: a fixed order, so
+// the result does not depend on timing.
+__global__ void __launch_bounds__(RED_COLS * RED_GROUPS)
 part_reduce_l2(const float* __restrict__ part, float* __restrict__ out,
                const float* __restrict__ part2, float* __restrict__ out2, int nb, int N) {
   pdl_wait();
   pdl_trigger();
-  const int n = blockIdx.x * 256 + threadIdx.x;
-  if (n >= N) return;
+  __shared__ float sh[2][RED_GROUPS][RED_COLS];
+  const int cl = threadIdx.x % RED_COLS, g = threadIdx.x / RED_COLS;
+  const int n = blockIdx.x * RED_COLS + cl;
   float s = 0.f, s2 = 0.f;
-#pragma unroll 4
-  for (int r = 0; r < nb; r += RED_ROWS) {
-    s += part[(int64_t)r * N + n];
-    if (part2) s2 += part2[(int64_t)r * N + n];
+  if (n < N) {
+    for (int r = g * RED_ROWS; r < nb; r += RED_GROUPS * RED_ROWS) {
+      s += part[(int64_t)r * N + n];
+      if (part2) s2 += part2[(int64_t)r * N + n];
+    }
   }
-  out[n] += s;
-  if (part2) out2[n] += s2;
+  sh[0][g][cl] = s;
+  sh[1][g][cl] = s2;
+  __syncthreads();
+  if (g == 0 && n < N) {
+    float t = 0.f, t2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < RED_GROUPS; ++k) {
+      t += sh[0][k][cl];
+      t2 += sh[1][k][cl];
+    }
+    out[n] += t;
+    if (part2) out2[n] += t2;
+  }
 }
 
 cudaError_t reduce_parts(float* part, float* out, float* part2, float* out2, int nb, int N,
@@ -605,8 +622,8 @@ cudaError_t reduce_parts(float* part, float* out, float* part2, float* out2, int
   cudaError_t e = launch_pdl(part_reduce_l1, dim3(gx, gy), dim3(256),
                              0, st, part, part2, nb, N);
   if (e != cudaSuccess) return e;
-  return launch_pdl(part_reduce_l2, dim3(gx), dim3(256), 0, st, (const float*)part, out,
-                    (const float*)part2, out2, nb, N);
+  return launch_pdl(part_reduce_l2, dim3((N + RED_COLS - 1) / RED_COLS), dim3(RED_COLS * RED_GROUPS),
+                    0, st, (const float*)part, out, (const float*)part2, out2, nb, N);
 }
 
 template <typename T>
