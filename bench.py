@@ -204,6 +204,15 @@ def dist_env():
     return rank, world, local
 
 
+def oracle_product(shape):
+    """Keyword arguments selecting the oracle's product for the workload's
+    dtype: the MX-FP8 product for an mxfp8 block, the exact one otherwise."""
+    if shape.dtype == "mxfp8":
+        import oracle.fp8 as fp8
+        return {"mm": fp8.mx_product_bf16}
+    return {}
+
+
 def oracle_rate(shape, recompute) -> float:
     """The oracle's FLOP/s on a small calibration sample of the workload (one
     sequence per sub-batch, at most 64 tokens).  Fixed costs weigh more on so
@@ -213,7 +222,7 @@ def oracle_rate(shape, recompute) -> float:
     cal = shape.replace(batch=shape.sub_batches, seq=min(shape.seq, 64))
     inp = block_inputs(cal, seed=0)
     t0 = time.perf_counter()
-    oracle.run_step(cal, inp, mode=recompute)
+    oracle.run_step(cal, inp, mode=recompute, **oracle_product(shape))
     return flops_fine(cal, recompute) / max(time.perf_counter() - t0, 1e-6)
 
 
@@ -258,7 +267,7 @@ def run_reference(args, shape):
     # (untimed, like the warm-up) and shrink it while it runs well over budget
     while True:
         t0 = time.perf_counter()
-        oracle.run_step(sample, inp, mode=args.recompute)
+        oracle.run_step(sample, inp, mode=args.recompute, **oracle_product(shape))
         if time.perf_counter() - t0 <= 1.25 * per_step or (
                 sample.batch == shape.sub_batches and sample.seq <= 8):
             break
@@ -268,10 +277,10 @@ def run_reference(args, shape):
             sample = sample.replace(seq=max(8, sample.seq // 2))
         inp = block_inputs(sample, seed=0)
     for _ in range(args.warmup):
-        oracle.run_step(sample, inp, mode=args.recompute)
+        oracle.run_step(sample, inp, mode=args.recompute, **oracle_product(shape))
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.run_step(sample, inp, mode=args.recompute)
+        oracle.run_step(sample, inp, mode=args.recompute, **oracle_product(shape))
     dt = (time.perf_counter() - t0) / args.steps
     value = flops_fine(sample, args.recompute) / dt / 1e12
     cores = len(os.sched_getaffinity(0))
@@ -298,7 +307,7 @@ def cpu_baseline(shape, recompute):
     inp = block_inputs(sample, seed=0)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.run_step(sample, inp, mode=recompute)
+        oracle.run_step(sample, inp, mode=recompute, **oracle_product(shape))
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= 10.0 or reps >= 50:
@@ -609,6 +618,9 @@ def main():
     ap.add_argument("--workload", default="stack4_bf16_h2560")
     ap.add_argument("--recompute", default="fine", choices=["fine", "full", "none", "selective"])
     ap.add_argument("--sub-batches", type=int, default=None)
+    ap.add_argument("--dtype", default=None, choices=["bf16", "mxfp8"],
+                    help="override the workload's dtype (mxfp8: bf16 storage, MX-FP8 GEMMs); "
+                         "the headline is the workload's own bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the step directly, not as a CUDA graph")
     ap.add_argument("--reduce", default="fused", choices=["fused", "separate"],
@@ -623,6 +635,8 @@ def main():
     shape = SHAPES[args.workload]
     if args.sub_batches:
         shape = shape.replace(sub_batches=args.sub_batches)
+    if args.dtype:
+        shape = shape.replace(dtype=args.dtype)
     if args.impl == "reference":
         run_reference(args, shape)
         return
@@ -724,7 +738,7 @@ def main():
     t_e2e = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, dev)
     fl = flops_fine(shape, args.recompute)
     value = whole_job_tflops(fl, world, t_step)
-    io = shape.rows * shape.hidden * (2 if shape.dtype == "bf16" else 4)
+    io = shape.rows * shape.hidden * (4 if shape.dtype == "f32" else 2)
 
     pk = peaks()
     rows = kernel_table(shape, pk) + mx_table(shape, pk)

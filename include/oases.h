@@ -74,7 +74,18 @@ typedef enum {
 } oases_status;
 
 typedef enum { OASES_BLOCK_FFN = 0, OASES_BLOCK_ATTN = 1, OASES_BLOCK_LAYER = 2 } oases_block_kind;
-typedef enum { OASES_F32 = 0, OASES_BF16 = 1 } oases_dtype;
+/* F32, BF16: storage and GEMM operand type of x, y, weights and activations
+ * (fp32 accumulation, fp32 weight gradients).
+ * MXFP8: storage as BF16, and every GEMM of the block (the column-parallel F_i,
+ *        the row-parallel F_j, their input-gradient and weight-gradient
+ *        products) multiplies MX-FP8 operands: E4M3 elements with one UE8M0
+ *        scale per 32 elements along the contraction, quantised from the
+ *        stored bf16 operands just before each GEMM (oases_mx.h), fp32
+ *        accumulation.  The attention operation itself stays bf16.  The pages
+ *        describe no 8-bit form; this variant follows the OCP Microscaling
+ *        Formats v1.0 definitions.  Requires the FUSED reduction, hidden, ffn/w
+ *        and hidden/w multiples of 32. */
+typedef enum { OASES_F32 = 0, OASES_BF16 = 1, OASES_MXFP8 = 2 } oases_dtype;
 /* NONE: keep every activation between forward and backward, no recompute.
  * FULL: keep only segment inputs; recompute the whole segment including the
  *       row GEMM and its reduction (Oases §IV-A, Fig. 4a, the default schedule).
@@ -108,7 +119,7 @@ typedef struct {
   int32_t dtype;        /* oases_dtype */
   int32_t batch;        /* sequences; >= 0, divisible by sub_batches */
   int32_t seq;          /* tokens per sequence; >= 0 */
-  int32_t hidden;       /* > 0; a multiple of 8 for bf16 */
+  int32_t hidden;       /* > 0; a multiple of 8 for bf16, of 32 for MXFP8 */
   int32_t ffn;          /* FFN width (ffn/layer kinds); divisible by w; multiple of 8 for bf16 */
   int32_t heads;        /* attention heads (attn/layer kinds); divisible by w */
   int32_t w;            /* simulated tensor-parallel shards, >= 1 */

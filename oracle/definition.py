@@ -34,17 +34,21 @@ def _ln(x, g, b, shape):
     return layer_norm(x, g, b, shape.eps)[0]
 
 
-def ffn_segment_plain(x, p, shape):
+def _exact(A, B):
+    return A @ B.T
+
+
+def ffn_segment_plain(x, p, shape, mm=_exact):
     u = _ln(x, p["ln2_g"], p["ln2_b"], shape)
-    h = gelu(u @ p["w1"].T + p["b1"])
-    y = h @ p["w2"].T + p["b2"]
+    h = gelu(mm(u, p["w1"]) + p["b1"])
+    y = mm(h, p["w2"]) + p["b2"]
     return y + x if shape.residual else y
 
 
-def attn_segment_plain(x, p, shape):
+def attn_segment_plain(x, p, shape, mm=_exact):
     H, d, S = shape.hidden, shape.head_dim, shape.seq
     u = _ln(x, p["ln1_g"], p["ln1_b"], shape)
-    qkv = u @ p["wqkv"].T + p["bqkv"]
+    qkv = mm(u, p["wqkv"]) + p["bqkv"]
     o = np.zeros_like(x)
     for b in range(x.shape[0] // S):
         r = slice(b * S, (b + 1) * S)
@@ -54,17 +58,19 @@ def attn_segment_plain(x, p, shape):
             k = qkv[r, H + h * d:H + (h + 1) * d]
             v = qkv[r, 2 * H + h * d:2 * H + (h + 1) * d]
             o[r, c] = attention_head(q, k, v, shape.causal)[0]
-    y = o @ p["wo"].T + p["bo"]
+    y = mm(o, p["wo"]) + p["bo"]
     return y + x if shape.residual else y
 
 
-def block_forward_plain(shape, x, layers):
-    """Forward of the whole block / layer / stack.  x is [rows, hidden]."""
+def block_forward_plain(shape, x, layers, mm=_exact):
+    """Forward of the whole block / layer / stack.  x is [rows, hidden].
+    mm(A, B) = A B^T is every matrix product (exact unless given)."""
     y = np.asarray(x, dtype=np.float64)
     for p in layers:
         p = {k: np.asarray(v, dtype=np.float64) for k, v in p.items()}
         for kind in segment_kinds(shape):
-            y = ffn_segment_plain(y, p, shape) if kind == "ffn" else attn_segment_plain(y, p, shape)
+            y = (ffn_segment_plain(y, p, shape, mm) if kind == "ffn"
+                 else attn_segment_plain(y, p, shape, mm))
     return y
 
 

@@ -98,3 +98,21 @@ def mx_gemm(A: np.ndarray, B: np.ndarray, block: int = MX_BLOCK) -> np.ndarray:
         s = slice(b * block, (b + 1) * block)
         D += (XA[:, b:b + 1] * XB[:, b][None, :]) * (PA[:, s] @ PB[:, s].T)
     return D
+
+
+def bf16_round(x) -> np.ndarray:
+    """x rounded to the nearest bfloat16 value (8 significant bits, exponent
+    range of float32), ties to the even significand: x = f 2^e with f in
+    [0.5, 1) becomes round_half_even(f 2^8) 2^(e-8).  Values below the bf16
+    normal range (2^-126) are rounded on the same grid as 2^-126."""
+    x = np.asarray(x, dtype=np.float64)
+    f, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    return np.ldexp(np.round(np.ldexp(x, 8 - e)), e - 8)
+
+
+def mx_product_bf16(A: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """The MX-FP8 form of one of the block's products, A B^T: both operands as
+    the block stores them (bf16), each MX-quantised along the contraction (the
+    columns of both), multiplied as mx_gemm does."""
+    return mx_gemm(bf16_round(A), bf16_round(B))

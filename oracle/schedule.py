@@ -81,10 +81,19 @@ class Trace(list):
         return sum(1 for e in self if e[0] == event)
 
 
+def exact_product(A, B):
+    """A B^T in float64: the products of the block as the pages define them."""
+    return A @ B.T
+
+
 class _Segment:
-    def __init__(self, index: int, layer: int, kind: str, p: Dict[str, np.ndarray], shape, w: int):
+    def __init__(self, index: int, layer: int, kind: str, p: Dict[str, np.ndarray], shape, w: int,
+                 mm=exact_product):
         self.s, self.layer, self.kind, self.shape, self.w = index, layer, kind, shape, w
         self.p = p
+        # every matrix product of the segment, forward and backward, is
+        # mm(A, B) = A B^T, contracting over the columns of both operands
+        self.mm = mm
         H = shape.hidden
         if kind == "ffn":
             F = shape.ffn
@@ -127,11 +136,11 @@ class _Segment:
         u = a[(self.s, "u")]
         wc, bc = self.p[self.names["wc"]], self.p[self.names["bc"]]
         if self.kind == "ffn":
-            A = [u @ wc[c].T + bc[c] for c in self.cols]
+            A = [self.mm(u, wc[c]) + bc[c] for c in self.cols]
             a[(self.s, "A")] = A
             a[(self.s, "H")] = [gelu(Ak) for Ak in A]
         else:
-            QKV = [u @ wc[r].T + bc[r] for r in self.qkv_rows]
+            QKV = [self.mm(u, wc[r]) + bc[r] for r in self.qkv_rows]
             a[(self.s, "QKV")] = QKV
             a[(self.s, "H")] = [self._attn_shard(q) for q in QKV]
 
@@ -141,7 +150,7 @@ class _Segment:
 
     def row_fwd(self, a):
         wr = self.p[self.names["wr"]]
-        a[(self.s, "P")] = [Hk @ wr[:, c].T for Hk, c in zip(a[(self.s, "H")], self.cols)]
+        a[(self.s, "P")] = [self.mm(Hk, wr[:, c]) for Hk, c in zip(a[(self.s, "H")], self.cols)]
 
     def g_fwd(self, a) -> np.ndarray:
         """C(F): y = sum_{k=0}^{w-1} P_k, then + bias (+ x_s)."""
@@ -166,8 +175,8 @@ class _Segment:
         wr = self.p[self.names["wr"]]
         dH = []
         for Hk, dPk, c in zip(a[(self.s, "H")], a[(self.s, "dP")], self.cols):
-            grads[self.names["wr"]][:, c] += dPk.T @ Hk
-            dH.append(dPk @ wr[:, c])
+            grads[self.names["wr"]][:, c] += self.mm(dPk.T, Hk.T)
+            dH.append(self.mm(dPk, wr[:, c].T))
         a[(self.s, "dH")] = dH
 
     def col_bwd(self, a, grads):
@@ -178,8 +187,8 @@ class _Segment:
             for Ak, dHk, c in zip(a[(self.s, "A")], a[(self.s, "dH")], self.cols):
                 dA = dHk * gelu_grad(Ak)
                 grads[self.names["bc"]][c] += dA.sum(axis=0)
-                grads[self.names["wc"]][c] += dA.T @ u
-                dus.append(dA @ wc[c])
+                grads[self.names["wc"]][c] += self.mm(dA.T, u.T)
+                dus.append(self.mm(dA, wc[c].T))
         else:
             S, d = self.shape.seq, self.shape.head_dim
             for qkv_k, dO, r in zip(a[(self.s, "QKV")], a[(self.s, "dH")], self.qkv_rows):
@@ -196,8 +205,8 @@ class _Segment:
                         dq, dk, dv = attention_head_backward(dO[rr, cq], q, k, v, p)
                         dqkv[rr, cq], dqkv[rr, ck], dqkv[rr, cv] = dq, dk, dv
                 grads[self.names["bc"]][r] += dqkv.sum(axis=0)
-                grads[self.names["wc"]][r] += dqkv.T @ u
-                dus.append(dqkv @ wc[r])
+                grads[self.names["wc"]][r] += self.mm(dqkv.T, u.T)
+                dus.append(self.mm(dqkv, wc[r].T))
         a[(self.s, "du_k")] = dus
 
     def f_bwd(self, a):
@@ -222,12 +231,12 @@ class _Segment:
         return dx
 
 
-def _segments(shape, layers, w):
+def _segments(shape, layers, w, mm=exact_product):
     kinds = ["attn", "ffn"] if shape.kind == "layer" else [shape.kind]
     segs = []
     for li, p in enumerate(layers):
         for kind in kinds:
-            segs.append(_Segment(len(segs), li, kind, p, shape, w))
+            segs.append(_Segment(len(segs), li, kind, p, shape, w, mm))
     return segs
 
 
@@ -254,8 +263,12 @@ def recompute_ops(seq: List[Op], mode: str, kind: str = None) -> List[Op]:
     return [op for op in seq if op.kind == "compute" and op.name != "row"]
 
 
-def run_step(shape, inputs, mode: str = "fine", sub_batches: int = None, w: int = None):
+def run_step(shape, inputs, mode: str = "fine", sub_batches: int = None, w: int = None,
+             mm=exact_product):
     """One training step (forward, recompute, backward) of the block.
+
+    mm(A, B) = A B^T is every matrix product of the step (default: exact);
+    oracle.fp8.mx_product_bf16 gives the MX-FP8 variant of the block's GEMMs.
 
     inputs: {"x": [rows, hidden], "g": [rows, hidden], "layers": [params...]}.
     Returns dict with y, dx (float64, [rows, hidden]), grads (list per layer of
@@ -271,7 +284,7 @@ def run_step(shape, inputs, mode: str = "fine", sub_batches: int = None, w: int 
     M = x.shape[0]
     assert M % n_sb == 0 and (M // n_sb) % max(shape.seq, 1) == 0
     Mb = M // n_sb
-    segs = _segments(shape, layers, w)
+    segs = _segments(shape, layers, w, mm)
     nS = len(segs)
     O = build_operator_sequence(nS)
     grads = [{k: np.zeros_like(v) for k, v in p.items()} for p in layers]

@@ -36,7 +36,7 @@ class BlockShape:
     n_layers > 1 makes a stack of identical-shape layers.
     """
     kind: str
-    dtype: str            # "f32" or "bf16": storage type of x, weights, activations
+    dtype: str            # "f32", "bf16" or "mxfp8" (bf16 storage, MX-FP8 GEMM operands)
     batch: int
     seq: int
     hidden: int
@@ -63,7 +63,7 @@ class BlockShape:
 
     def validate(self) -> None:
         assert self.kind in ("ffn", "attn", "layer"), self.kind
-        assert self.dtype in ("f32", "bf16"), self.dtype
+        assert self.dtype in ("f32", "bf16", "mxfp8"), self.dtype
         assert self.batch >= 0 and self.seq >= 0 and self.hidden > 0
         assert self.sub_batches >= 1 and self.batch % self.sub_batches == 0
         if self.kind in ("ffn", "layer"):
@@ -120,7 +120,7 @@ def block_inputs(s: BlockShape, seed: int = 0, affine: bool = False) -> Dict:
     """Draw x [rows, hidden], per-layer parameters and g [rows, hidden].
 
     Returns {"x": ndarray, "g": ndarray, "layers": [ {name: ndarray}, ... ]},
-    all float32 (bf16-representable when ``s.dtype == "bf16"``).
+    all float32 (bf16-representable when ``s.dtype`` is "bf16" or "mxfp8").
     """
     s.validate()
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -157,7 +157,7 @@ def block_inputs(s: BlockShape, seed: int = 0, affine: bool = False) -> Dict:
                 p[name] = normal(shape, 0.02) if affine else np.zeros(shape, np.float32)
         layers.append(p)
     g = normal((M, H))
-    if s.dtype == "bf16":
+    if s.dtype in ("bf16", "mxfp8"):
         x = bf16_round(x)
         g = bf16_round(g)
         layers = [{k: bf16_round(v) for k, v in p.items()} for p in layers]

@@ -22,7 +22,7 @@ _lib = None
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT",
           6: "INJECTED"}
 KIND = {"ffn": 0, "attn": 1, "layer": 2}
-DTYPE = {"f32": 0, "bf16": 1}
+DTYPE = {"f32": 0, "bf16": 1, "mxfp8": 2}
 RECOMPUTE = {"none": 0, "full": 1, "fine": 2, "selective": 3}
 REDUCE = {"fused": 0, "separate": 1}
 EVENTS = ["F", "R", "B", "C(F)", "C(R)", "C(B)", "Sync"]

@@ -118,6 +118,7 @@ struct Step {
 struct Shape {
   int kind, B, S, H, F, nh, d, w, nsb, pre_ln, residual, causal, mode, reduce;
   DType t;
+  bool mx;  // MX-FP8 GEMM operands (bf16 storage)
   float eps;
   int64_t M, Ms;
   size_t esz;
@@ -130,7 +131,7 @@ struct Shape {
 
 oases_status validate(const oases_block_desc* d, int n_layers, Shape* s) {
   if (!d || n_layers < 1) return OASES_ERR_INVALID_ARG;
-  if (d->kind < 0 || d->kind > 2 || d->dtype < 0 || d->dtype > 1) return OASES_ERR_INVALID_ARG;
+  if (d->kind < 0 || d->kind > 2 || d->dtype < 0 || d->dtype > 2) return OASES_ERR_INVALID_ARG;
   if (d->batch < 0 || d->seq < 0 || d->hidden <= 0 || d->w < 1 || d->sub_batches < 1)
     return OASES_ERR_INVALID_ARG;
   if (d->batch % d->sub_batches != 0) return OASES_ERR_INVALID_ARG;
@@ -146,6 +147,13 @@ oases_status validate(const oases_block_desc* d, int n_layers, Shape* s) {
     if (hd > 128 || hd % 8 != 0) return OASES_ERR_UNSUPPORTED;
   }
   if (d->dtype == OASES_BF16 && (d->hidden % 8 != 0 || (has_ffn && d->ffn % 8 != 0)))
+    return OASES_ERR_UNSUPPORTED;
+  // MX-FP8: scale blocks of 32 along every contraction must not straddle a
+  // shard's slice (so the shard sum of Eq. (1) is the full-width product), and
+  // the shard partials exist only inside the fused GEMMs
+  if (d->dtype == OASES_MXFP8 &&
+      (d->hidden % 32 != 0 || (has_ffn && (d->ffn / d->w) % 32 != 0) ||
+       (has_attn && (d->hidden / d->w) % 32 != 0) || d->reduce != OASES_REDUCE_FUSED))
     return OASES_ERR_UNSUPPORTED;
   const int64_t M = (int64_t)d->batch * d->seq;
   const int64_t widest = has_ffn ? (d->ffn > 3 * d->hidden ? d->ffn : 3 * (int64_t)d->hidden)
@@ -166,6 +174,7 @@ oases_status validate(const oases_block_desc* d, int n_layers, Shape* s) {
   s->mode = d->recompute;
   s->reduce = d->reduce;
   s->t = d->dtype == OASES_F32 ? DType::F32 : DType::BF16;
+  s->mx = d->dtype == OASES_MXFP8;
   s->eps = d->ln_eps;
   s->M = M;
   s->Ms = M / d->sub_batches;
@@ -188,8 +197,13 @@ struct ActSet {  // offsets relative to the workspace base
          red = 0;  // separate-reduction partials, fp32 [w][M][H]
 };
 
+struct MxScratch {  // one sub-batch stream's quantised GEMM operands
+  size_t qa = 0, sfa = 0, qb = 0, sfb = 0;
+};
+
 struct Layout {
   size_t stage[4] = {0, 0, 0, 0};  // x, g, y, dx staging for host buffers
+  MxScratch mx[2];                 // MX-FP8 blocks: per stream
   std::vector<size_t> ckpt;        // input of segment s (s >= 1)
   size_t grad[2] = {0, 0};
   size_t yr = 0;
@@ -284,6 +298,29 @@ Layout make_layout(const Shape& s) {
         made[k] = true;
       }
       L.act[i] = per_kind[k];
+    }
+  }
+  if (s.mx) {
+    // the largest A and B operands (rows x contraction) of any GEMM of the
+    // block, as MX codes (rows padded to 16 bytes) and scale tiles
+    const int64_t Ms = s.Ms, H = s.H, W = std::max<int64_t>(std::max<int64_t>(s.F, 3 * (int64_t)s.H), s.H);
+    auto rup = [](int64_t v) { return (v + 15) / 16 * 16; };
+    const std::pair<int64_t, int64_t> As[] = {{Ms, W}, {W, Ms}, {Ms, H}, {H, Ms}};
+    const std::pair<int64_t, int64_t> Bs[] = {{W, H}, {H, W}, {W, Ms}, {H, Ms}};
+    size_t qa = 0, sfa = 0, qb = 0, sfb = 0;
+    for (auto p : As) {
+      qa = std::max(qa, (size_t)(p.first * rup(p.second)));
+      sfa = std::max(sfa, (size_t)mx_sf_bytes((int)p.first, (int)p.second));
+    }
+    for (auto p : Bs) {
+      qb = std::max(qb, (size_t)(p.first * rup(p.second)));
+      sfb = std::max(sfb, (size_t)mx_sf_bytes((int)p.first, (int)p.second));
+    }
+    for (int k = 0; k < 2; ++k) {
+      L.mx[k].qa = take(qa);
+      L.mx[k].sfa = take(sfa);
+      L.mx[k].qb = take(qb);
+      L.mx[k].sfb = take(sfb);
     }
   }
   L.total = off;
@@ -461,6 +498,39 @@ struct Exec {
     if (b + 1 < s.nsb && st[0] != st[1]) ok(cudaEventRecord(gev(seg, grp), stream(b)));
   }
 
+  // One of the block's GEMMs: bf16 (or fp32) as described, or, for an MX-FP8
+  // block, both operands quantised along the contraction into this stream's
+  // scratch (row-wise for a K-major operand, transposed for an MN-major one)
+  // and multiplied by the block-scaled MMA with the same epilogue.
+  cudaError_t run_gemm(const GemmArgs& g, int b) {
+    if (!s.mx) return gemm(g, stream(b));
+    if (g.M == 0 || g.N == 0) return cudaSuccess;
+    const MxScratch& sc = L.mx[b & 1];
+    const int64_t lqa = (g.K + 15) / 16 * 16, lqb = lqa;
+    uint8_t* qa = at<uint8_t>(sc.qa);
+    uint8_t* qb = at<uint8_t>(sc.qb);
+    uint8_t* sfa = at<uint8_t>(sc.sfa);
+    uint8_t* sfb = at<uint8_t>(sc.sfb);
+    cudaError_t e = g.a_kmajor ? mx_quantize_rows(g.A, g.lda, g.M, g.K, g.in_t, qa, lqa, sfa, stream(b))
+                               : mx_quantize_cols(g.A, g.lda, g.K, g.M, g.in_t, qa, lqa, sfa, stream(b));
+    if (e != cudaSuccess) return e;
+    e = g.b_kmajor ? mx_quantize_rows(g.B, g.ldb, g.N, g.K, g.in_t, qb, lqb, sfb, stream(b))
+                   : mx_quantize_cols(g.B, g.ldb, g.K, g.N, g.in_t, qb, lqb, sfb, stream(b));
+    if (e != cudaSuccess) return e;
+    GemmArgs m = g;
+    m.in_t = DType::E4M3;
+    m.A = qa;
+    m.lda = lqa;
+    m.a_kmajor = true;
+    m.a_sf = sfa;
+    m.B = qb;
+    m.ldb = lqb;
+    m.b_kmajor = true;
+    m.b_sf = sfb;
+    m.aux_t = DType::BF16;
+    return gemm_mx(m, stream(b));
+  }
+
   GemmArgs base_gemm() const {
     GemmArgs g;
     g.in_t = s.t;
@@ -504,7 +574,7 @@ struct Exec {
       g.C = rowp(at(a.h), b, s.F, s.esz);
       g.ldc = s.F;
       g.C2 = keep_grad ? rowp(at(a.a), b, s.F, s.esz) : nullptr;
-      ok(gemm(g, stream(b)));
+      ok(run_gemm(g, b));
     } else {
       g.N = 3 * s.H;
       g.B = p.wc;
@@ -513,7 +583,7 @@ struct Exec {
       g.bias = p.bc;
       g.C = rowp(at(a.qkv), b, 3 * s.H, s.esz);
       g.ldc = 3 * s.H;
-      ok(gemm(g, stream(b)));
+      ok(run_gemm(g, b));
       ok(attention_fwd(attn_args(seg, b), stream(b)));
     }
   }
@@ -561,7 +631,7 @@ struct Exec {
     } else {
       g.epi = Epi::Bias;
     }
-    ok(gemm(g, stream(b)));
+    ok(run_gemm(g, b));
   }
 
   // SEPARATE mode: shard k's partial of sub-batch b, fp32 [Ms, H] rows of [w][M][H].
@@ -654,7 +724,7 @@ struct Exec {
     w.c_t = DType::F32;
     w.ldc = Kin;
     grad_wait(seg, GRP_WR, b);
-    ok(gemm(w, stream(b)));
+    ok(run_gemm(w, b));
     grad_done(seg, GRP_WR, b);
     // d(hin) = dy W_row; FFN: dA = dH * G with G = gelu'(A) kept by the forward or the
     // recompute, written over G.
@@ -678,7 +748,7 @@ struct Exec {
       d.epi = Epi::Store;
       d.C = rowp(at(a.d_o), b, s.H, s.esz);
     }
-    ok(gemm(d, stream(b)));
+    ok(run_gemm(d, b));
   }
 
   void bwd_col(int seg, int b) {
@@ -713,7 +783,7 @@ struct Exec {
     w.c_t = DType::F32;
     w.ldc = s.H;
     grad_wait(seg, GRP_WC, b);
-    ok(gemm(w, stream(b)));
+    ok(run_gemm(w, b));
     grad_done(seg, GRP_WC, b);
   }
 
@@ -739,7 +809,7 @@ struct Exec {
     g.C = rowp(at<float>(a.du), b, s.H, 4);
     g.c_t = DType::F32;
     g.ldc = s.H;
-    ok(gemm(g, stream(b)));
+    ok(run_gemm(g, b));
   }
 
   // SEPARATE mode: du_k = dcol[:, cols of shard k] W_col[rows of shard k, :] in

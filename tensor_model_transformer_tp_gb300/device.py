@@ -14,7 +14,8 @@ from . import (PARAM_NAMES, desc_from_shape, grads_struct, oases_block_fwd,
                oases_block_recompute_bwd, oases_stack_step, oases_workspace_bytes,
                weights_struct)
 
-TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+# storage type per block dtype (MX-FP8 blocks store bf16 and quantise per GEMM)
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "mxfp8": torch.bfloat16}
 
 
 class DeviceBlock:
