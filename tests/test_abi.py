@@ -90,7 +90,8 @@ def test_invalid_descriptors_rejected(L, bad, status):
 
 
 @pytest.mark.parametrize("field,value", [("recompute", 4), ("recompute", -1), ("reduce", 2),
-                                         ("reduce", -1), ("kind", 3), ("dtype", 2)])
+                                         ("reduce", -1), ("kind", 3), ("dtype", 3),
+                                         ("dtype", -1)])
 def test_out_of_range_codes_rejected(L, field, value):
     d = _desc()
     setattr(d, field, value)
@@ -170,3 +171,17 @@ def test_selective_workspace_between_fine_and_none(L):
     assert n["fine"] < n["selective"] < n["none"]
     f = {m: oz.oases_workspace_bytes(_desc(recompute=m), 2) for m in ("none", "selective")}
     assert f["none"] == f["selective"]          # FFN only: nothing to recompute
+
+
+def test_mxfp8_descriptors(L):
+    """MX-FP8 blocks store bf16 and add per-stream scratch for the quantised
+    operands; shapes whose 32-blocks would straddle a shard's slice, and the
+    separate reduction, are refused."""
+    bf = oz.oases_workspace_bytes(_desc(dtype="bf16"))
+    mx = oz.oases_workspace_bytes(_desc(dtype="mxfp8"))
+    assert mx > bf > 0
+    assert oz.oases_workspace_bytes(_desc(dtype="mxfp8", ffn=192)) > 0       # ffn / w = 96
+    assert oz.oases_workspace_bytes(_desc(dtype="mxfp8", ffn=96)) == 0       # ffn / w = 48
+    assert oz.oases_workspace_bytes(_desc(dtype="mxfp8", hidden=48)) == 0    # hidden % 32
+    assert oz.oases_workspace_bytes(_desc(dtype="mxfp8", reduce="separate")) == 0
+    assert _fwd_status(_desc(dtype="mxfp8", ffn=96)) == 2
