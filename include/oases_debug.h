@@ -99,8 +99,8 @@ int oases_debug_trace_read(double *out, int cap);
  * row-parallel bias (added once after the shard sum) gets
  *   out[n] += sum_{m < M} in[m * ld + n],   n < N,
  * (also used for the column-parallel bias with in = dA).  Deterministic:
- * blocks of 8 rows are summed into partial rows in scratch, then the partial
- * rows are added in order.  in: device, type dtype (oases_dtype), leading
+ * blocks of 32 rows are summed into partial rows in scratch, then the partial
+ * rows are added in a fixed order.  in: device, type dtype (oases_dtype), leading
  * dimension ld >= N.  out: device fp32 [N], accumulated.  scratch: device,
  * at least oases_debug_bias_grad_scratch_bytes(M, N) bytes, owned by the
  * caller.  Asynchronous on stream. */
@@ -159,7 +159,7 @@ oases_status oases_debug_shard_sum(const float *part, int64_t pstride, int w, co
  * argument: the partial rows live in a static device array of
  * OASES_NOALLOC_SCRATCH_FLOATS fp32 values (4 MiB) that every GPU which loads
  * the library keeps until the process exits.  Sizes whose partial rows do not
- * fit, ceil(M / 8) * N > OASES_NOALLOC_SCRATCH_FLOATS, are rejected with
+ * fit, ceil(M / 32) * N > OASES_NOALLOC_SCRATCH_FLOATS, are rejected with
  * OASES_ERR_UNSUPPORTED before anything is enqueued (oases_last_error() says
  * how many floats were needed).  Nothing is allocated or freed, by this call
  * or by any library routine it uses.

@@ -14,7 +14,8 @@
 namespace oases {
 namespace {
 
-constexpr int ROWS_PER_PART = 8;  // rows per partial row of a column sum
+constexpr int ROWS_PER_PART = 8;  // rows per partial row of the LayerNorm backward's column sums
+constexpr int COLSUM_ROWS = 32;   // rows per partial row of a bias-gradient column sum
 constexpr int WARPS = 8;
 constexpr int COLS_PER_THREAD = 2;
 constexpr int COL_THREADS = 256;
@@ -58,23 +59,26 @@ ln_fwd_bf16_reg(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __rest
   uint4 v[NV];
 #pragma unroll
   for (int j = 0; j < NV; ++j) v[j] = __ldg(xr + lane + 32 * j);
-  float s = 0.f;
+  // sums in eight independent chains (one per element of a vector), then a tree
+  float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     float f[8];
     bf16x8_to_f32(v[j], f);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s += f[i];
+    for (int i = 0; i < 8; ++i) s8[i] += f[i];
   }
+  const float s = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
   const float mu = warp_sum(s) / H;
-  float q = 0.f;
+  float q8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     float f[8];
     bf16x8_to_f32(v[j], f);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q = fmaf(f[i] - mu, f[i] - mu, q);
+    for (int i = 0; i < 8; ++i) q8[i] = fmaf(f[i] - mu, f[i] - mu, q8[i]);
   }
+  const float q = ((q8[0] + q8[1]) + (q8[2] + q8[3])) + ((q8[4] + q8[5]) + (q8[6] + q8[7]));
   const float rs = rsqrtf(warp_sum(q) / H + eps);
   const uint4* gr = reinterpret_cast<const uint4*>(gamma);
   const uint4* br = reinterpret_cast<const uint4*>(beta);
@@ -353,29 +357,38 @@ ln_bwd_rows(const float* __restrict__ du, const T* __restrict__ x, const float* 
     ag[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     ab[j] = ag[j];
   }
-#pragma unroll 1
-  for (int it = 0; it < ROWS_PER_PART / RB; ++it) {
-    const int par = it & 1;
-    using R = typename Raw4<T>::type;
-    float4 d[RB][NCH];
-    R xv[RB][NCH], rv[RB][NCH];
-    float mu[RB], rs[RB], s1[RB], s2[RB];
+  using R = typename Raw4<T>::type;
+  // the row group's inputs; the next group's loads are issued before this
+  // group's block-wide reduction, so they are in flight while it waits (not
+  // with four chunks per thread: the second set would not fit in registers)
+  constexpr bool PF = NCH < 4;
+  float4 d[RB][NCH], nd[RB][NCH];
+  R xv[RB][NCH], rv[RB][NCH], nxv[RB][NCH], nrv[RB][NCH];
+  float mu[RB], rs[RB], nmu[RB], nrs[RB];
+  auto load_group = [&](int it, float4 (&dd)[RB][NCH], R (&xx)[RB][NCH], R (&rr)[RB][NCH],
+                        float (&mm)[RB], float (&ss)[RB]) {
 #pragma unroll
     for (int i = 0; i < RB; ++i) {
       const int row = m0 + it * RB + i;
       const bool ok = row < M;
-      mu[i] = ok ? mean[row] : 0.f;
-      rs[i] = ok ? rstd[row] : 0.f;
+      mm[i] = ok ? mean[row] : 0.f;
+      ss[i] = ok ? rstd[row] : 0.f;
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         const int c = (tid + LNB_THREADS * j) * 4;
         const int64_t o = (int64_t)row * H + c;
         const bool in = ok && c < H;
-        d[i][j] = in ? ld4(du + o) : make_float4(0.f, 0.f, 0.f, 0.f);
-        xv[i][j] = in ? raw_ld(x + o) : raw_zero<R>();
-        rv[i][j] = (in && dres) ? raw_ld(dres + o) : raw_zero<R>();
+        dd[i][j] = in ? ld4(du + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xx[i][j] = in ? raw_ld(x + o) : raw_zero<R>();
+        rr[i][j] = (in && dres) ? raw_ld(dres + o) : raw_zero<R>();
       }
     }
+  };
+  load_group(0, d, xv, rv, mu, rs);
+#pragma unroll 1
+  for (int it = 0; it < ROWS_PER_PART / RB; ++it) {
+    const int par = it & 1;
+    float s1[RB], s2[RB];
 #pragma unroll
     for (int i = 0; i < RB; ++i) {
       float a = 0.f, b = 0.f;
@@ -399,6 +412,7 @@ ln_bwd_rows(const float* __restrict__ du, const T* __restrict__ x, const float* 
         red[par][warp][2 * i + 1] = s2[i];
       }
     }
+    if (PF && it + 1 < ROWS_PER_PART / RB) load_group(it + 1, nd, nxv, nrv, nmu, nrs);
     __syncthreads();  // (the other parity's slots are free: every thread has passed it)
 #pragma unroll
     for (int i = 0; i < RB; ++i) {
@@ -432,6 +446,21 @@ ln_bwd_rows(const float* __restrict__ du, const T* __restrict__ x, const float* 
         ab[j].z += dd.z;
         ab[j].w += dd.w;
       }
+    }
+    if constexpr (PF) {
+#pragma unroll
+      for (int i = 0; i < RB; ++i) {
+        mu[i] = nmu[i];
+        rs[i] = nrs[i];
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          d[i][j] = nd[i][j];
+          xv[i][j] = nxv[i][j];
+          rv[i][j] = nrv[i][j];
+        }
+      }
+    } else if (it + 1 < ROWS_PER_PART / RB) {
+      load_group(it + 1, d, xv, rv, mu, rs);
     }
   }
 #pragma unroll
@@ -468,28 +497,40 @@ cudaError_t ln_bwd_rows_launch(const float* du, const void* x, const float* mean
   }
 }
 
-// Column sums of a block of ROWS_PER_PART rows, 4 columns per thread (N % 4 == 0).
+// Column sums of a block of COLSUM_ROWS rows: each thread takes the 16 bytes
+// of 16 / sizeof(T) columns (N a multiple of that) and adds the block's rows in
+// order; partial row p covers rows COLSUM_ROWS p .. + COLSUM_ROWS - 1.
 template <typename T>
 __global__ void __launch_bounds__(COL_THREADS)
 colsum_vec_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
-  const int c = (blockIdx.x * COL_THREADS + threadIdx.x) * 4;
+  constexpr int V = 16 / sizeof(T);
+  const int c = (blockIdx.x * COL_THREADS + threadIdx.x) * V;
   if (c >= N) return;
-  // partial row p sums rows 8p .. 8p+7; CTA row y takes p = y, y + gridDim.y, ...
-  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
+  // CTA row y takes the partial rows y, y + gridDim.y, ...
+  const int nb = (M + COLSUM_ROWS - 1) / COLSUM_ROWS;
   for (int p = blockIdx.y; p < nb; p += gridDim.y) {
-    const int m0 = p * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+    const int m0 = p * COLSUM_ROWS, m1 = min(M, m0 + COLSUM_ROWS);
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
     for (int m = m0; m < m1; ++m) {
-      const float4 v = ld4(in + (int64_t)m * ld + c);
-      a.x += v.x;
-      a.y += v.y;
-      a.z += v.z;
-      a.w += v.w;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(in + (int64_t)m * ld + c));
+      if constexpr (sizeof(T) == 2) {
+        float f[8];
+        bf16x8_to_f32(w, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] += f[i];
+      } else {
+        a[0] += __uint_as_float(w.x);
+        a[1] += __uint_as_float(w.y);
+        a[2] += __uint_as_float(w.z);
+        a[3] += __uint_as_float(w.w);
+      }
     }
-    st4(part + (int64_t)p * N + c, a);
+    float* o = part + (int64_t)p * N + c;
+    st4(o, make_float4(a[0], a[1], a[2], a[3]));
+    if constexpr (V == 8) st4(o + 4, make_float4(a[4], a[5], a[6], a[7]));
   }
 }
 
@@ -500,9 +541,9 @@ colsum_part_kernel(const T* __restrict__ in, int64_t ld, int M, int N, float* __
   pdl_trigger();
   const int c0 = (blockIdx.x * COL_THREADS + threadIdx.x) * COLS_PER_THREAD;
   if (c0 >= N) return;
-  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
+  const int nb = (M + COLSUM_ROWS - 1) / COLSUM_ROWS;
   for (int p = blockIdx.y; p < nb; p += gridDim.y) {
-    const int m0 = p * ROWS_PER_PART, m1 = min(M, m0 + ROWS_PER_PART);
+    const int m0 = p * COLSUM_ROWS, m1 = min(M, m0 + COLSUM_ROWS);
     float s[COLS_PER_THREAD] = {};
 #pragma unroll 8
     for (int m = m0; m < m1; ++m) {
@@ -743,7 +784,7 @@ cudaError_t shard_sum(const float* part, int64_t pstride, int w, const void* bia
 }
 
 int ln_bwd_blocks(int M) { return (M + ROWS_PER_PART - 1) / ROWS_PER_PART; }
-int colsum_blocks(int M) { return (M + ROWS_PER_PART - 1) / ROWS_PER_PART; }
+int colsum_blocks(int M) { return (M + COLSUM_ROWS - 1) / COLSUM_ROWS; }
 
 cudaError_t layer_norm_fwd(const void* x, const void* gamma, const void* beta, void* u,
                            float* mean, float* rstd, int M, int H, float eps, DType t,
@@ -821,8 +862,9 @@ cudaError_t colsum_accum(const void* in, int64_t ld, int M, int N, DType t, floa
   const dim3 pgrid((N + COLS_PER_CTA - 1) / COLS_PER_CTA, gy);
   cudaError_t e;
   const size_t esz = t == DType::F32 ? 4 : 2;
-  if (N % 4 == 0 && ld % 4 == 0 && ((uintptr_t)in % (4 * esz)) == 0) {
-    const dim3 vgrid((N + 4 * COL_THREADS - 1) / (4 * COL_THREADS), gy);
+  const int V = 16 / (int)esz;  // columns per thread of the vector kernel
+  if (N % V == 0 && ld % V == 0 && ((uintptr_t)in % 16) == 0) {
+    const dim3 vgrid((N + V * COL_THREADS - 1) / (V * COL_THREADS), gy);
     if (t == DType::F32)
       e = launch_pdl(colsum_vec_kernel<float>, vgrid, dim3(COL_THREADS), 0, st, (const float*)in,
                      ld, M, N, part);

@@ -27,11 +27,12 @@ def L():
     return L
 
 
-# (600000, 4) and (530000, 3): more partial rows of 8 (75000, 66250) than one
+# (2200000, 8) and (2100000, 3): more partial rows of 32 (68750, 65625) than one
 # grid dimension holds (65535), on the vector and the scalar kernel
 @pytest.mark.parametrize("M,N,ld,dtype", [(1, 1, 1, "f32"), (33, 70, 75, "f32"), (2048, 4096, 4096, "bf16"),
                                           (100, 1030, 1030, "bf16"), (0, 16, 16, "bf16"),
-                                          (600000, 4, 4, "bf16"), (530000, 3, 3, "f32")])
+                                          (2200000, 8, 8, "bf16"), (2100000, 3, 3, "f32"),
+                                          (1000, 12, 12, "f32"), (64, 40, 40, "bf16")])
 def test_bias_grad(L, M, N, ld, dtype):
     g = torch.Generator().manual_seed(M + N)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32

@@ -40,7 +40,7 @@ def L():
 
 
 def test_noalloc_matches_scratch_entry_point_twice(L):
-    M, N = 2048, 512           # ceil(2048/8) * 512 = 131072 partial floats
+    M, N = 2048, 512           # ceil(2048/32) * 512 = 32768 partial floats
     gen = torch.Generator().manual_seed(7)
     stream = torch.cuda.current_stream().cuda_stream
     init = torch.randn(N, generator=gen)
@@ -68,9 +68,9 @@ def test_noalloc_matches_scratch_entry_point_twice(L):
 
 
 def test_noalloc_narrow_input_with_many_partial_rows(L):
-    """N = 4 columns, 600000 rows: 75000 partial rows of 8, more than one grid
-    dimension holds (65535), within the static array (300000 floats)."""
-    M, N = 600000, 4
+    """N = 4 columns, 2.2 million rows: 68750 partial rows of 32, more than one
+    grid dimension holds (65535), within the static array (275000 floats)."""
+    M, N = 2200000, 4
     gen = torch.Generator().manual_seed(8)
     xh = torch.randn(M, N, generator=gen).to(torch.bfloat16)
     x = xh.cuda()
@@ -85,7 +85,7 @@ def test_noalloc_narrow_input_with_many_partial_rows(L):
 
 def test_noalloc_rejects_sizes_beyond_the_array(L):
     N = 4096
-    M = 8 * (NOALLOC_FLOATS // N) + 1    # one 8-row partial row too many
+    M = 32 * (NOALLOC_FLOATS // N) + 1    # one 32-row partial row too many
     out = torch.zeros(N, device="cuda")
     x = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
     st = L.oases_bias_grad_noalloc(x.data_ptr(), N, M, N, 1, out.data_ptr(), None)
