@@ -51,7 +51,12 @@ METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300; % of dense BF16 peak"
 # per launch, by workload, with the sha256 of the GEMM sources they were
 # measured on (kernel_source_sha).  Reported only while those sources are
 # unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # the 14 GEMMs of one sub-batch of one layer, each launched twice (28 launches),
+    # profiles/gemm_tc_stack4_h2560_traffic.md
+    "stack4_bf16_h2560": {"source_sha256": "a287ca93fe8a6e1c1032190771ffdede7caab1fafd1d9538ebf736fb38d0ce0c",
+                          "bytes_per_launch": 400300242},
+}
 
 
 GEMM_SOURCES = ("gemm_tc.cu", "common.cuh", "epilogue.cuh", "sm100_ptx.cuh")
