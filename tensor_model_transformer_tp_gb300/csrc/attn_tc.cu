@@ -530,20 +530,38 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, BWD_WAIT));
 }
 
-// dq kernel shared-memory map: Q, dO, four K/V stages of 64 keys (a stage is
-// refilled only after the block's dQ MMA, so the ring must cover the load
-// latency), two dS buffers.
-constexpr int DQ_KST = 4;
+// dq kernel: one CTA per 128 queries, 128-key blocks, 576 threads:
+//   warp 0       TMA loads (Q and dO once, then K_j into a three-stage ring
+//                and V_j into a two-stage ring);
+//   warp 1       TMEM allocation; one thread issues the MMAs;
+//   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
+//                query row each) and columns 32 ((w - 2) / 4) .. + 31 of a block.
+// Per block j:
+//   S_j = Q K_j^T, dP_j = dO V_j^T    N = 128, into TMEM (one buffer each); the
+//                                    element-wise warps load their 32 columns of
+//                                    both and release the buffers at once, so
+//                                    S_{j+1}, dP_{j+1} are computed while they
+//                                    form dS_j = P_j * (dP_j - delta)
+//   dS_j                             packed bf16 into TMEM (64 columns)
+//   dQ += dS_j K_j                   A = dS_j from TMEM, B = K_j (MN-major)
+// MMA issue order: SdP_0, then SdP_j, ACC_{j-1} for j >= 1, then ACC_{n-1}.
+// V_j is released when SdP_j completes, K_j when ACC_j completes: with three
+// K stages and two V stages the loads of the next blocks are never behind the
+// MMAs that wait for them.  Every MMA is 128 x 128 x 16 (one MMA's tensor
+// work, 64 clocks, exceeds its issue cost).
+// TMEM: S 0..127, dP 128..255, dQ 256..383, dS 384..447.
+constexpr int DQ_NT = 576;
+constexpr int DQ_EW = 16;               // element-wise warps, four per lane quarter
+constexpr int DQ_KST = 3, DQ_VST = 2;   // K and V stages of 128 keys
 constexpr int DQ_OFF_Q = 0, DQ_OFF_DO = TILE, DQ_OFF_K = 2 * TILE;
-constexpr int DQ_OFF_V = DQ_OFF_K + DQ_KST * T64, DQ_OFF_DS = DQ_OFF_V + DQ_KST * T64;
-constexpr int DQ_OFF_BAR = DQ_OFF_DS + 2 * PB;
-// q+dO, kv_full[3], kv_empty[3], sdp_full[2], sdp_empty[2], ds_full[2], ds_empty[2], fin
-constexpr int DQ_NBAR = 1 + 2 * DQ_KST + 8 + 1;
+constexpr int DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE, DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE;
+// q+dO, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full, sdp_empty, ds_full, ds_empty, fin
+constexpr int DQ_NBAR = 1 + 2 * DQ_KST + 2 * DQ_VST + 5;
 constexpr int DQ_SMEM = DQ_OFF_BAR + 8 * DQ_NBAR + 16 + 1024;
 static_assert(DQ_SMEM <= 232448, "dq kernel: more than 227 KB of shared memory");
 
-__global__ void __launch_bounds__(BWD_NT, 1)
-attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_constant__ CUtensorMap tq64,
+__global__ void __launch_bounds__(DQ_NT, 1)
+attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
                       const __grid_constant__ CUtensorMap tdo128, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -551,13 +569,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_co
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + DQ_OFF_BAR;
   const uint32_t bar_qdo = bars;
-  auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bars + 8u * (1 + DQ_KST + s); };
-  auto sdp_full = [&](int b) { return bars + 8u * (1 + 2 * DQ_KST + b); };
-  auto sdp_empty = [&](int b) { return bars + 8u * (3 + 2 * DQ_KST + b); };
-  auto ds_full = [&](int b) { return bars + 8u * (5 + 2 * DQ_KST + b); };
-  auto ds_empty = [&](int b) { return bars + 8u * (7 + 2 * DQ_KST + b); };
-  const uint32_t bar_fin = bars + 8u * (9 + 2 * DQ_KST);
+  auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bars + 8u * (1 + DQ_KST + s); };
+  auto v_full = [&](int s) { return bars + 8u * (1 + 2 * DQ_KST + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * DQ_KST + DQ_VST + s); };
+  const uint32_t sdp_full = bars + 8u * (1 + 2 * DQ_KST + 2 * DQ_VST), sdp_empty = sdp_full + 8u;
+  const uint32_t ds_full = sdp_full + 16u, ds_empty = sdp_full + 24u, bar_fin = sdp_full + 32u;
   const uint32_t tslot = bars + 8u * DQ_NBAR;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -565,27 +582,28 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_co
   const int tile = gridDim.z - 1 - blockIdx.z;
   const int h = blockIdx.x, bb = blockIdx.y;
   const int q0 = tile * BQ, row0 = bb * a.S;
-  const int nkv_all = (a.S + BK - 1) / BK;
-  const int n = a.causal ? min(2 * tile + 2, nkv_all) : nkv_all;
+  const int nkv_all = (a.S + BKV - 1) / BKV;
+  const int n = a.causal ? min(tile + 1, nkv_all) : nkv_all;
   const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
   if (tid == 0) tl_cta(1, 0);
 
   if (tid == 0) {
     ptx::mbar_init(bar_qdo, 1);
     for (int s = 0; s < DQ_KST; ++s) {
-      ptx::mbar_init(kv_full(s), 1);
-      ptx::mbar_init(kv_empty(s), 1);
+      ptx::mbar_init(k_full(s), 1);
+      ptx::mbar_init(k_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(sdp_full(b), 1);
-      ptx::mbar_init(sdp_empty(b), 8);
-      ptx::mbar_init(ds_full(b), 8);
-      ptx::mbar_init(ds_empty(b), 1);
+    for (int s = 0; s < DQ_VST; ++s) {
+      ptx::mbar_init(v_full(s), 1);
+      ptx::mbar_init(v_empty(s), 1);
     }
+    ptx::mbar_init(sdp_full, 1);
+    ptx::mbar_init(sdp_empty, DQ_EW);
+    ptx::mbar_init(ds_full, DQ_EW);
+    ptx::mbar_init(ds_empty, 1);
     ptx::mbar_init(bar_fin, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tq128);
-    ptx::prefetch_tmap(&tq64);
     ptx::prefetch_tmap(&tdo128);
   }
   if (warp == 1) {
@@ -596,9 +614,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_co
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
-  auto t_s = [&](int b) { return tmem + (uint32_t)(b * 128); };
-  auto t_dp = [&](int b) { return tmem + (uint32_t)(b * 128 + 64); };
-  const uint32_t t_dq = tmem + 256;
+  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256, t_ds = tmem + 384;
   progress(1, 2);
   pdl_wait();
   pdl_trigger();
@@ -612,64 +628,77 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_co
       ptx::tma_load_2d(base + DQ_OFF_Q + BOX, &tq128, bar_qdo, col_q + 64, row0 + q0);
       ptx::tma_load_2d(base + DQ_OFF_DO, &tdo128, bar_qdo, h * D, row0 + q0);
       ptx::tma_load_2d(base + DQ_OFF_DO + BOX, &tdo128, bar_qdo, h * D + 64, row0 + q0);
-      uint32_t issued = 0, par = 0;
+      int nk = 0, nv = 0;  // blocks whose K, V loads were issued
       for (int j = 0; j < n; ++j) {
-        const int s = j % DQ_KST;
-        if (j >= DQ_KST && !ptx::mbar_wait(kv_empty(s), ((j / DQ_KST) & 1) ^ 1, BWD_WAIT)) {
+        const int sk = j % DQ_KST, sv = j % DQ_VST, r = row0 + j * BKV;
+        if (j >= DQ_KST && !ptx::mbar_wait(k_empty(sk), ((j / DQ_KST) & 1) ^ 1, BWD_WAIT)) {
           ok = false;
           wait_failed(101);
           break;
         }
-        ptx::mbar_arrive_expect_tx(kv_full(s), 2 * T64);
-        const uint32_t kt = base + DQ_OFF_K + s * T64, vt = base + DQ_OFF_V + s * T64;
-        const int r = row0 + j * BK;
-        ptx::tma_load_2d(kt, &tq64, kv_full(s), col_k, r);
-        ptx::tma_load_2d(kt + BOX64, &tq64, kv_full(s), col_k + 64, r);
-        ptx::tma_load_2d(vt, &tq64, kv_full(s), col_v, r);
-        ptx::tma_load_2d(vt + BOX64, &tq64, kv_full(s), col_v + 64, r);
-        issued |= 1u << s;
-        par = (par & ~(1u << s)) | ((uint32_t)((j / DQ_KST) & 1) << s);
+        const uint32_t kt = base + DQ_OFF_K + sk * TILE;
+        ptx::mbar_arrive_expect_tx(k_full(sk), TILE);
+        ptx::tma_load_2d(kt, &tq128, k_full(sk), col_k, r);
+        ptx::tma_load_2d(kt + BOX, &tq128, k_full(sk), col_k + 64, r);
+        nk = j + 1;
+        if (j >= DQ_VST && !ptx::mbar_wait(v_empty(sv), ((j / DQ_VST) & 1) ^ 1, BWD_WAIT)) {
+          ok = false;
+          wait_failed(101);
+          break;
+        }
+        const uint32_t vt = base + DQ_OFF_V + sv * TILE;
+        ptx::mbar_arrive_expect_tx(v_full(sv), TILE);
+        ptx::tma_load_2d(vt, &tq128, v_full(sv), col_v, r);
+        ptx::tma_load_2d(vt + BOX, &tq128, v_full(sv), col_v + 64, r);
+        nv = j + 1;
       }
       // every load issued has landed before the CTA may exit
       bool dr = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
-      for (int s = 0; s < DQ_KST; ++s)
-        if ((issued >> s) & 1u) dr = ptx::mbar_wait(kv_full(s), (par >> s) & 1u, BWD_WAIT) && dr;
+      // (stage s of a ring of R stages last held block s + R ((m - 1 - s) / R)
+      // of the m issued, in round (m - 1 - s) / R)
+      for (int s = 0; s < DQ_KST && s < nk; ++s)
+        dr = ptx::mbar_wait(k_full(s), ((nk - 1 - s) / DQ_KST) & 1, BWD_WAIT) && dr;
+      for (int s = 0; s < DQ_VST && s < nv; ++s)
+        dr = ptx::mbar_wait(v_full(s), ((nv - 1 - s) / DQ_VST) & 1, BWD_WAIT) && dr;
       if (!dr) wait_failed(102);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       ok = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
       if (!ok) wait_failed(103);
-      auto sdp = [&](int j) {  // S_j = Q K_j^T, dP_j = dO V_j^T into TMEM buffer j % 2
-        const int s = j % DQ_KST, b = j & 1;
-        if (!ptx::mbar_wait(kv_full(s), (j / DQ_KST) & 1, BWD_WAIT)) { wait_failed(104); return false; }
-        if (j >= 2 && !ptx::mbar_wait(sdp_empty(b), ((j / 2) & 1) ^ 1, BWD_WAIT)) {
-          wait_failed(105);
+      auto sdp = [&](int j) {  // S_j = Q K_j^T, dP_j = dO V_j^T
+        const int sk = j % DQ_KST, sv = j % DQ_VST;
+        if (!ptx::mbar_wait(k_full(sk), (j / DQ_KST) & 1, BWD_WAIT) ||
+            !ptx::mbar_wait(v_full(sv), (j / DQ_VST) & 1, BWD_WAIT)) {
+          wait_failed(104);
           return false;
         }
+        // the element-wise warps have loaded block j-1's S and dP
+        if (j >= 1 && !ptx::mbar_wait(sdp_empty, (j - 1) & 1, BWD_WAIT)) { wait_failed(105); return false; }
         ptx::tc_fence_after();
-        const uint32_t kt = base + DQ_OFF_K + s * T64, vt = base + DQ_OFF_V + s * T64;
+        const uint32_t kt = base + DQ_OFF_K + sk * TILE, vt = base + DQ_OFF_V + sv * TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16(t_s(b), kmajor_desc(base + DQ_OFF_Q, kk), kmajor64_desc(kt, kk), IDESC_N64, kk > 0);
+          ptx::mma_bf16(t_s, kmajor_desc(base + DQ_OFF_Q, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16(t_dp(b), kmajor_desc(base + DQ_OFF_DO, kk), kmajor64_desc(vt, kk), IDESC_N64, kk > 0);
-        ptx::mma_commit(sdp_full(b));
+          ptx::mma_bf16(t_dp, kmajor_desc(base + DQ_OFF_DO, kk), kmajor_desc(vt, kk), IDESC_S, kk > 0);
+        ptx::mma_commit(sdp_full);
+        ptx::mma_commit(v_empty(sv));
         tl_block(1, j, 0);
         return true;
       };
-      auto acc = [&](int j) {  // dQ += dS_j K_j
-        const int s = j % DQ_KST, b = j & 1;
-        if (!ptx::mbar_wait(ds_full(b), (j / 2) & 1, BWD_WAIT)) { wait_failed(106); return false; }
+      auto acc = [&](int j) {  // dQ += dS_j K_j (contraction over the block's 128 keys)
+        const int sk = j % DQ_KST;
+        if (!ptx::mbar_wait(ds_full, j & 1, BWD_WAIT)) { wait_failed(106); return false; }
         ptx::tc_fence_after();
-        const uint32_t kt = base + DQ_OFF_K + s * T64;
+        const uint32_t kt = base + DQ_OFF_K + sk * TILE;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          ptx::mma_bf16(t_dq, kmajor_blk_desc(base + DQ_OFF_DS + b * PB, kk), mnmajor64_desc(kt, kk),
-                        IDESC_ACC, (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(ds_empty(b));
-        ptx::mma_commit(kv_empty(s));
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          ptx::mma_bf16_ts(t_dq, t_ds + 8u * kk, mnmajor_desc(kt, kk), IDESC_PV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(ds_empty);
+        ptx::mma_commit(k_empty(sk));
         tl_block(1, j, 1);
         return true;
       };
@@ -680,34 +709,33 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_co
       if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(107); }
     }
   } else {
-    const int qq = warp & 3, half = (warp - 2) >> 2;
+    const int qq = warp & 3, sub = (warp - 2) >> 2;  // lane quarter; columns 32 sub .. + 31
     const int row = qq * 32 + lane, qi = q0 + row;
     const bool valid_q = qi < a.S;
     const float lse2 = valid_q ? a.lse[(int64_t)h * a.M + row0 + qi] * 1.4426950408889634f : 0.f;
     const float dlt = valid_q ? a.delta[(int64_t)h * a.M + row0 + qi] : 0.f;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     for (int j = 0; j < n && ok; ++j) {
-      const int b = j & 1;
-      if (!warp_wait(sdp_full(b), (j / 2) & 1)) { ok = false; if (lane == 0) wait_failed(108); break; }
+      if (!warp_wait(sdp_full, j & 1)) { ok = false; if (lane == 0) wait_failed(108); break; }
       if (warp == 2 && lane == 0) tl_block(1, j, 2);
       ptx::tc_fence_after();
       float v[32], w[32];
-      ptx::tmem_ld32x2(t_s(b) + lane_off + half * 32, t_dp(b) + lane_off + half * 32, v, w);
+      ptx::tmem_ld32x2(t_s + lane_off + sub * 32, t_dp + lane_off + sub * 32, v, w);
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sdp_empty(b));  // the TMEM buffer may be overwritten
-      const int kbase = j * BK + half * 32;
+      if (lane == 0) ptx::mbar_arrive(sdp_empty);  // the TMEM buffers may be overwritten
+      const int kbase = j * BKV + sub * 32;
       // a block wholly visible to every row of the tile needs no mask (CTA-uniform)
-      const bool full = q0 + BQ <= a.S && (j + 1) * BK <= a.S && (!a.causal || (j + 1) * BK <= q0 + 1);
+      const bool full = q0 + BQ <= a.S && (j + 1) * BKV <= a.S && (!a.causal || (j + 1) * BKV <= q0 + 1);
+      uint32_t pk[16];  // dS as packed bf16 pairs (keys 2i, 2i+1 of these 32)
       if (full) {
         const uint64_t sc = f2_splat(a.scale_log2), nl = f2_splat(-lse2), nd = f2_splat(-dlt);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const uint64_t x = f2_fma(f2_pack(v[i], v[i + 1]), sc, nl);
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), sc, nl);
           const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
-          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[i], w[i + 1]), nd));
-          v[i] = f2_lo(ds);
-          v[i + 1] = f2_hi(ds);
+          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[2 * i], w[2 * i + 1]), nd));
+          pk[i] = pack2(f2_lo(ds), f2_hi(ds));
         }
       } else {
 #pragma unroll
@@ -717,37 +745,36 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128, const __grid_co
           const float p = valid ? fast_exp2(v[i] * a.scale_log2 - lse2) : 0.f;
           v[i] = p * (w[i] - dlt);
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack2(v[2 * i], v[2 * i + 1]);
       }
-      if (j >= 2 && !warp_wait(ds_empty(b), ((j / 2) & 1) ^ 1)) {
+      // the dS columns are free once the previous block's dQ MMAs are done
+      if (j >= 1 && !warp_wait(ds_empty, (j - 1) & 1)) {
         ok = false;
         if (lane == 0) wait_failed(109);
         break;
       }
-      store_row_half(gbase + DQ_OFF_DS + b * PB, row, half, v);
-      ptx::fence_async_smem();
+      ptx::tc_fence_after();
+      ptx::tmem_st16_nowait(t_ds + lane_off + sub * 16, pk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ds_full(b));
+      if (lane == 0) ptx::mbar_arrive(ds_full);
       if (warp == 2 && lane == 0) tl_block(1, j, 3);
     }
     // the last accumulation is complete (or the MMA thread gave up)
     const bool fin = warp_wait(bar_fin, 0);
     ptx::tc_fence_after();
-    float v0[32], v1[32];  // tcgen05.ld is warp-collective: every lane loads
-    ptx::tmem_ld32(t_dq + lane_off + half * 64, v0);
-    ptx::tmem_ld32(t_dq + lane_off + half * 64 + 32, v1);
+    float v0[32];  // tcgen05.ld is warp-collective: every lane loads
+    ptx::tmem_ld32(t_dq + lane_off + sub * 32, v0);
     if (ok && fin && valid_q) {
-      uint4* out = reinterpret_cast<uint4*>(a.dqkv + (int64_t)(row0 + qi) * 3 * a.H + h * D + half * 64);
+      uint4* out = reinterpret_cast<uint4*>(a.dqkv + (int64_t)(row0 + qi) * 3 * a.H + h * D + sub * 32);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 4; ++u)
         out[u] = make_uint4(pack2(v0[8 * u] * a.scale, v0[8 * u + 1] * a.scale),
                             pack2(v0[8 * u + 2] * a.scale, v0[8 * u + 3] * a.scale),
                             pack2(v0[8 * u + 4] * a.scale, v0[8 * u + 5] * a.scale),
                             pack2(v0[8 * u + 6] * a.scale, v0[8 * u + 7] * a.scale));
-        out[4 + u] = make_uint4(pack2(v1[8 * u] * a.scale, v1[8 * u + 1] * a.scale),
-                                pack2(v1[8 * u + 2] * a.scale, v1[8 * u + 3] * a.scale),
-                                pack2(v1[8 * u + 4] * a.scale, v1[8 * u + 5] * a.scale),
-                                pack2(v1[8 * u + 6] * a.scale, v1[8 * u + 7] * a.scale));
-      }
     }
     if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 3);
   }
@@ -1133,8 +1160,8 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   ba.scale_log2 = 1.4426950408889634f * ba.scale;
   const int tiles = (a.seq + 127) / 128;
   if (tiles > 65535) return cudaErrorInvalidConfiguration;
-  e = launch_pdl(attn_bwd_dq_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(BWD_NT), DQ_SMEM, st,
-                 tq128, tq64, tdo128, ba);
+  e = launch_pdl(attn_bwd_dq_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(DQ_NT), DQ_SMEM, st,
+                 tq128, tdo128, ba);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(BWD_NT), KV_SMEM,
                     st, tq128, tq64, tdo64, ba);
