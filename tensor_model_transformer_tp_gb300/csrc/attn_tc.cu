@@ -479,28 +479,19 @@ struct BwdArgs {
   float scale;       // 1 / sqrt(d)
 };
 
-// Both backward kernels are warp-specialised pipelines over blocks of 64
-// keys (dq kernel) or 64 queries (dkv kernel), 320 threads:
-//   warp 0      TMA loads (a ring of operand stages);
-//   warp 1      TMEM allocation; one thread issues the MMAs;
-//   warps 2..9  element-wise work: warp w owns TMEM lanes 32 (w % 4) .. + 31
-//               (one row each) and half (w - 2) / 4 of the block's 64 columns.
-// S and dP of a block land in one of two TMEM buffers, dS (and P) in one of
-// two shared-memory buffers, so while the element-wise warps turn block j into
-// dS the tensor core computes S, dP of block j + 1 and the accumulation of
-// block j - 1.  MMA issue order: SdP_0, then SdP_j, ACC_{j-1} for j >= 1,
-// then ACC_{n-1}.
-constexpr int BWD_NT = 320;
+// Both backward kernels are warp-specialised pipelines: one warp issues the
+// TMA loads, one thread the MMAs, sixteen warps do the element-wise work
+// between them (their layouts are described at each kernel).
 constexpr int BK = 64;                  // keys or queries per block
 constexpr int BOX64 = 64 * 64 * 2;      // one TMA box: 64 rows x 64 bf16 (8 KB)
 constexpr int T64 = 2 * BOX64;          // 64 rows x 128 dims (16 KB)
 constexpr int PB = 128 * 64 * 2;        // 128 rows x 64 bf16, one box width (16 KB)
 constexpr uint64_t BWD_WAIT = 1ull << 29;  // cycles before a wait gives up (~0.25 s)
-// S = Q K_j^T and dP = dO V_j^T (dq), S^T = K Q_i^T and dP^T = V dO_i^T (dkv):
-// M = 128 rows, N = 64 block columns, both operands K-major over d.
+// S^T = K Q_i^T and dP^T = V dO_i^T (dkv): M = 128 keys, N = 64 queries,
+// both operands K-major over d.
 constexpr uint32_t IDESC_N64 = ptx::idesc_bf16_f32(128, BK, false, false);
-// dQ += dS K_j, dV += P^T dO_i, dK += dS^T Q_i: M = 128, N = 128 dims, A
-// K-major over the 64 block columns, B MN-major.
+// dV += P^T dO_i, dK += dS^T Q_i (dkv): M = 128 keys, N = 128 dims, A K-major
+// over the 64 queries of the block, B MN-major.
 constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(128, D, false, true);
 
 // [64 rows][128 cols] K-major tile stored as two 64-column boxes, k-step kk of 8.
@@ -514,16 +505,6 @@ __device__ __forceinline__ uint64_t mnmajor64_desc(uint32_t tile, int kk) {
 // [128 rows][64 cols] K-major buffer (one box width), k-step kk of 4.
 __device__ __forceinline__ uint64_t kmajor_blk_desc(uint32_t buf, int kk) {
   return desc_step(ptx::smem_desc_sw128(buf, 16, 1024), kk * 32);
-}
-// Writes this thread's 32 values (columns 32 half .. + 31 of its row) as bf16
-// into a [128 rows][64 cols] 128-byte-swizzled buffer.
-__device__ __forceinline__ void store_row_half(uint8_t* buf, int row, int half, const float (&v)[32]) {
-  uint8_t* r = buf + row * 128;
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-    *reinterpret_cast<uint4*>(r + (((half * 4 + u) ^ (row & 7)) << 4)) =
-        make_uint4(pack2(v[8 * u], v[8 * u + 1]), pack2(v[8 * u + 2], v[8 * u + 3]),
-                   pack2(v[8 * u + 4], v[8 * u + 5]), pack2(v[8 * u + 6], v[8 * u + 7]));
 }
 // Warp-uniform bounded wait (every lane waits; the warp agrees on the outcome).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
@@ -789,21 +770,45 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
   if (tid == 0) tl_cta(1, 1);
 }
 
-// dkv kernel shared-memory map: K, V of the CTA's 128 keys, three Q/dO stages
-// of 64 queries with their LSE (log2 units) and delta, two P^T and two dS^T
-// buffers.
-constexpr int KV_QST = 3;
+// dkv kernel: one CTA per 128 keys, 64-query blocks, 576 threads:
+//   warp 0       TMA loads (K and V once, then Q_i and dO_i into a four-stage ring);
+//   warp 1       TMEM allocation; one thread issues the MMAs;
+//   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
+//                key row each) and columns 16 ((w - 2) / 4) .. + 15 of a block.
+// Per query block i:
+//   S^T = K Q_i^T, dP^T = V dO_i^T     N = 64, into one of two TMEM buffers
+//   P^T = exp2(S^T scale - LSE), dS^T = P^T (dP^T - delta)
+//                                     (LSE and delta of the block's queries are
+//                                     read by each warp from global memory one
+//                                     block ahead and shared by lane shuffles),
+//                                     bf16 into one shared-memory buffer each
+//   dV += P^T dO_i, dK += dS^T Q_i     N = 128 (d), contraction over the 64 queries
+// MMA issue order: SdP_0, then SdP_i, ACC_{i-1} for i >= 1, then ACC_{n-1}.
+// The element-wise warps write block i's P^T and dS^T once the MMAs of
+// block i-1's accumulation are done; they are still computing when those
+// MMAs end, so one buffer each suffices and the shared memory goes to a
+// fourth Q/dO stage, which keeps the loads ahead of the MMAs that wait for them.
+constexpr int KV_NT = 576;
+constexpr int KV_EW = 16;               // element-wise warps, four per lane quarter
+constexpr int KV_QST = 4;               // Q/dO stages of 64 queries
 constexpr int KV_OFF_K = 0, KV_OFF_V = TILE, KV_OFF_Q = 2 * TILE;
 constexpr int KV_OFF_DO = KV_OFF_Q + KV_QST * T64;
-constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + 2 * PB;
-constexpr int KV_OFF_STAT = KV_OFF_DST + 2 * PB;  // [stage][lse2[64] | delta[64]] fp32
-constexpr int KV_OFF_BAR = KV_OFF_STAT + KV_QST * 2 * BK * 4;
-// kv, q_full[2], q_empty[2], sdp_full[2], sdp_empty[2], pd_full[2], pd_empty[2], fin
-constexpr int KV_NBAR = 1 + 2 * KV_QST + 8 + 1;
+constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + PB;
+constexpr int KV_OFF_BAR = KV_OFF_DST + PB;
+// kv, q_full[4], q_empty[4], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin
+constexpr int KV_NBAR = 1 + 2 * KV_QST + 4 + 3;
 constexpr int KV_SMEM = KV_OFF_BAR + 8 * KV_NBAR + 16 + 1024;
 static_assert(KV_SMEM <= 232448, "dkv kernel: more than 227 KB of shared memory");
 
-__global__ void __launch_bounds__(BWD_NT, 1)
+// Writes 8 words of packed bf16 pairs (16 values: columns 16 c .. + 15 of this
+// thread's row) into a [128 rows][64 cols] 128-byte-swizzled buffer.
+__device__ __forceinline__ void store_row_quarter(uint8_t* buf, int row, int c, const uint32_t (&w)[8]) {
+  uint8_t* r = buf + row * 128;
+  *reinterpret_cast<uint4*>(r + (((2 * c) ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(r + (((2 * c + 1) ^ (row & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__global__ void __launch_bounds__(KV_NT, 1)
 attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
                        const __grid_constant__ CUtensorMap tdo64, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -816,11 +821,8 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   auto q_empty = [&](int s) { return bars + 8u * (1 + KV_QST + s); };
   auto sdp_full = [&](int b) { return bars + 8u * (1 + 2 * KV_QST + b); };
   auto sdp_empty = [&](int b) { return bars + 8u * (3 + 2 * KV_QST + b); };
-  auto pd_full = [&](int b) { return bars + 8u * (5 + 2 * KV_QST + b); };
-  auto pd_empty = [&](int b) { return bars + 8u * (7 + 2 * KV_QST + b); };
-  const uint32_t bar_fin = bars + 8u * (9 + 2 * KV_QST);
+  const uint32_t pd_full = bars + 8u * (5 + 2 * KV_QST), pd_empty = pd_full + 8u, bar_fin = pd_full + 16u;
   const uint32_t tslot = bars + 8u * KV_NBAR;
-  float* stat = reinterpret_cast<float*>(gbase + KV_OFF_STAT);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   // grid (heads, batch, tiles): key tile 0 (the most query blocks) first
@@ -840,10 +842,10 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(sdp_full(b), 1);
-      ptx::mbar_init(sdp_empty(b), 8);
-      ptx::mbar_init(pd_full(b), 8);
-      ptx::mbar_init(pd_empty(b), 1);
+      ptx::mbar_init(sdp_empty(b), KV_EW);
     }
+    ptx::mbar_init(pd_full, KV_EW);
+    ptx::mbar_init(pd_empty, 1);
     ptx::mbar_init(bar_fin, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tkv);
@@ -868,46 +870,34 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   bool ok = true;
 
   if (warp == 0) {
-    uint32_t issued = 0, par = 0;
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(bar_kv, 2 * TILE);
       ptx::tma_load_2d(base + KV_OFF_K, &tkv, bar_kv, col_k, row0 + k0);
       ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, bar_kv, col_k + 64, row0 + k0);
       ptx::tma_load_2d(base + KV_OFF_V, &tkv, bar_kv, col_v, row0 + k0);
       ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, bar_kv, col_v + 64, row0 + k0);
-    }
-    for (int ii = 0; ii < n; ++ii) {
-      const int s = ii % KV_QST, i = i0 + ii;
-      if (ii >= KV_QST && !warp_wait(q_empty(s), ((ii / KV_QST) & 1) ^ 1)) {
-        ok = false;
-        if (lane == 0) wait_failed(201);
-        break;
-      }
-      // the block's LSE (log2 units) and delta, written by the whole warp
-      float* st = stat + s * 2 * BK;
-      for (int t = lane; t < BK; t += 32) {
-        const int q = i * BK + t;
-        const bool vq = q < a.S;
-        st[t] = vq ? a.lse[(int64_t)h * a.M + row0 + q] * 1.4426950408889634f : 0.f;
-        st[BK + t] = vq ? a.delta[(int64_t)h * a.M + row0 + q] : 0.f;
-      }
-      __syncwarp();  // the warp's stores precede lane 0's arrive on the stage barrier
-      if (lane == 0) {
+      int nl = 0;  // query blocks whose loads were issued
+      for (int ii = 0; ii < n; ++ii) {
+        const int s = ii % KV_QST;
+        if (ii >= KV_QST && !ptx::mbar_wait(q_empty(s), ((ii / KV_QST) & 1) ^ 1, BWD_WAIT)) {
+          ok = false;
+          wait_failed(201);
+          break;
+        }
         ptx::mbar_arrive_expect_tx(q_full(s), 2 * T64);
         const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
-        const int r = row0 + i * BK;
+        const int r = row0 + (i0 + ii) * BK;
         ptx::tma_load_2d(qt, &tq64, q_full(s), col_q, r);
         ptx::tma_load_2d(qt + BOX64, &tq64, q_full(s), col_q + 64, r);
         ptx::tma_load_2d(dt, &tdo64, q_full(s), h * D, r);
         ptx::tma_load_2d(dt + BOX64, &tdo64, q_full(s), h * D + 64, r);
-        issued |= 1u << s;
-        par = (par & ~(1u << s)) | ((uint32_t)((ii / KV_QST) & 1) << s);
+        nl = ii + 1;
       }
-    }
-    if (lane == 0) {
+      // every load issued has landed before the CTA may exit (stage s last
+      // held block s + R ((m - 1 - s) / R) of the m issued)
       bool dr = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
-      for (int s = 0; s < KV_QST; ++s)
-        if ((issued >> s) & 1u) dr = ptx::mbar_wait(q_full(s), (par >> s) & 1u, BWD_WAIT) && dr;
+      for (int s = 0; s < KV_QST && s < nl; ++s)
+        dr = ptx::mbar_wait(q_full(s), ((nl - 1 - s) / KV_QST) & 1, BWD_WAIT) && dr;
       if (!dr) wait_failed(202);
     }
   } else if (warp == 1) {
@@ -917,6 +907,7 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
       auto sdp = [&](int ii) {  // S^T = K Q_i^T, dP^T = V dO_i^T into TMEM buffer ii % 2
         const int s = ii % KV_QST, b = ii & 1;
         if (!ptx::mbar_wait(q_full(s), (ii / KV_QST) & 1, BWD_WAIT)) { wait_failed(204); return false; }
+        // the element-wise warps have loaded block ii-2 from this buffer
         if (ii >= 2 && !ptx::mbar_wait(sdp_empty(b), ((ii / 2) & 1) ^ 1, BWD_WAIT)) {
           wait_failed(205);
           return false;
@@ -934,19 +925,17 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
         return true;
       };
       auto acc = [&](int ii) {  // dV += P^T dO_i, dK += dS^T Q_i
-        const int s = ii % KV_QST, b = ii & 1;
-        if (!ptx::mbar_wait(pd_full(b), (ii / 2) & 1, BWD_WAIT)) { wait_failed(206); return false; }
+        const int s = ii % KV_QST;
+        if (!ptx::mbar_wait(pd_full, ii & 1, BWD_WAIT)) { wait_failed(206); return false; }
         ptx::tc_fence_after();
         const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint32_t accum = (ii > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT + b * PB, kk), mnmajor64_desc(dt, kk),
-                        IDESC_ACC, accum);
-          ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST + b * PB, kk), mnmajor64_desc(qt, kk),
-                        IDESC_ACC, accum);
+          ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT, kk), mnmajor64_desc(dt, kk), IDESC_ACC, accum);
+          ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST, kk), mnmajor64_desc(qt, kk), IDESC_ACC, accum);
         }
-        ptx::mma_commit(pd_empty(b));
+        ptx::mma_commit(pd_empty);
         ptx::mma_commit(q_empty(s));
         tl_block(2, ii, 1);
         return true;
@@ -958,63 +947,79 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
       if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(207); }
     }
   } else {
-    const int qq = warp & 3, half = (warp - 2) >> 2;
+    const int qq = warp & 3, c = (warp - 2) >> 2;  // lane quarter; columns 16 c .. + 15
     const int row = qq * 32 + lane, kj = k0 + row;
     const bool valid_k = kj < a.S;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    // lane l holds, for query 16 c + (l % 16) of a block, LSE in log2 units
+    // (l < 16) or delta (l >= 16); loaded one block ahead
+    auto stat = [&](int ii) {
+      const int q = (i0 + ii) * BK + c * 16 + (lane & 15);
+      if (ii >= n || q >= a.S) return 0.f;
+      const int64_t at = (int64_t)h * a.M + row0 + q;
+      return lane < 16 ? a.lse[at] * 1.4426950408889634f : a.delta[at];
+    };
+    float nxt = stat(0);
     for (int ii = 0; ii < n && ok; ++ii) {
-      const int s = ii % KV_QST, b = ii & 1, i = i0 + ii;
-      // this block's S^T, dP^T are in TMEM (which also means its stage has landed)
-      if (!warp_wait(sdp_full(b), (ii / 2) & 1) || !warp_wait(q_full(s), (ii / KV_QST) & 1)) {
+      const int b = ii & 1, i = i0 + ii;
+      // this block's S^T, dP^T are in TMEM
+      if (!warp_wait(sdp_full(b), (ii / 2) & 1)) {
         ok = false;
         if (lane == 0) wait_failed(208);
         break;
       }
       if (warp == 2 && lane == 0) tl_block(2, ii, 2);
       ptx::tc_fence_after();
-      float v[32], w[32];
-      ptx::tmem_ld32x2(t_st(b) + lane_off + half * 32, t_dpt(b) + lane_off + half * 32, v, w);
+      float v[16], w[16];
+      ptx::tmem_ld16x2(t_st(b) + lane_off + c * 16, t_dpt(b) + lane_off + c * 16, v, w);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
-      const float* st = stat + s * 2 * BK + half * 32;
-      const int qbase = i * BK + half * 32;
+      const float cur = nxt;
+      nxt = stat(ii + 1);
+      uint32_t pp[8], pd[8];
       // a query block that sees every key of the tile needs no mask (CTA-uniform)
       const bool full = k0 + 128 <= a.S && (i + 1) * BK <= a.S && (!a.causal || i * BK >= k0 + 127);
       if (full) {
         const uint64_t sc = f2_splat(a.scale_log2);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 l2 = *reinterpret_cast<const float2*>(st + c);       // LSE (log2 units)
-          const float2 dl = *reinterpret_cast<const float2*>(st + BK + c);  // delta
-          const uint64_t x = f2_fma(f2_pack(v[c], v[c + 1]), sc, f2_pack(-l2.x, -l2.y));
+        for (int k = 0; k < 16; k += 2) {
+          const float l0 = __shfl_sync(0xffffffffu, cur, k), l1 = __shfl_sync(0xffffffffu, cur, k + 1);
+          const float d0 = __shfl_sync(0xffffffffu, cur, 16 + k), d1 = __shfl_sync(0xffffffffu, cur, 17 + k);
+          const uint64_t x = f2_fma(f2_pack(v[k], v[k + 1]), sc, f2_pack(-l0, -l1));
           const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
-          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[c], w[c + 1]), f2_pack(-dl.x, -dl.y)));
-          v[c] = f2_lo(p);
-          v[c + 1] = f2_hi(p);
-          w[c] = f2_lo(ds);
-          w[c + 1] = f2_hi(ds);
+          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[k], w[k + 1]), f2_pack(-d0, -d1)));
+          pp[k / 2] = pack2(f2_lo(p), f2_hi(p));
+          pd[k / 2] = pack2(f2_lo(ds), f2_hi(ds));
         }
       } else {
+        const int qbase = i * BK + c * 16;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int q = qbase + c;
+        for (int k = 0; k < 16; ++k) {
+          const float l2 = __shfl_sync(0xffffffffu, cur, k), dl = __shfl_sync(0xffffffffu, cur, 16 + k);
+          const int q = qbase + k;
           const bool valid = valid_k && q < a.S && (!a.causal || kj <= q);
-          const float p = valid ? fast_exp2(v[c] * a.scale_log2 - st[c]) : 0.f;
-          v[c] = p;
-          w[c] = p * (w[c] - st[BK + c]);
+          const float p = valid ? fast_exp2(v[k] * a.scale_log2 - l2) : 0.f;
+          v[k] = p;
+          w[k] = p * (w[k] - dl);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          pp[k] = pack2(v[2 * k], v[2 * k + 1]);
+          pd[k] = pack2(w[2 * k], w[2 * k + 1]);
         }
       }
-      if (ii >= 2 && !warp_wait(pd_empty(b), ((ii / 2) & 1) ^ 1)) {
+      // the P^T / dS^T buffers are free once block ii-1's accumulation is done
+      if (ii >= 1 && !warp_wait(pd_empty, (ii - 1) & 1)) {
         ok = false;
         if (lane == 0) wait_failed(209);
         break;
       }
-      store_row_half(gbase + KV_OFF_PT + b * PB, row, half, v);
-      store_row_half(gbase + KV_OFF_DST + b * PB, row, half, w);
+      store_row_quarter(gbase + KV_OFF_PT, row, c, pp);
+      store_row_quarter(gbase + KV_OFF_DST, row, c, pd);
       ptx::fence_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(pd_full(b));
+      if (lane == 0) ptx::mbar_arrive(pd_full);
       if (warp == 2 && lane == 0) tl_block(2, ii, 3);
     }
     const bool fin = warp_wait(bar_fin, 0);
@@ -1022,20 +1027,15 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
     __nv_bfloat16* rowp = a.dqkv + (int64_t)(row0 + kj) * 3 * a.H;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {  // dK (scaled), then dV
-      float v0[32], v1[32];  // tcgen05.ld is warp-collective: every lane loads
-      const uint32_t t = (part == 0 ? t_dk : t_dv) + lane_off + half * 64;
-      ptx::tmem_ld32(t, v0);
-      ptx::tmem_ld32(t + 32, v1);
+      float v0[32];  // tcgen05.ld is warp-collective: every lane loads
+      ptx::tmem_ld32((part == 0 ? t_dk : t_dv) + lane_off + c * 32, v0);
       const float sc = part == 0 ? a.scale : 1.f;
       if (ok && fin && valid_k) {
-        uint4* out = reinterpret_cast<uint4*>(rowp + (part == 0 ? a.H : 2 * a.H) + h * D + half * 64);
+        uint4* out = reinterpret_cast<uint4*>(rowp + (part == 0 ? a.H : 2 * a.H) + h * D + c * 32);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 4; ++u)
           out[u] = make_uint4(pack2(v0[8 * u] * sc, v0[8 * u + 1] * sc), pack2(v0[8 * u + 2] * sc, v0[8 * u + 3] * sc),
                               pack2(v0[8 * u + 4] * sc, v0[8 * u + 5] * sc), pack2(v0[8 * u + 6] * sc, v0[8 * u + 7] * sc));
-          out[4 + u] = make_uint4(pack2(v1[8 * u] * sc, v1[8 * u + 1] * sc), pack2(v1[8 * u + 2] * sc, v1[8 * u + 3] * sc),
-                                  pack2(v1[8 * u + 4] * sc, v1[8 * u + 5] * sc), pack2(v1[8 * u + 6] * sc, v1[8 * u + 7] * sc));
-        }
       }
     }
     if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 5);
@@ -1163,7 +1163,7 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   e = launch_pdl(attn_bwd_dq_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(DQ_NT), DQ_SMEM, st,
                  tq128, tdo128, ba);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(BWD_NT), KV_SMEM,
+  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(KV_NT), KV_SMEM,
                     st, tq128, tq64, tdo64, ba);
 }
 
