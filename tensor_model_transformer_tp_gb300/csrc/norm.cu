@@ -36,6 +36,20 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
     f[2 * i + 1] = t.y;
   }
 }
+// The same unpacking as opaque instructions, so that the compiler converts the
+// packed row again in each pass instead of keeping every element live as fp32
+// (which needs twice the registers and halves the resident warps).
+__device__ __forceinline__ void bf16x8_to_f32_each_pass(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo, hi;
+    asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w[i]));
+    asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w[i]));
+    f[2 * i] = __uint_as_float(lo);
+    f[2 * i + 1] = __uint_as_float(hi);
+  }
+}
 __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
   uint4 u;
   __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
@@ -47,7 +61,7 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
 // ---- LayerNorm forward -------------------------------------------------------
 // bf16, H = 256 * NV: lane j holds 16-byte vectors j, j+32, ... of its row.
 template <int NV>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, NV <= 8 ? 4 : (NV <= 12 ? 3 : 2))
 ln_fwd_bf16_reg(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
                 const __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ u,
                 float* __restrict__ mean, float* __restrict__ rstd, int M, int H, float eps) {
@@ -64,7 +78,7 @@ ln_fwd_bf16_reg(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __rest
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     float f[8];
-    bf16x8_to_f32(v[j], f);
+    bf16x8_to_f32_each_pass(v[j], f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) s8[i] += f[i];
   }
@@ -74,7 +88,7 @@ ln_fwd_bf16_reg(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __rest
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     float f[8];
-    bf16x8_to_f32(v[j], f);
+    bf16x8_to_f32_each_pass(v[j], f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) q8[i] = fmaf(f[i] - mu, f[i] - mu, q8[i]);
   }
@@ -86,7 +100,7 @@ ln_fwd_bf16_reg(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __rest
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     float f[8], g[8], b[8];
-    bf16x8_to_f32(v[j], f);
+    bf16x8_to_f32_each_pass(v[j], f);
     bf16x8_to_f32(__ldg(gr + lane + 32 * j), g);
     bf16x8_to_f32(__ldg(br + lane + 32 * j), b);
 #pragma unroll
