@@ -36,6 +36,7 @@
 #include "oases.h"
 
 namespace oases {
+int norm_read_and_clear_error();  // norm.cu: a LayerNorm kernel's wait gave up
 thread_local int g_launch_count = 0;
 
 uint64_t current_ctx_id() {
@@ -1271,9 +1272,10 @@ oases_status oases_shutdown(void) {
 oases_status oases_check_device(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
-  const int v = gemm_read_and_clear_error(), w = attention_read_and_clear_error();
-  if (v < 0 || w < 0) return cuda_fail(cudaGetLastError());
-  return (v || w) ? OASES_ERR_TIMEOUT : OASES_OK;
+  const int v = gemm_read_and_clear_error(), w = attention_read_and_clear_error(),
+            u = norm_read_and_clear_error();
+  if (v < 0 || w < 0 || u < 0) return cuda_fail(cudaGetLastError());
+  return (v || w || u) ? OASES_ERR_TIMEOUT : OASES_OK;
 }
 
 }  // extern "C"

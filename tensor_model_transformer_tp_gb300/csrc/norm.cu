@@ -10,8 +10,13 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace oases {
+
+// Set by a norm kernel whose bounded wait gave up; read by oases_check_device.
+__device__ int g_norm_error;
+
 namespace {
 
 constexpr int ROWS_PER_PART = 8;  // rows per partial row of the LayerNorm backward's column sums
@@ -487,10 +492,214 @@ ln_bwd_rows(const float* __restrict__ du, const T* __restrict__ x, const float* 
   }
 }
 
+// The same computation with each row's inputs (du, x, dres) staged through a
+// ring of LNS_STAGES shared-memory buffers by bulk copies (cp.async.bulk, one
+// per row and tensor, completion on the stage's mbarrier), so that several
+// rows per CTA are in flight without holding them in registers.  A
+// persistent grid: CTA b takes the row blocks b, b + gridDim.x, ... and their
+// rows in order, writing one partial row per block as ln_bwd_rows does (the
+// same partial rows, added in the same order, so the results are identical).
+// Thread 0 refills stage s with row k + LNS_STAGES after the block barrier of
+// row k + 1, which every thread passes only when done with row k.  A wait that
+// gives up (about 0.25 s) sets g_norm_error and ends the CTA's loop; all
+// threads of the CTA leave together.
+constexpr int LNS_STAGES = 4;
+constexpr uint64_t LNS_WAIT = 1ull << 29;
+
+template <typename T, int NCH>
+__global__ void __launch_bounds__(LNB_THREADS, 1)
+ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float* __restrict__ mean,
+              const float* __restrict__ rstd, const T* __restrict__ gamma,
+              const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ pg,
+              float* __restrict__ pb, int M, int H) {
+  extern __shared__ __align__(128) uint8_t lns_smem[];
+  constexpr int NW = LNB_THREADS / 32;
+  __shared__ float red[2][NW][2];
+  __shared__ __align__(8) uint64_t full[LNS_STAGES];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART, G = gridDim.x, b = blockIdx.x;
+  const int nblk = b < nb ? (nb - 1 - b) / G + 1 : 0;
+  const int last = b + (nblk - 1) * G;  // only the grid's last block can be short
+  const int nrows = nblk == 0 ? 0 : (nblk - 1) * ROWS_PER_PART + min(ROWS_PER_PART, M - last * ROWS_PER_PART);
+  const uint32_t dbytes = (uint32_t)H * 4u, xbytes = (uint32_t)H * (uint32_t)sizeof(T);
+  const uint32_t stage = dbytes + (dres ? 2u : 1u) * xbytes;
+  const uint32_t sbase = ptx::smem_u32(lns_smem);
+  auto row_of = [&](int k) { return (b + (k / ROWS_PER_PART) * G) * ROWS_PER_PART + k % ROWS_PER_PART; };
+  auto bar = [&](int s) { return ptx::smem_u32(&full[s]); };
+  auto issue = [&](int k) {
+    const int s = k % LNS_STAGES;
+    const int64_t o = (int64_t)row_of(k) * H;
+    const uint32_t dst = sbase + (uint32_t)s * stage;
+    ptx::mbar_arrive_expect_tx(bar(s), stage);
+    ptx::bulk_load(dst, du + o, dbytes, bar(s));
+    ptx::bulk_load(dst + dbytes, x + o, xbytes, bar(s));
+    if (dres) ptx::bulk_load(dst + dbytes + xbytes, dres + o, xbytes, bar(s));
+  };
+  if (tid == 0) {
+    for (int s = 0; s < LNS_STAGES; ++s) ptx::mbar_init(bar(s), 1);
+    ptx::fence_mbar_init();
+    for (int k = 0; k < LNS_STAGES && k < nrows; ++k) issue(k);
+  }
+  __syncthreads();
+  float4 gv[NCH], ag[NCH], ab[NCH];
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int c = (tid + LNB_THREADS * j) * 4;
+    gv[j] = c < H ? ld4(gamma + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ag[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    ab[j] = ag[j];
+  }
+  using R = typename Raw4<T>::type;
+  // the row statistics are read one row ahead
+  float mu_n = nrows > 0 ? mean[row_of(0)] : 0.f, rs_n = nrows > 0 ? rstd[row_of(0)] : 0.f;
+  int k = 0;
+  for (; k < nrows; ++k) {
+    const int s = k % LNS_STAGES, par = k & 1, row = row_of(k);
+    const float mu = mu_n, rs = rs_n;
+    if (k + 1 < nrows) {
+      mu_n = mean[row_of(k + 1)];
+      rs_n = rstd[row_of(k + 1)];
+    }
+    const bool ok = ptx::mbar_wait(bar(s), (uint32_t)(k / LNS_STAGES) & 1u, LNS_WAIT);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) atomicExch(&g_norm_error, 1);
+      break;
+    }
+    const uint8_t* st = lns_smem + (size_t)s * stage;
+    const float* sd = reinterpret_cast<const float*>(st);
+    const T* sx = reinterpret_cast<const T*>(st + dbytes);
+    const T* sr = reinterpret_cast<const T*>(st + dbytes + xbytes);
+    float a = 0.f, bsum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = (tid + LNB_THREADS * j) * 4;
+      if (c < H) {
+        const float4 dd = *reinterpret_cast<const float4*>(sd + c);
+        const float4 xx = raw_f4(*reinterpret_cast<const R*>(sx + c)), g = gv[j];
+        const float g0 = dd.x * g.x, g1 = dd.y * g.y, g2 = dd.z * g.z, g3 = dd.w * g.w;
+        a += (g0 + g1) + (g2 + g3);
+        bsum = fmaf(g0, (xx.x - mu) * rs, bsum);
+        bsum = fmaf(g1, (xx.y - mu) * rs, bsum);
+        bsum = fmaf(g2, (xx.z - mu) * rs, bsum);
+        bsum = fmaf(g3, (xx.w - mu) * rs, bsum);
+      }
+    }
+    a = warp_sum(a);
+    bsum = warp_sum(bsum);
+    if (lane == 0) {
+      red[par][warp][0] = a;
+      red[par][warp][1] = bsum;
+    }
+    __syncthreads();  // (every thread is done with row k - 1: its stage may be refilled)
+    if (tid == 0 && k >= 1 && k - 1 + LNS_STAGES < nrows) {
+      ptx::fence_async_smem();
+      issue(k - 1 + LNS_STAGES);
+    }
+    float sa = 0.f, sb = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      sa += red[par][w][0];
+      sb += red[par][w][1];
+    }
+    const float a1 = sa / H, a2 = sb / H;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = (tid + LNB_THREADS * j) * 4;
+      if (c >= H) continue;
+      const float4 dd = *reinterpret_cast<const float4*>(sd + c);
+      const float4 xx = raw_f4(*reinterpret_cast<const R*>(sx + c)), g = gv[j];
+      const float4 rr = dres ? raw_f4(*reinterpret_cast<const R*>(sr + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float h0 = (xx.x - mu) * rs, h1 = (xx.y - mu) * rs, h2 = (xx.z - mu) * rs, h3 = (xx.w - mu) * rs;
+      st4(dx + (int64_t)row * H + c,
+          make_float4(fmaf(rs, dd.x * g.x - a1 - h0 * a2, rr.x), fmaf(rs, dd.y * g.y - a1 - h1 * a2, rr.y),
+                      fmaf(rs, dd.z * g.z - a1 - h2 * a2, rr.z), fmaf(rs, dd.w * g.w - a1 - h3 * a2, rr.w)));
+      ag[j].x = fmaf(dd.x, h0, ag[j].x);
+      ag[j].y = fmaf(dd.y, h1, ag[j].y);
+      ag[j].z = fmaf(dd.z, h2, ag[j].z);
+      ag[j].w = fmaf(dd.w, h3, ag[j].w);
+      ab[j].x += dd.x;
+      ab[j].y += dd.y;
+      ab[j].z += dd.z;
+      ab[j].w += dd.w;
+    }
+    if (k % ROWS_PER_PART == ROWS_PER_PART - 1 || k == nrows - 1) {  // the block's partial row
+      const int64_t prow = (int64_t)(b + (k / ROWS_PER_PART) * G) * H;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int c = (tid + LNB_THREADS * j) * 4;
+        if (c < H) {
+          st4(pg + prow + c, ag[j]);
+          st4(pb + prow + c, ab[j]);
+        }
+        ag[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ab[j] = ag[j];
+      }
+    }
+  }
+  // every copy issued has landed before the CTA may exit (the waits above
+  // consumed rows 0 .. k - 1; the issued ones are rows up to min(nrows, ...))
+  if (tid == 0) {
+    const int issued = min(nrows, k >= 1 ? k - 1 + LNS_STAGES : LNS_STAGES);
+    bool dr = true;
+    for (int q = k; q < issued; ++q)
+      dr = ptx::mbar_wait(bar(q % LNS_STAGES), (uint32_t)(q / LNS_STAGES) & 1u, LNS_WAIT) && dr;
+    if (!dr) atomicExch(&g_norm_error, 2);
+  }
+}
+
+template <typename T, int NCH>
+cudaError_t ln_bwd_staged_launch_n(const float* du, const T* x, const float* mean, const float* rstd,
+                                   const T* gamma, const T* dres, T* dx, float* pg, float* pb, int M,
+                                   int H, cudaStream_t st) {
+  static DeviceOnce attr;
+  const cudaError_t ea = attr.run([] {
+    return cudaFuncSetAttribute(ln_bwd_staged<T, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                LNS_STAGES * 4096 * (4 + 2 * (int)sizeof(T)));
+  });
+  if (ea != cudaSuccess) return ea;
+  const int smem = LNS_STAGES * H * (4 + (dres ? 2 : 1) * (int)sizeof(T));
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_bwd_staged<T, NCH>, LNB_THREADS, smem);
+  if (e != cudaSuccess) return e;
+  const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
+  const int grid = std::max(1, std::min(nb, sms * std::max(per_sm, 1)));
+  return launch_pdl(ln_bwd_staged<T, NCH>, dim3(grid), dim3(LNB_THREADS), smem, st, du, x, mean, rstd,
+                    gamma, dres, dx, pg, pb, M, H);
+}
+
+// Rows staged through shared memory by bulk copies: every row's start and
+// length 16-byte aligned.
+template <typename T>
+bool ln_bwd_staged_ok(const float* du, const void* x, const void* dres, int H) {
+  return H % (16 / (int)sizeof(T)) == 0 && H <= 4096 &&
+         (((uintptr_t)du | (uintptr_t)x | (uintptr_t)dres) & 15) == 0;
+}
+
+template <typename T>
+cudaError_t ln_bwd_staged_launch(const float* du, const void* x, const float* mean, const float* rstd,
+                                 const void* gamma, const void* dres, void* dx, float* pg, float* pb,
+                                 int M, int H, cudaStream_t st) {
+  const T *xt = (const T*)x, *gt = (const T*)gamma, *rt = (const T*)dres;
+  T* dt = (T*)dx;
+  switch ((H / 4 + LNB_THREADS - 1) / LNB_THREADS) {
+    case 1: return ln_bwd_staged_launch_n<T, 1>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
+    case 2: return ln_bwd_staged_launch_n<T, 2>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
+    case 3: return ln_bwd_staged_launch_n<T, 3>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
+    default: return ln_bwd_staged_launch_n<T, 4>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
+  }
+}
+
 template <typename T>
 cudaError_t ln_bwd_rows_launch(const float* du, const void* x, const float* mean, const float* rstd,
                                const void* gamma, const void* dres, void* dx, float* pg,
                                float* pb, int M, int H, cudaStream_t st) {
+  if (ln_bwd_staged_ok<T>(du, x, dres, H))
+    return ln_bwd_staged_launch<T>(du, x, mean, rstd, gamma, dres, dx, pg, pb, M, H, st);
   const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
   const int nch = (H / 4 + LNB_THREADS - 1) / LNB_THREADS;  // 1 .. 4
   const T *xt = (const T*)x, *gt = (const T*)gamma, *rt = (const T*)dres;
@@ -795,6 +1004,13 @@ cudaError_t shard_sum(const float* part, int64_t pstride, int w, const void* bia
                               : shard_sum_t<float, __nv_bfloat16>(part, pstride, w, bias, resid, out, M, N, st);
   return in_t == DType::F32 ? shard_sum_t<__nv_bfloat16, float>(part, pstride, w, bias, resid, out, M, N, st)
                             : shard_sum_t<__nv_bfloat16, __nv_bfloat16>(part, pstride, w, bias, resid, out, M, N, st);
+}
+
+int norm_read_and_clear_error() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_norm_error, sizeof(int)) != cudaSuccess) return -1;
+  if (v) cudaMemcpyToSymbol(g_norm_error, &z, sizeof(int));
+  return v;
 }
 
 int ln_bwd_blocks(int M) { return (M + ROWS_PER_PART - 1) / ROWS_PER_PART; }
