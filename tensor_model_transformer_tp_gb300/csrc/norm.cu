@@ -497,8 +497,9 @@ ln_bwd_rows(const float* __restrict__ du, const T* __restrict__ x, const float* 
 // per row and tensor, completion on the stage's mbarrier), so that several
 // rows per CTA are in flight without holding them in registers.  A
 // persistent grid: CTA b takes the row blocks b, b + gridDim.x, ... and their
-// rows in order, writing one partial row per block as ln_bwd_rows does (the
-// same partial rows, added in the same order, so the results are identical).
+// rows in order, and writes one partial row of dgamma, dbeta sums over all of
+// them: gridDim.x partial rows (at most two per SM), which one launch of
+// part_reduce_kernel adds in a fixed order.
 // Thread 0 refills stage s with row k + LNS_STAGES after the block barrier of
 // row k + 1, which every thread passes only when done with row k.  A wait that
 // gives up (about 0.25 s) sets g_norm_error and ends the CTA's loop; all
@@ -624,18 +625,14 @@ ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float
       ab[j].z += dd.z;
       ab[j].w += dd.w;
     }
-    if (k % ROWS_PER_PART == ROWS_PER_PART - 1 || k == nrows - 1) {  // the block's partial row
-      const int64_t prow = (int64_t)(b + (k / ROWS_PER_PART) * G) * H;
+  }
+  // the CTA's partial column sums over all of its rows, one partial row per CTA
 #pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const int c = (tid + LNB_THREADS * j) * 4;
-        if (c < H) {
-          st4(pg + prow + c, ag[j]);
-          st4(pb + prow + c, ab[j]);
-        }
-        ag[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        ab[j] = ag[j];
-      }
+  for (int j = 0; j < NCH; ++j) {
+    const int c = (tid + LNB_THREADS * j) * 4;
+    if (c < H) {
+      st4(pg + (int64_t)b * H + c, ag[j]);
+      st4(pb + (int64_t)b * H + c, ab[j]);
     }
   }
   // every copy issued has landed before the CTA may exit (the waits above
@@ -652,7 +649,7 @@ ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float
 template <typename T, int NCH>
 cudaError_t ln_bwd_staged_launch_n(const float* du, const T* x, const float* mean, const float* rstd,
                                    const T* gamma, const T* dres, T* dx, float* pg, float* pb, int M,
-                                   int H, cudaStream_t st) {
+                                   int H, cudaStream_t st, int* parts) {
   static DeviceOnce attr;
   const cudaError_t ea = attr.run([] {
     return cudaFuncSetAttribute(ln_bwd_staged<T, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -668,6 +665,7 @@ cudaError_t ln_bwd_staged_launch_n(const float* du, const T* x, const float* mea
   if (e != cudaSuccess) return e;
   const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
   const int grid = std::max(1, std::min(nb, sms * std::max(per_sm, 1)));
+  *parts = grid;
   return launch_pdl(ln_bwd_staged<T, NCH>, dim3(grid), dim3(LNB_THREADS), smem, st, du, x, mean, rstd,
                     gamma, dres, dx, pg, pb, M, H);
 }
@@ -680,17 +678,18 @@ bool ln_bwd_staged_ok(const float* du, const void* x, const void* dres, int H) {
          (((uintptr_t)du | (uintptr_t)x | (uintptr_t)dres) & 15) == 0;
 }
 
+// Launches ln_bwd_staged; *parts = the partial rows it writes.
 template <typename T>
 cudaError_t ln_bwd_staged_launch(const float* du, const void* x, const float* mean, const float* rstd,
                                  const void* gamma, const void* dres, void* dx, float* pg, float* pb,
-                                 int M, int H, cudaStream_t st) {
+                                 int M, int H, cudaStream_t st, int* parts) {
   const T *xt = (const T*)x, *gt = (const T*)gamma, *rt = (const T*)dres;
   T* dt = (T*)dx;
   switch ((H / 4 + LNB_THREADS - 1) / LNB_THREADS) {
-    case 1: return ln_bwd_staged_launch_n<T, 1>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
-    case 2: return ln_bwd_staged_launch_n<T, 2>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
-    case 3: return ln_bwd_staged_launch_n<T, 3>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
-    default: return ln_bwd_staged_launch_n<T, 4>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st);
+    case 1: return ln_bwd_staged_launch_n<T, 1>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
+    case 2: return ln_bwd_staged_launch_n<T, 2>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
+    case 3: return ln_bwd_staged_launch_n<T, 3>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
+    default: return ln_bwd_staged_launch_n<T, 4>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
   }
 }
 
@@ -698,8 +697,6 @@ template <typename T>
 cudaError_t ln_bwd_rows_launch(const float* du, const void* x, const float* mean, const float* rstd,
                                const void* gamma, const void* dres, void* dx, float* pg,
                                float* pb, int M, int H, cudaStream_t st) {
-  if (ln_bwd_staged_ok<T>(du, x, dres, H))
-    return ln_bwd_staged_launch<T>(du, x, mean, rstd, gamma, dres, dx, pg, pb, M, H, st);
   const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
   const int nch = (H / 4 + LNB_THREADS - 1) / LNB_THREADS;  // 1 .. 4
   const T *xt = (const T*)x, *gt = (const T*)gamma, *rt = (const T*)dres;
@@ -881,6 +878,13 @@ part_reduce_l2(const float* __restrict__ part, float* __restrict__ out,
 
 cudaError_t reduce_parts(float* part, float* out, float* part2, float* out2, int nb, int N,
                          cudaStream_t st) {
+  // up to 512 partial rows (the bias gradients of 8192 rows, the LayerNorm
+  // backward's per-CTA rows): one launch, each of the eight thread groups
+  // adding at most 64 rows
+  if (nb <= 64 * RED_GROUPS)
+    return launch_pdl(part_reduce_kernel, dim3((N + RED_COLS - 1) / RED_COLS),
+                      dim3(RED_COLS * RED_GROUPS), 0, st, (const float*)part, out,
+                      (const float*)part2, out2, nb, N);
   const int gx = (N + 255) / 256;
   const int gy = std::min((nb + RED_ROWS - 1) / RED_ROWS, 65535);
   cudaError_t e = launch_pdl(part_reduce_l1, dim3(gx, gy), dim3(256),
@@ -1051,6 +1055,18 @@ cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, co
                    (((uintptr_t)x | (uintptr_t)gamma | (uintptr_t)dres | (uintptr_t)dx) &
                     (t == DType::BF16 ? 7 : 15)) == 0 &&
                    ((uintptr_t)part_g & 15) == 0 && ((uintptr_t)part_b & 15) == 0;
+  if (H <= 4 * LNB_THREADS * 4 && ((uintptr_t)part_g & 15) == 0 && ((uintptr_t)part_b & 15) == 0 &&
+      (t == DType::F32 ? ln_bwd_staged_ok<float>(du, x, dres, H)
+                       : ln_bwd_staged_ok<__nv_bfloat16>(du, x, dres, H))) {
+    int parts = 0;
+    cudaError_t e = t == DType::F32
+                        ? ln_bwd_staged_launch<float>(du, x, mean, rstd, gamma, dres, dx, part_g,
+                                                      part_b, M, H, st, &parts)
+                        : ln_bwd_staged_launch<__nv_bfloat16>(du, x, mean, rstd, gamma, dres, dx,
+                                                              part_g, part_b, M, H, st, &parts);
+    if (e != cudaSuccess) return e;
+    return reduce_parts(part_g, dgamma, part_b, dbeta, parts, H, st);
+  }
   if (vec && H <= 4 * LNB_THREADS * 4) {
     const int nb = ln_bwd_blocks(M);
     cudaError_t e = t == DType::F32
