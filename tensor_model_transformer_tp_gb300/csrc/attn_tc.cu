@@ -511,12 +511,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, BWD_WAIT));
 }
 
-// dq kernel: one CTA per 128 queries, 128-key blocks, 576 threads:
+// dq kernel: one CTA per 128 queries, 128-key blocks, 608 threads:
 //   warp 0       TMA loads (Q and dO once, then K_j into a three-stage ring
 //                and V_j into a two-stage ring);
-//   warp 1       TMEM allocation; one thread issues the MMAs;
+//   warp 1       TMEM allocation; one thread issues the S and dP MMAs;
 //   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
-//                query row each) and columns 32 ((w - 2) / 4) .. + 31 of a block.
+//                query row each) and columns 32 ((w - 2) / 4) .. + 31 of a block;
+//   warp 18      one thread issues the dQ accumulation MMAs.
 // Per block j:
 //   S_j = Q K_j^T, dP_j = dO V_j^T    N = 128, into TMEM (one buffer each); the
 //                                    element-wise warps load their 32 columns of
@@ -525,19 +526,23 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
 //                                    form dS_j = P_j * (dP_j - delta)
 //   dS_j                             packed bf16 into TMEM (64 columns)
 //   dQ += dS_j K_j                   A = dS_j from TMEM, B = K_j (MN-major)
-// MMA issue order: SdP_0, then SdP_j, ACC_{j-1} for j >= 1, then ACC_{n-1}.
+// The two kinds of MMA come from two threads, so neither waits behind the
+// other's barrier (an issuing thread cannot run ahead of its own waits, and
+// the tensor core drains while it waits); their outputs are disjoint and each
+// thread's commits track its own MMAs.
 // V_j is released when SdP_j completes, K_j when ACC_j completes: with three
 // K stages and two V stages the loads of the next blocks are never behind the
 // MMAs that wait for them.  Every MMA is 128 x 128 x 16 (one MMA's tensor
 // work, 64 clocks, exceeds its issue cost).
 // TMEM: S 0..127, dP 128..255, dQ 256..383, dS 384..447.
-constexpr int DQ_NT = 576;
+constexpr int DQ_NT = 608;
+constexpr int DQ_ACC_WARP = 18;  // issues the dQ accumulation MMAs
 constexpr int DQ_EW = 16;               // element-wise warps, four per lane quarter
 constexpr int DQ_KST = 3, DQ_VST = 2;   // K and V stages of 128 keys
 constexpr int DQ_OFF_Q = 0, DQ_OFF_DO = TILE, DQ_OFF_K = 2 * TILE;
 constexpr int DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE, DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE;
-// q+dO, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full, sdp_empty, ds_full, ds_empty, fin
-constexpr int DQ_NBAR = 1 + 2 * DQ_KST + 2 * DQ_VST + 5;
+// dO, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full, sdp_empty, ds_full, ds_empty, fin, sdp_drain
+constexpr int DQ_NBAR = 1 + 2 * DQ_KST + 2 * DQ_VST + 6;
 constexpr int DQ_SMEM = DQ_OFF_BAR + 8 * DQ_NBAR + 16 + 1024;
 static_assert(DQ_SMEM <= 232448, "dq kernel: more than 227 KB of shared memory");
 
@@ -556,6 +561,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
   auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * DQ_KST + DQ_VST + s); };
   const uint32_t sdp_full = bars + 8u * (1 + 2 * DQ_KST + 2 * DQ_VST), sdp_empty = sdp_full + 8u;
   const uint32_t ds_full = sdp_full + 16u, ds_empty = sdp_full + 24u, bar_fin = sdp_full + 32u;
+  const uint32_t sdp_drain = sdp_full + 40u;
   const uint32_t tslot = bars + 8u * DQ_NBAR;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -583,6 +589,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
     ptx::mbar_init(ds_full, DQ_EW);
     ptx::mbar_init(ds_empty, 1);
     ptx::mbar_init(bar_fin, 1);
+    ptx::mbar_init(sdp_drain, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tq128);
     ptx::prefetch_tmap(&tdo128);
@@ -669,6 +676,14 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
         tl_block(1, j, 0);
         return true;
       };
+      for (int j = 0; j < n && ok; ++j) ok = sdp(j);
+      ptx::mma_commit(sdp_drain);  // completes once every MMA this thread issued has
+      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) { ok = false; wait_failed(107); }
+    }
+  } else if (warp == DQ_ACC_WARP) {
+    if (lane == 0) {
+      ok = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
+      if (!ok) wait_failed(110);
       auto acc = [&](int j) {  // dQ += dS_j K_j (contraction over the block's 128 keys)
         const int sk = j % DQ_KST;
         if (!ptx::mbar_wait(ds_full, j & 1, BWD_WAIT)) { wait_failed(106); return false; }
@@ -678,16 +693,16 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
         for (int kk = 0; kk < BKV / 16; ++kk)
           ptx::mma_bf16_ts(t_dq, t_ds + 8u * kk, mnmajor_desc(kt, kk), IDESC_PV,
                            (j > 0 || kk > 0) ? 1u : 0u);
+        // S_j, dP_j (which also read K_j) completed before the element-wise
+        // warps could hand over dS_j, so K_j is free once these MMAs are
         ptx::mma_commit(ds_empty);
         ptx::mma_commit(k_empty(sk));
         tl_block(1, j, 1);
         return true;
       };
-      if (ok && n > 0) ok = sdp(0);
-      for (int j = 1; j < n && ok; ++j) ok = sdp(j) && acc(j - 1);
-      if (ok && n > 0) ok = acc(n - 1);
-      ptx::mma_commit(bar_fin);  // completes once every MMA issued above has
-      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(107); }
+      for (int j = 0; j < n && ok; ++j) ok = acc(j);
+      ptx::mma_commit(bar_fin);  // completes once every MMA this thread issued has
+      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(111); }
     }
   } else {
     const int qq = warp & 3, sub = (warp - 2) >> 2;  // lane quarter; columns 32 sub .. + 31
@@ -770,11 +785,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
   if (tid == 0) tl_cta(1, 1);
 }
 
-// dkv kernel: one CTA per 128 keys, 64-query blocks, 576 threads:
+// dkv kernel: one CTA per 128 keys, 64-query blocks, 608 threads:
 //   warp 0       TMA loads (K and V once, then Q_i and dO_i into a four-stage ring);
-//   warp 1       TMEM allocation; one thread issues the MMAs;
+//   warp 1       TMEM allocation; one thread issues the S^T and dP^T MMAs;
 //   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
-//                key row each) and columns 16 ((w - 2) / 4) .. + 15 of a block.
+//                key row each) and columns 16 ((w - 2) / 4) .. + 15 of a block;
+//   warp 18      one thread issues the dV and dK accumulation MMAs.
 // Per query block i:
 //   S^T = K Q_i^T, dP^T = V dO_i^T     N = 64, into one of two TMEM buffers
 //   P^T = exp2(S^T scale - LSE), dS^T = P^T (dP^T - delta)
@@ -783,20 +799,21 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
 //                                     block ahead and shared by lane shuffles),
 //                                     bf16 into one shared-memory buffer each
 //   dV += P^T dO_i, dK += dS^T Q_i     N = 128 (d), contraction over the 64 queries
-// MMA issue order: SdP_0, then SdP_i, ACC_{i-1} for i >= 1, then ACC_{n-1}.
+// The two kinds of MMA come from two threads, as in the dq kernel.
 // The element-wise warps write block i's P^T and dS^T once the MMAs of
 // block i-1's accumulation are done; they are still computing when those
 // MMAs end, so one buffer each suffices and the shared memory goes to a
 // fourth Q/dO stage, which keeps the loads ahead of the MMAs that wait for them.
-constexpr int KV_NT = 576;
+constexpr int KV_NT = 608;
+constexpr int KV_ACC_WARP = 18;  // issues the dV and dK accumulation MMAs
 constexpr int KV_EW = 16;               // element-wise warps, four per lane quarter
 constexpr int KV_QST = 4;               // Q/dO stages of 64 queries
 constexpr int KV_OFF_K = 0, KV_OFF_V = TILE, KV_OFF_Q = 2 * TILE;
 constexpr int KV_OFF_DO = KV_OFF_Q + KV_QST * T64;
 constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + PB;
 constexpr int KV_OFF_BAR = KV_OFF_DST + PB;
-// kv, q_full[4], q_empty[4], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin
-constexpr int KV_NBAR = 1 + 2 * KV_QST + 4 + 3;
+// kv, q_full[4], q_empty[4], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin, sdp_drain
+constexpr int KV_NBAR = 1 + 2 * KV_QST + 4 + 4;
 constexpr int KV_SMEM = KV_OFF_BAR + 8 * KV_NBAR + 16 + 1024;
 static_assert(KV_SMEM <= 232448, "dkv kernel: more than 227 KB of shared memory");
 
@@ -822,6 +839,7 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   auto sdp_full = [&](int b) { return bars + 8u * (1 + 2 * KV_QST + b); };
   auto sdp_empty = [&](int b) { return bars + 8u * (3 + 2 * KV_QST + b); };
   const uint32_t pd_full = bars + 8u * (5 + 2 * KV_QST), pd_empty = pd_full + 8u, bar_fin = pd_full + 16u;
+  const uint32_t sdp_drain = pd_full + 24u;
   const uint32_t tslot = bars + 8u * KV_NBAR;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -847,6 +865,7 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
     ptx::mbar_init(pd_full, KV_EW);
     ptx::mbar_init(pd_empty, 1);
     ptx::mbar_init(bar_fin, 1);
+    ptx::mbar_init(sdp_drain, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tkv);
     ptx::prefetch_tmap(&tq64);
@@ -924,6 +943,14 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
         tl_block(2, ii, 0);
         return true;
       };
+      for (int ii = 0; ii < n && ok; ++ii) ok = sdp(ii);
+      ptx::mma_commit(sdp_drain);  // completes once every MMA this thread issued has
+      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) { ok = false; wait_failed(207); }
+    }
+  } else if (warp == KV_ACC_WARP) {
+    if (lane == 0) {
+      ok = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
+      if (!ok) wait_failed(210);
       auto acc = [&](int ii) {  // dV += P^T dO_i, dK += dS^T Q_i
         const int s = ii % KV_QST;
         if (!ptx::mbar_wait(pd_full, ii & 1, BWD_WAIT)) { wait_failed(206); return false; }
@@ -935,16 +962,17 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
           ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT, kk), mnmajor64_desc(dt, kk), IDESC_ACC, accum);
           ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST, kk), mnmajor64_desc(qt, kk), IDESC_ACC, accum);
         }
+        // S^T, dP^T of block ii (which also read Q_i, dO_i) completed before
+        // the element-wise warps could hand over P^T, dS^T: the stage is free
+        // once these MMAs are
         ptx::mma_commit(pd_empty);
         ptx::mma_commit(q_empty(s));
         tl_block(2, ii, 1);
         return true;
       };
-      if (ok && n > 0) ok = sdp(0);
-      for (int ii = 1; ii < n && ok; ++ii) ok = sdp(ii) && acc(ii - 1);
-      if (ok && n > 0) ok = acc(n - 1);
-      ptx::mma_commit(bar_fin);
-      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(207); }
+      for (int ii = 0; ii < n && ok; ++ii) ok = acc(ii);
+      ptx::mma_commit(bar_fin);  // completes once every MMA this thread issued has
+      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(211); }
     }
   } else {
     const int qq = warp & 3, c = (warp - 2) >> 2;  // lane quarter; columns 16 c .. + 15
