@@ -786,7 +786,9 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
 }
 
 // dkv kernel: one CTA per 128 keys, 64-query blocks, 608 threads:
-//   warp 0       TMA loads (K and V once, then Q_i and dO_i into a four-stage ring);
+//   warp 0       TMA loads (K and V once, then Q_i and dO_i into a three-stage
+//                ring, each stage with its queries' LSE and delta, which the
+//                warp reads from global memory a block ahead);
 //   warp 1       TMEM allocation; one thread issues the S^T and dP^T MMAs;
 //   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
 //                key row each) and columns 16 ((w - 2) / 4) .. + 15 of a block;
@@ -794,25 +796,24 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
 // Per query block i:
 //   S^T = K Q_i^T, dP^T = V dO_i^T     N = 64, into one of two TMEM buffers
 //   P^T = exp2(S^T scale - LSE), dS^T = P^T (dP^T - delta)
-//                                     (LSE and delta of the block's queries are
-//                                     read by each warp from global memory one
-//                                     block ahead and shared by lane shuffles),
+//                                     (LSE and delta of the block's queries
+//                                     from the stage, broadcast loads),
 //                                     bf16 into one shared-memory buffer each
 //   dV += P^T dO_i, dK += dS^T Q_i     N = 128 (d), contraction over the 64 queries
 // The two kinds of MMA come from two threads, as in the dq kernel.
 // The element-wise warps write block i's P^T and dS^T once the MMAs of
 // block i-1's accumulation are done; they are still computing when those
-// MMAs end, so one buffer each suffices and the shared memory goes to a
-// fourth Q/dO stage, which keeps the loads ahead of the MMAs that wait for them.
+// MMAs end, so one buffer each suffices.
 constexpr int KV_NT = 608;
 constexpr int KV_ACC_WARP = 18;  // issues the dV and dK accumulation MMAs
 constexpr int KV_EW = 16;               // element-wise warps, four per lane quarter
-constexpr int KV_QST = 4;               // Q/dO stages of 64 queries
+constexpr int KV_QST = 3;               // Q/dO stages of 64 queries
 constexpr int KV_OFF_K = 0, KV_OFF_V = TILE, KV_OFF_Q = 2 * TILE;
 constexpr int KV_OFF_DO = KV_OFF_Q + KV_QST * T64;
 constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + PB;
-constexpr int KV_OFF_BAR = KV_OFF_DST + PB;
-// kv, q_full[4], q_empty[4], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin, sdp_drain
+constexpr int KV_OFF_STAT = KV_OFF_DST + PB;  // [stage][lse2[64] | delta[64]] fp32
+constexpr int KV_OFF_BAR = KV_OFF_STAT + KV_QST * 2 * BK * 4;
+// kv, q_full[3], q_empty[3], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin, sdp_drain
 constexpr int KV_NBAR = 1 + 2 * KV_QST + 4 + 4;
 constexpr int KV_SMEM = KV_OFF_BAR + 8 * KV_NBAR + 16 + 1024;
 static_assert(KV_SMEM <= 232448, "dkv kernel: more than 227 KB of shared memory");
@@ -841,6 +842,7 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   const uint32_t pd_full = bars + 8u * (5 + 2 * KV_QST), pd_empty = pd_full + 8u, bar_fin = pd_full + 16u;
   const uint32_t sdp_drain = pd_full + 24u;
   const uint32_t tslot = bars + 8u * KV_NBAR;
+  float* stat = reinterpret_cast<float*>(gbase + KV_OFF_STAT);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   // grid (heads, batch, tiles): key tile 0 (the most query blocks) first
@@ -895,14 +897,40 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
       ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, bar_kv, col_k + 64, row0 + k0);
       ptx::tma_load_2d(base + KV_OFF_V, &tkv, bar_kv, col_v, row0 + k0);
       ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, bar_kv, col_v + 64, row0 + k0);
-      int nl = 0;  // query blocks whose loads were issued
-      for (int ii = 0; ii < n; ++ii) {
-        const int s = ii % KV_QST;
-        if (ii >= KV_QST && !ptx::mbar_wait(q_empty(s), ((ii / KV_QST) & 1) ^ 1, BWD_WAIT)) {
-          ok = false;
-          wait_failed(201);
-          break;
-        }
+    }
+    // LSE (log2 units) and delta of block ii's 64 queries, two of each per lane;
+    // the next block's are loaded before the wait for its stage
+    auto ld_stat = [&](int ii, float (&v)[4]) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = (i0 + ii) * BK + lane + 32 * u;
+        const bool vq = ii < n && q < a.S;
+        const int64_t at = (int64_t)h * a.M + row0 + q;
+        v[u] = vq ? a.lse[at] * 1.4426950408889634f : 0.f;
+        v[2 + u] = vq ? a.delta[at] : 0.f;
+      }
+    };
+    float cur[4];
+    ld_stat(0, cur);
+    int nl = 0;  // query blocks whose loads were issued
+    for (int ii = 0; ii < n; ++ii) {
+      const int s = ii % KV_QST;
+      float nxt[4];
+      ld_stat(ii + 1, nxt);
+      bool w = true;
+      if (lane == 0 && ii >= KV_QST) w = ptx::mbar_wait(q_empty(s), ((ii / KV_QST) & 1) ^ 1, BWD_WAIT);
+      if (!__shfl_sync(0xffffffffu, w, 0)) {
+        ok = false;
+        if (lane == 0) wait_failed(201);
+        break;
+      }
+      float* st = stat + s * 2 * BK;
+      st[lane] = cur[0];
+      st[lane + 32] = cur[1];
+      st[BK + lane] = cur[2];
+      st[BK + lane + 32] = cur[3];
+      __syncwarp();  // the warp's stores precede lane 0's arrive on the stage barrier
+      if (lane == 0) {
         ptx::mbar_arrive_expect_tx(q_full(s), 2 * T64);
         const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
         const int r = row0 + (i0 + ii) * BK;
@@ -910,8 +938,12 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
         ptx::tma_load_2d(qt + BOX64, &tq64, q_full(s), col_q + 64, r);
         ptx::tma_load_2d(dt, &tdo64, q_full(s), h * D, r);
         ptx::tma_load_2d(dt + BOX64, &tdo64, q_full(s), h * D + 64, r);
-        nl = ii + 1;
       }
+      nl = ii + 1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+    }
+    if (lane == 0) {
       // every load issued has landed before the CTA may exit (stage s last
       // held block s + R ((m - 1 - s) / R) of the m issued)
       bool dr = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
@@ -979,19 +1011,11 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
     const int row = qq * 32 + lane, kj = k0 + row;
     const bool valid_k = kj < a.S;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    // lane l holds, for query 16 c + (l % 16) of a block, LSE in log2 units
-    // (l < 16) or delta (l >= 16); loaded one block ahead
-    auto stat = [&](int ii) {
-      const int q = (i0 + ii) * BK + c * 16 + (lane & 15);
-      if (ii >= n || q >= a.S) return 0.f;
-      const int64_t at = (int64_t)h * a.M + row0 + q;
-      return lane < 16 ? a.lse[at] * 1.4426950408889634f : a.delta[at];
-    };
-    float nxt = stat(0);
     for (int ii = 0; ii < n && ok; ++ii) {
-      const int b = ii & 1, i = i0 + ii;
-      // this block's S^T, dP^T are in TMEM
-      if (!warp_wait(sdp_full(b), (ii / 2) & 1)) {
+      const int s = ii % KV_QST, b = ii & 1, i = i0 + ii;
+      // this block's S^T, dP^T are in TMEM (which also means its stage, and
+      // the LSE / delta stored with it, have landed)
+      if (!warp_wait(sdp_full(b), (ii / 2) & 1) || !warp_wait(q_full(s), (ii / KV_QST) & 1)) {
         ok = false;
         if (lane == 0) wait_failed(208);
         break;
@@ -1003,28 +1027,33 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
-      const float cur = nxt;
-      nxt = stat(ii + 1);
+      const float* st = stat + s * 2 * BK + c * 16;  // LSE of these 16 queries; delta at + BK
       uint32_t pp[8], pd[8];
       // a query block that sees every key of the tile needs no mask (CTA-uniform)
       const bool full = k0 + 128 <= a.S && (i + 1) * BK <= a.S && (!a.causal || i * BK >= k0 + 127);
       if (full) {
         const uint64_t sc = f2_splat(a.scale_log2);
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          const float l0 = __shfl_sync(0xffffffffu, cur, k), l1 = __shfl_sync(0xffffffffu, cur, k + 1);
-          const float d0 = __shfl_sync(0xffffffffu, cur, 16 + k), d1 = __shfl_sync(0xffffffffu, cur, 17 + k);
-          const uint64_t x = f2_fma(f2_pack(v[k], v[k + 1]), sc, f2_pack(-l0, -l1));
-          const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
-          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[k], w[k + 1]), f2_pack(-d0, -d1)));
-          pp[k / 2] = pack2(f2_lo(p), f2_hi(p));
-          pd[k / 2] = pack2(f2_lo(ds), f2_hi(ds));
+        for (int k = 0; k < 16; k += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(st + k);
+          const float4 d4 = *reinterpret_cast<const float4*>(st + BK + k);
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const float l0 = e == 0 ? l4.x : l4.z, l1 = e == 0 ? l4.y : l4.w;
+            const float d0 = e == 0 ? d4.x : d4.z, d1 = e == 0 ? d4.y : d4.w;
+            const int kk = k + e;
+            const uint64_t x = f2_fma(f2_pack(v[kk], v[kk + 1]), sc, f2_pack(-l0, -l1));
+            const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
+            const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[kk], w[kk + 1]), f2_pack(-d0, -d1)));
+            pp[kk / 2] = pack2(f2_lo(p), f2_hi(p));
+            pd[kk / 2] = pack2(f2_lo(ds), f2_hi(ds));
+          }
         }
       } else {
         const int qbase = i * BK + c * 16;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float l2 = __shfl_sync(0xffffffffu, cur, k), dl = __shfl_sync(0xffffffffu, cur, 16 + k);
+          const float l2 = st[k], dl = st[BK + k];
           const int q = qbase + k;
           const bool valid = valid_k && q < a.S && (!a.causal || kj <= q);
           const float p = valid ? fast_exp2(v[k] * a.scale_log2 - l2) : 0.f;
