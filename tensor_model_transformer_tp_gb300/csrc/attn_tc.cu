@@ -807,7 +807,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
 constexpr int KV_NT = 608;
 constexpr int KV_ACC_WARP = 18;  // issues the dV and dK accumulation MMAs
 constexpr int KV_EW = 16;               // element-wise warps, four per lane quarter
-constexpr int KV_QST = 3;               // Q/dO stages of 64 queries
+constexpr int KV_QST = 4;               // Q/dO stages of 64 queries
 constexpr int KV_OFF_K = 0, KV_OFF_V = TILE, KV_OFF_Q = 2 * TILE;
 constexpr int KV_OFF_DO = KV_OFF_Q + KV_QST * T64;
 constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + PB;
@@ -815,8 +815,13 @@ constexpr int KV_OFF_STAT = KV_OFF_DST + PB;  // [stage][lse2[64] | delta[64]] f
 constexpr int KV_OFF_BAR = KV_OFF_STAT + KV_QST * 2 * BK * 4;
 // kv, q_full[3], q_empty[3], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin, sdp_drain
 constexpr int KV_NBAR = 1 + 2 * KV_QST + 4 + 4;
-constexpr int KV_SMEM = KV_OFF_BAR + 8 * KV_NBAR + 16 + 1024;
-static_assert(KV_SMEM <= 232448, "dkv kernel: more than 227 KB of shared memory");
+// The dynamic shared memory is rounded up to a 1024-byte boundary (the
+// swizzled tiles need it); this kernel's layout leaves room for at most
+// KV_SLACK bytes of rounding, and the kernel checks the actual amount (the
+// window starts 1024-byte aligned on this GPU, so none is used).
+constexpr int KV_SLACK = 232448 - (KV_OFF_BAR + 8 * KV_NBAR + 16);
+constexpr int KV_SMEM = 232448;
+static_assert(KV_SLACK >= 0, "dkv kernel: more than 227 KB of shared memory");
 
 // Writes 8 words of packed bf16 pairs (16 values: columns 16 c .. + 15 of this
 // thread's row) into a [128 rows][64 cols] 128-byte-swizzled buffer.
@@ -832,6 +837,10 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  if (base - raw > (uint32_t)KV_SLACK) {  // the layout would not fit (uniform: every thread leaves)
+    if (threadIdx.x == 0) atomicExch(&g_attn_error, 6);
+    return;
+  }
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + KV_OFF_BAR;
   const uint32_t bar_kv = bars;
