@@ -81,6 +81,13 @@ oases_status oases_debug_attention_timeline(unsigned long long *device_buffer);
  * issued and its epilogue done, exit); NULL switches it off. */
 oases_status oases_debug_gemm_timeline(unsigned long long *device_buffer);
 int oases_debug_attention_error_word(void);
+/* Failure-detection probe: launches one thread that waits, with the bounded
+ * mbarrier wait the tensor-core kernels use, on a barrier nothing arrives on.
+ * The wait gives up after limit_cycles SM clocks (1 .. 2^32; about 2 ms at
+ * 2^22) and records error site 999, so the next oases_check_device on that
+ * stream returns OASES_ERR_TIMEOUT while the CUDA context stays usable.
+ * Returns OASES_ERR_INVALID_ARG for a limit out of range (nothing launched). */
+oases_status oases_debug_wait_probe(uint64_t limit_cycles, void *stream);
 
 /* Per-operator timeline of the block scheduler (debugging aid).  With
  * tracing on (a process-wide switch), every following block call records a

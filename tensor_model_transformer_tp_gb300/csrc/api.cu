@@ -1495,6 +1495,20 @@ extern "C" int oases_debug_attention_error_word(void) {
 }
 
 namespace oases {
+cudaError_t attention_wait_probe(uint64_t limit_cycles, cudaStream_t st);
+}
+extern "C" oases_status oases_debug_wait_probe(uint64_t limit_cycles, void* stream) {
+  t_last_error.clear();
+  if (limit_cycles == 0 || limit_cycles > (1ull << 32)) {
+    t_last_error = "limit_cycles must be in 1 .. 2^32";
+    return OASES_ERR_INVALID_ARG;
+  }
+  cudaError_t e = oases::attention_wait_probe(limit_cycles, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return OASES_OK;
+}
+
+namespace oases {
 cudaError_t gemm_set_timeline(unsigned long long* p);
 }
 extern "C" oases_status oases_debug_gemm_timeline(unsigned long long* device_buffer) {

@@ -1237,6 +1237,25 @@ cudaError_t attention_set_progress(int* p) {
   return cudaMemcpyToSymbol(g_attn_progress, &p, sizeof(p));
 }
 
+namespace {
+// One thread waits, with the bounded wait every tensor-core kernel here uses,
+// on an mbarrier that nothing arrives on: the wait gives up after
+// limit_cycles and records site 999, as a real stalled wait would.
+__global__ void attn_wait_probe_kernel(uint64_t limit_cycles) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = ptx::smem_u32(&bar);
+  ptx::mbar_init(b, 1);
+  ptx::fence_mbar_init();
+  if (!ptx::mbar_wait(b, 0, limit_cycles)) wait_failed(999);
+}
+}  // namespace
+
+cudaError_t attention_wait_probe(uint64_t limit_cycles, cudaStream_t st) {
+  attn_wait_probe_kernel<<<1, 1, 0, st>>>(limit_cycles);
+  ++g_launch_count;
+  return cudaGetLastError();
+}
+
 cudaError_t attention_set_timeline(unsigned long long* p) {
   return cudaMemcpyToSymbol(g_attn_timeline, &p, sizeof(p));
 }
