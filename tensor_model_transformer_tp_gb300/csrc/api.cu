@@ -37,6 +37,12 @@
 
 namespace oases {
 int norm_read_and_clear_error();  // norm.cu: a LayerNorm kernel's wait gave up
+cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float* mean,
+                                     const float* rstd, const void* gamma, const void* dres, void* dx,
+                                     float* part_g, float* part_b, float2* stat, float* dgamma,
+                                     float* dbeta, int M, int H, DType t, cudaStream_t st,
+                                     float* part_x, int part_x_cap, int* n_part_x);
+cudaError_t reduce_partial_rows(float* part, float* out, int nparts, int N, cudaStream_t st);
 thread_local int g_launch_count = 0;
 
 uint64_t current_ctx_id() {
@@ -464,6 +470,9 @@ struct Exec {
   const void* dy;             // gradient w.r.t. y
   void* dx;                   // gradient w.r.t. x
   cudaError_t err = cudaSuccess;
+  // partial rows of colsum(grad_out(seg)) for sub-batch b that the LayerNorm
+  // backward of segment seg + 1 left in cpart(seg, b) (0: none; [seg * nsb + b])
+  std::vector<int> xparts;
   EventPool* P = nullptr;  // this thread's events on the call's device
   size_t ev_base = 2;      // P->ev[0], [1]: call entry / exit joins
 
@@ -697,8 +706,13 @@ struct Exec {
 
   void bwd_g(int seg, int b) {  // db_row += colsum(dy); Eq. (1): dP_k = dy, nothing else to do
     grad_wait(seg, GRP_BR, b);
-    ok(colsum_accum(rowp(grad_out(seg), b, s.H, s.esz), s.H, (int)s.Ms, s.H, s.t, cpart(seg, b),
-                    sp[seg].dbr, stream(b)));
+    int& xp = xparts[(size_t)seg * s.nsb + b];
+    if (xp > 0)  // the column sums of dy were taken as it was written (LayerNorm backward)
+      ok(reduce_partial_rows(cpart(seg, b), sp[seg].dbr, xp, s.H, stream(b)));
+    else
+      ok(colsum_accum(rowp(grad_out(seg), b, s.H, s.esz), s.H, (int)s.Ms, s.H, s.t, cpart(seg, b),
+                      sp[seg].dbr, stream(b)));
+    xp = 0;
     grad_done(seg, GRP_BR, b);
   }
 
@@ -873,12 +887,20 @@ struct Exec {
     void* dxo = rowp(grad_in(seg), b, s.H, s.esz);
     if (s.pre_ln) {
       grad_wait(seg, GRP_LN, b);
-      ok(layer_norm_bwd(du, rowp(seg_in(seg), b, s.H, s.esz), rowp(at<float>(a.mu), b, 1, 4),
-                        rowp(at<float>(a.rstd), b, 1, 4), sp[seg].g, dres, dxo,
-                        at<float>(a.lpart_g) + (size_t)b * L.lpart_n,
-                        at<float>(a.lpart_b) + (size_t)b * L.lpart_n,
-                        rowp(at<float2>(a.lstat), b, 1, 8), sp[seg].dg, sp[seg].db,
-                        (int)s.Ms, s.H, s.t, stream(b)));
+      // dx is the previous segment's output gradient: its column sums (that
+      // segment's row-bias gradient) are taken here, as dx is written, into
+      // the previous segment's colsum scratch, which nothing else of this
+      // sub-batch uses before that segment's bwd_g reduces them
+      float* px = seg >= 1 ? cpart(seg - 1, b) : nullptr;
+      const int cap = (int)std::min<size_t>(L.cpart_n / (size_t)s.H, 1u << 20);
+      int np = 0;
+      ok(layer_norm_bwd_dx_colsum(du, rowp(seg_in(seg), b, s.H, s.esz), rowp(at<float>(a.mu), b, 1, 4),
+                                  rowp(at<float>(a.rstd), b, 1, 4), sp[seg].g, dres, dxo,
+                                  at<float>(a.lpart_g) + (size_t)b * L.lpart_n,
+                                  at<float>(a.lpart_b) + (size_t)b * L.lpart_n,
+                                  rowp(at<float2>(a.lstat), b, 1, 8), sp[seg].dg, sp[seg].db,
+                                  (int)s.Ms, s.H, s.t, stream(b), px, cap, &np));
+      if (seg >= 1) xparts[(size_t)(seg - 1) * s.nsb + b] = np;
       grad_done(seg, GRP_LN, b);
     } else {
       ok(add_into(dres, du, dxo, (int64_t)s.Ms * s.H, s.t, stream(b)));
@@ -997,6 +1019,7 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   ex.st[1] = static_cast<cudaStream_t>(s1);
   ex.sp.resize(s.nseg);
   for (int i = 0; i < s.nseg; ++i) ex.sp[i] = seg_params(s, i, w, gr);
+  ex.xparts.assign((size_t)s.nseg * s.nsb, 0);
   if (!params_ok(s, ex.sp, bwd)) return OASES_ERR_INVALID_ARG;
   const void* io[4] = {x, dy, y, dx};  // device unless staged from host memory
   if (!stage_host)

@@ -351,6 +351,13 @@ __device__ __forceinline__ float4 raw_f4(uint2 u) {
   const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
   return make_float4(a.x, a.y, b.x, b.y);
 }
+// Four fp32 values as a T store would keep them.
+template <typename T> __device__ __forceinline__ float4 round4(float4 v);
+template <> __device__ __forceinline__ float4 round4<float>(float4 v) { return v; }
+template <> __device__ __forceinline__ float4 round4<__nv_bfloat16>(float4 v) {
+  return make_float4(__bfloat162float(__float2bfloat16(v.x)), __bfloat162float(__float2bfloat16(v.y)),
+                     __bfloat162float(__float2bfloat16(v.z)), __bfloat162float(__float2bfloat16(v.w)));
+}
 template <typename R> __device__ __forceinline__ R raw_zero();
 template <> __device__ __forceinline__ float4 raw_zero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 template <> __device__ __forceinline__ uint2 raw_zero<uint2>() { return make_uint2(0u, 0u); }
@@ -512,7 +519,7 @@ __global__ void __launch_bounds__(LNB_THREADS, 1)
 ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float* __restrict__ mean,
               const float* __restrict__ rstd, const T* __restrict__ gamma,
               const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ pg,
-              float* __restrict__ pb, int M, int H) {
+              float* __restrict__ pb, float* __restrict__ px, int M, int H) {
   extern __shared__ __align__(128) uint8_t lns_smem[];
   constexpr int NW = LNB_THREADS / 32;
   __shared__ float red[2][NW][2];
@@ -544,13 +551,14 @@ ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float
     for (int k = 0; k < LNS_STAGES && k < nrows; ++k) issue(k);
   }
   __syncthreads();
-  float4 gv[NCH], ag[NCH], ab[NCH];
+  float4 gv[NCH], ag[NCH], ab[NCH], ax[NCH];
 #pragma unroll
   for (int j = 0; j < NCH; ++j) {
     const int c = (tid + LNB_THREADS * j) * 4;
     gv[j] = c < H ? ld4(gamma + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     ag[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     ab[j] = ag[j];
+    ax[j] = ag[j];
   }
   using R = typename Raw4<T>::type;
   // the row statistics are read one row ahead
@@ -613,9 +621,16 @@ ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float
       const float4 xx = raw_f4(*reinterpret_cast<const R*>(sx + c)), g = gv[j];
       const float4 rr = dres ? raw_f4(*reinterpret_cast<const R*>(sr + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
       const float h0 = (xx.x - mu) * rs, h1 = (xx.y - mu) * rs, h2 = (xx.z - mu) * rs, h3 = (xx.w - mu) * rs;
-      st4(dx + (int64_t)row * H + c,
-          make_float4(fmaf(rs, dd.x * g.x - a1 - h0 * a2, rr.x), fmaf(rs, dd.y * g.y - a1 - h1 * a2, rr.y),
-                      fmaf(rs, dd.z * g.z - a1 - h2 * a2, rr.z), fmaf(rs, dd.w * g.w - a1 - h3 * a2, rr.w)));
+      const float4 o = make_float4(fmaf(rs, dd.x * g.x - a1 - h0 * a2, rr.x), fmaf(rs, dd.y * g.y - a1 - h1 * a2, rr.y),
+                                   fmaf(rs, dd.z * g.z - a1 - h2 * a2, rr.z), fmaf(rs, dd.w * g.w - a1 - h3 * a2, rr.w));
+      st4(dx + (int64_t)row * H + c, o);
+      if (px) {  // the column sums of dx as stored (rounded to T)
+        const float4 q = round4<T>(o);
+        ax[j].x += q.x;
+        ax[j].y += q.y;
+        ax[j].z += q.z;
+        ax[j].w += q.w;
+      }
       ag[j].x = fmaf(dd.x, h0, ag[j].x);
       ag[j].y = fmaf(dd.y, h1, ag[j].y);
       ag[j].z = fmaf(dd.z, h2, ag[j].z);
@@ -633,6 +648,7 @@ ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float
     if (c < H) {
       st4(pg + (int64_t)b * H + c, ag[j]);
       st4(pb + (int64_t)b * H + c, ab[j]);
+      if (px) st4(px + (int64_t)b * H + c, ax[j]);
     }
   }
   // every copy issued has landed before the CTA may exit (the waits above
@@ -648,8 +664,8 @@ ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float
 
 template <typename T, int NCH>
 cudaError_t ln_bwd_staged_launch_n(const float* du, const T* x, const float* mean, const float* rstd,
-                                   const T* gamma, const T* dres, T* dx, float* pg, float* pb, int M,
-                                   int H, cudaStream_t st, int* parts) {
+                                   const T* gamma, const T* dres, T* dx, float* pg, float* pb,
+                                   float*& px, int px_cap, int M, int H, cudaStream_t st, int* parts) {
   static DeviceOnce attr;
   const cudaError_t ea = attr.run([] {
     return cudaFuncSetAttribute(ln_bwd_staged<T, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -666,8 +682,9 @@ cudaError_t ln_bwd_staged_launch_n(const float* du, const T* x, const float* mea
   const int nb = (M + ROWS_PER_PART - 1) / ROWS_PER_PART;
   const int grid = std::max(1, std::min(nb, sms * std::max(per_sm, 1)));
   *parts = grid;
+  if (grid > px_cap) px = nullptr;  // no room for the dx partial rows: not taken
   return launch_pdl(ln_bwd_staged<T, NCH>, dim3(grid), dim3(LNB_THREADS), smem, st, du, x, mean, rstd,
-                    gamma, dres, dx, pg, pb, M, H);
+                    gamma, dres, dx, pg, pb, px, M, H);
 }
 
 // Rows staged through shared memory by bulk copies: every row's start and
@@ -682,14 +699,14 @@ bool ln_bwd_staged_ok(const float* du, const void* x, const void* dres, int H) {
 template <typename T>
 cudaError_t ln_bwd_staged_launch(const float* du, const void* x, const float* mean, const float* rstd,
                                  const void* gamma, const void* dres, void* dx, float* pg, float* pb,
-                                 int M, int H, cudaStream_t st, int* parts) {
+                                 float*& px, int px_cap, int M, int H, cudaStream_t st, int* parts) {
   const T *xt = (const T*)x, *gt = (const T*)gamma, *rt = (const T*)dres;
   T* dt = (T*)dx;
   switch ((H / 4 + LNB_THREADS - 1) / LNB_THREADS) {
-    case 1: return ln_bwd_staged_launch_n<T, 1>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
-    case 2: return ln_bwd_staged_launch_n<T, 2>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
-    case 3: return ln_bwd_staged_launch_n<T, 3>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
-    default: return ln_bwd_staged_launch_n<T, 4>(du, xt, mean, rstd, gt, rt, dt, pg, pb, M, H, st, parts);
+    case 1: return ln_bwd_staged_launch_n<T, 1>(du, xt, mean, rstd, gt, rt, dt, pg, pb, px, px_cap, M, H, st, parts);
+    case 2: return ln_bwd_staged_launch_n<T, 2>(du, xt, mean, rstd, gt, rt, dt, pg, pb, px, px_cap, M, H, st, parts);
+    case 3: return ln_bwd_staged_launch_n<T, 3>(du, xt, mean, rstd, gt, rt, dt, pg, pb, px, px_cap, M, H, st, parts);
+    default: return ln_bwd_staged_launch_n<T, 4>(du, xt, mean, rstd, gt, rt, dt, pg, pb, px, px_cap, M, H, st, parts);
   }
 }
 
@@ -1010,6 +1027,12 @@ cudaError_t shard_sum(const float* part, int64_t pstride, int w, const void* bia
                             : shard_sum_t<__nv_bfloat16, __nv_bfloat16>(part, pstride, w, bias, resid, out, M, N, st);
 }
 
+// out[n] += the sum of the nparts partial rows part[r][n], in a fixed order.
+cudaError_t reduce_partial_rows(float* part, float* out, int nparts, int N, cudaStream_t st) {
+  if (nparts <= 0 || N <= 0) return cudaSuccess;
+  return reduce_parts(part, out, nullptr, nullptr, nparts, N, st);
+}
+
 int norm_read_and_clear_error() {
   int v = 0, z = 0;
   if (cudaMemcpyFromSymbol(&v, g_norm_error, sizeof(int)) != cudaSuccess) return -1;
@@ -1044,10 +1067,31 @@ cudaError_t layer_norm_fwd(const void* x, const void* gamma, const void* beta, v
                     mean, rstd, M, H, eps);
 }
 
+cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float* mean,
+                                     const float* rstd, const void* gamma, const void* dres, void* dx,
+                                     float* part_g, float* part_b, float2* stat, float* dgamma,
+                                     float* dbeta, int M, int H, DType t, cudaStream_t st,
+                                     float* part_x, int part_x_cap, int* n_part_x);
+
 cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, const float* rstd,
                            const void* gamma, const void* dres, void* dx, float* part_g,
                            float* part_b, float2* stat, float* dgamma, float* dbeta, int M, int H,
                            DType t, cudaStream_t st) {
+  return layer_norm_bwd_dx_colsum(du, x, mean, rstd, gamma, dres, dx, part_g, part_b, stat, dgamma,
+                                  dbeta, M, H, t, st, nullptr, 0, nullptr);
+}
+
+// The same, and where the staged kernel runs and at most part_x_cap partial
+// rows are needed, also the column sums of dx as stored: *n_part_x partial
+// rows of H floats in part_x (16-byte aligned), for a fixed-order reduction by
+// the caller.  Otherwise *n_part_x = 0 and part_x is not written.
+cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float* mean,
+                                     const float* rstd, const void* gamma, const void* dres, void* dx,
+                                     float* part_g, float* part_b, float2* stat, float* dgamma,
+                                     float* dbeta, int M, int H, DType t, cudaStream_t st,
+                                     float* part_x, int part_x_cap, int* n_part_x) {
+  if (n_part_x) *n_part_x = 0;
+  if ((uintptr_t)part_x & 15) part_x = nullptr;
   if (M == 0) return cudaSuccess;
   // du is fp32 (16-byte vector loads); x, gamma, dres, dx 8-byte (bf16) or
   // 16-byte (fp32) vectors of 4 elements
@@ -1059,11 +1103,14 @@ cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, co
       (t == DType::F32 ? ln_bwd_staged_ok<float>(du, x, dres, H)
                        : ln_bwd_staged_ok<__nv_bfloat16>(du, x, dres, H))) {
     int parts = 0;
+    float* px = part_x;
     cudaError_t e = t == DType::F32
                         ? ln_bwd_staged_launch<float>(du, x, mean, rstd, gamma, dres, dx, part_g,
-                                                      part_b, M, H, st, &parts)
+                                                      part_b, px, part_x_cap, M, H, st, &parts)
                         : ln_bwd_staged_launch<__nv_bfloat16>(du, x, mean, rstd, gamma, dres, dx,
-                                                              part_g, part_b, M, H, st, &parts);
+                                                              part_g, part_b, px, part_x_cap, M, H, st,
+                                                              &parts);
+    if (n_part_x) *n_part_x = px ? parts : 0;
     if (e != cudaSuccess) return e;
     return reduce_parts(part_g, dgamma, part_b, dbeta, parts, H, st);
   }
