@@ -70,10 +70,18 @@ oases_status oases_debug_attention_progress(int *host_mapped);
  * [8192 + 2c] (dK/dV kernel); for CTA 0 and block j < 64, four stamps at
  * [16384 + 4j] (dQ) and [16640 + 4j] (dK/dV): S and dP MMAs issued,
  * accumulation MMAs issued, element-wise warp 2 saw S and dP, and handed over
- * its rows.  Forward: for CTA 0, query tile t (0, 1) and key block j < 64,
- * eight stamps at [16896 + 8 (64 t + j)]: S_t(j) issued, the softmax warp of
- * lane quarter 2 saw S_t(j), the warps of lane quarters 0..3 published P_t(j),
- * PV_t(j) issued.  The buffer then holds 17920 stamps.  NULL switches it off. */
+ * its rows.  Forward (persistent; an item is 256 queries of one sequence and
+ * head, items numbered heaviest first): for the first item of CTA 0, query
+ * tile t (0, 1) and key block j < 64, eight stamps at [16896 + 8 (64 t + j)]:
+ * S_t(j) issued, the softmax warp of lane quarter 2 saw S_t(j), the warps of
+ * lane quarters 0..3 published P_t(j), PV_t(j) issued, PV_t(j) about to be
+ * issued (its P and V ready); for every item
+ * i < 4096, eight stamps at [17920 + 8i]: its CTA's entry, its CTA set up, Q
+ * and K_0 of the item landed, tile 0's softmax saw S_0(0), tile 0's and tile
+ * 1's last PV complete, tile 1's O stored, its CTA's exit; at [50688 ..
+ * 50691] CTA 0's globaltimer and clock64 at its entry and exit (their deltas
+ * give the SM clock).  The buffer then holds 50692 stamps.  NULL switches it
+ * off. */
 oases_status oases_debug_attention_timeline(unsigned long long *device_buffer);
 /* Timeline of the tensor-core GEMM (debugging aid): device_buffer holds 16
  * uint64 %globaltimer stamps per CTA of every following launch (entry,

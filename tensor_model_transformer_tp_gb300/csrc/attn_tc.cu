@@ -111,7 +111,8 @@ __device__ __forceinline__ void tl_block(int kid, int j, int what) {
 }
 // Forward, CTA 0, tile t, key block j < 64: [0] S_t(j) issued, [1] the
 // softmax warp of lane quarter 2 saw S_t(j), [2 + q] the warp of lane quarter
-// q published P_t(j), [6] PV_t(j) issued.
+// q published P_t(j), [6] PV_t(j) issued, [7] PV_t(j) about to be issued (its
+// P and V ready).
 __device__ __forceinline__ void tl_fwd(int t, int j, int what) {
   unsigned long long* tb = g_attn_timeline;
   if (tb != nullptr && linear_cta() == 0 && j < 64) tb[16896 + 8 * (64 * t + j) + what] = ptx::globaltimer();
@@ -125,13 +126,23 @@ struct FwdArgs {
   int S, H, heads, M;  // sequence length, hidden, heads, rows of this call
   int causal;
   float scale_log2;    // log2(e) / sqrt(d)
+  int batch, pairs;    // sequences; pairs of 128-query tiles per sequence
+  int items;           // batch * heads * pairs
 };
 
-// Forward: one CTA per 256 queries of one (sequence, head), as two tiles of
-// 128 queries that share every K/V block, 320 threads:
-//   warp 0      TMA loads: Q of both tiles once, then K_j and V_j into
-//               two-stage rings;
-//   warp 1      TMEM allocation (512 columns); one thread issues the MMAs;
+// Forward: a persistent kernel, one CTA per SM.  A work item is 256 queries
+// of one (sequence, head): two tiles of 128 queries that share every K/V
+// block.  Items are numbered heaviest first (the causal pairs nearest the end
+// of the sequence have the most key blocks); CTA c of G takes items
+// c, 2G - 1 - c, 2G + c, ... (a snake over rounds of G, so the light items of
+// later rounds even out the heavy ones).  320 threads:
+//   warp 0      TMA loads, in the order the MMAs consume them: per item Q_0,
+//               then K_j and V_j into two-stage rings that run on across
+//               items, Q_1 after the first block; a tile's Q buffer is
+//               refilled for the next item as soon as the tile's last S MMA
+//               of this item has read it;
+//   warp 1      TMEM allocation (512 columns, once); one thread issues the
+//               MMAs;
 //   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1: thread r
 //               (TMEM lane r of its warp's quarter) owns one query row.
 // TMEM: S_t (then P_t) in columns 128 t .. +127, O_t in 256 + 128 t .. +127.
@@ -153,15 +164,71 @@ struct FwdArgs {
 // stays <= 256 and O is rescaled rarely.  Key blocks past the diagonal are
 // skipped; keys past the diagonal inside it (and past the sequence end) get
 // weight 0.  LSE = m + log(l) per (head, row) for the backward.
+// Across items: once the round that issues tile t's last PV of an item is
+// done, the MMA thread issues S_t(0) of the next item, so a tile whose item
+// ends a block early (the lower tile of a causal pair) starts the next item
+// while the other tile finishes its diagonal block, and its softmax warps
+// store O of the finished item meanwhile.  The next item's first PV_t, which
+// overwrites O_t, waits for P_t(0), which those warps publish only after
+// they have read O_t out.
 constexpr int F_NT = 320;
 constexpr int F_KST = 2, F_VST = 2;
 constexpr int F_OFF_Q = 0, F_OFF_K = 2 * TILE, F_OFF_V = F_OFF_K + F_KST * TILE;
-constexpr int F_OFF_BAR = F_OFF_V + F_VST * TILE;
-// q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full[2], drain
-constexpr int F_NBAR = 1 + 2 * F_KST + 2 * F_VST + 6 + 1;
+constexpr int F_OFF_EPI = F_OFF_V + F_VST * TILE;  // O staging: 4 KB per softmax warp
+constexpr int F_OFF_BAR = F_OFF_EPI + 8 * 4096;
+// q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2],
+// s_full[2], p_full[2], o_full[2], drain
+constexpr int F_NBAR = 4 + 2 * F_KST + 2 * F_VST + 6 + 1;
 constexpr int FWD_SMEM = F_OFF_BAR + 8 * F_NBAR + 16 + 1024;
 static_assert(FWD_SMEM <= 232448, "attention forward: more than 227 KB of shared memory");
 constexpr float RESCALE_LOG2 = 8.f;
+
+// Item k of CTA c (of G): heavy-first rounds of G items, snake order.
+__device__ __forceinline__ int fwd_item_of(int k, int c, int G) {
+  return k * G + ((k & 1) ? G - 1 - c : c);
+}
+struct FwdItem {
+  int h, b, q0;  // head, sequence, first query of the pair
+  int n0, n1;    // key blocks of each tile (0: the tile lies past the sequence end)
+};
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int i) {
+  const int bh = a.heads * a.batch;
+  FwdItem it;
+  const int pair = a.pairs - 1 - i / bh, r = i % bh;
+  it.h = r % a.heads;
+  it.b = r / a.heads;
+  it.q0 = pair * 2 * BQ;
+  const int nkv_all = (a.S + BKV - 1) / BKV;
+  const int q1 = it.q0 + BQ;
+  it.n0 = a.causal ? min(it.q0 / BKV + 1, nkv_all) : nkv_all;  // q0 < S: the pair exists
+  it.n1 = q1 >= a.S ? 0 : (a.causal ? min(q1 / BKV + 1, nkv_all) : nkv_all);
+  return it;
+}
+// Forward, every item i < 4096 (256 queries of one sequence and head): eight
+// stamps at [17920 + 8i]: [0] its CTA's entry, [1] its CTA set up, [2] Q_0 and
+// K_0 of the item landed (MMA thread), [3] tile 0's softmax saw S_0(0), [4]
+// tile 0's and [5] tile 1's last PV complete, [6] tile 1's O stored, [7] its
+// CTA's exit.
+__device__ __forceinline__ void tl_fitem(int i, int what) {
+  unsigned long long* tb = g_attn_timeline;
+  if (tb != nullptr && i < 4096) tb[17920 + 8 * i + what] = ptx::globaltimer();
+}
+__device__ __forceinline__ void tl_fitems(int items, int c, int G, int what) {
+  unsigned long long* tb = g_attn_timeline;
+  if (tb == nullptr) return;
+  const unsigned long long now = ptx::globaltimer();
+  // CTA 0's globaltimer and SM clock at entry (what 0) and exit (what 7) at
+  // [50688 + 0..3]: the two deltas give the SM clock rate over the launch
+  if (c == 0 && (what == 0 || what == 7)) {
+    tb[50688 + (what ? 2 : 0)] = now;
+    tb[50689 + (what ? 2 : 0)] = (unsigned long long)clock64();
+  }
+  for (int k = 0;; ++k) {
+    const int i = fwd_item_of(k, c, G);
+    if (i >= items) break;
+    if (i < 4096) tb[17920 + 8 * i + what] = now;
+  }
+}
 
 __global__ void __launch_bounds__(F_NT, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
@@ -170,35 +237,27 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + F_OFF_BAR;
-  const uint32_t bar_q = bars;
-  auto k_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto k_empty = [&](int s) { return bars + 8u * (1 + F_KST + s); };
-  auto v_full = [&](int s) { return bars + 8u * (1 + 2 * F_KST + s); };
-  auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * F_KST + F_VST + s); };
-  auto s_full = [&](int t) { return bars + 8u * (1 + 2 * F_KST + 2 * F_VST + t); };
-  auto p_full = [&](int t) { return bars + 8u * (3 + 2 * F_KST + 2 * F_VST + t); };
-  auto o_full = [&](int t) { return bars + 8u * (5 + 2 * F_KST + 2 * F_VST + t); };
-  const uint32_t bar_drain = bars + 8u * (7 + 2 * F_KST + 2 * F_VST);
+  auto q_full = [&](int t) { return bars + 8u * t; };
+  auto q_empty = [&](int t) { return bars + 8u * (2 + t); };
+  auto k_full = [&](int s) { return bars + 8u * (4 + s); };
+  auto k_empty = [&](int s) { return bars + 8u * (4 + F_KST + s); };
+  auto v_full = [&](int s) { return bars + 8u * (4 + 2 * F_KST + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (4 + 2 * F_KST + F_VST + s); };
+  auto s_full = [&](int t) { return bars + 8u * (4 + 2 * F_KST + 2 * F_VST + t); };
+  auto p_full = [&](int t) { return bars + 8u * (6 + 2 * F_KST + 2 * F_VST + t); };
+  auto o_full = [&](int t) { return bars + 8u * (8 + 2 * F_KST + 2 * F_VST + t); };
+  const uint32_t bar_drain = bars + 8u * (10 + 2 * F_KST + 2 * F_VST);
   const uint32_t tslot = bars + 8u * F_NBAR;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  // grid (heads, batch, pairs of tiles): the slowest index runs heavy (late) pairs first
-  const int pair = gridDim.z - 1 - blockIdx.z;
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int q0 = pair * 2 * BQ;
-  const int row0 = b * a.S;
-  const int nkv_all = (a.S + BKV - 1) / BKV;
-  int n[2];  // key blocks of each tile (0: the tile lies past the sequence end)
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qt = q0 + t * BQ;
-    n[t] = qt >= a.S ? 0 : (a.causal ? min(qt / BKV + 1, nkv_all) : nkv_all);
-  }
-  const int nmax = max(n[0], n[1]);
-  const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
+  const int cta = blockIdx.x, G = gridDim.x;
+  if (tid == 0) tl_fitems(a.items, cta, G, 0);
 
   if (tid == 0) {
-    ptx::mbar_init(bar_q, 1);
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(q_full(t), 1);
+      ptx::mbar_init(q_empty(t), 1);
+    }
     for (int s = 0; s < F_KST; ++s) {
       ptx::mbar_init(k_full(s), 1);
       ptx::mbar_init(k_empty(s), 1);
@@ -225,6 +284,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
   progress(0, 2);
+  if (tid == 0) tl_fitems(a.items, cta, G, 1);
   pdl_wait();
   pdl_trigger();
   progress(0, 3);
@@ -232,104 +292,182 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
 
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
-      const int nq = n[1] > 0 ? 2 : 1;
-      ptx::mbar_arrive_expect_tx(bar_q, nq * TILE);
-      for (int t = 0; t < nq; ++t) {
+      // ring entries loaded so far (entry e sits in stage e % depth), Q loads per tile
+      uint32_t ke = 0, ve = 0, qn[2] = {0u, 0u};
+      auto load_q = [&](const FwdItem& it, int t) {
+        if (qn[t] > 0 && !ptx::mbar_wait(q_empty(t), (qn[t] - 1) & 1)) {
+          wait_failed(10);
+          return false;
+        }
+        ptx::mbar_arrive_expect_tx(q_full(t), TILE);
         const uint32_t qt = base + F_OFF_Q + t * TILE;
-        ptx::tma_load_2d(qt, &tm, bar_q, col_q, row0 + q0 + t * BQ);
-        ptx::tma_load_2d(qt + BOX, &tm, bar_q, col_q + 64, row0 + q0 + t * BQ);
-      }
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int s = j % F_KST, r = row0 + j * BKV;
-        if (j >= F_KST && !ptx::mbar_wait(k_empty(s), ((j / F_KST) & 1) ^ 1)) {
-          ok = false;
-          wait_failed(11);
-          break;
+        const int r = it.b * a.S + it.q0 + t * BQ;
+        ptx::tma_load_2d(qt, &tm, q_full(t), it.h * D, r);
+        ptx::tma_load_2d(qt + BOX, &tm, q_full(t), it.h * D + 64, r);
+        ++qn[t];
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        const int i = fwd_item_of(k, cta, G);
+        if (i >= a.items) break;
+        const FwdItem it = fwd_item(a, i);
+        const int nmax = max(it.n0, it.n1);
+        const int col_k = a.H + it.h * D, col_v = 2 * a.H + it.h * D;
+        ok = load_q(it, 0);
+        for (int j = 0; j < nmax && ok; ++j) {
+          const int r = it.b * a.S + j * BKV;
+          const uint32_t s = ke % F_KST, u = ke / F_KST;
+          if (u > 0 && !ptx::mbar_wait(k_empty(s), (u - 1) & 1)) {
+            ok = false;
+            wait_failed(11);
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(k_full(s), TILE);
+          const uint32_t kt = base + F_OFF_K + s * TILE;
+          ptx::tma_load_2d(kt, &tm, k_full(s), col_k, r);
+          ptx::tma_load_2d(kt + BOX, &tm, k_full(s), col_k + 64, r);
+          ++ke;
+          const uint32_t sv = ve % F_VST, uv = ve / F_VST;
+          if (uv > 0 && !ptx::mbar_wait(v_empty(sv), (uv - 1) & 1)) {
+            ok = false;
+            wait_failed(12);
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(v_full(sv), TILE);
+          const uint32_t vt = base + F_OFF_V + sv * TILE;
+          ptx::tma_load_2d(vt, &tm, v_full(sv), col_v, r);
+          ptx::tma_load_2d(vt + BOX, &tm, v_full(sv), col_v + 64, r);
+          ++ve;
+          if (j == 0 && it.n1 > 0) ok = load_q(it, 1);
         }
-        ptx::mbar_arrive_expect_tx(k_full(s), TILE);
-        const uint32_t kt = base + F_OFF_K + s * TILE;
-        ptx::tma_load_2d(kt, &tm, k_full(s), col_k, r);
-        ptx::tma_load_2d(kt + BOX, &tm, k_full(s), col_k + 64, r);
-        k_issued |= 1u << s;
-        k_par = (k_par & ~(1u << s)) | ((uint32_t)((j / F_KST) & 1) << s);
-        const int sv = j % F_VST;
-        if (j >= F_VST && !ptx::mbar_wait(v_empty(sv), ((j / F_VST) & 1) ^ 1)) {
-          ok = false;
-          wait_failed(12);
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(v_full(sv), TILE);
-        const uint32_t vt = base + F_OFF_V + sv * TILE;
-        ptx::tma_load_2d(vt, &tm, v_full(sv), col_v, r);
-        ptx::tma_load_2d(vt + BOX, &tm, v_full(sv), col_v + 64, r);
-        v_issued |= 1u << sv;
-        v_par = (v_par & ~(1u << sv)) | ((uint32_t)((j / F_VST) & 1) << sv);
       }
-      // every load issued has landed before the CTA may exit
-      bool dr = ptx::mbar_wait(bar_q, 0);
-      for (int s = 0; s < F_KST; ++s)
-        if ((k_issued >> s) & 1u) dr = ptx::mbar_wait(k_full(s), (k_par >> s) & 1u) && dr;
-      for (int s = 0; s < F_VST; ++s)
-        if ((v_issued >> s) & 1u) dr = ptx::mbar_wait(v_full(s), (v_par >> s) & 1u) && dr;
+      // every load issued has landed before the CTA may exit: the last
+      // entry of each stage, the last Q of each tile
+      bool dr = true;
+      for (uint32_t s = 0; s < F_KST; ++s)
+        if (ke > s) {
+          const uint32_t e = ke - 1 - (ke - 1 + F_KST - s) % F_KST;
+          dr = ptx::mbar_wait(k_full(s), (e / F_KST) & 1) && dr;
+        }
+      for (uint32_t s = 0; s < F_VST; ++s)
+        if (ve > s) {
+          const uint32_t e = ve - 1 - (ve - 1 + F_VST - s) % F_VST;
+          dr = ptx::mbar_wait(v_full(s), (e / F_VST) & 1) && dr;
+        }
+      for (int t = 0; t < 2; ++t)
+        if (qn[t] > 0) dr = ptx::mbar_wait(q_full(t), (qn[t] - 1) & 1) && dr;
       if (!dr) wait_failed(13);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int k_have = -1, v_have = -1;  // K / V blocks already waited for
-      auto need_k = [&](int j) {
-        if (j <= k_have) return true;
-        k_have = j;
-        if (!ptx::mbar_wait(k_full(j % F_KST), (j / F_KST) & 1)) { wait_failed(14); return false; }
-        return true;
-      };
-      auto need_v = [&](int j) {
-        if (j <= v_have) return true;
-        v_have = j;
-        if (!ptx::mbar_wait(v_full(j % F_VST), (j / F_VST) & 1)) { wait_failed(15); return false; }
-        return true;
-      };
-      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
-        if (!need_k(j)) return false;
+      uint32_t qc0 = 0u, qc1 = 0u;  // Q loads consumed per tile
+      uint32_t pc0 = 0u, pc1 = 0u;  // P_t hand-overs consumed per tile
+      // K and V ring entries advance in step, one per key block of an item.
+      // Tile 1 reads an entry after tile 0 does (within an item the rounds
+      // issue tile 0 first; across items tile 1 never starts the next item
+      // before tile 0), so an entry is released by tile 1's MMA, or by tile
+      // 0's where tile 1 does not read it (last = true).
+      auto issue_s = [&](int t, uint32_t e, bool last) {  // S_t = Q_t K_e^T
+        const uint32_t s = e % F_KST;
+        if (!ptx::mbar_wait(k_full(s), (e / F_KST) & 1)) {
+          wait_failed(14);
+          return false;
+        }
         ptx::tc_fence_after();
-        const uint32_t qt = base + F_OFF_Q + t * TILE, kt = base + F_OFF_K + (j % F_KST) * TILE;
+        const uint32_t qt = base + F_OFF_Q + t * TILE, kt = base + F_OFF_K + s * TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           ptx::mma_bf16(tmem + 128u * t, kmajor_desc(qt, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
         ptx::mma_commit(s_full(t));
-        tl_fwd(t, j, 0);
+        if (last) ptx::mma_commit(k_empty(s));
         return true;
       };
-      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t read from tensor memory
-        if (!ptx::mbar_wait(p_full(t), j & 1)) { wait_failed(16); return false; }
-        if (!need_v(j)) return false;
+      auto issue_pv = [&](int t, uint32_t e, int j, int k, bool last) {  // O_t += P_t V_e
+        uint32_t& pc = t ? pc1 : pc0;
+        if (!ptx::mbar_wait(p_full(t), pc & 1)) {
+          wait_failed(16);
+          return false;
+        }
+        ++pc;
+        const uint32_t s = e % F_VST;
+        if (!ptx::mbar_wait(v_full(s), (e / F_VST) & 1)) {
+          wait_failed(15);
+          return false;
+        }
         ptx::tc_fence_after();
-        const uint32_t vt = base + F_OFF_V + (j % F_VST) * TILE;
+        if (k == 0) tl_fwd(t, j, 7);
+        const uint32_t vt = base + F_OFF_V + s * TILE;
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
           ptx::mma_bf16_ts(tmem + 256u + 128u * t, tmem + 128u * t + 8u * kk, mnmajor_desc(vt, kk),
                            IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        tl_fwd(t, j, 6);
+        if (last) ptx::mma_commit(v_empty(s));
         return true;
       };
-      ok = ptx::mbar_wait(bar_q, 0);
-      if (!ok) wait_failed(17);
-      for (int t = 0; t < 2 && ok; ++t)
-        if (n[t] > 0) ok = issue_s(t, 0);
-      if (ok && nmax > 0) ptx::mma_commit(k_empty(0));
-      for (int j = 0; j < nmax && ok; ++j) {
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n[t]) continue;
-          ok = issue_pv(t, j);
-          if (!ok) break;
-          if (j + 1 < n[t])
-            ok = issue_s(t, j + 1);
-          else
-            ptx::mma_commit(o_full(t));  // the tile's last PV
+      // S_t(0) of item it (index i, k-th of this CTA), block 0 at ring entry e0
+      auto start_tile = [&](const FwdItem& it, int i, int k, int t, uint32_t e0) {
+        uint32_t& qc = t ? qc1 : qc0;
+        if (!ptx::mbar_wait(q_full(t), qc & 1)) {
+          wait_failed(17);
+          return false;
         }
-        if (!ok) break;
-        ptx::mma_commit(v_empty(j % F_VST));                       // V_j read by both PVs
-        if (j + 1 < nmax) ptx::mma_commit(k_empty((j + 1) % F_KST));  // K_{j+1} by both S
+        ++qc;
+        if (t == 0) {
+          if (!ptx::mbar_wait(k_full(e0 % F_KST), (e0 / F_KST) & 1)) {
+            wait_failed(14);
+            return false;
+          }
+          tl_fitem(i, 2);
+        }
+        if (!issue_s(t, e0, t == 1 || it.n1 == 0)) return false;
+        if (k == 0) tl_fwd(t, 0, 0);
+        if ((t ? it.n1 : it.n0) == 1) ptx::mma_commit(q_empty(t));  // the tile's last S of the item
+        return true;
+      };
+      int k = 0, i = fwd_item_of(0, cta, G);
+      uint32_t kb = 0;  // ring entry of the current item's block 0
+      FwdItem it{};
+      if (i < a.items) {
+        it = fwd_item(a, i);
+        ok = start_tile(it, i, 0, 0, 0u);
+        if (ok && it.n1 > 0) ok = start_tile(it, i, 0, 1, 0u);
+      }
+      while (ok && i < a.items) {
+        const int nmax = max(it.n0, it.n1);
+        const int inext = fwd_item_of(k + 1, cta, G);
+        const bool has_next = inext < a.items;
+        FwdItem nx{};
+        if (has_next) nx = fwd_item(a, inext);
+        const uint32_t kb_next = kb + (uint32_t)nmax;
+        for (int j = 0; j < nmax && ok; ++j) {
+          bool done0 = false, done1 = false;  // the tile's last PV of the item issued in this round
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int n = t ? it.n1 : it.n0;
+            if (!ok || j >= n) continue;
+            ok = issue_pv(t, kb + j, j, k, t == 1 || it.n1 <= j);
+            if (!ok) break;
+            if (k == 0) tl_fwd(t, j, 6);
+            if (j + 1 < n) {
+              ok = issue_s(t, kb + j + 1, t == 1 || it.n1 <= j + 1);
+              if (!ok) break;
+              if (k == 0) tl_fwd(t, j + 1, 0);
+              if (j + 2 == n) ptx::mma_commit(q_empty(t));  // the tile's last S of the item
+            } else {
+              ptx::mma_commit(o_full(t));  // the tile's last PV of the item
+              if (t) done1 = true; else done0 = true;
+            }
+          }
+          // a tile whose item ended in this round starts the next item
+          if (ok && done0 && has_next) ok = start_tile(nx, inext, k + 1, 0, kb_next);
+          if (ok && done1 && has_next && nx.n1 > 0) ok = start_tile(nx, inext, k + 1, 1, kb_next);
+        }
+        // a tile with no blocks in this item starts the next one here
+        if (ok && has_next && it.n1 == 0 && nx.n1 > 0) ok = start_tile(nx, inext, k + 1, 1, kb_next);
+        kb = kb_next;
+        it = nx;
+        i = inext;
+        ++k;
       }
       ptx::mma_commit(bar_drain);  // completes once every MMA issued above has
       if (!ptx::mbar_wait(bar_drain, 0)) {
@@ -339,117 +477,153 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
     }
   } else {
     const int t = (warp - 2) >> 2, qq = warp & 3;
-    const int row = qq * 32 + lane, qi = q0 + t * BQ + row;
+    const int row = qq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     const uint32_t t_s = tmem + 128u * t + lane_off, t_o = tmem + 256u + 128u * t + lane_off;
-    const int qt0 = q0 + t * BQ;  // first query of the tile
-    float m_ref = -INFINITY, l = 0.f;
-    for (int j = 0; j < n[t] && ok; ++j) {
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(s_full(t), j & 1))) {
-        ok = false;
-        if (lane == 0) wait_failed(19);
-        break;
-      }
-      ptx::tc_fence_after();
-      if (qq == 2 && lane == 0) tl_fwd(t, j, 1);
-      float sv[BKV];
-      ptx::tmem_ld128(t_s, sv);
-      const int kbase = j * BKV;
-      // a block every row of the tile sees whole needs no mask (warp-uniform)
-      const bool full = (j + 1) * BKV <= a.S && (!a.causal || (j + 1) * BKV <= qt0 + 1);
-      if (!full) {
-#pragma unroll
-        for (int i = 0; i < BKV; ++i) {
-          const int key = kbase + i;
-          if (!(key < a.S && (!a.causal || key <= qi))) sv[i] = -INFINITY;
+    uint32_t sc = 0u, oc = 0u;  // S_t blocks and finished items of this tile so far
+    for (int k = 0; ok; ++k) {
+      const int i = fwd_item_of(k, cta, G);
+      if (i >= a.items) break;
+      const FwdItem it = fwd_item(a, i);
+      const int nt = t ? it.n1 : it.n0;
+      if (nt == 0) continue;
+      const int h = it.h, row0 = it.b * a.S;
+      const int qt0 = it.q0 + t * BQ;  // first query of the tile
+      const int qi = qt0 + row;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < nt && ok; ++j, ++sc) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(s_full(t), sc & 1))) {
+          ok = false;
+          if (lane == 0) wait_failed(19);
+          break;
         }
-      }
-      // row maximum of the raw scores in eight independent chains (the scale
-      // is positive, so it is applied to the maximum alone)
-      float pm[8];
+        ptx::tc_fence_after();
+        if (k == 0 && qq == 2 && lane == 0) tl_fwd(t, j, 1);
+        if (j == 0 && t == 0 && qq == 0 && lane == 0) tl_fitem(i, 3);
+        float sv[BKV];
+        ptx::tmem_ld128(t_s, sv);
+        const int kbase = j * BKV;
+        // a block every row of the tile sees whole needs no mask (warp-uniform)
+        const bool full = (j + 1) * BKV <= a.S && (!a.causal || (j + 1) * BKV <= qt0 + 1);
+        if (!full) {
+          // keys kbase + i with i >= nvis are past the diagonal or the sequence end
+          const int nvis = (a.causal ? min(qi + 1, a.S) : a.S) - kbase;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) pm[c] = sv[c];
+          for (int i = 0; i < BKV; ++i)
+            if (i >= nvis) sv[i] = -INFINITY;
+        }
+        // row maximum of the raw scores in eight independent chains (the scale
+        // is positive, so it is applied to the maximum alone)
+        float pm[8];
 #pragma unroll
-      for (int i = 8; i < BKV; ++i) pm[i % 8] = fmaxf(pm[i % 8], sv[i]);
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * a.scale_log2;
-      const float m_new = fmaxf(m_ref, mx);
-      if (j == 0) {
-        m_ref = m_new;
-      } else {
-        const bool need = m_new > m_ref + RESCALE_LOG2;
-        // S_t(j) complete => PV_t(j-1) complete: O_t may be rescaled in place
-        if (__any_sync(0xffffffffu, need)) {  // warp-uniform: tcgen05.ld/st are collective
-          const float f = need ? exp2f(m_ref - m_new) : 1.f;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            float v[32];
-            ptx::tmem_ld32(t_o + c0, v);
+        for (int c = 0; c < 8; ++c) pm[c] = sv[c];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= f;
-            ptx::tmem_st32(t_o + c0, v);
-          }
+        for (int i = 8; i < BKV; ++i) pm[i % 8] = fmaxf(pm[i % 8], sv[i]);
+        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * a.scale_log2;
+        const float m_new = fmaxf(m_ref, mx);
+        // O_t is rescaled by f (below, once P no longer needs S's registers)
+        // where the reference maximum is raised
+        float f = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_ref = m_new;
+        } else {
+          const bool need = m_new > m_ref + RESCALE_LOG2;
+          rescale = __any_sync(0xffffffffu, need);  // warp-uniform: tcgen05.ld/st are collective
           if (need) {
+            f = exp2f(m_ref - m_new);
             l *= f;
             m_ref = m_new;
           }
         }
-      }
-      // P = exp2(s * scale - m_ref) as packed bf16 over S's first 64 columns.
-      // Scale and shift in one fp32x2 FMA per pair, the row sum in four fp32x2
-      // accumulators.
-      const bool live = m_ref != -INFINITY;
-      const uint64_t sc2 = f2_splat(a.scale_log2), nm2 = f2_splat(-m_ref);
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-      // the packed word of keys (2i, 2i+1) goes to sv[i] (already consumed), so
-      // P needs no registers beyond S's
+        // P = exp2(s * scale - m_ref) as packed bf16 over S's first 64 columns.
+        // Scale and shift in one fp32x2 FMA per pair, the row sum in four fp32x2
+        // accumulators.
+        const bool live = m_ref != -INFINITY;
+        const uint64_t sc2 = f2_splat(a.scale_log2), nm2 = f2_splat(-m_ref);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        // the packed word of keys (2i, 2i+1) goes to sv[i] (already consumed), so
+        // P needs no registers beyond S's
 #pragma unroll
-      for (int i = 0; i < BKV / 2; ++i) {
-        const uint64_t x = f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), sc2, nm2);
-        float p0 = fast_exp2(f2_lo(x)), p1 = fast_exp2(f2_hi(x));
-        if (!live) p0 = p1 = 0.f;  // (a row with no visible key; x is NaN there)
-        acc[i % 4] = f2_add(acc[i % 4], f2_pack(p0, p1));
-        sv[i] = __uint_as_float(pack2(p0, p1));
-      }
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(sv[32 * half + i]);
-        ptx::tmem_st32_nowait(t_s + 32u * half, w);
-      }
-      const uint64_t acc2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-      const float rs = f2_lo(acc2) + f2_hi(acc2);
-      ptx::tmem_wait_st();
-      l += rs;
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_full(t));
-      if (lane == 0) tl_fwd(t, j, 2 + qq);
-    }
-    if (n[t] > 0) {
-      // the tile's last PV is complete (or the MMA thread gave up)
-      const bool fin = __all_sync(0xffffffffu, ptx::mbar_wait(o_full(t), 0));
-      if (!fin && lane == 0) wait_failed(20);
-      ptx::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool store = ok && fin && qi < a.S;
-      uint4* orow = reinterpret_cast<uint4*>(a.o + (int64_t)(row0 + qi) * a.H + h * D);
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(t_o + c0, v);  // every lane: warp-collective
-        if (store) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            orow[c0 / 8 + u] = make_uint4(pack2(v[8 * u] * inv, v[8 * u + 1] * inv),
-                                          pack2(v[8 * u + 2] * inv, v[8 * u + 3] * inv),
-                                          pack2(v[8 * u + 4] * inv, v[8 * u + 5] * inv),
-                                          pack2(v[8 * u + 6] * inv, v[8 * u + 7] * inv));
+        for (int i = 0; i < BKV / 2; ++i) {
+          const uint64_t x = f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), sc2, nm2);
+          float p0 = fast_exp2(f2_lo(x)), p1 = fast_exp2(f2_hi(x));
+          if (!live) p0 = p1 = 0.f;  // (a row with no visible key; x is NaN there)
+          acc[i % 4] = f2_add(acc[i % 4], f2_pack(p0, p1));
+          sv[i] = __uint_as_float(pack2(p0, p1));
         }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(sv[32 * half + i]);
+          ptx::tmem_st32_nowait(t_s + 32u * half, w);
+        }
+        const uint64_t acc2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+        const float rs = f2_lo(acc2) + f2_hi(acc2);
+        if (rescale) {
+          // S_t(j) complete => PV_t(j-1) complete: O_t may be rescaled in
+          // place; PV_t(j) waits for this warp's arrival below
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float v[32];
+            ptx::tmem_ld32(t_o + c0, v);
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i] * f);
+            ptx::tmem_st32_nowait(t_o + c0, w);
+          }
+        }
+        ptx::tmem_wait_st();
+        l += rs;
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(p_full(t));
+        if (k == 0 && lane == 0) tl_fwd(t, j, 2 + qq);
       }
-      if (store) a.lse[(int64_t)h * a.M + row0 + qi] = (m_ref + log2f(l)) * 0.69314718055994531f;
-      if (!(ok && fin)) ok = false;
+      if (!ok) break;
+      {
+        // the tile's last PV of the item is complete (or the MMA thread gave up)
+        const bool fin = __all_sync(0xffffffffu, ptx::mbar_wait(o_full(t), oc & 1));
+        ++oc;
+        if (!fin && lane == 0) wait_failed(20);
+        if (qq == 0 && lane == 0) tl_fitem(i, 4 + t);
+        ptx::tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool store = ok && fin && qi < a.S;
+        // O rows through this warp's 4 KB slice of shared memory, 64 columns
+        // at a time: lane r writes its row's 128 bytes as eight 16-byte
+        // chunks (chunk c at c ^ (r & 7), so eight lanes cover all banks),
+        // then each store instruction writes 4 rows x 128 contiguous bytes
+        uint8_t* stg = gbase + F_OFF_EPI + (warp - 2) * 4096;
+        const int rw0 = qt0 + qq * 32;  // first query row of this warp
+        __nv_bfloat16* ow = a.o + (int64_t)(row0 + rw0) * a.H + h * D;
+        float v[D];
+        ptx::tmem_ld128(t_o, v);  // the whole row in one load (every lane: warp-collective)
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 64) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float* x = v + c0 + 8 * c;
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(pack2(x[0] * inv, x[1] * inv), pack2(x[2] * inv, x[3] * inv),
+                           pack2(x[4] * inv, x[5] * inv), pack2(x[6] * inv, x[7] * inv));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = 4 * u + (lane >> 3), c = lane & 7;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
+            if (ok && fin && rw0 + r < a.S)
+              *reinterpret_cast<uint4*>(ow + (int64_t)r * a.H + c0 + 8 * c) = w;
+          }
+          __syncwarp();
+        }
+        if (store) a.lse[(int64_t)h * a.M + row0 + qi] = (m_ref + log2f(l)) * 0.69314718055994531f;
+        if (!(ok && fin)) ok = false;
+        if (t == 1 && qq == 0 && lane == 0) tl_fitem(i, 6);
+      }
     }
   }
   if (!ok) atomicExch(&g_attn_error, 1);
@@ -460,6 +634,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
     ptx::tmem_dealloc(tmem, 512);
   }
   progress(0, 999);
+  if (tid == 0) tl_fitems(a.items, cta, G, 7);
 }
 
 // ---------------------------------------------------------------------------
@@ -1183,10 +1358,19 @@ cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   fa.M = M;
   fa.causal = a.causal ? 1 : 0;
   fa.scale_log2 = 1.4426950408889634f / sqrtf((float)a.head_dim);
-  const int pairs = (a.seq + 2 * BQ - 1) / (2 * BQ);
-  if (pairs > 65535 || a.batch > 65535) return cudaErrorInvalidConfiguration;
-  const dim3 grid(a.heads, a.batch, pairs);
-  return launch_pdl(attn_fwd_tc_kernel, grid, dim3(F_NT), FWD_SMEM, st, m, fa);
+  const int64_t pairs = (a.seq + 2 * BQ - 1) / (2 * BQ);
+  const int64_t items = pairs * a.batch * a.heads;
+  if (items > (int64_t)INT32_MAX / 2) return cudaErrorInvalidConfiguration;
+  fa.batch = a.batch;
+  fa.pairs = (int)pairs;
+  fa.items = (int)items;
+  // persistent: one CTA per SM (shared memory and tensor memory allow one)
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<int64_t>(items, std::max(sms, 1));
+  return launch_pdl(attn_fwd_tc_kernel, dim3(grid), dim3(F_NT), FWD_SMEM, st, m, fa);
 }
 
 cudaError_t attention_delta(const AttnArgs& a, cudaStream_t st);
