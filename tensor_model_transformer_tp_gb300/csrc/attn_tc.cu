@@ -98,10 +98,10 @@ __device__ __forceinline__ void progress(int kid, int code) {
 __device__ __forceinline__ int linear_cta() {
   return blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
 }
-// kid 1 = dq, 2 = dK/dV; what 0 = entry, 1 = exit (thread 0)
-__device__ __forceinline__ void tl_cta(int kid, int what) {
+// kid 1 = dq, 2 = dK/dV; work item c of the persistent kernel; what 0 =
+// start (its first MMAs issued), 1 = end (its gradient stored)
+__device__ __forceinline__ void tl_unit(int kid, int c, int what) {
   unsigned long long* t = g_attn_timeline;
-  const int c = linear_cta();
   if (t != nullptr && c < 4096) t[(kid - 1) * 8192 + 2 * c + what] = ptx::globaltimer();
 }
 __device__ __forceinline__ void tl_block(int kid, int j, int what) {
@@ -183,8 +183,9 @@ constexpr int FWD_SMEM = F_OFF_BAR + 8 * F_NBAR + 16 + 1024;
 static_assert(FWD_SMEM <= 232448, "attention forward: more than 227 KB of shared memory");
 constexpr float RESCALE_LOG2 = 8.f;
 
-// Item k of CTA c (of G): heavy-first rounds of G items, snake order.
-__device__ __forceinline__ int fwd_item_of(int k, int c, int G) {
+// Item k of CTA c (of G) in a persistent kernel whose items are numbered
+// heaviest first: rounds of G items, in snake order.
+__device__ __forceinline__ int persistent_item(int k, int c, int G) {
   return k * G + ((k & 1) ? G - 1 - c : c);
 }
 struct FwdItem {
@@ -224,7 +225,7 @@ __device__ __forceinline__ void tl_fitems(int items, int c, int G, int what) {
     tb[50689 + (what ? 2 : 0)] = (unsigned long long)clock64();
   }
   for (int k = 0;; ++k) {
-    const int i = fwd_item_of(k, c, G);
+    const int i = persistent_item(k, c, G);
     if (i >= items) break;
     if (i < 4096) tb[17920 + 8 * i + what] = now;
   }
@@ -308,7 +309,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         return true;
       };
       for (int k = 0; ok; ++k) {
-        const int i = fwd_item_of(k, cta, G);
+        const int i = persistent_item(k, cta, G);
         if (i >= a.items) break;
         const FwdItem it = fwd_item(a, i);
         const int nmax = max(it.n0, it.n1);
@@ -424,7 +425,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         if ((t ? it.n1 : it.n0) == 1) ptx::mma_commit(q_empty(t));  // the tile's last S of the item
         return true;
       };
-      int k = 0, i = fwd_item_of(0, cta, G);
+      int k = 0, i = persistent_item(0, cta, G);
       uint32_t kb = 0;  // ring entry of the current item's block 0
       FwdItem it{};
       if (i < a.items) {
@@ -434,7 +435,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
       }
       while (ok && i < a.items) {
         const int nmax = max(it.n0, it.n1);
-        const int inext = fwd_item_of(k + 1, cta, G);
+        const int inext = persistent_item(k + 1, cta, G);
         const bool has_next = inext < a.items;
         FwdItem nx{};
         if (has_next) nx = fwd_item(a, inext);
@@ -482,7 +483,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
     const uint32_t t_s = tmem + 128u * t + lane_off, t_o = tmem + 256u + 128u * t + lane_off;
     uint32_t sc = 0u, oc = 0u;  // S_t blocks and finished items of this tile so far
     for (int k = 0; ok; ++k) {
-      const int i = fwd_item_of(k, cta, G);
+      const int i = persistent_item(k, cta, G);
       if (i >= a.items) break;
       const FwdItem it = fwd_item(a, i);
       const int nt = t ? it.n1 : it.n0;
@@ -652,6 +653,8 @@ struct BwdArgs {
   int S, H, heads, M, causal;
   float scale_log2;  // log2(e) / sqrt(d)
   float scale;       // 1 / sqrt(d)
+  int batch, tiles;  // sequences; 128-row tiles per sequence
+  int items;         // batch * heads * tiles
 };
 
 // Both backward kernels are warp-specialised pipelines: one warp issues the
@@ -686,9 +689,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, BWD_WAIT));
 }
 
-// dq kernel: one CTA per 128 queries, 128-key blocks, 608 threads:
-//   warp 0       TMA loads (Q and dO once, then K_j into a three-stage ring
-//                and V_j into a two-stage ring);
+// dq kernel: persistent, one CTA per SM.  A work item is 128 queries of one
+// (sequence, head), looped over 128-key blocks; items are numbered heaviest
+// first (the causal tiles nearest the end of a sequence see the most keys)
+// and CTA c of G takes items c, 2G - 1 - c, 2G + c, ...  608 threads:
+//   warp 0       TMA loads in the order they are consumed: per item K_0 and
+//                V_0, then Q and dO (once the previous item's last S and dP
+//                MMAs have read them), then K_j into a three-stage and V_j
+//                into a two-stage ring; the rings run on across items;
 //   warp 1       TMEM allocation; one thread issues the S and dP MMAs;
 //   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
 //                query row each) and columns 32 ((w - 2) / 4) .. + 31 of a block;
@@ -710,16 +718,43 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
 // MMAs that wait for them.  Every MMA is 128 x 128 x 16 (one MMA's tensor
 // work, 64 clocks, exceeds its issue cost).
 // TMEM: S 0..127, dP 128..255, dQ 256..383, dS 384..447.
+// Across items: the next item's first dQ MMA (which overwrites dQ) waits for
+// its first dS, which the element-wise warps hand over only after they have
+// read the finished item's dQ out of TMEM.
 constexpr int DQ_NT = 608;
 constexpr int DQ_ACC_WARP = 18;  // issues the dQ accumulation MMAs
 constexpr int DQ_EW = 16;               // element-wise warps, four per lane quarter
 constexpr int DQ_KST = 3, DQ_VST = 2;   // K and V stages of 128 keys
 constexpr int DQ_OFF_Q = 0, DQ_OFF_DO = TILE, DQ_OFF_K = 2 * TILE;
 constexpr int DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE, DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE;
-// dO, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full, sdp_empty, ds_full, ds_empty, fin, sdp_drain
-constexpr int DQ_NBAR = 1 + 2 * DQ_KST + 2 * DQ_VST + 6;
+// qdo_full, qdo_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full,
+// sdp_empty, ds_full, ds_empty, fin, sdp_drain
+constexpr int DQ_NBAR = 2 + 2 * DQ_KST + 2 * DQ_VST + 6;
 constexpr int DQ_SMEM = DQ_OFF_BAR + 8 * DQ_NBAR + 16 + 1024;
 static_assert(DQ_SMEM <= 232448, "dq kernel: more than 227 KB of shared memory");
+
+// Brings a 2-D box of the tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+struct DqItem {
+  int h, bb, q0, n;  // head, sequence, first query, key blocks
+};
+__device__ __forceinline__ DqItem dq_item(const BwdArgs& a, int i) {
+  const int bh = a.heads * a.batch;
+  const int tile = a.tiles - 1 - i / bh, r = i % bh;
+  const int nkv_all = (a.S + BKV - 1) / BKV;
+  DqItem it;
+  it.h = r % a.heads;
+  it.bb = r / a.heads;
+  it.q0 = tile * BQ;
+  it.n = a.causal ? min(tile + 1, nkv_all) : nkv_all;
+  return it;
+}
 
 __global__ void __launch_bounds__(DQ_NT, 1)
 attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
@@ -729,28 +764,22 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + DQ_OFF_BAR;
-  const uint32_t bar_qdo = bars;
-  auto k_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto k_empty = [&](int s) { return bars + 8u * (1 + DQ_KST + s); };
-  auto v_full = [&](int s) { return bars + 8u * (1 + 2 * DQ_KST + s); };
-  auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * DQ_KST + DQ_VST + s); };
-  const uint32_t sdp_full = bars + 8u * (1 + 2 * DQ_KST + 2 * DQ_VST), sdp_empty = sdp_full + 8u;
+  const uint32_t qdo_full = bars, qdo_empty = bars + 8u;
+  auto k_full = [&](uint32_t s) { return bars + 8u * (2 + s); };
+  auto k_empty = [&](uint32_t s) { return bars + 8u * (2 + DQ_KST + s); };
+  auto v_full = [&](uint32_t s) { return bars + 8u * (2 + 2 * DQ_KST + s); };
+  auto v_empty = [&](uint32_t s) { return bars + 8u * (2 + 2 * DQ_KST + DQ_VST + s); };
+  const uint32_t sdp_full = bars + 8u * (2 + 2 * DQ_KST + 2 * DQ_VST), sdp_empty = sdp_full + 8u;
   const uint32_t ds_full = sdp_full + 16u, ds_empty = sdp_full + 24u, bar_fin = sdp_full + 32u;
   const uint32_t sdp_drain = sdp_full + 40u;
   const uint32_t tslot = bars + 8u * DQ_NBAR;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  // grid (heads, batch, tiles): the slowest index runs longest causal rows first
-  const int tile = gridDim.z - 1 - blockIdx.z;
-  const int h = blockIdx.x, bb = blockIdx.y;
-  const int q0 = tile * BQ, row0 = bb * a.S;
-  const int nkv_all = (a.S + BKV - 1) / BKV;
-  const int n = a.causal ? min(tile + 1, nkv_all) : nkv_all;
-  const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
-  if (tid == 0) tl_cta(1, 0);
+  const int cta = blockIdx.x, G = gridDim.x;
 
   if (tid == 0) {
-    ptx::mbar_init(bar_qdo, 1);
+    ptx::mbar_init(qdo_full, 1);
+    ptx::mbar_init(qdo_empty, 1);
     for (int s = 0; s < DQ_KST; ++s) {
       ptx::mbar_init(k_full(s), 1);
       ptx::mbar_init(k_empty(s), 1);
@@ -786,168 +815,260 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
 
   if (warp == 0) {
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(bar_qdo, 2 * TILE);
-      ptx::tma_load_2d(base + DQ_OFF_Q, &tq128, bar_qdo, col_q, row0 + q0);
-      ptx::tma_load_2d(base + DQ_OFF_Q + BOX, &tq128, bar_qdo, col_q + 64, row0 + q0);
-      ptx::tma_load_2d(base + DQ_OFF_DO, &tdo128, bar_qdo, h * D, row0 + q0);
-      ptx::tma_load_2d(base + DQ_OFF_DO + BOX, &tdo128, bar_qdo, h * D + 64, row0 + q0);
-      int nk = 0, nv = 0;  // blocks whose K, V loads were issued
-      for (int j = 0; j < n; ++j) {
-        const int sk = j % DQ_KST, sv = j % DQ_VST, r = row0 + j * BKV;
-        if (j >= DQ_KST && !ptx::mbar_wait(k_empty(sk), ((j / DQ_KST) & 1) ^ 1, BWD_WAIT)) {
-          ok = false;
-          wait_failed(101);
-          break;
-        }
+      // K and V ring entries loaded (entry e in stage e % depth), Q/dO loads
+      uint32_t ke = 0, ve = 0, nq = 0;
+      auto load_kv = [&](int r, int col_k, int col_v) {
+        const uint32_t sk = ke % DQ_KST, uk = ke / DQ_KST;
+        if (uk > 0 && !ptx::mbar_wait(k_empty(sk), (uk - 1) & 1, BWD_WAIT)) return false;
         const uint32_t kt = base + DQ_OFF_K + sk * TILE;
         ptx::mbar_arrive_expect_tx(k_full(sk), TILE);
         ptx::tma_load_2d(kt, &tq128, k_full(sk), col_k, r);
         ptx::tma_load_2d(kt + BOX, &tq128, k_full(sk), col_k + 64, r);
-        nk = j + 1;
-        if (j >= DQ_VST && !ptx::mbar_wait(v_empty(sv), ((j / DQ_VST) & 1) ^ 1, BWD_WAIT)) {
-          ok = false;
-          wait_failed(101);
-          break;
-        }
+        ++ke;
+        const uint32_t sv = ve % DQ_VST, uv = ve / DQ_VST;
+        if (uv > 0 && !ptx::mbar_wait(v_empty(sv), (uv - 1) & 1, BWD_WAIT)) return false;
         const uint32_t vt = base + DQ_OFF_V + sv * TILE;
         ptx::mbar_arrive_expect_tx(v_full(sv), TILE);
         ptx::tma_load_2d(vt, &tq128, v_full(sv), col_v, r);
         ptx::tma_load_2d(vt + BOX, &tq128, v_full(sv), col_v + 64, r);
-        nv = j + 1;
+        ++ve;
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        const int i = persistent_item(k, cta, G);
+        if (i >= a.items) break;
+        const DqItem it = dq_item(a, i);
+        const int row0 = it.bb * a.S, col_k = a.H + it.h * D, col_v = 2 * a.H + it.h * D;
+        ok = load_kv(row0, col_k, col_v);
+        // Q and dO are free once the previous item's last S and dP are done
+        if (ok && nq > 0 && !ptx::mbar_wait(qdo_empty, (nq - 1) & 1, BWD_WAIT)) ok = false;
+        if (!ok) {
+          wait_failed(101);
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(qdo_full, 2 * TILE);
+        ptx::tma_load_2d(base + DQ_OFF_Q, &tq128, qdo_full, it.h * D, row0 + it.q0);
+        ptx::tma_load_2d(base + DQ_OFF_Q + BOX, &tq128, qdo_full, it.h * D + 64, row0 + it.q0);
+        ptx::tma_load_2d(base + DQ_OFF_DO, &tdo128, qdo_full, it.h * D, row0 + it.q0);
+        ptx::tma_load_2d(base + DQ_OFF_DO + BOX, &tdo128, qdo_full, it.h * D + 64, row0 + it.q0);
+        ++nq;
+        // the next item's Q and dO into L2, so that their load at the item
+        // change (Q and dO are single-buffered) comes from L2
+        const int inext = persistent_item(k + 1, cta, G);
+        if (inext < a.items) {
+          const DqItem nx = dq_item(a, inext);
+          const int rn = nx.bb * a.S + nx.q0;
+          tma_prefetch_l2(&tq128, nx.h * D, rn);
+          tma_prefetch_l2(&tq128, nx.h * D + 64, rn);
+          tma_prefetch_l2(&tdo128, nx.h * D, rn);
+          tma_prefetch_l2(&tdo128, nx.h * D + 64, rn);
+        }
+        for (int j = 1; j < it.n && ok; ++j) ok = load_kv(row0 + j * BKV, col_k, col_v);
+        if (!ok) wait_failed(101);
       }
-      // every load issued has landed before the CTA may exit
-      bool dr = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
-      // (stage s of a ring of R stages last held block s + R ((m - 1 - s) / R)
-      // of the m issued, in round (m - 1 - s) / R)
-      for (int s = 0; s < DQ_KST && s < nk; ++s)
-        dr = ptx::mbar_wait(k_full(s), ((nk - 1 - s) / DQ_KST) & 1, BWD_WAIT) && dr;
-      for (int s = 0; s < DQ_VST && s < nv; ++s)
-        dr = ptx::mbar_wait(v_full(s), ((nv - 1 - s) / DQ_VST) & 1, BWD_WAIT) && dr;
+      // every load issued has landed before the CTA may exit: the last entry
+      // of each stage, the last Q/dO
+      bool dr = true;
+      for (uint32_t s = 0; s < DQ_KST; ++s)
+        if (ke > s) {
+          const uint32_t e = ke - 1 - (ke - 1 - s) % DQ_KST;
+          dr = ptx::mbar_wait(k_full(s), (e / DQ_KST) & 1, BWD_WAIT) && dr;
+        }
+      for (uint32_t s = 0; s < DQ_VST; ++s)
+        if (ve > s) {
+          const uint32_t e = ve - 1 - (ve - 1 - s) % DQ_VST;
+          dr = ptx::mbar_wait(v_full(s), (e / DQ_VST) & 1, BWD_WAIT) && dr;
+        }
+      if (nq > 0) dr = ptx::mbar_wait(qdo_full, (nq - 1) & 1, BWD_WAIT) && dr;
       if (!dr) wait_failed(102);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      ok = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
-      if (!ok) wait_failed(103);
-      auto sdp = [&](int j) {  // S_j = Q K_j^T, dP_j = dO V_j^T
-        const int sk = j % DQ_KST, sv = j % DQ_VST;
-        if (!ptx::mbar_wait(k_full(sk), (j / DQ_KST) & 1, BWD_WAIT) ||
-            !ptx::mbar_wait(v_full(sv), (j / DQ_VST) & 1, BWD_WAIT)) {
-          wait_failed(104);
-          return false;
+      uint32_t g = 0;  // blocks so far over all items (= K/V ring entries)
+      for (int k = 0; ok; ++k) {
+        const int i = persistent_item(k, cta, G);
+        if (i >= a.items) break;
+        const DqItem it = dq_item(a, i);
+        if (!ptx::mbar_wait(qdo_full, k & 1, BWD_WAIT)) {
+          ok = false;
+          wait_failed(103);
+          break;
         }
-        // the element-wise warps have loaded block j-1's S and dP
-        if (j >= 1 && !ptx::mbar_wait(sdp_empty, (j - 1) & 1, BWD_WAIT)) { wait_failed(105); return false; }
-        ptx::tc_fence_after();
-        const uint32_t kt = base + DQ_OFF_K + sk * TILE, vt = base + DQ_OFF_V + sv * TILE;
+        for (int j = 0; j < it.n && ok; ++j, ++g) {  // S_j = Q K_j^T, dP_j = dO V_j^T
+          const uint32_t sk = g % DQ_KST, sv = g % DQ_VST;
+          if (!ptx::mbar_wait(k_full(sk), (g / DQ_KST) & 1, BWD_WAIT) ||
+              !ptx::mbar_wait(v_full(sv), (g / DQ_VST) & 1, BWD_WAIT)) {
+            ok = false;
+            wait_failed(104);
+            break;
+          }
+          // the element-wise warps have loaded the previous block's S and dP
+          if (g >= 1 && !ptx::mbar_wait(sdp_empty, (g - 1) & 1, BWD_WAIT)) {
+            ok = false;
+            wait_failed(105);
+            break;
+          }
+          ptx::tc_fence_after();
+          if (j == 0) tl_unit(1, i, 0);
+          const uint32_t kt = base + DQ_OFF_K + sk * TILE, vt = base + DQ_OFF_V + sv * TILE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16(t_s, kmajor_desc(base + DQ_OFF_Q, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_bf16(t_s, kmajor_desc(base + DQ_OFF_Q, kk), kmajor_desc(kt, kk), IDESC_S, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16(t_dp, kmajor_desc(base + DQ_OFF_DO, kk), kmajor_desc(vt, kk), IDESC_S, kk > 0);
-        ptx::mma_commit(sdp_full);
-        ptx::mma_commit(v_empty(sv));
-        tl_block(1, j, 0);
-        return true;
-      };
-      for (int j = 0; j < n && ok; ++j) ok = sdp(j);
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_bf16(t_dp, kmajor_desc(base + DQ_OFF_DO, kk), kmajor_desc(vt, kk), IDESC_S, kk > 0);
+          ptx::mma_commit(sdp_full);
+          ptx::mma_commit(v_empty(sv));
+          if (j + 1 == it.n) ptx::mma_commit(qdo_empty);  // the item's last read of Q and dO
+          if (k == 0) tl_block(1, j, 0);
+        }
+      }
       ptx::mma_commit(sdp_drain);  // completes once every MMA this thread issued has
-      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) { ok = false; wait_failed(107); }
+      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) {
+        ok = false;
+        wait_failed(107);
+      }
     }
   } else if (warp == DQ_ACC_WARP) {
     if (lane == 0) {
-      ok = ptx::mbar_wait(bar_qdo, 0, BWD_WAIT);
-      if (!ok) wait_failed(110);
-      auto acc = [&](int j) {  // dQ += dS_j K_j (contraction over the block's 128 keys)
-        const int sk = j % DQ_KST;
-        if (!ptx::mbar_wait(ds_full, j & 1, BWD_WAIT)) { wait_failed(106); return false; }
-        ptx::tc_fence_after();
-        const uint32_t kt = base + DQ_OFF_K + sk * TILE;
+      uint32_t g = 0;
+      int nk = 0;  // items finished
+      for (int k = 0; ok; ++k) {
+        const int i = persistent_item(k, cta, G);
+        if (i >= a.items) break;
+        const DqItem it = dq_item(a, i);
+        for (int j = 0; j < it.n && ok; ++j, ++g) {  // dQ += dS_j K_j (over the block's 128 keys)
+          const uint32_t sk = g % DQ_KST;
+          if (!ptx::mbar_wait(ds_full, g & 1, BWD_WAIT)) {
+            ok = false;
+            wait_failed(106);
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t kt = base + DQ_OFF_K + sk * TILE;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          ptx::mma_bf16_ts(t_dq, t_ds + 8u * kk, mnmajor_desc(kt, kk), IDESC_PV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-        // S_j, dP_j (which also read K_j) completed before the element-wise
-        // warps could hand over dS_j, so K_j is free once these MMAs are
-        ptx::mma_commit(ds_empty);
-        ptx::mma_commit(k_empty(sk));
-        tl_block(1, j, 1);
-        return true;
-      };
-      for (int j = 0; j < n && ok; ++j) ok = acc(j);
-      ptx::mma_commit(bar_fin);  // completes once every MMA this thread issued has
-      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(111); }
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            ptx::mma_bf16_ts(t_dq, t_ds + 8u * kk, mnmajor_desc(kt, kk), IDESC_PV,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+          // S_j, dP_j (which also read K_j) completed before the element-wise
+          // warps could hand over dS_j, so K_j is free once these MMAs are
+          ptx::mma_commit(ds_empty);
+          ptx::mma_commit(k_empty(sk));
+          if (k == 0) tl_block(1, j, 1);
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar_fin);  // the item's dQ is complete once this does
+        nk = k + 1;
+      }
+      // every MMA this thread issued is complete before the CTA may exit
+      if (nk > 0 && !ptx::mbar_wait(bar_fin, (nk - 1) & 1, BWD_WAIT)) {
+        ok = false;
+        wait_failed(111);
+      }
+      if (!ok) {  // one more commit drains whatever was issued after the last finished item
+        ptx::mma_commit(bar_fin);
+        (void)ptx::mbar_wait(bar_fin, nk & 1, BWD_WAIT);
+      }
     }
   } else {
     const int qq = warp & 3, sub = (warp - 2) >> 2;  // lane quarter; columns 32 sub .. + 31
-    const int row = qq * 32 + lane, qi = q0 + row;
-    const bool valid_q = qi < a.S;
-    const float lse2 = valid_q ? a.lse[(int64_t)h * a.M + row0 + qi] * 1.4426950408889634f : 0.f;
-    const float dlt = valid_q ? a.delta[(int64_t)h * a.M + row0 + qi] : 0.f;
+    const int row = qq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    for (int j = 0; j < n && ok; ++j) {
-      if (!warp_wait(sdp_full, j & 1)) { ok = false; if (lane == 0) wait_failed(108); break; }
-      if (warp == 2 && lane == 0) tl_block(1, j, 2);
-      ptx::tc_fence_after();
-      float v[32], w[32];
-      ptx::tmem_ld32x2(t_s + lane_off + sub * 32, t_dp + lane_off + sub * 32, v, w);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sdp_empty);  // the TMEM buffers may be overwritten
-      const int kbase = j * BKV + sub * 32;
-      // a block wholly visible to every row of the tile needs no mask (CTA-uniform)
-      const bool full = q0 + BQ <= a.S && (j + 1) * BKV <= a.S && (!a.causal || (j + 1) * BKV <= q0 + 1);
-      uint32_t pk[16];  // dS as packed bf16 pairs (keys 2i, 2i+1 of these 32)
-      if (full) {
-        const uint64_t sc = f2_splat(a.scale_log2), nl = f2_splat(-lse2), nd = f2_splat(-dlt);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), sc, nl);
-          const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
-          const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[2 * i], w[2 * i + 1]), nd));
-          pk[i] = pack2(f2_lo(ds), f2_hi(ds));
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = kbase + i;
-          const bool valid = valid_q && key < a.S && (!a.causal || key <= qi);
-          const float p = valid ? fast_exp2(v[i] * a.scale_log2 - lse2) : 0.f;
-          v[i] = p * (w[i] - dlt);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack2(v[2 * i], v[2 * i + 1]);
+    uint32_t g = 0;
+    // this row's LSE (base 2) and delta of an item, read one item ahead
+    auto stats = [&](int i, float& lse2, float& dlt) {
+      lse2 = 0.f;
+      dlt = 0.f;
+      if (i >= a.items) return;
+      const DqItem it = dq_item(a, i);
+      const int qi = it.q0 + row;
+      if (qi < a.S) {
+        const int64_t o = (int64_t)it.h * a.M + it.bb * a.S + qi;
+        lse2 = a.lse[o] * 1.4426950408889634f;
+        dlt = a.delta[o];
       }
-      // the dS columns are free once the previous block's dQ MMAs are done
-      if (j >= 1 && !warp_wait(ds_empty, (j - 1) & 1)) {
-        ok = false;
-        if (lane == 0) wait_failed(109);
-        break;
-      }
-      ptx::tc_fence_after();
-      ptx::tmem_st16_nowait(t_ds + lane_off + sub * 16, pk);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ds_full);
-      if (warp == 2 && lane == 0) tl_block(1, j, 3);
-    }
-    // the last accumulation is complete (or the MMA thread gave up)
-    const bool fin = warp_wait(bar_fin, 0);
-    ptx::tc_fence_after();
-    float v0[32];  // tcgen05.ld is warp-collective: every lane loads
-    ptx::tmem_ld32(t_dq + lane_off + sub * 32, v0);
-    if (ok && fin && valid_q) {
-      uint4* out = reinterpret_cast<uint4*>(a.dqkv + (int64_t)(row0 + qi) * 3 * a.H + h * D + sub * 32);
+    };
+    float lse2_next, dlt_next;
+    stats(persistent_item(0, cta, G), lse2_next, dlt_next);
+    for (int k = 0; ok; ++k) {
+      const int i = persistent_item(k, cta, G);
+      if (i >= a.items) break;
+      const DqItem it = dq_item(a, i);
+      const int q0 = it.q0, row0 = it.bb * a.S, h = it.h, n = it.n;
+      const int qi = q0 + row;
+      const bool valid_q = qi < a.S;
+      const float lse2 = lse2_next, dlt = dlt_next;
+      stats(persistent_item(k + 1, cta, G), lse2_next, dlt_next);
+      for (int j = 0; j < n && ok; ++j, ++g) {
+        if (!warp_wait(sdp_full, g & 1)) {
+          ok = false;
+          if (lane == 0) wait_failed(108);
+          break;
+        }
+        if (k == 0 && warp == 2 && lane == 0) tl_block(1, j, 2);
+        ptx::tc_fence_after();
+        float v[32], w[32];
+        ptx::tmem_ld32x2(t_s + lane_off + sub * 32, t_dp + lane_off + sub * 32, v, w);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sdp_empty);  // the TMEM buffers may be overwritten
+        // a block wholly visible to every row of the tile needs no mask (CTA-uniform)
+        const bool full = q0 + BQ <= a.S && (j + 1) * BKV <= a.S && (!a.causal || (j + 1) * BKV <= q0 + 1);
+        uint32_t pk[16];  // dS as packed bf16 pairs (keys 2i, 2i+1 of these 32)
+        if (full) {
+          const uint64_t sc = f2_splat(a.scale_log2), nl = f2_splat(-lse2), nd = f2_splat(-dlt);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        out[u] = make_uint4(pack2(v0[8 * u] * a.scale, v0[8 * u + 1] * a.scale),
-                            pack2(v0[8 * u + 2] * a.scale, v0[8 * u + 3] * a.scale),
-                            pack2(v0[8 * u + 4] * a.scale, v0[8 * u + 5] * a.scale),
-                            pack2(v0[8 * u + 6] * a.scale, v0[8 * u + 7] * a.scale));
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const uint64_t x = f2_fma(f2_pack(v[2 * i2], v[2 * i2 + 1]), sc, nl);
+            const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
+            const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[2 * i2], w[2 * i2 + 1]), nd));
+            pk[i2] = pack2(f2_lo(ds), f2_hi(ds));
+          }
+        } else {
+          // keys j BKV + 32 sub + c with c >= nvis are past the diagonal or the
+          // sequence end (all of them for a row past the end)
+          const int nvis = valid_q ? (a.causal ? min(qi + 1, a.S) : a.S) - (j * BKV + sub * 32) : 0;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p = c < nvis ? fast_exp2(v[c] * a.scale_log2 - lse2) : 0.f;
+            v[c] = p * (w[c] - dlt);
+          }
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) pk[i2] = pack2(v[2 * i2], v[2 * i2 + 1]);
+        }
+        // the dS columns are free once the previous block's dQ MMAs are done
+        if (g >= 1 && !warp_wait(ds_empty, (g - 1) & 1)) {
+          ok = false;
+          if (lane == 0) wait_failed(109);
+          break;
+        }
+        ptx::tc_fence_after();
+        ptx::tmem_st16_nowait(t_ds + lane_off + sub * 16, pk);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ds_full);
+        if (k == 0 && warp == 2 && lane == 0) tl_block(1, j, 3);
+      }
+      if (!ok) break;
+      // the item's last accumulation is complete (or the MMA thread gave up)
+      const bool fin = warp_wait(bar_fin, k & 1);
+      ptx::tc_fence_after();
+      float v0[32];  // tcgen05.ld is warp-collective: every lane loads
+      ptx::tmem_ld32(t_dq + lane_off + sub * 32, v0);
+      if (fin && valid_q) {
+        uint4* out = reinterpret_cast<uint4*>(a.dqkv + (int64_t)(row0 + qi) * 3 * a.H + h * D + sub * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          out[u] = make_uint4(pack2(v0[8 * u] * a.scale, v0[8 * u + 1] * a.scale),
+                              pack2(v0[8 * u + 2] * a.scale, v0[8 * u + 3] * a.scale),
+                              pack2(v0[8 * u + 4] * a.scale, v0[8 * u + 5] * a.scale),
+                              pack2(v0[8 * u + 6] * a.scale, v0[8 * u + 7] * a.scale));
+      }
+      if (!fin) ok = false;
+      if (warp == 2 && lane == 0) tl_unit(1, i, 1);
     }
-    if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 3);
+    if (!ok && lane == 0) atomicExch(&g_attn_error, 3);
   }
   progress(1, 990);
   ptx::tc_fence_before();
@@ -957,13 +1078,19 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
     ptx::tmem_dealloc(tmem, 512);
   }
   progress(1, 999);
-  if (tid == 0) tl_cta(1, 1);
 }
 
-// dkv kernel: one CTA per 128 keys, 64-query blocks, 608 threads:
-//   warp 0       TMA loads (K and V once, then Q_i and dO_i into a three-stage
-//                ring, each stage with its queries' LSE and delta, which the
-//                warp reads from global memory a block ahead);
+// dkv kernel: persistent, one CTA per SM.  A work item is 128 keys of one
+// (sequence, head), looped over 64-query blocks; items are numbered heaviest
+// first (key tile 0 sees every query block of a causal sequence) and CTA c of
+// G takes items c, 2G - 1 - c, 2G + c, ...  608 threads:
+//   warp 0       TMA loads in the order they are consumed: per item its first
+//                Q_i/dO_i block, then K and V (once the previous item's last
+//                S^T and dP^T MMAs have read them; the next item's K and V are
+//                prefetched into L2), then the remaining Q_i and dO_i into a
+//                four-stage ring that runs on across items, each stage with
+//                its queries' LSE and delta, which the warp reads from global
+//                memory one block ahead;
 //   warp 1       TMEM allocation; one thread issues the S^T and dP^T MMAs;
 //   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
 //                key row each) and columns 16 ((w - 2) / 4) .. + 15 of a block;
@@ -988,8 +1115,9 @@ constexpr int KV_OFF_DO = KV_OFF_Q + KV_QST * T64;
 constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + PB;
 constexpr int KV_OFF_STAT = KV_OFF_DST + PB;  // [stage][lse2[64] | delta[64]] fp32
 constexpr int KV_OFF_BAR = KV_OFF_STAT + KV_QST * 2 * BK * 4;
-// kv, q_full[3], q_empty[3], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin, sdp_drain
-constexpr int KV_NBAR = 1 + 2 * KV_QST + 4 + 4;
+// kv_full, kv_empty, q_full[4], q_empty[4], sdp_full[2], sdp_empty[2], pd_full,
+// pd_empty, fin, sdp_drain
+constexpr int KV_NBAR = 2 + 2 * KV_QST + 4 + 4;
 // The dynamic shared memory is rounded up to a 1024-byte boundary (the
 // swizzled tiles need it); this kernel's layout leaves room for at most
 // KV_SLACK bytes of rounding, and the kernel checks the actual amount (the
@@ -1006,6 +1134,22 @@ __device__ __forceinline__ void store_row_quarter(uint8_t* buf, int row, int c, 
   *reinterpret_cast<uint4*>(r + (((2 * c + 1) ^ (row & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+struct KvItem {
+  int h, bb, k0, i0, n;  // head, sequence, first key, first query block, query blocks
+};
+__device__ __forceinline__ KvItem kv_item(const BwdArgs& a, int i) {
+  const int bh = a.heads * a.batch;
+  const int kt = i / bh, r = i % bh;  // key tile 0 (the most query blocks) first
+  const int nq_all = (a.S + BK - 1) / BK;
+  KvItem it;
+  it.h = r % a.heads;
+  it.bb = r / a.heads;
+  it.k0 = kt * 128;
+  it.i0 = a.causal ? it.k0 / BK : 0;  // query blocks before the diagonal see none of these keys
+  it.n = nq_all - it.i0;
+  return it;
+}
+
 __global__ void __launch_bounds__(KV_NT, 1)
 attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
                        const __grid_constant__ CUtensorMap tdo64, const BwdArgs a) {
@@ -1018,28 +1162,22 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   }
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + KV_OFF_BAR;
-  const uint32_t bar_kv = bars;
-  auto q_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto q_empty = [&](int s) { return bars + 8u * (1 + KV_QST + s); };
-  auto sdp_full = [&](int b) { return bars + 8u * (1 + 2 * KV_QST + b); };
-  auto sdp_empty = [&](int b) { return bars + 8u * (3 + 2 * KV_QST + b); };
-  const uint32_t pd_full = bars + 8u * (5 + 2 * KV_QST), pd_empty = pd_full + 8u, bar_fin = pd_full + 16u;
+  const uint32_t kv_full = bars, kv_empty = bars + 8u;
+  auto q_full = [&](uint32_t s) { return bars + 8u * (2 + s); };
+  auto q_empty = [&](uint32_t s) { return bars + 8u * (2 + KV_QST + s); };
+  auto sdp_full = [&](uint32_t b) { return bars + 8u * (2 + 2 * KV_QST + b); };
+  auto sdp_empty = [&](uint32_t b) { return bars + 8u * (4 + 2 * KV_QST + b); };
+  const uint32_t pd_full = bars + 8u * (6 + 2 * KV_QST), pd_empty = pd_full + 8u, bar_fin = pd_full + 16u;
   const uint32_t sdp_drain = pd_full + 24u;
   const uint32_t tslot = bars + 8u * KV_NBAR;
   float* stat = reinterpret_cast<float*>(gbase + KV_OFF_STAT);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  // grid (heads, batch, tiles): key tile 0 (the most query blocks) first
-  const int ktile = blockIdx.z, h = blockIdx.x, bb = blockIdx.y;
-  const int k0 = ktile * 128, row0 = bb * a.S;
-  const int nq_all = (a.S + BK - 1) / BK;
-  const int i0 = a.causal ? k0 / BK : 0;  // query blocks before the diagonal see none of these keys
-  const int n = nq_all - i0;
-  const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
-  if (tid == 0) tl_cta(2, 0);
+  const int cta = blockIdx.x, G = gridDim.x;
 
   if (tid == 0) {
-    ptx::mbar_init(bar_kv, 1);
+    ptx::mbar_init(kv_full, 1);
+    ptx::mbar_init(kv_empty, 1);
     for (int s = 0; s < KV_QST; ++s) {
       ptx::mbar_init(q_full(s), 1);
       ptx::mbar_init(q_empty(s), 1);
@@ -1065,8 +1203,8 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
-  auto t_st = [&](int b) { return tmem + (uint32_t)(b * 128); };
-  auto t_dpt = [&](int b) { return tmem + (uint32_t)(b * 128 + 64); };
+  auto t_st = [&](uint32_t b) { return tmem + b * 128u; };
+  auto t_dpt = [&](uint32_t b) { return tmem + b * 128u + 64u; };
   const uint32_t t_dv = tmem + 256, t_dk = tmem + 384;
   progress(2, 2);
   pdl_wait();
@@ -1075,211 +1213,302 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   bool ok = true;
 
   if (warp == 0) {
-    if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(bar_kv, 2 * TILE);
-      ptx::tma_load_2d(base + KV_OFF_K, &tkv, bar_kv, col_k, row0 + k0);
-      ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, bar_kv, col_k + 64, row0 + k0);
-      ptx::tma_load_2d(base + KV_OFF_V, &tkv, bar_kv, col_v, row0 + k0);
-      ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, bar_kv, col_v + 64, row0 + k0);
-    }
-    // LSE (log2 units) and delta of block ii's 64 queries, two of each per lane;
-    // the next block's are loaded before the wait for its stage
-    auto ld_stat = [&](int ii, float (&v)[4]) {
+    // LSE (log2 units) and delta of query block ii of an item, two of each
+    // per lane; the next entry's are loaded before the wait for its stage
+    auto ld_stat = [&](int i, int ii, float (&v)[4]) {
+      v[0] = v[1] = v[2] = v[3] = 0.f;
+      if (i >= a.items) return;
+      const KvItem it = kv_item(a, i);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int q = (i0 + ii) * BK + lane + 32 * u;
-        const bool vq = ii < n && q < a.S;
-        const int64_t at = (int64_t)h * a.M + row0 + q;
-        v[u] = vq ? a.lse[at] * 1.4426950408889634f : 0.f;
-        v[2 + u] = vq ? a.delta[at] : 0.f;
+        const int q = (it.i0 + ii) * BK + lane + 32 * u;
+        if (ii < it.n && q < a.S) {
+          const int64_t at = (int64_t)it.h * a.M + it.bb * a.S + q;
+          v[u] = a.lse[at] * 1.4426950408889634f;
+          v[2 + u] = a.delta[at];
+        }
       }
     };
+    uint32_t e = 0, nkv = 0;  // Q/dO ring entries and K/V loads issued
     float cur[4];
-    ld_stat(0, cur);
-    int nl = 0;  // query blocks whose loads were issued
-    for (int ii = 0; ii < n; ++ii) {
-      const int s = ii % KV_QST;
-      float nxt[4];
-      ld_stat(ii + 1, nxt);
-      bool w = true;
-      if (lane == 0 && ii >= KV_QST) w = ptx::mbar_wait(q_empty(s), ((ii / KV_QST) & 1) ^ 1, BWD_WAIT);
-      if (!__shfl_sync(0xffffffffu, w, 0)) {
-        ok = false;
-        if (lane == 0) wait_failed(201);
-        break;
-      }
-      float* st = stat + s * 2 * BK;
-      st[lane] = cur[0];
-      st[lane + 32] = cur[1];
-      st[BK + lane] = cur[2];
-      st[BK + lane + 32] = cur[3];
-      __syncwarp();  // the warp's stores precede lane 0's arrive on the stage barrier
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(q_full(s), 2 * T64);
-        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
-        const int r = row0 + (i0 + ii) * BK;
-        ptx::tma_load_2d(qt, &tq64, q_full(s), col_q, r);
-        ptx::tma_load_2d(qt + BOX64, &tq64, q_full(s), col_q + 64, r);
-        ptx::tma_load_2d(dt, &tdo64, q_full(s), h * D, r);
-        ptx::tma_load_2d(dt + BOX64, &tdo64, q_full(s), h * D + 64, r);
-      }
-      nl = ii + 1;
+    ld_stat(persistent_item(0, cta, G), 0, cur);
+    for (int k = 0; ok; ++k) {
+      const int i = persistent_item(k, cta, G);
+      if (i >= a.items) break;
+      const KvItem it = kv_item(a, i);
+      const int row0 = it.bb * a.S, col_q = it.h * D;
+      const int inext = persistent_item(k + 1, cta, G);
+      for (int ii = 0; ii < it.n && ok; ++ii, ++e) {
+        const uint32_t s = e % KV_QST, u = e / KV_QST;
+        float nxt[4];
+        if (ii + 1 < it.n)
+          ld_stat(i, ii + 1, nxt);
+        else
+          ld_stat(inext, 0, nxt);
+        bool w = true;
+        if (lane == 0 && u > 0) w = ptx::mbar_wait(q_empty(s), (u - 1) & 1, BWD_WAIT);
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          if (lane == 0) wait_failed(201);
+          break;
+        }
+        float* st = stat + s * 2 * BK;
+        st[lane] = cur[0];
+        st[lane + 32] = cur[1];
+        st[BK + lane] = cur[2];
+        st[BK + lane + 32] = cur[3];
+        __syncwarp();  // the warp's stores precede lane 0's arrive on the stage barrier
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(q_full(s), 2 * T64);
+          const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+          const int r = row0 + (it.i0 + ii) * BK;
+          ptx::tma_load_2d(qt, &tq64, q_full(s), col_q, r);
+          ptx::tma_load_2d(qt + BOX64, &tq64, q_full(s), col_q + 64, r);
+          ptx::tma_load_2d(dt, &tdo64, q_full(s), it.h * D, r);
+          ptx::tma_load_2d(dt + BOX64, &tdo64, q_full(s), it.h * D + 64, r);
+        }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+        for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
+        if (ii == 0) {
+          // K and V after the item's first Q/dO block: they are free once the
+          // previous item's last S^T and dP^T MMAs are done
+          bool wk = true;
+          if (lane == 0) {
+            if (nkv > 0) wk = ptx::mbar_wait(kv_empty, (nkv - 1) & 1, BWD_WAIT);
+            if (wk) {
+              const int col_k = a.H + it.h * D, col_v = 2 * a.H + it.h * D;
+              ptx::mbar_arrive_expect_tx(kv_full, 2 * TILE);
+              ptx::tma_load_2d(base + KV_OFF_K, &tkv, kv_full, col_k, row0 + it.k0);
+              ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, kv_full, col_k + 64, row0 + it.k0);
+              ptx::tma_load_2d(base + KV_OFF_V, &tkv, kv_full, col_v, row0 + it.k0);
+              ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, kv_full, col_v + 64, row0 + it.k0);
+              // the next item's K and V into L2 (single-buffered here)
+              if (inext < a.items) {
+                const KvItem nx = kv_item(a, inext);
+                const int rn = nx.bb * a.S + nx.k0;
+                tma_prefetch_l2(&tkv, a.H + nx.h * D, rn);
+                tma_prefetch_l2(&tkv, a.H + nx.h * D + 64, rn);
+                tma_prefetch_l2(&tkv, 2 * a.H + nx.h * D, rn);
+                tma_prefetch_l2(&tkv, 2 * a.H + nx.h * D + 64, rn);
+              }
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, wk, 0)) {
+            ok = false;
+            if (lane == 0) wait_failed(201);
+            ++e;
+            break;
+          }
+          ++nkv;
+        }
+      }
     }
     if (lane == 0) {
-      // every load issued has landed before the CTA may exit (stage s last
-      // held block s + R ((m - 1 - s) / R) of the m issued)
-      bool dr = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
-      for (int s = 0; s < KV_QST && s < nl; ++s)
-        dr = ptx::mbar_wait(q_full(s), ((nl - 1 - s) / KV_QST) & 1, BWD_WAIT) && dr;
+      // every load issued has landed before the CTA may exit: the last entry
+      // of each stage, the last K/V
+      bool dr = true;
+      for (uint32_t s = 0; s < KV_QST; ++s)
+        if (e > s) {
+          const uint32_t x = e - 1 - (e - 1 - s) % KV_QST;
+          dr = ptx::mbar_wait(q_full(s), (x / KV_QST) & 1, BWD_WAIT) && dr;
+        }
+      if (nkv > 0) dr = ptx::mbar_wait(kv_full, (nkv - 1) & 1, BWD_WAIT) && dr;
       if (!dr) wait_failed(202);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      ok = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
-      if (!ok) wait_failed(203);
-      auto sdp = [&](int ii) {  // S^T = K Q_i^T, dP^T = V dO_i^T into TMEM buffer ii % 2
-        const int s = ii % KV_QST, b = ii & 1;
-        if (!ptx::mbar_wait(q_full(s), (ii / KV_QST) & 1, BWD_WAIT)) { wait_failed(204); return false; }
-        // the element-wise warps have loaded block ii-2 from this buffer
-        if (ii >= 2 && !ptx::mbar_wait(sdp_empty(b), ((ii / 2) & 1) ^ 1, BWD_WAIT)) {
-          wait_failed(205);
-          return false;
+      uint32_t g = 0;  // query blocks so far over all items (= Q/dO ring entries)
+      for (int k = 0; ok; ++k) {
+        const int i = persistent_item(k, cta, G);
+        if (i >= a.items) break;
+        const KvItem it = kv_item(a, i);
+        if (!ptx::mbar_wait(kv_full, k & 1, BWD_WAIT)) {
+          ok = false;
+          wait_failed(203);
+          break;
         }
-        ptx::tc_fence_after();
-        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+        for (int ii = 0; ii < it.n && ok; ++ii, ++g) {  // S^T = K Q_i^T, dP^T = V dO_i^T into buffer g % 2
+          const uint32_t s = g % KV_QST, b = g & 1;
+          if (!ptx::mbar_wait(q_full(s), (g / KV_QST) & 1, BWD_WAIT)) {
+            ok = false;
+            wait_failed(204);
+            break;
+          }
+          // the element-wise warps have loaded block g-2 from this buffer
+          if (g >= 2 && !ptx::mbar_wait(sdp_empty(b), ((g / 2) - 1) & 1, BWD_WAIT)) {
+            ok = false;
+            wait_failed(205);
+            break;
+          }
+          ptx::tc_fence_after();
+          if (ii == 0) tl_unit(2, i, 0);
+          const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16(t_st(b), kmajor_desc(base + KV_OFF_K, kk), kmajor64_desc(qt, kk), IDESC_N64, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_bf16(t_st(b), kmajor_desc(base + KV_OFF_K, kk), kmajor64_desc(qt, kk), IDESC_N64, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16(t_dpt(b), kmajor_desc(base + KV_OFF_V, kk), kmajor64_desc(dt, kk), IDESC_N64, kk > 0);
-        ptx::mma_commit(sdp_full(b));
-        tl_block(2, ii, 0);
-        return true;
-      };
-      for (int ii = 0; ii < n && ok; ++ii) ok = sdp(ii);
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_bf16(t_dpt(b), kmajor_desc(base + KV_OFF_V, kk), kmajor64_desc(dt, kk), IDESC_N64, kk > 0);
+          ptx::mma_commit(sdp_full(b));
+          if (ii + 1 == it.n) ptx::mma_commit(kv_empty);  // the item's last read of K and V
+          if (k == 0) tl_block(2, ii, 0);
+        }
+      }
       ptx::mma_commit(sdp_drain);  // completes once every MMA this thread issued has
-      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) { ok = false; wait_failed(207); }
+      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) {
+        ok = false;
+        wait_failed(207);
+      }
     }
   } else if (warp == KV_ACC_WARP) {
     if (lane == 0) {
-      ok = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
-      if (!ok) wait_failed(210);
-      auto acc = [&](int ii) {  // dV += P^T dO_i, dK += dS^T Q_i
-        const int s = ii % KV_QST;
-        if (!ptx::mbar_wait(pd_full, ii & 1, BWD_WAIT)) { wait_failed(206); return false; }
-        ptx::tc_fence_after();
-        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+      uint32_t g = 0;
+      int nk = 0;  // items finished
+      for (int k = 0; ok; ++k) {
+        const int i = persistent_item(k, cta, G);
+        if (i >= a.items) break;
+        const KvItem it = kv_item(a, i);
+        for (int ii = 0; ii < it.n && ok; ++ii, ++g) {  // dV += P^T dO_i, dK += dS^T Q_i
+          const uint32_t s = g % KV_QST;
+          if (!ptx::mbar_wait(pd_full, g & 1, BWD_WAIT)) {
+            ok = false;
+            wait_failed(206);
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint32_t accum = (ii > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT, kk), mnmajor64_desc(dt, kk), IDESC_ACC, accum);
-          ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST, kk), mnmajor64_desc(qt, kk), IDESC_ACC, accum);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t accum = (ii > 0 || kk > 0) ? 1u : 0u;
+            ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT, kk), mnmajor64_desc(dt, kk), IDESC_ACC, accum);
+            ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST, kk), mnmajor64_desc(qt, kk), IDESC_ACC, accum);
+          }
+          // S^T, dP^T of the block (which also read Q_i, dO_i) completed before
+          // the element-wise warps could hand over P^T, dS^T: the stage is free
+          // once these MMAs are
+          ptx::mma_commit(pd_empty);
+          ptx::mma_commit(q_empty(s));
+          if (k == 0) tl_block(2, ii, 1);
         }
-        // S^T, dP^T of block ii (which also read Q_i, dO_i) completed before
-        // the element-wise warps could hand over P^T, dS^T: the stage is free
-        // once these MMAs are
-        ptx::mma_commit(pd_empty);
-        ptx::mma_commit(q_empty(s));
-        tl_block(2, ii, 1);
-        return true;
-      };
-      for (int ii = 0; ii < n && ok; ++ii) ok = acc(ii);
-      ptx::mma_commit(bar_fin);  // completes once every MMA this thread issued has
-      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(211); }
+        if (!ok) break;
+        ptx::mma_commit(bar_fin);  // the item's dK and dV are complete once this does
+        nk = k + 1;
+      }
+      // every MMA this thread issued is complete before the CTA may exit
+      if (ok && nk > 0 && !ptx::mbar_wait(bar_fin, (nk - 1) & 1, BWD_WAIT)) {
+        ok = false;
+        wait_failed(211);
+      }
+      if (!ok) {  // one more commit drains whatever was issued after the last finished item
+        ptx::mma_commit(bar_fin);
+        (void)ptx::mbar_wait(bar_fin, nk & 1, BWD_WAIT);
+      }
     }
   } else {
     const int qq = warp & 3, c = (warp - 2) >> 2;  // lane quarter; columns 16 c .. + 15
-    const int row = qq * 32 + lane, kj = k0 + row;
-    const bool valid_k = kj < a.S;
+    const int row = qq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    for (int ii = 0; ii < n && ok; ++ii) {
-      const int s = ii % KV_QST, b = ii & 1, i = i0 + ii;
-      // this block's S^T, dP^T are in TMEM (which also means its stage, and
-      // the LSE / delta stored with it, have landed)
-      if (!warp_wait(sdp_full(b), (ii / 2) & 1) || !warp_wait(q_full(s), (ii / KV_QST) & 1)) {
-        ok = false;
-        if (lane == 0) wait_failed(208);
-        break;
-      }
-      if (warp == 2 && lane == 0) tl_block(2, ii, 2);
-      ptx::tc_fence_after();
-      float v[16], w[16];
-      ptx::tmem_ld16x2(t_st(b) + lane_off + c * 16, t_dpt(b) + lane_off + c * 16, v, w);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
-      const float* st = stat + s * 2 * BK + c * 16;  // LSE of these 16 queries; delta at + BK
-      uint32_t pp[8], pd[8];
-      // a query block that sees every key of the tile needs no mask (CTA-uniform)
-      const bool full = k0 + 128 <= a.S && (i + 1) * BK <= a.S && (!a.causal || i * BK >= k0 + 127);
-      if (full) {
-        const uint64_t sc = f2_splat(a.scale_log2);
+    uint32_t g = 0;
+    for (int k = 0; ok; ++k) {
+      const int it_i = persistent_item(k, cta, G);
+      if (it_i >= a.items) break;
+      const KvItem it = kv_item(a, it_i);
+      const int k0 = it.k0, row0 = it.bb * a.S, h = it.h, n = it.n;
+      const int kj = k0 + row;
+      const bool valid_k = kj < a.S;
+      for (int ii = 0; ii < n && ok; ++ii, ++g) {
+        const uint32_t s = g % KV_QST, b = g & 1;
+        const int i = it.i0 + ii;
+        // this block's S^T, dP^T are in TMEM (which also means its stage, and
+        // the LSE / delta stored with it, have landed)
+        if (!warp_wait(sdp_full(b), (g / 2) & 1) || !warp_wait(q_full(s), (g / KV_QST) & 1)) {
+          ok = false;
+          if (lane == 0) wait_failed(208);
+          break;
+        }
+        if (k == 0 && warp == 2 && lane == 0) tl_block(2, ii, 2);
+        ptx::tc_fence_after();
+        float v[16], w[16];
+        ptx::tmem_ld16x2(t_st(b) + lane_off + c * 16, t_dpt(b) + lane_off + c * 16, v, w);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
+        const float* st = stat + s * 2 * BK + c * 16;  // LSE of these 16 queries; delta at + BK
+        uint32_t pp[8], pd[8];
+        // a query block that sees every key of the tile needs no mask (CTA-uniform)
+        const bool full = k0 + 128 <= a.S && (i + 1) * BK <= a.S && (!a.causal || i * BK >= k0 + 127);
+        if (full) {
+          const uint64_t sc = f2_splat(a.scale_log2);
 #pragma unroll
-        for (int k = 0; k < 16; k += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(st + k);
-          const float4 d4 = *reinterpret_cast<const float4*>(st + BK + k);
+          for (int q = 0; q < 16; q += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(st + q);
+            const float4 d4 = *reinterpret_cast<const float4*>(st + BK + q);
 #pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const float l0 = e == 0 ? l4.x : l4.z, l1 = e == 0 ? l4.y : l4.w;
-            const float d0 = e == 0 ? d4.x : d4.z, d1 = e == 0 ? d4.y : d4.w;
-            const int kk = k + e;
-            const uint64_t x = f2_fma(f2_pack(v[kk], v[kk + 1]), sc, f2_pack(-l0, -l1));
-            const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
-            const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[kk], w[kk + 1]), f2_pack(-d0, -d1)));
-            pp[kk / 2] = pack2(f2_lo(p), f2_hi(p));
-            pd[kk / 2] = pack2(f2_lo(ds), f2_hi(ds));
+            for (int x = 0; x < 4; x += 2) {
+              const float l0 = x == 0 ? l4.x : l4.z, l1 = x == 0 ? l4.y : l4.w;
+              const float d0 = x == 0 ? d4.x : d4.z, d1 = x == 0 ? d4.y : d4.w;
+              const int kk = q + x;
+              const uint64_t y = f2_fma(f2_pack(v[kk], v[kk + 1]), sc, f2_pack(-l0, -l1));
+              const uint64_t p = f2_pack(fast_exp2(f2_lo(y)), fast_exp2(f2_hi(y)));
+              const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[kk], w[kk + 1]), f2_pack(-d0, -d1)));
+              pp[kk / 2] = pack2(f2_lo(p), f2_hi(p));
+              pd[kk / 2] = pack2(f2_lo(ds), f2_hi(ds));
+            }
+          }
+        } else {
+          // queries i BK + 16 c + q with q < q_lo are before this key (causal),
+          // those with q >= q_hi past the sequence end; a key past the end
+          // sees none
+          const int qbase = i * BK + c * 16;
+          const int q_lo = a.causal ? kj - qbase : -1 << 30, q_hi = valid_k ? a.S - qbase : 0;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float l2 = st[q], dl = st[BK + q];
+            const float p = (q >= q_lo && q < q_hi) ? fast_exp2(v[q] * a.scale_log2 - l2) : 0.f;
+            v[q] = p;
+            w[q] = p * (w[q] - dl);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            pp[q] = pack2(v[2 * q], v[2 * q + 1]);
+            pd[q] = pack2(w[2 * q], w[2 * q + 1]);
           }
         }
-      } else {
-        const int qbase = i * BK + c * 16;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float l2 = st[k], dl = st[BK + k];
-          const int q = qbase + k;
-          const bool valid = valid_k && q < a.S && (!a.causal || kj <= q);
-          const float p = valid ? fast_exp2(v[k] * a.scale_log2 - l2) : 0.f;
-          v[k] = p;
-          w[k] = p * (w[k] - dl);
+        // the P^T / dS^T buffers are free once the previous block's accumulation is done
+        if (g >= 1 && !warp_wait(pd_empty, (g - 1) & 1)) {
+          ok = false;
+          if (lane == 0) wait_failed(209);
+          break;
         }
+        store_row_quarter(gbase + KV_OFF_PT, row, c, pp);
+        store_row_quarter(gbase + KV_OFF_DST, row, c, pd);
+        ptx::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(pd_full);
+        if (k == 0 && warp == 2 && lane == 0) tl_block(2, ii, 3);
+      }
+      if (!ok) break;
+      // the item's last accumulation is complete (or the MMA thread gave up)
+      const bool fin = warp_wait(bar_fin, k & 1);
+      ptx::tc_fence_after();
+      __nv_bfloat16* rowp = a.dqkv + (int64_t)(row0 + kj) * 3 * a.H;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          pp[k] = pack2(v[2 * k], v[2 * k + 1]);
-          pd[k] = pack2(w[2 * k], w[2 * k + 1]);
+      for (int part = 0; part < 2; ++part) {  // dK (scaled), then dV
+        float v0[32];  // tcgen05.ld is warp-collective: every lane loads
+        ptx::tmem_ld32((part == 0 ? t_dk : t_dv) + lane_off + c * 32, v0);
+        const float sc = part == 0 ? a.scale : 1.f;
+        if (fin && valid_k) {
+          uint4* out = reinterpret_cast<uint4*>(rowp + (part == 0 ? a.H : 2 * a.H) + h * D + c * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            out[u] = make_uint4(pack2(v0[8 * u] * sc, v0[8 * u + 1] * sc), pack2(v0[8 * u + 2] * sc, v0[8 * u + 3] * sc),
+                                pack2(v0[8 * u + 4] * sc, v0[8 * u + 5] * sc), pack2(v0[8 * u + 6] * sc, v0[8 * u + 7] * sc));
         }
       }
-      // the P^T / dS^T buffers are free once block ii-1's accumulation is done
-      if (ii >= 1 && !warp_wait(pd_empty, (ii - 1) & 1)) {
-        ok = false;
-        if (lane == 0) wait_failed(209);
-        break;
-      }
-      store_row_quarter(gbase + KV_OFF_PT, row, c, pp);
-      store_row_quarter(gbase + KV_OFF_DST, row, c, pd);
-      ptx::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(pd_full);
-      if (warp == 2 && lane == 0) tl_block(2, ii, 3);
+      if (!fin) ok = false;
+      if (warp == 2 && lane == 0) tl_unit(2, it_i, 1);
     }
-    const bool fin = warp_wait(bar_fin, 0);
-    ptx::tc_fence_after();
-    __nv_bfloat16* rowp = a.dqkv + (int64_t)(row0 + kj) * 3 * a.H;
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {  // dK (scaled), then dV
-      float v0[32];  // tcgen05.ld is warp-collective: every lane loads
-      ptx::tmem_ld32((part == 0 ? t_dk : t_dv) + lane_off + c * 32, v0);
-      const float sc = part == 0 ? a.scale : 1.f;
-      if (ok && fin && valid_k) {
-        uint4* out = reinterpret_cast<uint4*>(rowp + (part == 0 ? a.H : 2 * a.H) + h * D + c * 32);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          out[u] = make_uint4(pack2(v0[8 * u] * sc, v0[8 * u + 1] * sc), pack2(v0[8 * u + 2] * sc, v0[8 * u + 3] * sc),
-                              pack2(v0[8 * u + 4] * sc, v0[8 * u + 5] * sc), pack2(v0[8 * u + 6] * sc, v0[8 * u + 7] * sc));
-      }
-    }
-    if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 5);
+    if (!ok && lane == 0) atomicExch(&g_attn_error, 5);
   }
   progress(2, 990);
   ptx::tc_fence_before();
@@ -1289,7 +1518,6 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
     ptx::tmem_dealloc(tmem, 512);
   }
   progress(2, 999);
-  if (tid == 0) tl_cta(2, 1);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1410,11 +1638,21 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   ba.scale_log2 = 1.4426950408889634f * ba.scale;
   const int tiles = (a.seq + 127) / 128;
   if (tiles > 65535) return cudaErrorInvalidConfiguration;
-  e = launch_pdl(attn_bwd_dq_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(DQ_NT), DQ_SMEM, st,
-                 tq128, tdo128, ba);
+  const int64_t items = (int64_t)tiles * a.batch * a.heads;
+  if (items > (int64_t)INT32_MAX / 2) return cudaErrorInvalidConfiguration;
+  ba.batch = a.batch;
+  ba.tiles = tiles;
+  ba.items = (int)items;
+  // both kernels are persistent: one CTA per SM
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(KV_NT), KV_SMEM,
-                    st, tq128, tq64, tdo64, ba);
+  e = launch_pdl(attn_bwd_dq_tc_kernel, dim3((int)std::min<int64_t>(items, std::max(sms, 1))),
+                 dim3(DQ_NT), DQ_SMEM, st, tq128, tdo128, ba);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3((int)std::min<int64_t>(items, std::max(sms, 1))),
+                    dim3(KV_NT), KV_SMEM, st, tq128, tq64, tdo64, ba);
 }
 
 cudaError_t attention_set_progress(int* p) {

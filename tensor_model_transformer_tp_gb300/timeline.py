@@ -12,8 +12,9 @@ GEMM: C[M, N] = A[M, K] B[N, K]^T in bf16 with the given epilogue (0 store,
 1 bias, 2 bias + GeLU; default 2), L2 flushed by a 256 MiB write before each
 launch; the CUDA-event time is the median of 20 launches, the stamps are from
 one more.  Attention backward: batch x seq, heads of 128, causal; the stamps
-are those of CTA 0 of the dQ and dK/dV kernels per block, and the span of
-each kernel from its first CTA's entry to its last CTA's exit.
+are those of the first item of CTA 0 of the dQ and dK/dV kernels per block,
+and the span of each kernel from its first item's start to its last item's
+end.
 """
 from __future__ import annotations
 
@@ -129,8 +130,19 @@ def attention_bwd(B: int, S: int, heads: int) -> dict:
         r = t[(kid - 1) * 8192:(kid - 1) * 8192 + 2 * min(ncta, 4096)].reshape(-1, 2)
         blk = t[16384 + (kid - 1) * 256:16384 + kid * 256].reshape(64, 4)
         b0 = blk[blk > 0].min() if (blk > 0).any() else 0
+        G = min(ncta, torch.cuda.get_device_properties(0).multi_processor_count)
+        t0 = r[:, 0][r[:, 0] > 0].min() if (r[:, 0] > 0).any() else 0
+        items0, k = [], 0  # CTA 0's items in the order it ran them: start, end (us)
+        while True:
+            i = k * G + (G - 1 if k % 2 else 0)
+            if i >= min(ncta, 4096):
+                break
+            items0.append((int(i), float(r[i, 0] - t0) / 1000.0, float(r[i, 1] - t0) / 1000.0))
+            k += 1
         out["kernels"][name] = {
+            "cta0_items": items0,
             "span_us": float(r[:, 1].max() - r[:, 0].min()) / 1000.0,
+            # per work item (both kernels are persistent)
             "cta_mean_us": float((r[:, 1] - r[:, 0]).mean()) / 1000.0,
             # per block of CTA 0: S/dP MMAs issued, accumulation MMAs issued,
             # element-wise warp 2 saw S, handed its dS (ns from the first stamp)
@@ -251,7 +263,8 @@ def main(argv):
     elif len(argv) == 4 and argv[0] == "attn_bwd":
         r = attention_bwd(int(argv[1]), int(argv[2]), int(argv[3]))
         for name, k in r["kernels"].items():
-            print("%s: span %.1f us, CTA mean %.1f us" % (name, k["span_us"], k["cta_mean_us"]))
+            print("%s: span %.1f us, item mean %.1f us" % (name, k["span_us"], k["cta_mean_us"]))
+            print("  CTA 0 items (us): " + ", ".join("%d: %.1f-%.1f" % x for x in k["cta0_items"]))
             print("  CTA 0 per block (ns): SdP issued, ACC issued, warp 2 saw S, warp 2 handed dS")
             for j, row in enumerate(k["cta0_blocks_ns"][:8]):
                 print("  block %d: %s" % (j, " ".join("%6d" % x for x in row)))
