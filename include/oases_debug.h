@@ -66,11 +66,11 @@ oases_status oases_debug_attention(const void *qkv, void *o, float *lse, const v
 oases_status oases_debug_attention_progress(int *host_mapped);
 /* Timeline of the tensor-core attention kernels (debugging aid): device_buffer
  * holds uint64 %globaltimer stamps, written by every following launch.
- * Backward (both kernels persistent): the start (first MMAs issued) and end
- * (gradient stored) of each work item i < 4096 at [2i] (dQ kernel: 128
- * queries of one sequence and head) and [8192 + 2i] (dK/dV kernel: 128 keys),
- * items numbered heaviest first; for the first item of CTA 0 and block
- * j < 64, four stamps at
+ * Backward: for the persistent dQ kernel, the start (first S and dP MMAs
+ * issued) and end (dQ stored) of each work item i < 4096 (128 queries of one
+ * sequence and head, numbered heaviest first) at [2i]; entry and exit of each
+ * dK/dV CTA c < 4096 at [8192 + 2c]; for CTA 0 (dQ: its first item) and
+ * block j < 64, four stamps at
  * [16384 + 4j] (dQ) and [16640 + 4j] (dK/dV): S and dP MMAs issued,
  * accumulation MMAs issued, element-wise warp 2 saw S and dP, and handed over
  * its rows.  Forward (persistent; an item is 256 queries of one sequence and

@@ -120,6 +120,36 @@ __global__ void attn_delta_kernel(const T* __restrict__ o, const T* __restrict__
   if (lane == 0) delta[(int64_t)h * M + row] = s;
 }
 
+// The same for bf16 with d = 128: sixteen threads per (row, head), each
+// taking 8 elements (16-byte loads) of O and dO; the two (row, head) pairs of
+// a warp are adjacent in memory.  Grid-stride over M * heads pairs.
+__global__ void __launch_bounds__(256)
+attn_delta_bf16_d128_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ d_o,
+                            float* __restrict__ delta, int M, int H, int heads) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t pairs = (int64_t)M * heads;
+  const int grp = threadIdx.x >> 4, sl = threadIdx.x & 15;
+  for (int64_t p = (int64_t)blockIdx.x * 16 + grp; p < pairs; p += (int64_t)gridDim.x * 16) {
+    const int row = (int)(p / heads), h = (int)(p % heads);
+    const int64_t idx = (int64_t)row * H + h * 128 + sl * 8;
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(o + idx));
+    const uint4 y = __ldg(reinterpret_cast<const uint4*>(d_o + idx));
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[k]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[k]));
+      s = fmaf(a.x, b.x, s);
+      s = fmaf(a.y, b.y, s);
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (sl == 0) delta[(int64_t)h * M + row] = s;
+  }
+}
+
 // dQ pass: grid (ceil(S/ROWS), heads, batch).
 template <typename T>
 __global__ void __launch_bounds__(NT)
@@ -288,6 +318,18 @@ cudaError_t attention_fwd_simt(const AttnArgs& a, cudaStream_t st) {
 cudaError_t attention_delta(const AttnArgs& a, cudaStream_t st) {
   const int M = a.batch * a.seq;
   if (M == 0) return cudaSuccess;
+  if (a.t == DType::BF16 && a.head_dim == 128 && a.hidden % 8 == 0 &&
+      (((uintptr_t)a.o | (uintptr_t)a.d_o) & 15) == 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = ((int64_t)M * a.heads + 15) / 16;
+    const int grid = (int)std::min<int64_t>(blocks, (int64_t)std::max(sms, 1) * 8);
+    return launch_pdl(attn_delta_bf16_d128_kernel, dim3(grid), dim3(256), 0, st,
+                      (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.d_o, a.delta, M, a.hidden,
+                      a.heads);
+  }
   const int warps = M * a.heads;
   const int grid = (warps + 7) / 8;
   if (a.t == DType::F32)

@@ -98,12 +98,13 @@ __device__ __forceinline__ void progress(int kid, int code) {
 __device__ __forceinline__ int linear_cta() {
   return blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
 }
-// kid 1 = dq, 2 = dK/dV; work item c of the persistent kernel; what 0 =
-// start (its first MMAs issued), 1 = end (its gradient stored)
+// kid 1 = dq (c = work item of the persistent kernel; what 0 = its first
+// MMAs issued, 1 = its dQ stored), 2 = dK/dV (c = CTA; 0 = entry, 1 = exit)
 __device__ __forceinline__ void tl_unit(int kid, int c, int what) {
   unsigned long long* t = g_attn_timeline;
   if (t != nullptr && c < 4096) t[(kid - 1) * 8192 + 2 * c + what] = ptx::globaltimer();
 }
+__device__ __forceinline__ void tl_cta(int kid, int what) { tl_unit(kid, linear_cta(), what); }
 __device__ __forceinline__ void tl_block(int kid, int j, int what) {
   unsigned long long* t = g_attn_timeline;
   if (t != nullptr && linear_cta() == 0 && j < 64)
@@ -1080,17 +1081,10 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
   progress(1, 999);
 }
 
-// dkv kernel: persistent, one CTA per SM.  A work item is 128 keys of one
-// (sequence, head), looped over 64-query blocks; items are numbered heaviest
-// first (key tile 0 sees every query block of a causal sequence) and CTA c of
-// G takes items c, 2G - 1 - c, 2G + c, ...  608 threads:
-//   warp 0       TMA loads in the order they are consumed: per item its first
-//                Q_i/dO_i block, then K and V (once the previous item's last
-//                S^T and dP^T MMAs have read them; the next item's K and V are
-//                prefetched into L2), then the remaining Q_i and dO_i into a
-//                four-stage ring that runs on across items, each stage with
-//                its queries' LSE and delta, which the warp reads from global
-//                memory one block ahead;
+// dkv kernel: one CTA per 128 keys, 64-query blocks, 608 threads:
+//   warp 0       TMA loads (K and V once, then Q_i and dO_i into a four-stage
+//                ring, each stage with its queries' LSE and delta, which the
+//                warp reads from global memory a block ahead);
 //   warp 1       TMEM allocation; one thread issues the S^T and dP^T MMAs;
 //   warps 2..17  element-wise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
 //                key row each) and columns 16 ((w - 2) / 4) .. + 15 of a block;
@@ -1115,9 +1109,8 @@ constexpr int KV_OFF_DO = KV_OFF_Q + KV_QST * T64;
 constexpr int KV_OFF_PT = KV_OFF_DO + KV_QST * T64, KV_OFF_DST = KV_OFF_PT + PB;
 constexpr int KV_OFF_STAT = KV_OFF_DST + PB;  // [stage][lse2[64] | delta[64]] fp32
 constexpr int KV_OFF_BAR = KV_OFF_STAT + KV_QST * 2 * BK * 4;
-// kv_full, kv_empty, q_full[4], q_empty[4], sdp_full[2], sdp_empty[2], pd_full,
-// pd_empty, fin, sdp_drain
-constexpr int KV_NBAR = 2 + 2 * KV_QST + 4 + 4;
+// kv, q_full[3], q_empty[3], sdp_full[2], sdp_empty[2], pd_full, pd_empty, fin, sdp_drain
+constexpr int KV_NBAR = 1 + 2 * KV_QST + 4 + 4;
 // The dynamic shared memory is rounded up to a 1024-byte boundary (the
 // swizzled tiles need it); this kernel's layout leaves room for at most
 // KV_SLACK bytes of rounding, and the kernel checks the actual amount (the
@@ -1134,22 +1127,6 @@ __device__ __forceinline__ void store_row_quarter(uint8_t* buf, int row, int c, 
   *reinterpret_cast<uint4*>(r + (((2 * c + 1) ^ (row & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-struct KvItem {
-  int h, bb, k0, i0, n;  // head, sequence, first key, first query block, query blocks
-};
-__device__ __forceinline__ KvItem kv_item(const BwdArgs& a, int i) {
-  const int bh = a.heads * a.batch;
-  const int kt = i / bh, r = i % bh;  // key tile 0 (the most query blocks) first
-  const int nq_all = (a.S + BK - 1) / BK;
-  KvItem it;
-  it.h = r % a.heads;
-  it.bb = r / a.heads;
-  it.k0 = kt * 128;
-  it.i0 = a.causal ? it.k0 / BK : 0;  // query blocks before the diagonal see none of these keys
-  it.n = nq_all - it.i0;
-  return it;
-}
-
 __global__ void __launch_bounds__(KV_NT, 1)
 attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
                        const __grid_constant__ CUtensorMap tdo64, const BwdArgs a) {
@@ -1162,22 +1139,28 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   }
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + KV_OFF_BAR;
-  const uint32_t kv_full = bars, kv_empty = bars + 8u;
-  auto q_full = [&](uint32_t s) { return bars + 8u * (2 + s); };
-  auto q_empty = [&](uint32_t s) { return bars + 8u * (2 + KV_QST + s); };
-  auto sdp_full = [&](uint32_t b) { return bars + 8u * (2 + 2 * KV_QST + b); };
-  auto sdp_empty = [&](uint32_t b) { return bars + 8u * (4 + 2 * KV_QST + b); };
-  const uint32_t pd_full = bars + 8u * (6 + 2 * KV_QST), pd_empty = pd_full + 8u, bar_fin = pd_full + 16u;
+  const uint32_t bar_kv = bars;
+  auto q_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto q_empty = [&](int s) { return bars + 8u * (1 + KV_QST + s); };
+  auto sdp_full = [&](int b) { return bars + 8u * (1 + 2 * KV_QST + b); };
+  auto sdp_empty = [&](int b) { return bars + 8u * (3 + 2 * KV_QST + b); };
+  const uint32_t pd_full = bars + 8u * (5 + 2 * KV_QST), pd_empty = pd_full + 8u, bar_fin = pd_full + 16u;
   const uint32_t sdp_drain = pd_full + 24u;
   const uint32_t tslot = bars + 8u * KV_NBAR;
   float* stat = reinterpret_cast<float*>(gbase + KV_OFF_STAT);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int cta = blockIdx.x, G = gridDim.x;
+  // grid (heads, batch, tiles): key tile 0 (the most query blocks) first
+  const int ktile = blockIdx.z, h = blockIdx.x, bb = blockIdx.y;
+  const int k0 = ktile * 128, row0 = bb * a.S;
+  const int nq_all = (a.S + BK - 1) / BK;
+  const int i0 = a.causal ? k0 / BK : 0;  // query blocks before the diagonal see none of these keys
+  const int n = nq_all - i0;
+  const int col_q = h * D, col_k = a.H + h * D, col_v = 2 * a.H + h * D;
+  if (tid == 0) tl_cta(2, 0);
 
   if (tid == 0) {
-    ptx::mbar_init(kv_full, 1);
-    ptx::mbar_init(kv_empty, 1);
+    ptx::mbar_init(bar_kv, 1);
     for (int s = 0; s < KV_QST; ++s) {
       ptx::mbar_init(q_full(s), 1);
       ptx::mbar_init(q_empty(s), 1);
@@ -1203,8 +1186,8 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
-  auto t_st = [&](uint32_t b) { return tmem + b * 128u; };
-  auto t_dpt = [&](uint32_t b) { return tmem + b * 128u + 64u; };
+  auto t_st = [&](int b) { return tmem + (uint32_t)(b * 128); };
+  auto t_dpt = [&](int b) { return tmem + (uint32_t)(b * 128 + 64); };
   const uint32_t t_dv = tmem + 256, t_dk = tmem + 384;
   progress(2, 2);
   pdl_wait();
@@ -1213,302 +1196,212 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
   bool ok = true;
 
   if (warp == 0) {
-    // LSE (log2 units) and delta of query block ii of an item, two of each
-    // per lane; the next entry's are loaded before the wait for its stage
-    auto ld_stat = [&](int i, int ii, float (&v)[4]) {
-      v[0] = v[1] = v[2] = v[3] = 0.f;
-      if (i >= a.items) return;
-      const KvItem it = kv_item(a, i);
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(bar_kv, 2 * TILE);
+      ptx::tma_load_2d(base + KV_OFF_K, &tkv, bar_kv, col_k, row0 + k0);
+      ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, bar_kv, col_k + 64, row0 + k0);
+      ptx::tma_load_2d(base + KV_OFF_V, &tkv, bar_kv, col_v, row0 + k0);
+      ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, bar_kv, col_v + 64, row0 + k0);
+    }
+    // LSE (log2 units) and delta of block ii's 64 queries, two of each per lane;
+    // the next block's are loaded before the wait for its stage
+    auto ld_stat = [&](int ii, float (&v)[4]) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int q = (it.i0 + ii) * BK + lane + 32 * u;
-        if (ii < it.n && q < a.S) {
-          const int64_t at = (int64_t)it.h * a.M + it.bb * a.S + q;
-          v[u] = a.lse[at] * 1.4426950408889634f;
-          v[2 + u] = a.delta[at];
-        }
+        const int q = (i0 + ii) * BK + lane + 32 * u;
+        const bool vq = ii < n && q < a.S;
+        const int64_t at = (int64_t)h * a.M + row0 + q;
+        v[u] = vq ? a.lse[at] * 1.4426950408889634f : 0.f;
+        v[2 + u] = vq ? a.delta[at] : 0.f;
       }
     };
-    uint32_t e = 0, nkv = 0;  // Q/dO ring entries and K/V loads issued
     float cur[4];
-    ld_stat(persistent_item(0, cta, G), 0, cur);
-    for (int k = 0; ok; ++k) {
-      const int i = persistent_item(k, cta, G);
-      if (i >= a.items) break;
-      const KvItem it = kv_item(a, i);
-      const int row0 = it.bb * a.S, col_q = it.h * D;
-      const int inext = persistent_item(k + 1, cta, G);
-      for (int ii = 0; ii < it.n && ok; ++ii, ++e) {
-        const uint32_t s = e % KV_QST, u = e / KV_QST;
-        float nxt[4];
-        if (ii + 1 < it.n)
-          ld_stat(i, ii + 1, nxt);
-        else
-          ld_stat(inext, 0, nxt);
-        bool w = true;
-        if (lane == 0 && u > 0) w = ptx::mbar_wait(q_empty(s), (u - 1) & 1, BWD_WAIT);
-        if (!__shfl_sync(0xffffffffu, w, 0)) {
-          ok = false;
-          if (lane == 0) wait_failed(201);
-          break;
-        }
-        float* st = stat + s * 2 * BK;
-        st[lane] = cur[0];
-        st[lane + 32] = cur[1];
-        st[BK + lane] = cur[2];
-        st[BK + lane + 32] = cur[3];
-        __syncwarp();  // the warp's stores precede lane 0's arrive on the stage barrier
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(q_full(s), 2 * T64);
-          const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
-          const int r = row0 + (it.i0 + ii) * BK;
-          ptx::tma_load_2d(qt, &tq64, q_full(s), col_q, r);
-          ptx::tma_load_2d(qt + BOX64, &tq64, q_full(s), col_q + 64, r);
-          ptx::tma_load_2d(dt, &tdo64, q_full(s), it.h * D, r);
-          ptx::tma_load_2d(dt + BOX64, &tdo64, q_full(s), it.h * D + 64, r);
-        }
-#pragma unroll
-        for (int x = 0; x < 4; ++x) cur[x] = nxt[x];
-        if (ii == 0) {
-          // K and V after the item's first Q/dO block: they are free once the
-          // previous item's last S^T and dP^T MMAs are done
-          bool wk = true;
-          if (lane == 0) {
-            if (nkv > 0) wk = ptx::mbar_wait(kv_empty, (nkv - 1) & 1, BWD_WAIT);
-            if (wk) {
-              const int col_k = a.H + it.h * D, col_v = 2 * a.H + it.h * D;
-              ptx::mbar_arrive_expect_tx(kv_full, 2 * TILE);
-              ptx::tma_load_2d(base + KV_OFF_K, &tkv, kv_full, col_k, row0 + it.k0);
-              ptx::tma_load_2d(base + KV_OFF_K + BOX, &tkv, kv_full, col_k + 64, row0 + it.k0);
-              ptx::tma_load_2d(base + KV_OFF_V, &tkv, kv_full, col_v, row0 + it.k0);
-              ptx::tma_load_2d(base + KV_OFF_V + BOX, &tkv, kv_full, col_v + 64, row0 + it.k0);
-              // the next item's K and V into L2 (single-buffered here)
-              if (inext < a.items) {
-                const KvItem nx = kv_item(a, inext);
-                const int rn = nx.bb * a.S + nx.k0;
-                tma_prefetch_l2(&tkv, a.H + nx.h * D, rn);
-                tma_prefetch_l2(&tkv, a.H + nx.h * D + 64, rn);
-                tma_prefetch_l2(&tkv, 2 * a.H + nx.h * D, rn);
-                tma_prefetch_l2(&tkv, 2 * a.H + nx.h * D + 64, rn);
-              }
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, wk, 0)) {
-            ok = false;
-            if (lane == 0) wait_failed(201);
-            ++e;
-            break;
-          }
-          ++nkv;
-        }
+    ld_stat(0, cur);
+    int nl = 0;  // query blocks whose loads were issued
+    for (int ii = 0; ii < n; ++ii) {
+      const int s = ii % KV_QST;
+      float nxt[4];
+      ld_stat(ii + 1, nxt);
+      bool w = true;
+      if (lane == 0 && ii >= KV_QST) w = ptx::mbar_wait(q_empty(s), ((ii / KV_QST) & 1) ^ 1, BWD_WAIT);
+      if (!__shfl_sync(0xffffffffu, w, 0)) {
+        ok = false;
+        if (lane == 0) wait_failed(201);
+        break;
       }
+      float* st = stat + s * 2 * BK;
+      st[lane] = cur[0];
+      st[lane + 32] = cur[1];
+      st[BK + lane] = cur[2];
+      st[BK + lane + 32] = cur[3];
+      __syncwarp();  // the warp's stores precede lane 0's arrive on the stage barrier
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(q_full(s), 2 * T64);
+        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+        const int r = row0 + (i0 + ii) * BK;
+        ptx::tma_load_2d(qt, &tq64, q_full(s), col_q, r);
+        ptx::tma_load_2d(qt + BOX64, &tq64, q_full(s), col_q + 64, r);
+        ptx::tma_load_2d(dt, &tdo64, q_full(s), h * D, r);
+        ptx::tma_load_2d(dt + BOX64, &tdo64, q_full(s), h * D + 64, r);
+      }
+      nl = ii + 1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
     }
     if (lane == 0) {
-      // every load issued has landed before the CTA may exit: the last entry
-      // of each stage, the last K/V
-      bool dr = true;
-      for (uint32_t s = 0; s < KV_QST; ++s)
-        if (e > s) {
-          const uint32_t x = e - 1 - (e - 1 - s) % KV_QST;
-          dr = ptx::mbar_wait(q_full(s), (x / KV_QST) & 1, BWD_WAIT) && dr;
-        }
-      if (nkv > 0) dr = ptx::mbar_wait(kv_full, (nkv - 1) & 1, BWD_WAIT) && dr;
+      // every load issued has landed before the CTA may exit (stage s last
+      // held block s + R ((m - 1 - s) / R) of the m issued)
+      bool dr = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
+      for (int s = 0; s < KV_QST && s < nl; ++s)
+        dr = ptx::mbar_wait(q_full(s), ((nl - 1 - s) / KV_QST) & 1, BWD_WAIT) && dr;
       if (!dr) wait_failed(202);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t g = 0;  // query blocks so far over all items (= Q/dO ring entries)
-      for (int k = 0; ok; ++k) {
-        const int i = persistent_item(k, cta, G);
-        if (i >= a.items) break;
-        const KvItem it = kv_item(a, i);
-        if (!ptx::mbar_wait(kv_full, k & 1, BWD_WAIT)) {
-          ok = false;
-          wait_failed(203);
-          break;
+      ok = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
+      if (!ok) wait_failed(203);
+      auto sdp = [&](int ii) {  // S^T = K Q_i^T, dP^T = V dO_i^T into TMEM buffer ii % 2
+        const int s = ii % KV_QST, b = ii & 1;
+        if (!ptx::mbar_wait(q_full(s), (ii / KV_QST) & 1, BWD_WAIT)) { wait_failed(204); return false; }
+        // the element-wise warps have loaded block ii-2 from this buffer
+        if (ii >= 2 && !ptx::mbar_wait(sdp_empty(b), ((ii / 2) & 1) ^ 1, BWD_WAIT)) {
+          wait_failed(205);
+          return false;
         }
-        for (int ii = 0; ii < it.n && ok; ++ii, ++g) {  // S^T = K Q_i^T, dP^T = V dO_i^T into buffer g % 2
-          const uint32_t s = g % KV_QST, b = g & 1;
-          if (!ptx::mbar_wait(q_full(s), (g / KV_QST) & 1, BWD_WAIT)) {
-            ok = false;
-            wait_failed(204);
-            break;
-          }
-          // the element-wise warps have loaded block g-2 from this buffer
-          if (g >= 2 && !ptx::mbar_wait(sdp_empty(b), ((g / 2) - 1) & 1, BWD_WAIT)) {
-            ok = false;
-            wait_failed(205);
-            break;
-          }
-          ptx::tc_fence_after();
-          if (ii == 0) tl_unit(2, i, 0);
-          const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+        ptx::tc_fence_after();
+        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            ptx::mma_bf16(t_st(b), kmajor_desc(base + KV_OFF_K, kk), kmajor64_desc(qt, kk), IDESC_N64, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16(t_st(b), kmajor_desc(base + KV_OFF_K, kk), kmajor64_desc(qt, kk), IDESC_N64, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            ptx::mma_bf16(t_dpt(b), kmajor_desc(base + KV_OFF_V, kk), kmajor64_desc(dt, kk), IDESC_N64, kk > 0);
-          ptx::mma_commit(sdp_full(b));
-          if (ii + 1 == it.n) ptx::mma_commit(kv_empty);  // the item's last read of K and V
-          if (k == 0) tl_block(2, ii, 0);
-        }
-      }
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16(t_dpt(b), kmajor_desc(base + KV_OFF_V, kk), kmajor64_desc(dt, kk), IDESC_N64, kk > 0);
+        ptx::mma_commit(sdp_full(b));
+        tl_block(2, ii, 0);
+        return true;
+      };
+      for (int ii = 0; ii < n && ok; ++ii) ok = sdp(ii);
       ptx::mma_commit(sdp_drain);  // completes once every MMA this thread issued has
-      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) {
-        ok = false;
-        wait_failed(207);
-      }
+      if (!ptx::mbar_wait(sdp_drain, 0, BWD_WAIT)) { ok = false; wait_failed(207); }
     }
   } else if (warp == KV_ACC_WARP) {
     if (lane == 0) {
-      uint32_t g = 0;
-      int nk = 0;  // items finished
-      for (int k = 0; ok; ++k) {
-        const int i = persistent_item(k, cta, G);
-        if (i >= a.items) break;
-        const KvItem it = kv_item(a, i);
-        for (int ii = 0; ii < it.n && ok; ++ii, ++g) {  // dV += P^T dO_i, dK += dS^T Q_i
-          const uint32_t s = g % KV_QST;
-          if (!ptx::mbar_wait(pd_full, g & 1, BWD_WAIT)) {
-            ok = false;
-            wait_failed(206);
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
+      ok = ptx::mbar_wait(bar_kv, 0, BWD_WAIT);
+      if (!ok) wait_failed(210);
+      auto acc = [&](int ii) {  // dV += P^T dO_i, dK += dS^T Q_i
+        const int s = ii % KV_QST;
+        if (!ptx::mbar_wait(pd_full, ii & 1, BWD_WAIT)) { wait_failed(206); return false; }
+        ptx::tc_fence_after();
+        const uint32_t qt = base + KV_OFF_Q + s * T64, dt = base + KV_OFF_DO + s * T64;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t accum = (ii > 0 || kk > 0) ? 1u : 0u;
-            ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT, kk), mnmajor64_desc(dt, kk), IDESC_ACC, accum);
-            ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST, kk), mnmajor64_desc(qt, kk), IDESC_ACC, accum);
-          }
-          // S^T, dP^T of the block (which also read Q_i, dO_i) completed before
-          // the element-wise warps could hand over P^T, dS^T: the stage is free
-          // once these MMAs are
-          ptx::mma_commit(pd_empty);
-          ptx::mma_commit(q_empty(s));
-          if (k == 0) tl_block(2, ii, 1);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t accum = (ii > 0 || kk > 0) ? 1u : 0u;
+          ptx::mma_bf16(t_dv, kmajor_blk_desc(base + KV_OFF_PT, kk), mnmajor64_desc(dt, kk), IDESC_ACC, accum);
+          ptx::mma_bf16(t_dk, kmajor_blk_desc(base + KV_OFF_DST, kk), mnmajor64_desc(qt, kk), IDESC_ACC, accum);
         }
-        if (!ok) break;
-        ptx::mma_commit(bar_fin);  // the item's dK and dV are complete once this does
-        nk = k + 1;
-      }
-      // every MMA this thread issued is complete before the CTA may exit
-      if (ok && nk > 0 && !ptx::mbar_wait(bar_fin, (nk - 1) & 1, BWD_WAIT)) {
-        ok = false;
-        wait_failed(211);
-      }
-      if (!ok) {  // one more commit drains whatever was issued after the last finished item
-        ptx::mma_commit(bar_fin);
-        (void)ptx::mbar_wait(bar_fin, nk & 1, BWD_WAIT);
-      }
+        // S^T, dP^T of block ii (which also read Q_i, dO_i) completed before
+        // the element-wise warps could hand over P^T, dS^T: the stage is free
+        // once these MMAs are
+        ptx::mma_commit(pd_empty);
+        ptx::mma_commit(q_empty(s));
+        tl_block(2, ii, 1);
+        return true;
+      };
+      for (int ii = 0; ii < n && ok; ++ii) ok = acc(ii);
+      ptx::mma_commit(bar_fin);  // completes once every MMA this thread issued has
+      if (!ptx::mbar_wait(bar_fin, 0, BWD_WAIT)) { ok = false; wait_failed(211); }
     }
   } else {
     const int qq = warp & 3, c = (warp - 2) >> 2;  // lane quarter; columns 16 c .. + 15
-    const int row = qq * 32 + lane;
+    const int row = qq * 32 + lane, kj = k0 + row;
+    const bool valid_k = kj < a.S;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    uint32_t g = 0;
-    for (int k = 0; ok; ++k) {
-      const int it_i = persistent_item(k, cta, G);
-      if (it_i >= a.items) break;
-      const KvItem it = kv_item(a, it_i);
-      const int k0 = it.k0, row0 = it.bb * a.S, h = it.h, n = it.n;
-      const int kj = k0 + row;
-      const bool valid_k = kj < a.S;
-      for (int ii = 0; ii < n && ok; ++ii, ++g) {
-        const uint32_t s = g % KV_QST, b = g & 1;
-        const int i = it.i0 + ii;
-        // this block's S^T, dP^T are in TMEM (which also means its stage, and
-        // the LSE / delta stored with it, have landed)
-        if (!warp_wait(sdp_full(b), (g / 2) & 1) || !warp_wait(q_full(s), (g / KV_QST) & 1)) {
-          ok = false;
-          if (lane == 0) wait_failed(208);
-          break;
-        }
-        if (k == 0 && warp == 2 && lane == 0) tl_block(2, ii, 2);
-        ptx::tc_fence_after();
-        float v[16], w[16];
-        ptx::tmem_ld16x2(t_st(b) + lane_off + c * 16, t_dpt(b) + lane_off + c * 16, v, w);
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
-        const float* st = stat + s * 2 * BK + c * 16;  // LSE of these 16 queries; delta at + BK
-        uint32_t pp[8], pd[8];
-        // a query block that sees every key of the tile needs no mask (CTA-uniform)
-        const bool full = k0 + 128 <= a.S && (i + 1) * BK <= a.S && (!a.causal || i * BK >= k0 + 127);
-        if (full) {
-          const uint64_t sc = f2_splat(a.scale_log2);
-#pragma unroll
-          for (int q = 0; q < 16; q += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(st + q);
-            const float4 d4 = *reinterpret_cast<const float4*>(st + BK + q);
-#pragma unroll
-            for (int x = 0; x < 4; x += 2) {
-              const float l0 = x == 0 ? l4.x : l4.z, l1 = x == 0 ? l4.y : l4.w;
-              const float d0 = x == 0 ? d4.x : d4.z, d1 = x == 0 ? d4.y : d4.w;
-              const int kk = q + x;
-              const uint64_t y = f2_fma(f2_pack(v[kk], v[kk + 1]), sc, f2_pack(-l0, -l1));
-              const uint64_t p = f2_pack(fast_exp2(f2_lo(y)), fast_exp2(f2_hi(y)));
-              const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[kk], w[kk + 1]), f2_pack(-d0, -d1)));
-              pp[kk / 2] = pack2(f2_lo(p), f2_hi(p));
-              pd[kk / 2] = pack2(f2_lo(ds), f2_hi(ds));
-            }
-          }
-        } else {
-          // queries i BK + 16 c + q with q < q_lo are before this key (causal),
-          // those with q >= q_hi past the sequence end; a key past the end
-          // sees none
-          const int qbase = i * BK + c * 16;
-          const int q_lo = a.causal ? kj - qbase : -1 << 30, q_hi = valid_k ? a.S - qbase : 0;
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float l2 = st[q], dl = st[BK + q];
-            const float p = (q >= q_lo && q < q_hi) ? fast_exp2(v[q] * a.scale_log2 - l2) : 0.f;
-            v[q] = p;
-            w[q] = p * (w[q] - dl);
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            pp[q] = pack2(v[2 * q], v[2 * q + 1]);
-            pd[q] = pack2(w[2 * q], w[2 * q + 1]);
-          }
-        }
-        // the P^T / dS^T buffers are free once the previous block's accumulation is done
-        if (g >= 1 && !warp_wait(pd_empty, (g - 1) & 1)) {
-          ok = false;
-          if (lane == 0) wait_failed(209);
-          break;
-        }
-        store_row_quarter(gbase + KV_OFF_PT, row, c, pp);
-        store_row_quarter(gbase + KV_OFF_DST, row, c, pd);
-        ptx::fence_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(pd_full);
-        if (k == 0 && warp == 2 && lane == 0) tl_block(2, ii, 3);
+    for (int ii = 0; ii < n && ok; ++ii) {
+      const int s = ii % KV_QST, b = ii & 1, i = i0 + ii;
+      // this block's S^T, dP^T are in TMEM (which also means its stage, and
+      // the LSE / delta stored with it, have landed)
+      if (!warp_wait(sdp_full(b), (ii / 2) & 1) || !warp_wait(q_full(s), (ii / KV_QST) & 1)) {
+        ok = false;
+        if (lane == 0) wait_failed(208);
+        break;
       }
-      if (!ok) break;
-      // the item's last accumulation is complete (or the MMA thread gave up)
-      const bool fin = warp_wait(bar_fin, k & 1);
+      if (warp == 2 && lane == 0) tl_block(2, ii, 2);
       ptx::tc_fence_after();
-      __nv_bfloat16* rowp = a.dqkv + (int64_t)(row0 + kj) * 3 * a.H;
+      float v[16], w[16];
+      ptx::tmem_ld16x2(t_st(b) + lane_off + c * 16, t_dpt(b) + lane_off + c * 16, v, w);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sdp_empty(b));
+      const float* st = stat + s * 2 * BK + c * 16;  // LSE of these 16 queries; delta at + BK
+      uint32_t pp[8], pd[8];
+      // a query block that sees every key of the tile needs no mask (CTA-uniform)
+      const bool full = k0 + 128 <= a.S && (i + 1) * BK <= a.S && (!a.causal || i * BK >= k0 + 127);
+      if (full) {
+        const uint64_t sc = f2_splat(a.scale_log2);
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {  // dK (scaled), then dV
-        float v0[32];  // tcgen05.ld is warp-collective: every lane loads
-        ptx::tmem_ld32((part == 0 ? t_dk : t_dv) + lane_off + c * 32, v0);
-        const float sc = part == 0 ? a.scale : 1.f;
-        if (fin && valid_k) {
-          uint4* out = reinterpret_cast<uint4*>(rowp + (part == 0 ? a.H : 2 * a.H) + h * D + c * 32);
+        for (int k = 0; k < 16; k += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(st + k);
+          const float4 d4 = *reinterpret_cast<const float4*>(st + BK + k);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            out[u] = make_uint4(pack2(v0[8 * u] * sc, v0[8 * u + 1] * sc), pack2(v0[8 * u + 2] * sc, v0[8 * u + 3] * sc),
-                                pack2(v0[8 * u + 4] * sc, v0[8 * u + 5] * sc), pack2(v0[8 * u + 6] * sc, v0[8 * u + 7] * sc));
+          for (int e = 0; e < 4; e += 2) {
+            const float l0 = e == 0 ? l4.x : l4.z, l1 = e == 0 ? l4.y : l4.w;
+            const float d0 = e == 0 ? d4.x : d4.z, d1 = e == 0 ? d4.y : d4.w;
+            const int kk = k + e;
+            const uint64_t x = f2_fma(f2_pack(v[kk], v[kk + 1]), sc, f2_pack(-l0, -l1));
+            const uint64_t p = f2_pack(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
+            const uint64_t ds = f2_mul(p, f2_add(f2_pack(w[kk], w[kk + 1]), f2_pack(-d0, -d1)));
+            pp[kk / 2] = pack2(f2_lo(p), f2_hi(p));
+            pd[kk / 2] = pack2(f2_lo(ds), f2_hi(ds));
+          }
+        }
+      } else {
+        // queries i BK + 16 c + k with k < k_lo are before this key (causal),
+        // those with k >= k_hi past the sequence end; a key past the end sees none
+        const int qbase = i * BK + c * 16;
+        const int k_lo = a.causal ? kj - qbase : -(1 << 30), k_hi = valid_k ? a.S - qbase : 0;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float l2 = st[k], dl = st[BK + k];
+          const float p = (k >= k_lo && k < k_hi) ? fast_exp2(v[k] * a.scale_log2 - l2) : 0.f;
+          v[k] = p;
+          w[k] = p * (w[k] - dl);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          pp[k] = pack2(v[2 * k], v[2 * k + 1]);
+          pd[k] = pack2(w[2 * k], w[2 * k + 1]);
         }
       }
-      if (!fin) ok = false;
-      if (warp == 2 && lane == 0) tl_unit(2, it_i, 1);
+      // the P^T / dS^T buffers are free once block ii-1's accumulation is done
+      if (ii >= 1 && !warp_wait(pd_empty, (ii - 1) & 1)) {
+        ok = false;
+        if (lane == 0) wait_failed(209);
+        break;
+      }
+      store_row_quarter(gbase + KV_OFF_PT, row, c, pp);
+      store_row_quarter(gbase + KV_OFF_DST, row, c, pd);
+      ptx::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(pd_full);
+      if (warp == 2 && lane == 0) tl_block(2, ii, 3);
     }
-    if (!ok && lane == 0) atomicExch(&g_attn_error, 5);
+    const bool fin = warp_wait(bar_fin, 0);
+    ptx::tc_fence_after();
+    __nv_bfloat16* rowp = a.dqkv + (int64_t)(row0 + kj) * 3 * a.H;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // dK (scaled), then dV
+      float v0[32];  // tcgen05.ld is warp-collective: every lane loads
+      ptx::tmem_ld32((part == 0 ? t_dk : t_dv) + lane_off + c * 32, v0);
+      const float sc = part == 0 ? a.scale : 1.f;
+      if (ok && fin && valid_k) {
+        uint4* out = reinterpret_cast<uint4*>(rowp + (part == 0 ? a.H : 2 * a.H) + h * D + c * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          out[u] = make_uint4(pack2(v0[8 * u] * sc, v0[8 * u + 1] * sc), pack2(v0[8 * u + 2] * sc, v0[8 * u + 3] * sc),
+                              pack2(v0[8 * u + 4] * sc, v0[8 * u + 5] * sc), pack2(v0[8 * u + 6] * sc, v0[8 * u + 7] * sc));
+      }
+    }
+    if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 5);
   }
   progress(2, 990);
   ptx::tc_fence_before();
@@ -1518,6 +1411,7 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
     ptx::tmem_dealloc(tmem, 512);
   }
   progress(2, 999);
+  if (tid == 0) tl_cta(2, 1);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1643,7 +1537,7 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   ba.batch = a.batch;
   ba.tiles = tiles;
   ba.items = (int)items;
-  // both kernels are persistent: one CTA per SM
+  // the dq kernel is persistent: one CTA per SM
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1651,8 +1545,8 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   e = launch_pdl(attn_bwd_dq_tc_kernel, dim3((int)std::min<int64_t>(items, std::max(sms, 1))),
                  dim3(DQ_NT), DQ_SMEM, st, tq128, tdo128, ba);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3((int)std::min<int64_t>(items, std::max(sms, 1))),
-                    dim3(KV_NT), KV_SMEM, st, tq128, tq64, tdo64, ba);
+  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(a.heads, a.batch, tiles), dim3(KV_NT), KV_SMEM,
+                    st, tq128, tq64, tdo64, ba);
 }
 
 cudaError_t attention_set_progress(int* p) {

@@ -808,7 +808,23 @@ part_reduce_kernel(const float* __restrict__ part, float* __restrict__ out,
   const int n = blockIdx.x * RED_COLS + cl;
   float s = 0.f, s2 = 0.f;
   if (n < N) {
-    for (int b = g; b < nb; b += RED_GROUPS) {
+    // eight rows' loads in flight before they are added, in the same order
+    constexpr int U = 8;
+    int b = g;
+    for (; b + (U - 1) * RED_GROUPS < nb; b += U * RED_GROUPS) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = part[(int64_t)(b + u * RED_GROUPS) * N + n];
+#pragma unroll
+      for (int u = 0; u < U; ++u) s += v[u];
+      if (part2) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = part2[(int64_t)(b + u * RED_GROUPS) * N + n];
+#pragma unroll
+        for (int u = 0; u < U; ++u) s2 += v[u];
+      }
+    }
+    for (; b < nb; b += RED_GROUPS) {
       s += part[(int64_t)b * N + n];
       if (part2) s2 += part2[(int64_t)b * N + n];
     }

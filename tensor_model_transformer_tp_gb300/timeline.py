@@ -12,9 +12,9 @@ GEMM: C[M, N] = A[M, K] B[N, K]^T in bf16 with the given epilogue (0 store,
 1 bias, 2 bias + GeLU; default 2), L2 flushed by a 256 MiB write before each
 launch; the CUDA-event time is the median of 20 launches, the stamps are from
 one more.  Attention backward: batch x seq, heads of 128, causal; the stamps
-are those of the first item of CTA 0 of the dQ and dK/dV kernels per block,
-and the span of each kernel from its first item's start to its last item's
-end.
+are those of CTA 0 of the dQ (its first item) and dK/dV kernels per block,
+and the span of each kernel from its first item's start (dQ) or first CTA's
+entry (dK/dV) to the last end.
 """
 from __future__ import annotations
 
@@ -132,8 +132,8 @@ def attention_bwd(B: int, S: int, heads: int) -> dict:
         b0 = blk[blk > 0].min() if (blk > 0).any() else 0
         G = min(ncta, torch.cuda.get_device_properties(0).multi_processor_count)
         t0 = r[:, 0][r[:, 0] > 0].min() if (r[:, 0] > 0).any() else 0
-        items0, k = [], 0  # CTA 0's items in the order it ran them: start, end (us)
-        while True:
+        items0, k = [], 0  # dq: CTA 0's items in the order it ran them: start, end (us)
+        while kid == 1:
             i = k * G + (G - 1 if k % 2 else 0)
             if i >= min(ncta, 4096):
                 break
@@ -142,7 +142,7 @@ def attention_bwd(B: int, S: int, heads: int) -> dict:
         out["kernels"][name] = {
             "cta0_items": items0,
             "span_us": float(r[:, 1].max() - r[:, 0].min()) / 1000.0,
-            # per work item (both kernels are persistent)
+            # dq: per work item (the kernel is persistent); dK/dV: per CTA
             "cta_mean_us": float((r[:, 1] - r[:, 0]).mean()) / 1000.0,
             # per block of CTA 0: S/dP MMAs issued, accumulation MMAs issued,
             # element-wise warp 2 saw S, handed its dS (ns from the first stamp)
@@ -263,8 +263,11 @@ def main(argv):
     elif len(argv) == 4 and argv[0] == "attn_bwd":
         r = attention_bwd(int(argv[1]), int(argv[2]), int(argv[3]))
         for name, k in r["kernels"].items():
-            print("%s: span %.1f us, item mean %.1f us" % (name, k["span_us"], k["cta_mean_us"]))
-            print("  CTA 0 items (us): " + ", ".join("%d: %.1f-%.1f" % x for x in k["cta0_items"]))
+            print("%s: span %.1f us, %s mean %.1f us" % (name, k["span_us"],
+                                                         "item" if name == "dq" else "CTA",
+                                                         k["cta_mean_us"]))
+            if k["cta0_items"]:
+                print("  CTA 0 items (us): " + ", ".join("%d: %.1f-%.1f" % x for x in k["cta0_items"]))
             print("  CTA 0 per block (ns): SdP issued, ACC issued, warp 2 saw S, warp 2 handed dS")
             for j, row in enumerate(k["cta0_blocks_ns"][:8]):
                 print("  block %d: %s" % (j, " ".join("%6d" % x for x in row)))
