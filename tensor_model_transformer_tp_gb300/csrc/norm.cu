@@ -909,8 +909,90 @@ part_reduce_l2(const float* __restrict__ part, float* __restrict__ out,
   }
 }
 
+// The same with 16-byte loads, for N % 4 == 0 and 16-byte aligned rows: a CTA
+// takes 16 columns (four float4 quads) with 64 row groups; group g adds rows
+// g, g + 64, ... in order (four loads in flight), then each column's 64 group
+// sums are added in a fixed two-stage order (groups 4k .. 4k + 3, then k =
+// 0 .. 15), so the result does not depend on timing.  Twice the CTAs of the
+// scalar kernel and four times the bytes per load keep enough reads in flight
+// for a few MB of partial rows.
+constexpr int RV_COLS = 16, RV_GROUPS = 64;
+__global__ void __launch_bounds__(256)
+part_reduce_v4_kernel(const float* __restrict__ part, float* __restrict__ out,
+                      const float* __restrict__ part2, float* __restrict__ out2, int nb, int N) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float4 sh[2][RV_GROUPS][RV_COLS / 4];
+  __shared__ float sh2[2][16][RV_COLS];
+  const int q = threadIdx.x & 3, g = threadIdx.x >> 2;
+  const int n = blockIdx.x * RV_COLS + q * 4;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f), s2 = s;
+  auto add4 = [](float4& a, const float4 b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+  };
+  if (n < N) {
+    constexpr int U = 4;
+    int b = g;
+    for (; b + (U - 1) * RV_GROUPS < nb; b += U * RV_GROUPS) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = *reinterpret_cast<const float4*>(part + (int64_t)(b + u * RV_GROUPS) * N + n);
+#pragma unroll
+      for (int u = 0; u < U; ++u) add4(s, v[u]);
+      if (part2) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          v[u] = *reinterpret_cast<const float4*>(part2 + (int64_t)(b + u * RV_GROUPS) * N + n);
+#pragma unroll
+        for (int u = 0; u < U; ++u) add4(s2, v[u]);
+      }
+    }
+    for (; b < nb; b += RV_GROUPS) {
+      add4(s, *reinterpret_cast<const float4*>(part + (int64_t)b * N + n));
+      if (part2) add4(s2, *reinterpret_cast<const float4*>(part2 + (int64_t)b * N + n));
+    }
+  }
+  sh[0][g][q] = s;
+  sh[1][g][q] = s2;
+  __syncthreads();
+  {  // stage 1: thread (k, c) adds groups 4k .. 4k + 3 of column c
+    const int c = threadIdx.x & (RV_COLS - 1), k = threadIdx.x >> 4;
+    float t = 0.f, t2 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float* a = reinterpret_cast<const float*>(&sh[0][4 * k + u][c >> 2]);
+      const float* a2 = reinterpret_cast<const float*>(&sh[1][4 * k + u][c >> 2]);
+      t += a[c & 3];
+      t2 += a2[c & 3];
+    }
+    sh2[0][k][c] = t;
+    sh2[1][k][c] = t2;
+  }
+  __syncthreads();
+  if (threadIdx.x < RV_COLS) {  // stage 2: k = 0 .. 15 in order
+    const int c = threadIdx.x, col = blockIdx.x * RV_COLS + c;
+    float t = 0.f, t2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      t += sh2[0][k][c];
+      t2 += sh2[1][k][c];
+    }
+    if (col < N) {
+      out[col] += t;
+      if (part2) out2[col] += t2;
+    }
+  }
+}
+
 cudaError_t reduce_parts(float* part, float* out, float* part2, float* out2, int nb, int N,
                          cudaStream_t st) {
+  if (nb <= 64 * RED_GROUPS && N % 4 == 0 &&
+      (((uintptr_t)part | (uintptr_t)(part2 ? part2 : part)) & 15) == 0)
+    return launch_pdl(part_reduce_v4_kernel, dim3((N + RV_COLS - 1) / RV_COLS), dim3(256), 0, st,
+                      (const float*)part, out, (const float*)part2, out2, nb, N);
   // up to 512 partial rows (the bias gradients of 8192 rows, the LayerNorm
   // backward's per-CTA rows): one launch, each of the eight thread groups
   // adding at most 64 rows
