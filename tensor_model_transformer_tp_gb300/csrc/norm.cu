@@ -511,11 +511,11 @@ ln_bwd_rows(const float* __restrict__ du, const T* __restrict__ x, const float* 
 // row k + 1, which every thread passes only when done with row k.  A wait that
 // gives up (about 0.25 s) sets g_norm_error and ends the CTA's loop; all
 // threads of the CTA leave together.
-constexpr int LNS_STAGES = 4;
+constexpr int LNS_STAGES = 3;
 constexpr uint64_t LNS_WAIT = 1ull << 29;
 
 template <typename T, int NCH>
-__global__ void __launch_bounds__(LNB_THREADS, 1)
+__global__ void __launch_bounds__(LNB_THREADS, NCH <= 3 ? 3 : 2)
 ln_bwd_staged(const float* __restrict__ du, const T* __restrict__ x, const float* __restrict__ mean,
               const float* __restrict__ rstd, const T* __restrict__ gamma,
               const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ pg,
