@@ -43,6 +43,9 @@ cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float
                                      float* dbeta, int M, int H, DType t, cudaStream_t st,
                                      float* part_x, int part_x_cap, int* n_part_x);
 cudaError_t reduce_partial_rows(float* part, float* out, int nparts, int N, cudaStream_t st);
+// attn_tc.cu: the tensor-core attention backward that also leaves the QKV
+// bias gradient's partial rows (batch * ceil(seq / 128) * 4 rows of 3H)
+cudaError_t attention_bwd_tc_bias(const AttnArgs& a, float* bias_part, cudaStream_t st);
 thread_local int g_launch_count = 0;
 
 uint64_t current_ctx_id() {
@@ -772,15 +775,27 @@ struct Exec {
     const bool ffn = s.seg_kind(seg) == SEG_FFN;
     const int Nc = ffn ? s.F : 3 * s.H;  // column GEMM output width
     const void* dcol;
+    int bias_rows = 0;  // > 0: the bias gradient's partial rows are in cpart(seg, b)
     if (ffn) {
       dcol = rowp(at(a.a), b, s.F, s.esz);  // dA
     } else {
       const AttnArgs at_ = attn_args(seg, b);
-      ok(attention_bwd(at_, stream(b)));
+      // the tensor-core backward sums dqkv's columns as it stores them
+      const int rows = at_.batch * ((at_.seq + 127) / 128) * 4;
+      if (attention_tc_supported(at_) && !(((uintptr_t)at_.d_o | (uintptr_t)at_.dqkv) & 15) &&
+          (size_t)rows * (size_t)Nc <= L.cpart_n && rows <= 512) {
+        ok(attention_bwd_tc_bias(at_, cpart(seg, b), stream(b)));
+        bias_rows = rows;
+      } else {
+        ok(attention_bwd(at_, stream(b)));
+      }
       dcol = at_.dqkv;
     }
     grad_wait(seg, GRP_BC, b);
-    ok(colsum_accum(dcol, Nc, (int)s.Ms, Nc, s.t, cpart(seg, b), p.dbc, stream(b)));
+    if (bias_rows > 0)
+      ok(reduce_partial_rows(cpart(seg, b), p.dbc, bias_rows, Nc, stream(b)));
+    else
+      ok(colsum_accum(dcol, Nc, (int)s.Ms, Nc, s.t, cpart(seg, b), p.dbc, stream(b)));
     grad_done(seg, GRP_BC, b);
     // dW_col[Nc, H] += dcol^T u
     GemmArgs w = base_gemm();

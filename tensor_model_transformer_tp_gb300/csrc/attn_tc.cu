@@ -656,7 +656,28 @@ struct BwdArgs {
   float scale;       // 1 / sqrt(d)
   int batch, tiles;  // sequences; 128-row tiles per sequence
   int items;         // batch * heads * tiles
+  // optional: column sums of dqkv as stored, one partial row of 3H floats per
+  // (sequence, 128-row tile, lane quarter): row (b tiles + t) 4 + q; null = off
+  float* bias_part;
 };
+
+// Column sums over the warp's 32 rows: lane l holds x[c] = its row's value in
+// column c (c < 32); on return lane l's x[0] is the sum over the 32 lanes of
+// column l (a fixed butterfly: 31 shuffles).
+__device__ __forceinline__ void warp_column_sums(float (&x)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? x[i] : x[i + off];
+      const float keep = upper ? x[i + off] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+}
+// A value as a bf16 store keeps it.
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16(v)); }
 
 // Both backward kernels are warp-specialised pipelines: one warp issues the
 // TMA loads, one thread the MMAs, sixteen warps do the element-wise work
@@ -1066,6 +1087,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq128,
                               pack2(v0[8 * u + 4] * a.scale, v0[8 * u + 5] * a.scale),
                               pack2(v0[8 * u + 6] * a.scale, v0[8 * u + 7] * a.scale));
       }
+      if (a.bias_part != nullptr) {  // this warp's 32 rows of the dQ columns, as stored
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v0[c] = (fin && valid_q) ? bf16_round(v0[c] * a.scale) : 0.f;
+        warp_column_sums(v0, lane);
+        a.bias_part[((int64_t)(it.bb * a.tiles + q0 / BQ) * 4 + qq) * 3 * a.H + h * D + sub * 32 + lane] = v0[0];
+      }
       if (!fin) ok = false;
       if (warp == 2 && lane == 0) tl_unit(1, i, 1);
     }
@@ -1400,6 +1427,13 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_con
           out[u] = make_uint4(pack2(v0[8 * u] * sc, v0[8 * u + 1] * sc), pack2(v0[8 * u + 2] * sc, v0[8 * u + 3] * sc),
                               pack2(v0[8 * u + 4] * sc, v0[8 * u + 5] * sc), pack2(v0[8 * u + 6] * sc, v0[8 * u + 7] * sc));
       }
+      if (a.bias_part != nullptr) {  // this warp's 32 keys of the dK or dV columns, as stored
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v0[x] = (ok && fin && valid_k) ? bf16_round(v0[x] * sc) : 0.f;
+        warp_column_sums(v0, lane);
+        a.bias_part[((int64_t)(bb * a.tiles + ktile) * 4 + qq) * 3 * a.H + (part == 0 ? a.H : 2 * a.H) +
+                    h * D + c * 32 + lane] = v0[0];
+      }
     }
     if (!(ok && fin) && lane == 0) atomicExch(&g_attn_error, 5);
   }
@@ -1497,7 +1531,16 @@ cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st) {
 
 cudaError_t attention_delta(const AttnArgs& a, cudaStream_t st);
 
+cudaError_t attention_bwd_tc_bias(const AttnArgs& a, float* bias_part, cudaStream_t st);
+
 cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
+  return attention_bwd_tc_bias(a, nullptr, st);
+}
+
+// The same, and the column sums of dqkv as stored (the QKV bias gradient) as
+// batch * ceil(seq / 128) * 4 partial rows of 3 hidden floats in bias_part,
+// every element written, for a fixed-order reduction by the caller.
+cudaError_t attention_bwd_tc_bias(const AttnArgs& a, float* bias_part, cudaStream_t st) {
   if (!attention_tc_supported(a) || ((uintptr_t)a.d_o | (uintptr_t)a.dqkv) & 15)
     return cudaErrorNotSupported;
   if (a.batch == 0 || a.seq == 0) return cudaSuccess;
@@ -1530,6 +1573,7 @@ cudaError_t attention_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   ba.causal = a.causal ? 1 : 0;
   ba.scale = 1.f / sqrtf((float)a.head_dim);
   ba.scale_log2 = 1.4426950408889634f * ba.scale;
+  ba.bias_part = bias_part;
   const int tiles = (a.seq + 127) / 128;
   if (tiles > 65535) return cudaErrorInvalidConfiguration;
   const int64_t items = (int64_t)tiles * a.batch * a.heads;
