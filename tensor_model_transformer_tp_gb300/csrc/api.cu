@@ -476,6 +476,9 @@ struct Exec {
   // partial rows of colsum(grad_out(seg)) for sub-batch b that the LayerNorm
   // backward of segment seg + 1 left in cpart(seg, b) (0: none; [seg * nsb + b])
   std::vector<int> xparts;
+  // partial rows of colsum(dA) that the dA GEMM's epilogue left in
+  // cpart(seg, b) for db1 (0: none; [seg * nsb + b])
+  std::vector<int> aparts;
   EventPool* P = nullptr;  // this thread's events on the call's device
   size_t ev_base = 2;      // P->ev[0], [1]: call entry / exit joins
 
@@ -762,6 +765,15 @@ struct Exec {
       d.aux = G;
       d.ld_aux = s.F;
       d.C = G;
+      // db1 = colsum(dA): the epilogue sums dA's columns as it stores them,
+      // into this segment's colsum scratch (nothing else of this sub-batch
+      // uses it before bwd_col reduces it)
+      int& ap = aparts[(size_t)seg * s.nsb + b];
+      ap = 0;
+      if ((size_t)((s.Ms + 31) / 32) * (size_t)s.F <= L.cpart_n) {
+        d.colsum_part = cpart(seg, b);
+        d.colsum_rows = &ap;
+      }
     } else {
       d.epi = Epi::Store;
       d.C = rowp(at(a.d_o), b, s.H, s.esz);
@@ -790,6 +802,10 @@ struct Exec {
         ok(attention_bwd(at_, stream(b)));
       }
       dcol = at_.dqkv;
+    }
+    if (ffn) {
+      bias_rows = aparts[(size_t)seg * s.nsb + b];
+      aparts[(size_t)seg * s.nsb + b] = 0;
     }
     grad_wait(seg, GRP_BC, b);
     if (bias_rows > 0)
@@ -1035,6 +1051,7 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   ex.sp.resize(s.nseg);
   for (int i = 0; i < s.nseg; ++i) ex.sp[i] = seg_params(s, i, w, gr);
   ex.xparts.assign((size_t)s.nseg * s.nsb, 0);
+  ex.aparts.assign((size_t)s.nseg * s.nsb, 0);
   if (!params_ok(s, ex.sp, bwd)) return OASES_ERR_INVALID_ARG;
   const void* io[4] = {x, dy, y, dx};  // device unless staged from host memory
   if (!stage_host)

@@ -264,6 +264,13 @@ struct GemmArgs {
   // aux stay bf16.
   const uint8_t* a_sf = nullptr;
   const uint8_t* b_sf = nullptr;
+  // Optional (bf16 C through the TMA-store epilogue, no split slabs): the
+  // column sums of C as stored, one partial row of N floats per 32-row slab
+  // of C (ceil(M / 32) rows, every element written), for a fixed-order
+  // reduction by the caller.  The launch sets *colsum_rows to that count when
+  // it takes them, and leaves it alone (and colsum_part unwritten) otherwise.
+  float* colsum_part = nullptr;
+  int* colsum_rows = nullptr;
 };
 
 // Returns cudaSuccess or the launch error.  Picks the tensor-core kernel when

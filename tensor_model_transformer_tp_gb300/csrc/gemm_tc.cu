@@ -279,6 +279,37 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
     for (int i = 0; i < CW; i += 2) gelu2_inplace(v[i], v[i + 1]);
   }
   stage_and_store(tmC, g.epi == Epi::Accum);
+  if constexpr (CW == 64) {
+    if (g.colsum_part != nullptr) {
+      // this warp's 32 rows of the 64 columns as stored: each lane reads its
+      // own row back from the staging buffer (bf16, 16-byte chunk u at
+      // u ^ (lane & 7)), and a butterfly of 31 shuffles per 32 columns leaves
+      // lane l with column n + 32 h + l of the slab's partial row
+      const uint8_t* row = stg + lane * 128;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row + (((4 * h + u) ^ (lane & 7)) << 4));
+          unpack8(w, x + 8 * u);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (!(m < g.M && n + 32 * h + i < g.N)) x[i] = 0.f;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const bool upper = (lane & off) != 0;
+#pragma unroll
+          for (int i = 0; i < off; ++i) {
+            const float send = upper ? x[i] : x[i + off];
+            x[i] = (upper ? x[i + off] : x[i]) + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+        }
+        if (n + 32 * h + lane < g.N) g.colsum_part[(int64_t)(mw / 32) * g.N + n + 32 * h + lane] = x[0];
+      }
+    }
+  }
 }
 
 // CL = 1: one CTA per 128 x BN tile.  CL = 2: a CTA pair (cluster of two)
@@ -716,6 +747,15 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
       (g.C2 == nullptr || make_map(&mc2, g.C2, g.N, g.M, g.ldc, cw, 32, ct)))
     ga.tma_store = 1;
   if (g.splits > 1 && !ga.tma_store) return cudaErrorNotSupported;  // slabs need the 3-D map
+  // column sums of C only in the bf16 TMA-store epilogue (64-column chunks)
+  if (ga.colsum_part != nullptr) {
+    if (ga.tma_store && g.c_t == DType::BF16 && g.splits == 1 && g.epi != Epi::Accum &&
+        ((uintptr_t)g.colsum_part & 3) == 0) {
+      if (g.colsum_rows) *g.colsum_rows = (g.M + 31) / 32;
+    } else {
+      ga.colsum_part = nullptr;
+    }
+  }
   auto kern = gemm_tc_kernel<BN, A_K, B_K, CL, GRP, MX>;
   static DeviceOnce attr;
   cudaError_t ea = attr.run([&] {
