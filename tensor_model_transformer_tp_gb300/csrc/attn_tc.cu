@@ -23,6 +23,8 @@
 #include <math.h>
 
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include "common.cuh"
 #include "sm100_ptx.cuh"
@@ -121,6 +123,15 @@ __device__ __forceinline__ void tl_fwd(int t, int j, int what) {
 // Records the first failed wait site (kernel * 100 + site) in g_attn_error.
 __device__ __forceinline__ void wait_failed(int code) { atomicCAS(&g_attn_error, 0, code); }
 
+// A work-item schedule for the persistent forward, computed on the host
+// (longest items first, each to the CTA with the least work so far): CTA c
+// runs order[start[c]] .. order[start[c + 1] - 1] in that order.
+constexpr int FWD_SCHED_ITEMS = 2048, FWD_SCHED_CTAS = 256;
+struct FwdSched {
+  uint16_t start[FWD_SCHED_CTAS + 1];
+  uint16_t order[FWD_SCHED_ITEMS];
+};
+
 struct FwdArgs {
   __nv_bfloat16* o;
   float* lse;
@@ -129,14 +140,18 @@ struct FwdArgs {
   float scale_log2;    // log2(e) / sqrt(d)
   int batch, pairs;    // sequences; pairs of 128-query tiles per sequence
   int items;           // batch * heads * pairs
+  int use_sched;       // 1: sched holds the item order; 0: the snake order
+  FwdSched sched;
 };
 
 // Forward: a persistent kernel, one CTA per SM.  A work item is 256 queries
 // of one (sequence, head): two tiles of 128 queries that share every K/V
 // block.  Items are numbered heaviest first (the causal pairs nearest the end
-// of the sequence have the most key blocks); CTA c of G takes items
-// c, 2G - 1 - c, 2G + c, ... (a snake over rounds of G, so the light items of
-// later rounds even out the heavy ones).  320 threads:
+// of the sequence have the most key blocks); the host assigns them longest
+// first, each to the CTA with the least work so far, and passes the order in
+// the kernel's parameters (for more than 2048 items or 256 CTAs, CTA c of G
+// takes items c, 2G - 1 - c, 2G + c, ...: a snake over rounds of G).  320
+// threads:
 //   warp 0      TMA loads, in the order the MMAs consume them: per item Q_0,
 //               then K_j and V_j into two-stage rings that run on across
 //               items, Q_1 after the first block; a tile's Q buffer is
@@ -189,6 +204,13 @@ constexpr float RESCALE_LOG2 = 8.f;
 __device__ __forceinline__ int persistent_item(int k, int c, int G) {
   return k * G + ((k & 1) ? G - 1 - c : c);
 }
+// Item k of CTA c (of G) of the forward: the host's schedule, else the snake.
+__device__ __forceinline__ int fwd_item_at(const FwdArgs& a, int k, int c, int G) {
+  if (!a.use_sched) return persistent_item(k, c, G);
+  const int s0 = a.sched.start[c], s1 = a.sched.start[c + 1];
+  return k < s1 - s0 ? (int)a.sched.order[s0 + k] : a.items;
+}
+
 struct FwdItem {
   int h, b, q0;  // head, sequence, first query of the pair
   int n0, n1;    // key blocks of each tile (0: the tile lies past the sequence end)
@@ -215,7 +237,8 @@ __device__ __forceinline__ void tl_fitem(int i, int what) {
   unsigned long long* tb = g_attn_timeline;
   if (tb != nullptr && i < 4096) tb[17920 + 8 * i + what] = ptx::globaltimer();
 }
-__device__ __forceinline__ void tl_fitems(int items, int c, int G, int what) {
+__device__ __forceinline__ void tl_fitems(const FwdArgs& a, int c, int G, int what) {
+  const int items = a.items;
   unsigned long long* tb = g_attn_timeline;
   if (tb == nullptr) return;
   const unsigned long long now = ptx::globaltimer();
@@ -226,14 +249,14 @@ __device__ __forceinline__ void tl_fitems(int items, int c, int G, int what) {
     tb[50689 + (what ? 2 : 0)] = (unsigned long long)clock64();
   }
   for (int k = 0;; ++k) {
-    const int i = persistent_item(k, c, G);
+    const int i = fwd_item_at(a, k, c, G);
     if (i >= items) break;
     if (i < 4096) tb[17920 + 8 * i + what] = now;
   }
 }
 
 __global__ void __launch_bounds__(F_NT, 1)
-attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
+attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -253,7 +276,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int cta = blockIdx.x, G = gridDim.x;
-  if (tid == 0) tl_fitems(a.items, cta, G, 0);
+  if (tid == 0) tl_fitems(a, cta, G, 0);
 
   if (tid == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -286,7 +309,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + (tslot - base));
   progress(0, 2);
-  if (tid == 0) tl_fitems(a.items, cta, G, 1);
+  if (tid == 0) tl_fitems(a, cta, G, 1);
   pdl_wait();
   pdl_trigger();
   progress(0, 3);
@@ -310,7 +333,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         return true;
       };
       for (int k = 0; ok; ++k) {
-        const int i = persistent_item(k, cta, G);
+        const int i = fwd_item_at(a, k, cta, G);
         if (i >= a.items) break;
         const FwdItem it = fwd_item(a, i);
         const int nmax = max(it.n0, it.n1);
@@ -426,7 +449,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
         if ((t ? it.n1 : it.n0) == 1) ptx::mma_commit(q_empty(t));  // the tile's last S of the item
         return true;
       };
-      int k = 0, i = persistent_item(0, cta, G);
+      int k = 0, i = fwd_item_at(a, 0, cta, G);
       uint32_t kb = 0;  // ring entry of the current item's block 0
       FwdItem it{};
       if (i < a.items) {
@@ -436,7 +459,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
       }
       while (ok && i < a.items) {
         const int nmax = max(it.n0, it.n1);
-        const int inext = persistent_item(k + 1, cta, G);
+        const int inext = fwd_item_at(a, k + 1, cta, G);
         const bool has_next = inext < a.items;
         FwdItem nx{};
         if (has_next) nx = fwd_item(a, inext);
@@ -484,7 +507,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
     const uint32_t t_s = tmem + 128u * t + lane_off, t_o = tmem + 256u + 128u * t + lane_off;
     uint32_t sc = 0u, oc = 0u;  // S_t blocks and finished items of this tile so far
     for (int k = 0; ok; ++k) {
-      const int i = persistent_item(k, cta, G);
+      const int i = fwd_item_at(a, k, cta, G);
       if (i >= a.items) break;
       const FwdItem it = fwd_item(a, i);
       const int nt = t ? it.n1 : it.n0;
@@ -636,7 +659,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const FwdArgs a) {
     ptx::tmem_dealloc(tmem, 512);
   }
   progress(0, 999);
-  if (tid == 0) tl_fitems(a.items, cta, G, 7);
+  if (tid == 0) tl_fitems(a, cta, G, 7);
 }
 
 // ---------------------------------------------------------------------------
@@ -1526,6 +1549,32 @@ cudaError_t attention_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<int64_t>(items, std::max(sms, 1));
+  fa.use_sched = 0;
+  if (items <= FWD_SCHED_ITEMS && grid <= FWD_SCHED_CTAS) {
+    // longest processing time first: items in index order (heaviest first),
+    // each to the CTA with the least work so far (ties: the lower CTA); the
+    // work of an item is its key blocks plus a share for the item change
+    const int nkv_all = (a.seq + BKV - 1) / BKV, bh = a.batch * a.heads;
+    std::vector<int> load(grid, 0), cnt(grid, 0), owner((size_t)items);
+    std::priority_queue<std::pair<int, int>, std::vector<std::pair<int, int>>, std::greater<>> q;
+    for (int c = 0; c < grid; ++c) q.push({0, c});
+    for (int i = 0; i < (int)items; ++i) {
+      const int pair = (int)pairs - 1 - i / bh, q1 = pair * 2 * BQ + BQ;
+      const int n1 = q1 >= a.seq ? 0 : (a.causal ? std::min(q1 / BKV + 1, nkv_all) : nkv_all);
+      const int n0 = a.causal ? std::min(pair * 2 * BQ / BKV + 1, nkv_all) : nkv_all;
+      const int w = 4 * std::max(n0, n1) + 3;
+      const auto top = q.top();
+      q.pop();
+      owner[i] = top.second;
+      ++cnt[top.second];
+      q.push({top.first + w, top.second});
+    }
+    fa.sched.start[0] = 0;
+    for (int c = 0; c < grid; ++c) fa.sched.start[c + 1] = (uint16_t)(fa.sched.start[c] + cnt[c]);
+    std::vector<int> fill(fa.sched.start, fa.sched.start + grid);
+    for (int i = 0; i < (int)items; ++i) fa.sched.order[fill[owner[i]]++] = (uint16_t)i;
+    fa.use_sched = 1;
+  }
   return launch_pdl(attn_fwd_tc_kernel, dim3(grid), dim3(F_NT), FWD_SMEM, st, m, fa);
 }
 

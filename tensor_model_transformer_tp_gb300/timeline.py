@@ -19,6 +19,7 @@ entry (dK/dV) to the last end.
 from __future__ import annotations
 
 import ctypes
+import heapq
 import sys
 
 import numpy as np
@@ -209,20 +210,28 @@ def attention_fwd(B: int, S: int, heads: int) -> dict:
                               for j in range(64) if (blk[t, j] > 0).any()] for t in range(2)]
     # items are numbered heaviest pair first: item i has pair pairs - 1 - i // (B heads)
     pair = pairs - 1 - np.arange(items) // (heads * B)
-    # the items of the first and the last CTA in the order they ran: CTA c of
-    # G takes items c, 2G - 1 - c, 2G + c, ... (G = min(items, SMs))
+    # the items of the first and the last CTA in the order they ran (the
+    # launch's schedule: items in index order, heaviest first, each to the
+    # CTA with the least work so far, ties to the lower CTA; work = 4 x the
+    # item's key blocks + 3)
     G = out["ctas"]
+    nkv = (S + 127) // 128
+    heap = [(0, c) for c in range(G)]
+    heapq.heapify(heap)
+    owner = []
+    for i in range(heads * B * pairs):
+        p = pairs - 1 - i // (heads * B)
+        q1 = p * 256 + 128
+        n1 = 0 if q1 >= S else min(q1 // 128 + 1, nkv)
+        n0 = min(p * 256 // 128 + 1, nkv)
+        load, c = heapq.heappop(heap)
+        owner.append(c)
+        heapq.heappush(heap, (load + 4 * max(n0, n1) + 3, c))
     out["cta_items"] = {}
     for c in (0, G - 1):
-        rows, k = [], 0
-        while True:
-            i = k * G + (G - 1 - c if k % 2 else c)
-            if i >= items:
-                break
-            rows.append((int(i), int(pair[i])) + tuple(round(float(x - t0) / 1000.0, 2) if x > 0 else -1.0
-                                                       for x in r[i, 2:7]))
-            k += 1
-        out["cta_items"][c] = rows
+        out["cta_items"][c] = [(int(i), int(pair[i])) + tuple(round(float(x - t0) / 1000.0, 2) if x > 0 else -1.0
+                                                             for x in r[i, 2:7])
+                               for i in range(items) if owner[i] == c]
     end = np.where(r[:, 6] > 0, r[:, 6], r[:, 4])  # O stored (tile 1), else tile 0's last PV
     for p in range(pairs - 1, -1, -1):
         sel = pair == p
