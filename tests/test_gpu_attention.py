@@ -121,3 +121,42 @@ def test_tc_backward_matches_cuda_core_backward(L):
     tc = run(L, qkv, B, S, nh, d, True, path=0, d_o=d_o)
     simt = run(L, qkv, B, S, nh, d, True, path=1, d_o=d_o)
     assert rel(tc["dqkv"], simt["dqkv"]) < 1e-2
+
+
+def test_results_do_not_depend_on_the_item_order(L):
+    """The persistent kernels hand out work items by a schedule: the forward
+    by the host's longest-first order up to 2048 items (a snake order over
+    rounds of CTAs beyond), the dQ kernel by the snake order.  16 sequences x
+    20 heads (2560 forward items, 5120 dQ items) against the same sequences
+    as two calls of 8 (1280 forward items each, the host's order): every
+    output bit-identical, since no item's arithmetic depends on which CTA
+    runs it or when."""
+    B, S, nh, d = 16, 2048, 20, 128
+    H = nh * d
+
+    def call(qkv, d_o, b):
+        M = b * S
+        o = torch.zeros(M, H, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros(nh, M, dtype=torch.float32, device="cuda")
+        delta = torch.zeros(nh, M, dtype=torch.float32, device="cuda")
+        dqkv = torch.zeros(M, 3 * H, dtype=torch.bfloat16, device="cuda")
+        assert L.oases_debug_attention(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), None, None, None,
+                                       b, S, nh, d, 1, 1, 0, 2, None) == 0
+        assert L.oases_debug_attention(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), d_o.data_ptr(),
+                                       delta.data_ptr(), dqkv.data_ptr(), b, S, nh, d, 1, 1, 1, 2,
+                                       None) == 0
+        torch.cuda.synchronize()
+        oz.oases_check_device(None)
+        return o, lse, dqkv
+
+    g = torch.Generator(device="cuda").manual_seed(7)
+    qkv = (torch.randn(B * S, 3 * H, generator=g, device="cuda") * 1.5).bfloat16()
+    d_o = torch.randn(B * S, H, generator=g, device="cuda").bfloat16()
+    o, lse, dqkv = call(qkv, d_o, B)
+    half = B * S // 2
+    for k, r in enumerate((0, half)):
+        o2, lse2, dqkv2 = call(qkv[r:r + half].contiguous(), d_o[r:r + half].contiguous(), B // 2)
+        assert torch.equal(o[r:r + half], o2)
+        assert torch.equal(lse[:, r:r + half], lse2)
+        assert torch.equal(dqkv[r:r + half], dqkv2)
+    assert bool(torch.isfinite(dqkv.float()).all())
