@@ -1059,7 +1059,7 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
       if (!aligned16(p)) return OASES_ERR_INVALID_ARG;
   const size_t ev_stage = ex.ev_base + (size_t)s.nseg * GRP_N;  // staging-copy events
   ex.P = &pool();
-  cudaError_t e = ex.P->ensure(ev_stage + 6);
+  cudaError_t e = ex.P->ensure(ev_stage + 6 + 2 * (size_t)s.nsb);
   if (e != cudaSuccess) return cuda_fail(e);
 
   // Host buffers (oases_stack_step only) are staged through the workspace.
@@ -1083,15 +1083,21 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
 
   const std::vector<cudaEvent_t>& pev = ex.P->ev;
   cudaEvent_t ev_in = pev[0], ev_out = pev[1];
-  cudaEvent_t ev_x = pev[ev_stage], ev_g = pev[ev_stage + 1];
+  cudaEvent_t ev_g = pev[ev_stage + 1];
   cudaEvent_t ev_y[2] = {pev[ev_stage + 2], pev[ev_stage + 3]};
   cudaEvent_t ev_end = pev[ev_stage + 4], ev_cs = pev[ev_stage + 5];
+  // per sub-batch: its rows of x landed, its rows of dx final
+  auto ev_xs = [&](int b) { return pev[ev_stage + 6 + b]; };
+  auto ev_dxs = [&](int b) { return pev[ev_stage + 6 + s.nsb + b]; };
+  const size_t MHs = (size_t)s.Ms * s.H * s.esz;  // one sub-batch's rows
   const bool two = ex.st[0] != ex.st[1];
   // Staging copies of host buffers go on a copy stream when nothing is being
-  // captured: x first (the compute streams wait for it), then g (waited for
-  // only before each stream's first backward operator); y is copied back as
-  // soon as both streams finish the forward, dx at the end, and s0 joins the
-  // copy stream before the call returns.  Under capture they stay on s0.
+  // captured: x first, one sub-batch's rows at a time (each sub-batch's first
+  // operator waits for its own rows), then g (waited for only before each
+  // stream's first backward operator); y is copied back as soon as both
+  // streams finish the forward, each sub-batch's rows of dx as soon as its
+  // last operator is done, and s0 joins the copy stream before the call
+  // returns.  Under capture they stay on s0.
   const bool any_host = host[0] || host[1] || host[2] || host[3];
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (any_host) ex.ok(cudaStreamIsCapturing(ex.st[0], &cap));
@@ -1101,12 +1107,12 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
     ex.ok(cudaEventRecord(ev_in, ex.st[0]));  // everything the caller enqueued before
     ex.ok(cudaStreamWaitEvent(cs, ev_in, 0));
     if (two) ex.ok(cudaStreamWaitEvent(ex.st[1], ev_in, 0));
-    if (host[0]) {
-      ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[0]), x, MH, cudaMemcpyHostToDevice, cs));
-      ex.ok(cudaEventRecord(ev_x, cs));
-      ex.ok(cudaStreamWaitEvent(ex.st[0], ev_x, 0));
-      if (two) ex.ok(cudaStreamWaitEvent(ex.st[1], ev_x, 0));
-    }
+    if (host[0])
+      for (int b = 0; b < s.nsb; ++b) {
+        ex.ok(cudaMemcpyAsync(ex.at<uint8_t>(ex.L.stage[0]) + b * MHs, static_cast<const uint8_t*>(x) + b * MHs,
+                              MHs, cudaMemcpyHostToDevice, cs));
+        ex.ok(cudaEventRecord(ev_xs(b), cs));
+      }
     if (host[1]) {
       ex.ok(cudaMemcpyAsync(ex.at(ex.L.stage[1]), g_host_or_dev, MH, cudaMemcpyHostToDevice, cs));
       ex.ok(cudaEventRecord(ev_g, cs));
@@ -1135,8 +1141,13 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
     tevs = &te.ev;
   }
   size_t tev = 0;
+  std::vector<char> x_waited((size_t)s.nsb, 0);
   if (s.M > 0)
     for (const Step& st : steps) {
+      if (cs && host[0] && !x_waited[(size_t)st.sb]) {  // this sub-batch's rows of x
+        x_waited[(size_t)st.sb] = 1;
+        ex.ok(cudaStreamWaitEvent(ex.stream(st.sb), ev_xs(st.sb), 0));
+      }
       TraceRec tr{st.ev, st.op, st.seg, st.sb, nullptr, nullptr};
       if (tracing) {
         while (tevs->size() < tev + 2) {
@@ -1163,6 +1174,13 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
         }
       }
       ex.run(st);
+      if (cs && host[3] && st.ev == EV_B && st.op == OP_LN && st.seg == 0) {
+        // the sub-batch's last operator: its rows of dx are final
+        ex.ok(cudaEventRecord(ev_dxs(st.sb), ex.stream(st.sb)));
+        ex.ok(cudaStreamWaitEvent(cs, ev_dxs(st.sb), 0));
+        ex.ok(cudaMemcpyAsync(static_cast<uint8_t*>(dx) + st.sb * MHs, ex.at<uint8_t>(ex.L.stage[3]) + st.sb * MHs,
+                              MHs, cudaMemcpyDeviceToHost, cs));
+      }
       if (tr.e1) {
         ex.ok(cudaEventRecord(tr.e1, ex.stream(st.sb)));
         g_trace.push_back(tr);
@@ -1179,11 +1197,7 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
       ex.ok(cudaStreamWaitEvent(cs, ev_end, 0));
       ex.ok(cudaMemcpyAsync(const_cast<void*>(y), ex.y, MH, cudaMemcpyDeviceToHost, cs));
     }
-    if (host[3]) {
-      ex.ok(cudaEventRecord(ev_end, ex.st[0]));
-      ex.ok(cudaStreamWaitEvent(cs, ev_end, 0));
-      ex.ok(cudaMemcpyAsync(dx, ex.dx, MH, cudaMemcpyDeviceToHost, cs));
-    }
+    // (dx went back one sub-batch at a time above)
     ex.ok(cudaEventRecord(ev_cs, cs));
     ex.ok(cudaStreamWaitEvent(ex.st[0], ev_cs, 0));  // completion is signalled on s0
   } else {

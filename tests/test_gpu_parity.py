@@ -213,9 +213,15 @@ def test_invalid_shape_raises_before_launch():
         DeviceBlock(shape, block_inputs(shape, seed=0)["layers"])
 
 
-def test_host_buffers_through_stack_step():
-    """x, g, y, dx in pinned host memory: staged through the workspace."""
-    shape = BlockShape("ffn", "bf16", batch=2, seq=64, hidden=256, ffn=512, w=2)
+@pytest.mark.parametrize("shape", [
+    BlockShape("ffn", "bf16", batch=2, seq=64, hidden=256, ffn=512, w=2),
+    # four sub-batches on two streams: x and dx staged one sub-batch's rows at a time
+    BlockShape("layer", "bf16", batch=4, seq=128, hidden=256, ffn=512, heads=2, w=2, sub_batches=4,
+               n_layers=2),
+])
+def test_host_buffers_through_stack_step(shape):
+    """x, g, y, dx in pinned host memory: staged through the workspace, bit
+    for bit the device-buffer results."""
     inp = block_inputs(shape, seed=12, affine=True)
     dev = run_gpu(shape, inp)
     blk = DeviceBlock(shape, inp["layers"])
