@@ -667,7 +667,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant
 //   dP = dO V^T,  dS = P * (dP - delta),
 //   dQ = dS K / sqrt(d),  dK = dS^T Q / sqrt(d),  dV = P^T dO.
 // Two kernels own disjoint outputs, so there are no atomics:
-//   dq kernel   one CTA per 128 queries, loops over 64-key blocks (row = query)
+//   dq kernel   persistent: one CTA per SM over work items of 128 queries,
+//               each looped over 128-key blocks (row = query)
 //   dkv kernel  one CTA per 128 keys, loops over 64-query blocks (row = key)
 // ---------------------------------------------------------------------------
 struct BwdArgs {
