@@ -54,8 +54,8 @@ METRIC = "block fwd+recompute+bwd TFLOP/s at 1 GB300; % of dense BF16 peak"
 NCU_TRAFFIC = {
     # the 14 GEMMs of one sub-batch of one layer, each launched twice (28 launches),
     # profiles/gemm_tc_stack4_h2560_traffic.md
-    "stack4_bf16_h2560": {"source_sha256": "ba165ee3aa5e875ae0a05e11c2dae47e536a0cbbeee8bf4e9ee5984eb8200646",
-                          "bytes_per_launch": 401128173},
+    "stack4_bf16_h2560": {"source_sha256": "f92fa70c280c5ff2880fbcbca69ab84ef2764cc6bcd2976a8bb970ddfe724d1d",
+                          "bytes_per_launch": 401570596},
 }
 
 

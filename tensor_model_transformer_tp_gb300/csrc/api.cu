@@ -479,6 +479,8 @@ struct Exec {
   // partial rows of colsum(dA) that the dA GEMM's epilogue left in
   // cpart(seg, b) for db1 (0: none; [seg * nsb + b])
   std::vector<int> aparts;
+  // 1: the dO GEMM's epilogue wrote delta = rowsum(dO * O) for (seg, b)
+  std::vector<int> dready;
   EventPool* P = nullptr;  // this thread's events on the call's device
   size_t ev_base = 2;      // P->ev[0], [1]: call entry / exit joins
 
@@ -777,6 +779,17 @@ struct Exec {
     } else {
       d.epi = Epi::Store;
       d.C = rowp(at(a.d_o), b, s.H, s.esz);
+      // the attention backward's delta = rowsum(dO * O) per head, summed by
+      // the epilogue as it stores dO (one head is 128 columns)
+      int& dr = dready[(size_t)seg * s.nsb + b];
+      dr = 0;
+      if (s.d == 128) {
+        d.rowdot_aux = rowp(at(a.o), b, s.H, s.esz);
+        d.rowdot_lda = s.H;
+        d.rowdot_out = at<float>(a.delta) + (size_t)b * s.nh * s.Ms;
+        d.rowdot_ld = (int64_t)s.Ms;
+        d.rowdot_done = &dr;
+      }
     }
     ok(run_gemm(d, b));
   }
@@ -791,7 +804,9 @@ struct Exec {
     if (ffn) {
       dcol = rowp(at(a.a), b, s.F, s.esz);  // dA
     } else {
-      const AttnArgs at_ = attn_args(seg, b);
+      AttnArgs at_ = attn_args(seg, b);
+      at_.delta_ready = dready[(size_t)seg * s.nsb + b] != 0;
+      dready[(size_t)seg * s.nsb + b] = 0;
       // the tensor-core backward sums dqkv's columns as it stores them
       const int rows = at_.batch * ((at_.seq + 127) / 128) * 4;
       if (attention_tc_supported(at_) && !(((uintptr_t)at_.d_o | (uintptr_t)at_.dqkv) & 15) &&
@@ -1052,6 +1067,7 @@ oases_status execute(const Shape& s, int n_layers, const oases_weights* w, const
   for (int i = 0; i < s.nseg; ++i) ex.sp[i] = seg_params(s, i, w, gr);
   ex.xparts.assign((size_t)s.nseg * s.nsb, 0);
   ex.aparts.assign((size_t)s.nseg * s.nsb, 0);
+  ex.dready.assign((size_t)s.nseg * s.nsb, 0);
   if (!params_ok(s, ex.sp, bwd)) return OASES_ERR_INVALID_ARG;
   const void* io[4] = {x, dy, y, dx};  // device unless staged from host memory
   if (!stage_host)

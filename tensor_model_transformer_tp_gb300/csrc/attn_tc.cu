@@ -1610,7 +1610,7 @@ cudaError_t attention_bwd_tc_bias(const AttnArgs& a, float* bias_part, cudaStrea
                                 KV_SMEM);
   });
   if (ea != cudaSuccess) return ea;
-  cudaError_t e = attention_delta(a, st);
+  cudaError_t e = a.delta_ready ? cudaSuccess : attention_delta(a, st);
   if (e != cudaSuccess) return e;
   BwdArgs ba;
   ba.lse = a.lse;

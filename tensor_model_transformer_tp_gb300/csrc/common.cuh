@@ -271,6 +271,17 @@ struct GemmArgs {
   // it takes them, and leaves it alone (and colsum_part unwritten) otherwise.
   float* colsum_part = nullptr;
   int* colsum_rows = nullptr;
+  // Optional (bf16 C through the TMA-store epilogue with 256-wide tiles, N a
+  // multiple of 128): for each row m and each group of 128 columns from n0,
+  // rowdot_out[(n0 / 128) * rowdot_ld + m] = the sum over the group of C[m][n]
+  // as stored times rowdot_aux[m][n] (bf16, leading dim rowdot_lda) -- the
+  // attention backward's delta = rowsum(dO * O) per head when C = dO.  The
+  // launch sets *rowdot_done = 1 when it takes it.
+  const void* rowdot_aux = nullptr;
+  int64_t rowdot_lda = 0;
+  float* rowdot_out = nullptr;
+  int64_t rowdot_ld = 0;
+  int* rowdot_done = nullptr;
 };
 
 // Returns cudaSuccess or the launch error.  Picks the tensor-core kernel when
@@ -349,6 +360,7 @@ struct AttnArgs {
   const void* d_o = nullptr;  // [M, H]
   float* delta = nullptr;     // [heads, M]: rowsum(dO * O)
   void* dqkv = nullptr;       // [M, 3H]
+  bool delta_ready = false;   // delta already holds rowsum(dO * O) (the dO GEMM's epilogue)
 };
 cudaError_t attention_fwd(const AttnArgs& a, cudaStream_t st);
 cudaError_t attention_bwd(const AttnArgs& a, cudaStream_t st);

@@ -177,7 +177,7 @@ template <int CW>
 __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorMap* tmC,
                                               const CUtensorMap* tmC2, uint8_t* stg,
                                               uint32_t stg_s, int m, int mw, int n, int z,
-                                              int lane, float (&v)[CW]) {
+                                              int lane, float (&v)[CW], float* rowdot = nullptr) {
   const bool bf = g.c_t == DType::BF16;
   if (g.epi == Epi::Bias || g.epi == Epi::BiasGelu || g.epi == Epi::BiasResid) {
     const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(g.bias) + n;
@@ -308,6 +308,23 @@ __device__ __forceinline__ void epi_tma_chunk(const GemmArgs& g, const CUtensorM
         }
         if (n + 32 * h + lane < g.N) g.colsum_part[(int64_t)(mw / 32) * g.N + n + 32 * h + lane] = x[0];
       }
+    }
+    if (rowdot != nullptr && m < g.M) {
+      // this lane's row of the 64 columns as stored (read back from the
+      // staging buffer) times the same row and columns of rowdot_aux
+      const uint8_t* row = stg + lane * 128;
+      const __nv_bfloat16* ax = static_cast<const __nv_bfloat16*>(g.rowdot_aux) + (int64_t)m * g.rowdot_lda + n;
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (n + 8 * u >= g.N) break;
+        float c[8], o[8];
+        unpack8(*reinterpret_cast<const uint4*>(row + ((u ^ (lane & 7)) << 4)), c);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(ax) + u), o);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = fmaf(c[i], o[i], acc);
+      }
+      *rowdot += acc;
     }
   }
 }
@@ -559,14 +576,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (g.tma_store && g.c_t == DType::BF16) {
         uint8_t* stg = gbase + C::EPI_OFF + (warp - 2) * 4096;
         const uint32_t stg_s = base + C::EPI_OFF + (warp - 2) * 4096;
+        float rd = 0.f;  // rowdot: this half of a 256-wide tile is one 128-column group
 #pragma unroll 1
         for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 64) {
           float v[64];
           ptx::tmem_ld32(trow + c0, *reinterpret_cast<float(*)[32]>(v));
           ptx::tmem_ld32(trow + c0 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
           if (mw < g.M && nb0 + c0 < g.N)
-            epi_tma_chunk<64>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, z, lane, v);
+            epi_tma_chunk<64>(g, &tmC, &tmC2, stg, stg_s, m, mw, nb0 + c0, z, lane, v,
+                              g.rowdot_out != nullptr ? &rd : nullptr);
         }
+        if (g.rowdot_out != nullptr && m < g.M && nb0 + half * (BN / 2) < g.N)
+          g.rowdot_out[(int64_t)((nb0 + half * (BN / 2)) / 128) * g.rowdot_ld + m] = rd;
       } else if (g.tma_store) {
         uint8_t* stg = gbase + C::EPI_OFF + (warp - 2) * 4096;
         const uint32_t stg_s = base + C::EPI_OFF + (warp - 2) * 4096;
@@ -747,6 +768,17 @@ cudaError_t launch_tc(const GemmArgs& g, cudaStream_t st) {
       (g.C2 == nullptr || make_map(&mc2, g.C2, g.N, g.M, g.ldc, cw, 32, ct)))
     ga.tma_store = 1;
   if (g.splits > 1 && !ga.tma_store) return cudaErrorNotSupported;  // slabs need the 3-D map
+  // row dots only in the bf16 TMA-store epilogue of 256-wide tiles (a warp's
+  // half of a tile is one 128-column group)
+  if (ga.rowdot_out != nullptr) {
+    if (BN == 256 && ga.tma_store && g.c_t == DType::BF16 && g.splits == 1 && g.epi != Epi::Accum &&
+        g.N % 128 == 0 && g.rowdot_aux != nullptr && g.rowdot_lda % 8 == 0 && g.rowdot_ld >= g.M &&
+        (((uintptr_t)g.rowdot_aux & 15) == 0) && (((uintptr_t)g.rowdot_out & 3) == 0)) {
+      if (g.rowdot_done) *g.rowdot_done = 1;
+    } else {
+      ga.rowdot_out = nullptr;
+    }
+  }
   // column sums of C only in the bf16 TMA-store epilogue (64-column chunks)
   if (ga.colsum_part != nullptr) {
     if (ga.tma_store && g.c_t == DType::BF16 && g.splits == 1 && g.epi != Epi::Accum &&
