@@ -30,6 +30,7 @@
 #include <mutex>
 #include <unordered_map>
 #include <string>
+#include <functional>
 #include <vector>
 
 #include "common.cuh"
@@ -41,7 +42,8 @@ cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float
                                      const float* rstd, const void* gamma, const void* dres, void* dx,
                                      float* part_g, float* part_b, float2* stat, float* dgamma,
                                      float* dbeta, int M, int H, DType t, cudaStream_t st,
-                                     float* part_x, int part_x_cap, int* n_part_x);
+                                     float* part_x, int part_x_cap, int* n_part_x, float* out_x,
+                                     const std::function<void(bool)>* before_reduce);
 cudaError_t reduce_partial_rows(float* part, float* out, int nparts, int N, cudaStream_t st);
 // attn_tc.cu: the tensor-core attention backward that also leaves the QKV
 // bias gradient's partial rows (batch * ceil(seq / 128) * 4 rows of 3H)
@@ -474,7 +476,8 @@ struct Exec {
   void* dx;                   // gradient w.r.t. x
   cudaError_t err = cudaSuccess;
   // partial rows of colsum(grad_out(seg)) for sub-batch b that the LayerNorm
-  // backward of segment seg + 1 left in cpart(seg, b) (0: none; [seg * nsb + b])
+  // backward of segment seg + 1 left in cpart(seg, b) (0: none; -1: that
+  // backward already added them into db_row; [seg * nsb + b])
   std::vector<int> xparts;
   // partial rows of colsum(dA) that the dA GEMM's epilogue left in
   // cpart(seg, b) for db1 (0: none; [seg * nsb + b])
@@ -713,8 +716,12 @@ struct Exec {
   }
 
   void bwd_g(int seg, int b) {  // db_row += colsum(dy); Eq. (1): dP_k = dy, nothing else to do
-    grad_wait(seg, GRP_BR, b);
     int& xp = xparts[(size_t)seg * s.nsb + b];
+    if (xp < 0) {  // summed and accumulated by the next segment's LayerNorm backward
+      xp = 0;
+      return;
+    }
+    grad_wait(seg, GRP_BR, b);
     if (xp > 0)  // the column sums of dy were taken as it was written (LayerNorm backward)
       ok(reduce_partial_rows(cpart(seg, b), sp[seg].dbr, xp, s.H, stream(b)));
     else
@@ -932,21 +939,31 @@ struct Exec {
     const void* dres = s.residual ? rowp(grad_out(seg), b, s.H, s.esz) : nullptr;
     void* dxo = rowp(grad_in(seg), b, s.H, s.esz);
     if (s.pre_ln) {
-      grad_wait(seg, GRP_LN, b);
       // dx is the previous segment's output gradient: its column sums (that
       // segment's row-bias gradient) are taken here, as dx is written, into
-      // the previous segment's colsum scratch, which nothing else of this
-      // sub-batch uses before that segment's bwd_g reduces them
+      // the previous segment's colsum scratch, and added into db_row by the
+      // same reduction launch as dgamma and dbeta (else by that segment's
+      // bwd_g).  The sub-batch order of both accumulations is kept by waits
+      // placed right before that launch: this sub-batch's LayerNorm kernel
+      // itself waits for nothing of the other's.
       float* px = seg >= 1 ? cpart(seg - 1, b) : nullptr;
       const int cap = (int)std::min<size_t>(L.cpart_n / (size_t)s.H, 1u << 20);
       int np = 0;
+      const std::function<void(bool)> before_reduce = [&](bool with_x) {
+        grad_wait(seg, GRP_LN, b);
+        if (with_x) grad_wait(seg - 1, GRP_BR, b);
+      };
       ok(layer_norm_bwd_dx_colsum(du, rowp(seg_in(seg), b, s.H, s.esz), rowp(at<float>(a.mu), b, 1, 4),
                                   rowp(at<float>(a.rstd), b, 1, 4), sp[seg].g, dres, dxo,
                                   at<float>(a.lpart_g) + (size_t)b * L.lpart_n,
                                   at<float>(a.lpart_b) + (size_t)b * L.lpart_n,
                                   rowp(at<float2>(a.lstat), b, 1, 8), sp[seg].dg, sp[seg].db,
-                                  (int)s.Ms, s.H, s.t, stream(b), px, cap, &np));
-      if (seg >= 1) xparts[(size_t)(seg - 1) * s.nsb + b] = np;
+                                  (int)s.Ms, s.H, s.t, stream(b), px, cap, &np,
+                                  seg >= 1 ? sp[seg - 1].dbr : nullptr, &before_reduce));
+      if (seg >= 1) {
+        xparts[(size_t)(seg - 1) * s.nsb + b] = np;
+        if (np < 0) grad_done(seg - 1, GRP_BR, b);
+      }
       grad_done(seg, GRP_LN, b);
     } else {
       ok(add_into(dres, du, dxo, (int64_t)s.Ms * s.H, s.t, stream(b)));

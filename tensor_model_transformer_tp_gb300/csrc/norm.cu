@@ -9,6 +9,8 @@
 // the partial rows in order.  No atomics, so results are bit-reproducible.
 #include <algorithm>
 
+#include <functional>
+
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -919,14 +921,15 @@ part_reduce_l2(const float* __restrict__ part, float* __restrict__ out,
 constexpr int RV_COLS = 16, RV_GROUPS = 64;
 __global__ void __launch_bounds__(256)
 part_reduce_v4_kernel(const float* __restrict__ part, float* __restrict__ out,
-                      const float* __restrict__ part2, float* __restrict__ out2, int nb, int N) {
+                      const float* __restrict__ part2, float* __restrict__ out2,
+                      const float* __restrict__ part3, float* __restrict__ out3, int nb, int N) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float4 sh[2][RV_GROUPS][RV_COLS / 4];
-  __shared__ float sh2[2][16][RV_COLS];
+  __shared__ float4 sh[3][RV_GROUPS][RV_COLS / 4];
+  __shared__ float sh2[3][16][RV_COLS];
   const int q = threadIdx.x & 3, g = threadIdx.x >> 2;
   const int n = blockIdx.x * RV_COLS + q * 4;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f), s2 = s;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f), s2 = s, s3 = s;
   auto add4 = [](float4& a, const float4 b) {
     a.x += b.x;
     a.y += b.y;
@@ -949,40 +952,48 @@ part_reduce_v4_kernel(const float* __restrict__ part, float* __restrict__ out,
 #pragma unroll
         for (int u = 0; u < U; ++u) add4(s2, v[u]);
       }
+      if (part3) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          v[u] = *reinterpret_cast<const float4*>(part3 + (int64_t)(b + u * RV_GROUPS) * N + n);
+#pragma unroll
+        for (int u = 0; u < U; ++u) add4(s3, v[u]);
+      }
     }
     for (; b < nb; b += RV_GROUPS) {
       add4(s, *reinterpret_cast<const float4*>(part + (int64_t)b * N + n));
       if (part2) add4(s2, *reinterpret_cast<const float4*>(part2 + (int64_t)b * N + n));
+      if (part3) add4(s3, *reinterpret_cast<const float4*>(part3 + (int64_t)b * N + n));
     }
   }
   sh[0][g][q] = s;
   sh[1][g][q] = s2;
+  sh[2][g][q] = s3;
   __syncthreads();
   {  // stage 1: thread (k, c) adds groups 4k .. 4k + 3 of column c
     const int c = threadIdx.x & (RV_COLS - 1), k = threadIdx.x >> 4;
-    float t = 0.f, t2 = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float* a = reinterpret_cast<const float*>(&sh[0][4 * k + u][c >> 2]);
-      const float* a2 = reinterpret_cast<const float*>(&sh[1][4 * k + u][c >> 2]);
-      t += a[c & 3];
-      t2 += a2[c & 3];
+    for (int a = 0; a < 3; ++a) {
+      float t = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t += reinterpret_cast<const float*>(&sh[a][4 * k + u][c >> 2])[c & 3];
+      sh2[a][k][c] = t;
     }
-    sh2[0][k][c] = t;
-    sh2[1][k][c] = t2;
   }
   __syncthreads();
   if (threadIdx.x < RV_COLS) {  // stage 2: k = 0 .. 15 in order
     const int c = threadIdx.x, col = blockIdx.x * RV_COLS + c;
-    float t = 0.f, t2 = 0.f;
+    float t = 0.f, t2 = 0.f, t3 = 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       t += sh2[0][k][c];
       t2 += sh2[1][k][c];
+      t3 += sh2[2][k][c];
     }
     if (col < N) {
       out[col] += t;
       if (part2) out2[col] += t2;
+      if (part3) out3[col] += t3;
     }
   }
 }
@@ -992,7 +1003,8 @@ cudaError_t reduce_parts(float* part, float* out, float* part2, float* out2, int
   if (nb <= 64 * RED_GROUPS && N % 4 == 0 &&
       (((uintptr_t)part | (uintptr_t)(part2 ? part2 : part)) & 15) == 0)
     return launch_pdl(part_reduce_v4_kernel, dim3((N + RV_COLS - 1) / RV_COLS), dim3(256), 0, st,
-                      (const float*)part, out, (const float*)part2, out2, nb, N);
+                      (const float*)part, out, (const float*)part2, out2, (const float*)nullptr,
+                      (float*)nullptr, nb, N);
   // up to 512 partial rows (the bias gradients of 8192 rows, the LayerNorm
   // backward's per-CTA rows): one launch, each of the eight thread groups
   // adding at most 64 rows
@@ -1125,6 +1137,18 @@ cudaError_t shard_sum(const float* part, int64_t pstride, int w, const void* bia
                             : shard_sum_t<__nv_bfloat16, __nv_bfloat16>(part, pstride, w, bias, resid, out, M, N, st);
 }
 
+// Three pairs of partial rows (the same count nb) reduced into their outputs:
+// one launch where the 16-byte kernel applies, else one pair at a time.
+cudaError_t reduce_parts3(float* p1, float* o1, float* p2, float* o2, float* p3, float* o3, int nb,
+                          int N, cudaStream_t st) {
+  if (nb <= 64 * RED_GROUPS && N % 4 == 0 && (((uintptr_t)p1 | (uintptr_t)p2 | (uintptr_t)p3) & 15) == 0)
+    return launch_pdl(part_reduce_v4_kernel, dim3((N + RV_COLS - 1) / RV_COLS), dim3(256), 0, st,
+                      (const float*)p1, o1, (const float*)p2, o2, (const float*)p3, o3, nb, N);
+  cudaError_t e = reduce_parts(p1, o1, p2, o2, nb, N, st);
+  if (e != cudaSuccess) return e;
+  return reduce_parts(p3, o3, nullptr, nullptr, nb, N, st);
+}
+
 // out[n] += the sum of the nparts partial rows part[r][n], in a fixed order.
 cudaError_t reduce_partial_rows(float* part, float* out, int nparts, int N, cudaStream_t st) {
   if (nparts <= 0 || N <= 0) return cudaSuccess;
@@ -1169,25 +1193,34 @@ cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float
                                      const float* rstd, const void* gamma, const void* dres, void* dx,
                                      float* part_g, float* part_b, float2* stat, float* dgamma,
                                      float* dbeta, int M, int H, DType t, cudaStream_t st,
-                                     float* part_x, int part_x_cap, int* n_part_x);
+                                     float* part_x, int part_x_cap, int* n_part_x, float* out_x,
+                                     const std::function<void(bool)>* before_reduce);
 
 cudaError_t layer_norm_bwd(const float* du, const void* x, const float* mean, const float* rstd,
                            const void* gamma, const void* dres, void* dx, float* part_g,
                            float* part_b, float2* stat, float* dgamma, float* dbeta, int M, int H,
                            DType t, cudaStream_t st) {
   return layer_norm_bwd_dx_colsum(du, x, mean, rstd, gamma, dres, dx, part_g, part_b, stat, dgamma,
-                                  dbeta, M, H, t, st, nullptr, 0, nullptr);
+                                  dbeta, M, H, t, st, nullptr, 0, nullptr, nullptr, nullptr);
 }
 
 // The same, and where the staged kernel runs and at most part_x_cap partial
 // rows are needed, also the column sums of dx as stored: *n_part_x partial
 // rows of H floats in part_x (16-byte aligned), for a fixed-order reduction by
-// the caller.  Otherwise *n_part_x = 0 and part_x is not written.
+// the caller, or, with out_x given, added into out_x by the same reduction
+// launch as dgamma and dbeta (*n_part_x = -1).  Otherwise *n_part_x = 0 and
+// part_x is not written.  before_reduce (optional) runs on the host right
+// before the dgamma / dbeta reduction is enqueued, with true when out_x is
+// reduced by it too: the caller's stream waits for accumulation order go there.
 cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float* mean,
                                      const float* rstd, const void* gamma, const void* dres, void* dx,
                                      float* part_g, float* part_b, float2* stat, float* dgamma,
                                      float* dbeta, int M, int H, DType t, cudaStream_t st,
-                                     float* part_x, int part_x_cap, int* n_part_x) {
+                                     float* part_x, int part_x_cap, int* n_part_x, float* out_x,
+                                     const std::function<void(bool)>* before_reduce) {
+  auto hook = [&](bool with_x) {
+    if (before_reduce) (*before_reduce)(with_x);
+  };
   if (n_part_x) *n_part_x = 0;
   if ((uintptr_t)part_x & 15) part_x = nullptr;
   if (M == 0) return cudaSuccess;
@@ -1208,8 +1241,14 @@ cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float
                         : ln_bwd_staged_launch<__nv_bfloat16>(du, x, mean, rstd, gamma, dres, dx,
                                                               part_g, part_b, px, part_x_cap, M, H, st,
                                                               &parts);
-    if (n_part_x) *n_part_x = px ? parts : 0;
     if (e != cudaSuccess) return e;
+    if (px && out_x) {
+      hook(true);
+      if (n_part_x) *n_part_x = -1;
+      return reduce_parts3(part_g, dgamma, part_b, dbeta, px, out_x, parts, H, st);
+    }
+    if (n_part_x) *n_part_x = px ? parts : 0;
+    hook(false);
     return reduce_parts(part_g, dgamma, part_b, dbeta, parts, H, st);
   }
   if (vec && H <= 4 * LNB_THREADS * 4) {
@@ -1220,6 +1259,7 @@ cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float
                         : ln_bwd_rows_launch<__nv_bfloat16>(du, x, mean, rstd, gamma, dres, dx,
                                                             part_g, part_b, M, H, st);
     if (e != cudaSuccess) return e;
+    hook(false);
     return reduce_parts(part_g, dgamma, part_b, dbeta, nb, H, st);
   }
   if (vec) {
@@ -1234,8 +1274,10 @@ cudaError_t layer_norm_bwd_dx_colsum(const float* du, const void* x, const float
                      (const __nv_bfloat16*)x, mean, rstd, (const __nv_bfloat16*)gamma,
                      (const __nv_bfloat16*)dres, (__nv_bfloat16*)dx, part_g, part_b, M, H);
     if (e != cudaSuccess) return e;
+    hook(false);
     return reduce_parts(part_g, dgamma, part_b, dbeta, nb, H, st);
   }
+  hook(false);  // (its reductions are inside ln_bwd_t)
   if (t == DType::F32)
     return ln_bwd_t<float>(du, x, mean, rstd, gamma, dres, dx, part_g, part_b, stat, dgamma,
                            dbeta, M, H, st);
